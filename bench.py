@@ -1,0 +1,463 @@
+"""Throughput bench of the fused ZeRO-2 synchronisation step on GB300.
+
+Default workload: P = 8 virtual ranks, Llama-style 1.1B tensor list (201
+tensors, 1,100,048,384 parameters), 25 MiB buckets, bf16 gradients
+N(0, 5e-4), AdamW (lr 2e-4, betas 0.9/0.95, eps 1e-8, wd 0.1) with global
+gradient-norm clipping at 1.0.  One step = dp_fused_zero_step over all buckets:
+reduce-scatter-mean (+ norm partials), clip coefficient, AdamW fused with the
+all-gather of bf16 parameters into all 8 replicas.
+
+Prints ONE JSON line (rank 0).  `value` is parameters synchronised per second
+over all GPUs (inputs resident in HBM, CUDA events, max over ranks); `e2e`
+repeats the step through the same call with the gradients copied in from
+pinned host memory and the norm read back every step; `roofline` reports the
+dominant kernel (AdamW + all-gather) against the measured HBM copy bandwidth;
+`cpu_baseline` times the CPU oracle on a bounded sample on this host's cores.
+
+`--impl reference` times only the CPU oracle (the reference implementation of
+the method for this build) on the same workload, sample by sample.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload on
+its own GPU (the method has no inter-GPU exchange here); value = all ranks'
+parameters / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import configs, device as wdev, gen  # noqa: E402
+
+KERNEL_BYTES_PER_PARAM = {
+    # algorithmic bytes per parameter of each launch (reads + writes)
+    "reduce_scatter": lambda P: 2 * P + 4,
+    "adamw_all_gather": lambda P: 4 + 12 + 12 + 2 * P,
+    "zero_fused": lambda P: 2 * P + 12 + 12 + 2 * P,
+    "allreduce": lambda P: 4 * P,
+}
+
+
+def workload_by_name(name):
+    table = {w.name: w for w in (configs.tiny_plumbing(), configs.gpt2_small_allreduce(),
+                                 configs.llama_1b1_zero2(), configs.gpt_2b5_clip(),
+                                 configs.llama_1b1_zero2(layers=2, embeddings=False))}
+    for cap in configs.SWEEP_BUCKETS:
+        for mode in ("zero", "allreduce"):
+            w = configs.sweep_small_tensors(cap, mode)
+            table[w.name] = w
+    if name not in table:
+        raise SystemExit(f"unknown workload {name}; known: {sorted(table)}")
+    return table[name]
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=15.0,
+                       max_buckets=64, step=1):
+    """Time the CPU oracle's fused step on consecutive buckets (skipping the
+    first, a single oversized head matrix), enough for ~budget_s of work.
+    Returns (params/s, params, seconds, threads, description)."""
+    import numpy as np
+    import oracle
+    orc = oracle.default()
+    sizes = wl.sizes
+    op = orc.plan(sizes, wl.bucket_bytes, wl.P)
+    nb = op["n_buckets"]
+    threads = os.cpu_count() or 1
+    done_params, done_s, b = 0, 0.0, min(1, nb - 1)
+    used = []
+    offsets = plan_sizes_offsets
+    cfg = oracle.adamw_cfg(wl.adamw, step)
+    while b < nb and done_s < budget_s and len(used) < max_buckets:
+        batch = list(range(b, min(nb, b + threads)))
+        tens = [t for t in range(len(sizes)) if op["t_bucket"][t] in batch]
+        tens.sort()
+        sub = [sizes[t] for t in tens]
+        dec = [wl.decay[t] for t in tens]
+        g = torch.cat([grads_dev[:, offsets[t]:offsets[t] + sizes[t]] for t in tens], dim=1)
+        g = g.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        mst = torch.cat([master_dev[offsets[t]:offsets[t] + sizes[t]] for t in tens]).cpu().numpy()
+        z = np.zeros_like(mst)
+        t0 = time.perf_counter()
+        orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g, mst, z, z, cfg, n_threads=threads)
+        done_s += time.perf_counter() - t0
+        done_params += sum(sub)
+        used += batch
+        b = batch[-1] + 1
+    desc = (f"buckets {used[0]}..{used[-1]} of {nb} ({done_params} params, "
+            f"{100.0 * done_params / wl.n_params:.1f}% of the workload), oracle fused ZeRO step "
+            f"with its own clip norm over the sample")
+    return done_params / done_s, done_params, done_s, threads, desc
+
+
+# --------------------------------------------------------------------------- GPU bench
+def run_gpu(args, rank, local, world):
+    import gradient_sync_zero_gb300 as dps
+
+    torch.cuda.set_device(local)
+    wl = workload_by_name(args.workload)
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    P, L, stride = plan.P, plan.L, plan.stride
+    off = plan.tensor_offsets()
+    ws = plan.new_workspace()
+    grads = plan.new_replicas()
+    wdev.fill_grads(grads, off, wl, step=1)
+    zero = wl.mode == "zero"
+    if zero:
+        params = plan.new_replicas()
+        master = plan.new_state()
+        wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
+        m, v = plan.new_state(), plan.new_state()
+        clip = wl.adamw.max_norm > 0
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def cfg(step):
+        a = wl.adamw
+        return dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, step)
+
+    n_ev = dps.dp_fused_zero_step_launches(cfg(1)) + 1 if zero else 2
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    def step_fn(step, evs=None):
+        if zero:
+            dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg(step), events=evs)
+        else:
+            if evs:
+                evs[0].record(stream)
+            dps.dp_allreduce_mean(plan, ws, grads)
+            if evs:
+                evs[1].record(stream)
+
+    step = 0
+    for _ in range(args.warmup):
+        step += 1
+        step_fn(step)
+    torch.cuda.synchronize()
+    ev_sets = [new_events() for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        t_begin.record(stream)
+        for k in range(args.steps):
+            step += 1
+            step_fn(step, ev_sets[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = t_begin.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    stage_ms = [[ev[i].elapsed_time(ev[i + 1]) for i in range(n_ev - 1)] for ev in ev_sets]
+    stage_avg = [sum(s[i] for s in stage_ms) / len(stage_ms) for i in range(n_ev - 1)]
+    norm = None
+    if zero and clip:
+        norm, coef, _ = dps.dp_read_norm(plan, ws)
+
+    # dominant kernel: the longest stage
+    if zero:
+        names = ["reduce_scatter", "norm_finalize", "adamw_all_gather"] if clip else ["zero_fused"]
+    else:
+        names = ["allreduce"]
+    dom = max(range(len(stage_avg)), key=lambda i: stage_avg[i])
+    dom_name = names[dom]
+    n_params = wl.n_params
+    dom_bytes = KERNEL_BYTES_PER_PARAM[dom_name](P) * n_params
+    peak, peak_src = measured_peaks()
+    achieved = dom_bytes / (stage_avg[dom] * 1e-3) / 1e9
+    step_bytes_pp = (KERNEL_BYTES_PER_PARAM["reduce_scatter"](P)
+                     + KERNEL_BYTES_PER_PARAM["adamw_all_gather"](P)) if (zero and clip) else \
+        KERNEL_BYTES_PER_PARAM[names[0]](P)
+    step_gbs = step_bytes_pp * n_params / (ms_step * 1e-3) / 1e9
+
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tf):
+        with open(tf) as f:
+            tdb = json.load(f)
+        key = f"{wl.name}:{dom_name}"
+        if key in tdb:
+            traffic = tdb[key]["bytes_per_launch"]
+
+    result = {
+        "metric": "fused ZeRO-2 step params/s and achieved HBM GB/s vs GB300 peak (P=8, 1 GPU)"
+        if zero else "bucketed mean all-reduce params/s",
+        "value": n_params * world / (ms_step * 1e-3),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "storage": "bf16 gradient and parameter replicas, fp32 master/m/v",
+        "data": "synthetic (seeded counter-based N(0, sigma) gradients, N(0, 0.02) master)",
+        "config": {
+            "workload": wl.name,
+            "P": P,
+            "n_params": n_params,
+            "padded_len": L,
+            "replica_stride": stride,
+            "n_tensors": len(wl.sizes),
+            "n_buckets": plan.n_buckets,
+            "bucket_bytes": wl.bucket_bytes,
+            "clip_max_norm": wl.adamw.max_norm if zero else None,
+            "parallelism": f"{P} virtual ranks per GPU x {world} GPU(s), independent replicas",
+            "l2": "inputs larger than L2 (no flush): "
+                  f"{step_bytes_pp * n_params / 1e9:.1f} GB moved per step vs 0.13 GB L2",
+        },
+        "step_gbs": step_gbs,
+        "stage_ms": dict(zip(names, stage_avg)),
+        "roofline": {
+            "kernel": dom_name,
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "bytes_per_param": KERNEL_BYTES_PER_PARAM[dom_name](P),
+        },
+        "gpu_launches": (n_ev - 1) * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if norm is not None:
+        result["grad_norm"] = norm
+        result["clip_coef"] = coef
+
+    # ---- end to end through the public call, host buffers ----
+    if not args.no_e2e:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        host = torch.empty_like(grads, device="cpu", pin_memory=True)
+        host.copy_(grads)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            step += 1
+            grads.copy_(host, non_blocking=True)
+            if zero:
+                step_fn(step)
+                dps.dp_read_norm(plan, ws)
+            else:
+                step_fn(step)
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+        result["e2e"] = {"value": n_params * world / e2e_s, "unit": "params/s",
+                         "h2d_bytes_per_step": host.numel() * host.element_size(),
+                         "d2h_bytes_per_step": 192 if zero else 0,
+                         "steps": e2e_steps}
+        del host
+
+    # ---- CPU oracle baseline (rank 0, N=1 only) ----
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and zero:
+        rate, npar, secs, thr, desc = oracle_sample_rate(wl, off, grads, master,
+                                                         budget_s=args.cpu_budget)
+        result["cpu_baseline"] = {"value": rate, "unit": "params/s", "cores": thr, "kind": "oracle",
+                                  "sample": desc, "seconds": secs}
+    return result
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample."""
+    import numpy as np
+    import oracle
+    if rank != 0:
+        return None
+    wl = workload_by_name(args.workload)
+    orc = oracle.default()
+    op = orc.plan(wl.sizes, wl.bucket_bytes, wl.P)
+    threads = os.cpu_count() or 1
+    nb = op["n_buckets"]
+    batch = list(range(min(1, nb - 1), min(nb, min(1, nb - 1) + max(1, min(threads, 4)))))
+    tens = sorted(t for t in range(len(wl.sizes)) if op["t_bucket"][t] in batch)
+    sub = [wl.sizes[t] for t in tens]
+    dec = [wl.decay[t] for t in tens]
+    base = wdev.tensor_bases(wl.sizes)
+    g = np.stack([torch.cat([gen.grad_values(wl, 1, r, base[t], wl.sizes[t]) for t in tens])
+                  .view(torch.int16).numpy().view(np.uint16) for r in range(wl.P)])
+    mst = torch.cat([gen.master_values(wl, base[t], wl.sizes[t]) for t in tens]).numpy()
+    z = np.zeros_like(mst)
+    step = 0
+    for _ in range(args.warmup):
+        step += 1
+        orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g, mst, z, z,
+                      oracle.adamw_cfg(wl.adamw, step), n_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step += 1
+        orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g, mst, z, z,
+                      oracle.adamw_cfg(wl.adamw, step), n_threads=threads)
+    secs = (time.perf_counter() - t0) / args.steps
+    value = sum(sub) / secs
+    desc = (f"buckets {batch[0]}..{batch[-1]} of {nb} ({sum(sub)} params per step), oracle fused "
+            f"ZeRO step with its own clip norm over the sample")
+    return {
+        "impl": "reference",
+        "metric": "fused ZeRO-2 step params/s and achieved HBM GB/s vs GB300 peak (P=8, 1 GPU)",
+        "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based)",
+        "config": {"workload": wl.name, "P": wl.P, "n_params": wl.n_params},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama-1.1B-P8-zero2")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: warm-up raised to the minimum of 3", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        # the CPU oracle runs on rank 0 only; other ranks exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, local, world = dist_setup()
+    res = run_gpu(args, rank, local, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,274 @@
+"""Python binding of libdpsync.so, the GB300 data-parallel gradient
+synchronisation library.
+
+Argument marshalling only: every step of the synchronisation runs in the CUDA
+kernels behind the C ABI declared in include/dpsync.h.  PyTorch supplies device
+memory (``tensor.data_ptr()``) and streams (``torch.cuda.current_stream()``).
+There is no fallback: if the shared library is missing or fails to load, import
+raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdpsync.so")
+
+DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM = 0, -1, -2, -3, -4, -5, -6
+DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE = 1, 2
+
+
+class DPError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+class PlanInfo(C.Structure):
+    _fields_ = [("n_params", C.c_int64), ("padded_len", C.c_int64), ("replica_stride", C.c_int64),
+                ("bucket_bytes", C.c_int64), ("n_tensors", C.c_int32), ("n_buckets", C.c_int32),
+                ("P", C.c_int32), ("tile_elems", C.c_int32), ("n_tiles", C.c_int64),
+                ("table_bytes", C.c_int64), ("workspace_bytes", C.c_int64)]
+
+
+class AdamWCfg(C.Structure):
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("eps", C.c_double), ("weight_decay", C.c_double), ("max_norm", C.c_double),
+                ("step", C.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libdpsync.so (raises if it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run gradient_sync_zero_gb300.build.build()")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64, f64 = C.c_void_p, C.c_int32, C.c_int64, C.c_double
+        sig = {
+            "dp_plan_buckets": [vp, vp, i32, i64, i32, vp],
+            "dp_plan_buckets_ex": [vp, vp, i32, i64, i32, i64, vp],
+            "dp_plan_info": [vp, vp],
+            "dp_plan_tensor": [vp, i32, vp, vp],
+            "dp_plan_bucket": [vp, i32, vp, vp, vp],
+            "dp_plan_upload": [vp, vp, vp],
+            "dp_reduce_scatter_mean": [vp, vp, vp, vp, i32, i32, i32, vp],
+            "dp_clip_coef": [vp, vp, f64, i32, i32, vp],
+            "dp_sharded_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp],
+            "dp_all_gather": [vp, vp, vp, i32, i32, vp],
+            "dp_broadcast": [vp, vp, vp, i32, i32, i32, vp],
+            "dp_allreduce_mean": [vp, vp, vp, i32, i32, vp],
+            "dp_fused_zero_step": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
+            "dp_fused_zero_step_launches": [vp],
+            "dp_read_norm": [vp, vp, vp, vp, vp, vp],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = C.c_int
+        L.dp_plan_free.argtypes = [vp]
+        L.dp_plan_free.restype = None
+        L.dp_last_error.argtypes = []
+        L.dp_last_error.restype = C.c_char_p
+        L.dp_version.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _check(rc):
+    if rc != DP_OK:
+        raise DPError(rc, lib().dp_last_error().decode())
+    return rc
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, dtype, numel, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+
+
+class Plan:
+    """A bucket plan (host object of the library)."""
+
+    def __init__(self, sizes, bucket_bytes, P, decay=None, replica_stride=0):
+        sizes = [int(s) for s in sizes]
+        n = len(sizes)
+        arr = (C.c_int64 * max(n, 1))(*sizes)
+        dec = None
+        if decay is not None:
+            dec = (C.c_uint8 * max(n, 1))(*[1 if d else 0 for d in decay])
+        h = C.c_void_p()
+        _check(lib().dp_plan_buckets_ex(arr, dec, n, int(bucket_bytes), int(P), int(replica_stride),
+                                        C.byref(h)))
+        self._h = h
+        info = PlanInfo()
+        _check(lib().dp_plan_info(h, C.byref(info)))
+        self.info = info
+        self.sizes = sizes
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.dp_plan_free(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    P = property(lambda self: self.info.P)
+    L = property(lambda self: self.info.padded_len)
+    stride = property(lambda self: self.info.replica_stride)
+    n_buckets = property(lambda self: self.info.n_buckets)
+
+    def tensor(self, t):
+        b, o = C.c_int32(), C.c_int64()
+        _check(lib().dp_plan_tensor(self._h, int(t), C.byref(b), C.byref(o)))
+        return b.value, o.value
+
+    def bucket(self, b):
+        o, n, s = C.c_int64(), C.c_int64(), C.c_int64()
+        _check(lib().dp_plan_bucket(self._h, int(b), C.byref(o), C.byref(n), C.byref(s)))
+        return o.value, n.value, s.value
+
+    def tensor_offsets(self):
+        return [self.tensor(t)[1] for t in range(len(self.sizes))]
+
+    # ---- device buffers (torch plumbing) ----
+    def new_replicas(self, device="cuda", dtype=torch.bfloat16):
+        return torch.zeros(self.P, self.stride, dtype=dtype, device=device)
+
+    def new_state(self, device="cuda"):
+        return torch.zeros(self.L, dtype=torch.float32, device=device)
+
+    def new_workspace(self, device="cuda", stream=None):
+        ws = torch.empty(self.info.workspace_bytes, dtype=torch.uint8, device=device)
+        self.upload(ws, stream)
+        return ws
+
+
+def adamw_cfg(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.0, step=1):
+    return AdamWCfg(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                    float(max_norm), int(step))
+
+
+def _ws(plan, ws):
+    _need(ws, torch.uint8, plan.info.workspace_bytes, "workspace")
+    return _ptr(ws)
+
+
+def _range(plan, b0, b1):
+    return int(b0), int(plan.n_buckets if b1 is None else b1)
+
+
+def dp_plan_upload(plan, ws, stream=None):
+    _check(lib().dp_plan_upload(plan.handle, _ws(plan, ws), _stream(stream)))
+
+
+Plan.upload = lambda self, ws, stream=None: dp_plan_upload(self, ws, stream)
+
+
+def dp_reduce_scatter_mean(plan, ws, grads, mean, b0=0, b1=None, want_sumsq=False, stream=None):
+    _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
+    _need(mean, torch.float32, plan.L, "mean")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_reduce_scatter_mean(plan.handle, _ws(plan, ws), _ptr(grads), _ptr(mean), b0, b1,
+                                        1 if want_sumsq else 0, _stream(stream)))
+
+
+def dp_clip_coef(plan, ws, max_norm, b0=0, b1=None, stream=None):
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_clip_coef(plan.handle, _ws(plan, ws), float(max_norm), b0, b1, _stream(stream)))
+
+
+def dp_sharded_adamw_step(plan, ws, grad, master, m, v, params, cfg, use_clip_coef=False, b0=0,
+                          b1=None, stream=None):
+    for t, name in ((grad, "grad"), (master, "master"), (m, "m"), (v, "v")):
+        _need(t, torch.float32, plan.L, name)
+    _need(params, torch.bfloat16, plan.P * plan.stride, "params")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_sharded_adamw_step(plan.handle, _ws(plan, ws), _ptr(grad), _ptr(master), _ptr(m),
+                                       _ptr(v), _ptr(params), C.byref(cfg),
+                                       1 if use_clip_coef else 0, b0, b1, _stream(stream)))
+
+
+def dp_all_gather(plan, ws, params, b0=0, b1=None, stream=None):
+    _need(params, torch.bfloat16, plan.P * plan.stride, "params")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_all_gather(plan.handle, _ws(plan, ws), _ptr(params), b0, b1, _stream(stream)))
+
+
+def dp_broadcast(plan, ws, params, src=0, b0=0, b1=None, stream=None):
+    _need(params, torch.bfloat16, plan.P * plan.stride, "params")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_broadcast(plan.handle, _ws(plan, ws), _ptr(params), int(src), b0, b1,
+                              _stream(stream)))
+
+
+def dp_allreduce_mean(plan, ws, grads, b0=0, b1=None, stream=None):
+    _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_allreduce_mean(plan.handle, _ws(plan, ws), _ptr(grads), b0, b1, _stream(stream)))
+
+
+def dp_fused_zero_step_launches(cfg):
+    return lib().dp_fused_zero_step_launches(C.byref(cfg))
+
+
+def dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg, events=None, stream=None):
+    """One fused ZeRO-1/2 step over all buckets.  `events`: optional list of
+    dp_fused_zero_step_launches(cfg)+1 torch.cuda.Event objects recorded around
+    each launch."""
+    _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
+    _need(params, torch.bfloat16, plan.P * plan.stride, "params")
+    for t, name in ((master, "master"), (m, "m"), (v, "v")):
+        _need(t, torch.float32, plan.L, name)
+    ev = None
+    if events is not None:
+        n = dp_fused_zero_step_launches(cfg) + 1
+        if len(events) != n:
+            raise ValueError(f"need {n} events, got {len(events)}")
+        for e in events:
+            if e.cuda_event == 0:
+                raise ValueError("events must have been recorded once (so they exist)")
+        ev = (C.c_void_p * n)(*[e.cuda_event for e in events])
+    _check(lib().dp_fused_zero_step(plan.handle, _ws(plan, ws), _ptr(grads), _ptr(params),
+                                    _ptr(master), _ptr(m), _ptr(v), C.byref(cfg), ev,
+                                    _stream(stream)))
+
+
+def dp_read_norm(plan, ws, stream=None, raise_on_status=True):
+    """Synchronises the stream; returns (norm, coef, status)."""
+    norm, coef, status = C.c_double(), C.c_float(), C.c_int32()
+    rc = lib().dp_read_norm(plan.handle, _ptr(ws), C.byref(norm), C.byref(coef), C.byref(status),
+                            _stream(stream))
+    if raise_on_status:
+        _check(rc)
+    return norm.value, coef.value, status.value
+
+
+def dp_version():
+    return lib().dp_version()

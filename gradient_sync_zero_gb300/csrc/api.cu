@@ -1,0 +1,214 @@
+// C ABI entry points: argument checks, bucket-range -> tile-range mapping, and
+// dispatch to the kernel launchers.  No device memory is allocated here; every
+// call only enqueues work on the caller's stream (dp_read_norm also syncs it).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "internal.h"
+
+using namespace dps;
+
+namespace {
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int cuda_fail(int err, const char* where) {
+  return fail(DP_ECUDA, std::string(where) + ": " +
+                            cudaGetErrorString(static_cast<cudaError_t>(err)));
+}
+
+// Common checks; fills the launch descriptor for buckets [b0, b1).
+int prepare(const char* fn, const dp_plan* plan, void* ws, int32_t b0, int32_t b1, void* stream,
+            Launch* L) {
+  clear_error();
+  const Plan* pl = as_plan(plan);
+  if (!pl) return fail(DP_EINVAL, std::string(fn) + ": NULL plan");
+  if (!ws) return fail(DP_EINVAL, std::string(fn) + ": NULL workspace");
+  if (misaligned(ws)) return fail(DP_EALIGN, std::string(fn) + ": workspace not 16-byte aligned");
+  const int nb = static_cast<int>(pl->b_off.size());
+  if (b0 < 0 || b1 < b0 || b1 > nb)
+    return fail(DP_EINVAL, std::string(fn) + ": bucket range [" + std::to_string(b0) + ", " +
+                               std::to_string(b1) + ") outside [0, " + std::to_string(nb) + ")");
+  L->plan = pl;
+  L->ws = static_cast<uint8_t*>(ws);
+  L->tile_begin = pl->b_tile0[b0];
+  L->tile_end = pl->b_tile0[b1];
+  L->stream = stream;
+  return DP_OK;
+}
+
+int check_ptrs(const char* fn, std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (!p) return fail(DP_EINVAL, std::string(fn) + ": NULL device pointer");
+    if (misaligned(p)) return fail(DP_EALIGN, std::string(fn) + ": device pointer not 16-byte aligned");
+  }
+  return DP_OK;
+}
+
+int adam_scalars(const char* fn, const dp_adamw_cfg* cfg, AdamScalars* s) {
+  if (!cfg) return fail(DP_EINVAL, std::string(fn) + ": NULL cfg");
+  if (cfg->step < 1) return fail(DP_EINVAL, std::string(fn) + ": step must be >= 1");
+  if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
+    return fail(DP_EINVAL, std::string(fn) + ": betas must be in [0, 1)");
+  // Scalar factors formed once in double and rounded to fp32 (torch.optim.AdamW
+  // forms them as Python floats): decay factor 1 - lr*wd, 1-b1, 1-b2,
+  // step size lr / (1 - b1^t) and sqrt(1 - b2^t).
+  const double t = static_cast<double>(cfg->step);
+  s->wd_factor = static_cast<float>(1.0 - cfg->lr * cfg->weight_decay);
+  s->b1 = static_cast<float>(cfg->beta1);
+  s->omb1 = static_cast<float>(1.0 - cfg->beta1);
+  s->b2 = static_cast<float>(cfg->beta2);
+  s->omb2 = static_cast<float>(1.0 - cfg->beta2);
+  s->step_size = static_cast<float>(cfg->lr / (1.0 - std::pow(cfg->beta1, t)));
+  s->sqrt_bc2 = static_cast<float>(std::sqrt(1.0 - std::pow(cfg->beta2, t)));
+  s->eps = static_cast<float>(cfg->eps);
+  return DP_OK;
+}
+
+float* stage_of(const Plan* pl, void* ws) {
+  DevHeader h;
+  std::memcpy(&h, pl->image.data(), sizeof(h));
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + h.off_stage);
+}
+
+int record(void* const* ev, int i, void* stream) {
+  if (!ev) return DP_OK;
+  const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]),
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "cudaEventRecord");
+}
+
+}  // namespace
+
+extern "C" {
+
+int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream) {
+  clear_error();
+  const Plan* pl = as_plan(plan);
+  if (!pl || !workspace) return fail(DP_EINVAL, "dp_plan_upload: NULL argument");
+  if (misaligned(workspace)) return fail(DP_EALIGN, "dp_plan_upload: workspace not 16-byte aligned");
+  const cudaError_t e = cudaMemcpyAsync(workspace, pl->image.data(), pl->image.size(),
+                                        cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "dp_plan_upload");
+}
+
+int dp_reduce_scatter_mean(const dp_plan* plan, void* workspace, const void* grads, float* mean,
+                           int32_t b0, int32_t b1, int32_t want_sumsq, void* stream) {
+  Launch L;
+  int rc = prepare("dp_reduce_scatter_mean", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_reduce_scatter_mean", {grads, mean}))) return rc;
+  const int e = launch_reduce_scatter(L, grads, mean, want_sumsq != 0);
+  return e ? cuda_fail(e, "dp_reduce_scatter_mean") : DP_OK;
+}
+
+int dp_clip_coef(const dp_plan* plan, void* workspace, double max_norm, int32_t b0, int32_t b1,
+                 void* stream) {
+  Launch L;
+  const int rc = prepare("dp_clip_coef", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  const int e = launch_norm_finalize(L, max_norm);
+  return e ? cuda_fail(e, "dp_clip_coef") : DP_OK;
+}
+
+int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* grad, float* master,
+                          float* m, float* v, void* params, const dp_adamw_cfg* cfg,
+                          int32_t use_clip_coef, int32_t b0, int32_t b1, void* stream) {
+  Launch L;
+  int rc = prepare("dp_sharded_adamw_step", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_sharded_adamw_step", {grad, master, m, v, params}))) return rc;
+  AdamScalars s;
+  if ((rc = adam_scalars("dp_sharded_adamw_step", cfg, &s))) return rc;
+  const int e = launch_adamw(L, grad, master, m, v, params, s, use_clip_coef != 0);
+  return e ? cuda_fail(e, "dp_sharded_adamw_step") : DP_OK;
+}
+
+int dp_all_gather(const dp_plan* plan, void* workspace, void* params, int32_t b0, int32_t b1,
+                  void* stream) {
+  Launch L;
+  int rc = prepare("dp_all_gather", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_all_gather", {params}))) return rc;
+  const int e = launch_all_gather(L, params);
+  return e ? cuda_fail(e, "dp_all_gather") : DP_OK;
+}
+
+int dp_broadcast(const dp_plan* plan, void* workspace, void* params, int32_t src, int32_t b0,
+                 int32_t b1, void* stream) {
+  Launch L;
+  int rc = prepare("dp_broadcast", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_broadcast", {params}))) return rc;
+  if (src < 0 || src >= L.plan->P) return fail(DP_EINVAL, "dp_broadcast: src rank out of range");
+  const int e = launch_broadcast(L, params, src);
+  return e ? cuda_fail(e, "dp_broadcast") : DP_OK;
+}
+
+int dp_allreduce_mean(const dp_plan* plan, void* workspace, void* grads, int32_t b0, int32_t b1,
+                      void* stream) {
+  Launch L;
+  int rc = prepare("dp_allreduce_mean", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_allreduce_mean", {grads}))) return rc;
+  const int e = launch_allreduce(L, grads);
+  return e ? cuda_fail(e, "dp_allreduce_mean") : DP_OK;
+}
+
+int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
+  return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
+}
+
+int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, void* params,
+                       float* master, float* m, float* v, const dp_adamw_cfg* cfg,
+                       void* const* stage_events, void* stream) {
+  Launch L;
+  const Plan* pl = as_plan(plan);
+  int rc = prepare("dp_fused_zero_step", plan, workspace, 0,
+                   pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_fused_zero_step", {grads, params, master, m, v}))) return rc;
+  AdamScalars s;
+  if ((rc = adam_scalars("dp_fused_zero_step", cfg, &s))) return rc;
+  if ((rc = record(stage_events, 0, stream))) return rc;
+  if (!(cfg->max_norm > 0.0)) {
+    const int e = launch_zero_fused(L, grads, params, master, m, v, s);
+    if (e) return cuda_fail(e, "dp_fused_zero_step");
+    return record(stage_events, 1, stream);
+  }
+  float* stage = stage_of(pl, workspace);
+  int e = launch_reduce_scatter(L, grads, stage, true);
+  if (e) return cuda_fail(e, "dp_fused_zero_step (reduce-scatter)");
+  if ((rc = record(stage_events, 1, stream))) return rc;
+  e = launch_norm_finalize(L, cfg->max_norm);
+  if (e) return cuda_fail(e, "dp_fused_zero_step (norm)");
+  if ((rc = record(stage_events, 2, stream))) return rc;
+  e = launch_adamw_all_gather(L, stage, params, master, m, v, s);
+  if (e) return cuda_fail(e, "dp_fused_zero_step (adamw + all-gather)");
+  return record(stage_events, 3, stream);
+}
+
+int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float* coef,
+                 int32_t* status, void* stream) {
+  clear_error();
+  if (!plan || !workspace) return fail(DP_EINVAL, "dp_read_norm: NULL argument");
+  DevHeader h;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_read_norm");
+  if (norm) *norm = h.norm;
+  if (coef) *coef = h.coef;
+  if (status) *status = h.status;
+  if (h.status & DP_STATUS_PLAN_MISMATCH)
+    return fail(DP_EPLAN, "dp_read_norm: a kernel found another plan's image in the workspace");
+  if (h.status & DP_STATUS_NONFINITE)
+    return fail(DP_ENONFINITE, "dp_read_norm: the global gradient norm was not finite");
+  return DP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// Internal declarations shared by the library's translation units (host
+// planner, C-ABI, kernel launchers).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "dpsync.h"
+
+namespace dps {
+
+constexpr int kThreads = 256;                 // threads per CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kVecElems = 8;                  // bf16 elements per 16-byte vector
+constexpr int kTileVec = 1024;                // vectors per tile (8192 elements)
+constexpr int kTileElems = kTileVec * kVecElems;
+constexpr int kMaxP = 64;
+constexpr uint64_t kMagic = 0x31304e5953435044ull;  // "DPCSYN01"
+
+// One work tile: a run of <= kTileVec vectors inside one bucket.
+struct TileDesc {
+  int64_t v0;      // first vector (flat vector index)
+  int64_t bvoff;   // first vector of the tile's bucket
+  int32_t nvec;    // vectors in the tile
+  int32_t svec;    // shard length of the bucket, in vectors (>= 1)
+  int32_t bucket;
+  int32_t pad_;
+};
+static_assert(sizeof(TileDesc) == 32, "TileDesc is one 32-byte sector");
+
+// Header at the start of the workspace (device).  The first part is uploaded
+// with the plan; the results part is written by kernels.
+struct DevHeader {
+  uint64_t magic;
+  uint64_t plan_id;
+  int64_t n_vec;
+  int64_t n_tiles;
+  int32_t n_buckets;
+  int32_t P;
+  int64_t off_tiles;      // byte offsets of the arrays inside the workspace
+  int64_t off_btile;      // int64 [n_buckets+1]: first tile of each bucket
+  int64_t off_decay;      // uint32 [ceil(n_vec/32)]
+  int64_t off_sumsq;      // float2 [n_tiles]: per-tile sum of mean^2, hi + lo (scratch)
+  int64_t off_stage;      // float [L] (scratch)
+  int64_t reserved_[4];
+  // ---- written by kernels ----
+  double norm2;
+  double norm;
+  float coef;
+  int32_t status;
+  int64_t reserved2_[7];
+};
+static_assert(sizeof(DevHeader) % 64 == 0, "header keeps the arrays aligned");
+
+struct Plan {
+  int32_t P = 0;
+  int64_t bucket_bytes = 0;
+  int64_t n_params = 0;
+  int64_t L = 0;
+  int64_t stride = 0;
+  uint64_t id = 0;
+  std::vector<int64_t> sizes;
+  std::vector<uint8_t> decay;
+  std::vector<int64_t> t_off;
+  std::vector<int32_t> t_bucket;
+  std::vector<int64_t> b_off, b_len;
+  std::vector<int64_t> b_tile0;     // [n_buckets+1]
+  std::vector<TileDesc> tiles;
+  std::vector<uint32_t> decay_bits; // bit per 16-byte vector
+  // workspace layout
+  int64_t table_bytes = 0;
+  int64_t workspace_bytes = 0;
+  std::vector<uint8_t> image;       // host copy of the device image (table_bytes)
+};
+
+// Thread-local last-error text (dp_last_error); fail() records and returns code.
+int fail(int code, const std::string& msg);
+void clear_error();
+const char* last_error_text();
+const Plan* as_plan(const dp_plan* p);
+
+// ---- kernel launchers (kernels_*.cu) ----
+struct AdamScalars {
+  float wd_factor, b1, omb1, b2, omb2, step_size, sqrt_bc2, eps;
+};
+
+struct Launch {
+  const Plan* plan;
+  uint8_t* ws;          // workspace base (device)
+  int64_t tile_begin;   // [tile_begin, tile_end)
+  int64_t tile_end;
+  void* stream;
+};
+
+// Each returns a cudaError_t value (0 = success).
+int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq);
+int launch_allreduce(const Launch& L, void* grads);
+int launch_norm_finalize(const Launch& L, double max_norm);
+int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
+                 void* params, const AdamScalars& s, bool use_coef);
+int launch_all_gather(const Launch& L, void* params);
+int launch_broadcast(const Launch& L, void* params, int src);
+int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,
+                      float* v, const AdamScalars& s);
+int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
+                            float* m, float* v, const AdamScalars& s);
+
+}  // namespace dps

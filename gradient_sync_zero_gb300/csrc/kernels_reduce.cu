@@ -1,0 +1,155 @@
+// Reduce-scatter-mean, fused mean all-reduce, and the global-norm finalisation.
+//
+// Roofline (HBM-bound): reduce-scatter reads 2P bytes and writes 4 bytes per
+// element; the all-reduce reads 2P and writes 2P ("4.1 Data parallelism in
+// depth", sec. 5.2: each ring phase moves (N-1)/N of the data; here every
+// replica is read or written exactly once).
+#include <cmath>
+
+#include "launch.cuh"
+
+namespace dps {
+
+// Reduce-scatter + 1/P: shard c of each bucket receives the fp32 mean rank c
+// owns; optionally one partial of sum(mean^2) per tile for the clip norm.
+//
+// The partials are accumulated in float-float arithmetic (value = hi + lo):
+// each square is split exactly into p + q with the FMA-based TwoProduct and
+// added with Knuth's TwoSum (Ogita, Rump & Oishi, "Accurate sum and dot
+// product", SIAM J. Sci. Comput. 26(6), 2005).  The norm is then good to
+// ~1e-13 relative, so its fp32 clip coefficient rounds like one computed from
+// an exact sum.  Partials are per tile, so the norm does not depend on the grid
+// size or on how the bucket range is split into launches.
+template <int P>
+__global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint4* __restrict__ g,
+                                                             float4* __restrict__ mean, int sumsq) {
+  if (!plan_ok(k)) return;
+  __shared__ FF warp_part[kWarps];
+  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
+    const TileDesc d = load_tile(k, tile);
+    FF ss{0.0f, 0.0f};
+#pragma unroll 1
+    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
+      const int64_t v = d.v0 + j;
+      const int c = owner_of(d, v);
+      float acc[8];
+      if constexpr (P > 0) {
+        uint4 x[P];
+#pragma unroll
+        for (int r = 0; r < P; ++r) x[r] = ld_stream(g + r * k.stride_vec + v);
+        ring_sum<P>(c, x, acc);
+      } else {
+        ring_sum_runtime(k.P, c, g, k.stride_vec, v, acc);
+      }
+      scale_mean<P>(acc, k.P);
+      store8(mean, v, acc);
+      if (sumsq) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ff_add_square(ss, acc[e]);
+      }
+    }
+    if (sumsq) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
+  }
+}
+
+// Fused mean all-reduce in place: sum in ring order, 1/P, bf16, written back to
+// every replica (the all-gather of the reduced shards).
+template <int P>
+__global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint4* g) {
+  if (!plan_ok(k)) return;
+  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
+    const TileDesc d = load_tile(k, tile);
+#pragma unroll 1
+    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
+      const int64_t v = d.v0 + j;
+      const int c = owner_of(d, v);
+      float acc[8];
+      if constexpr (P > 0) {
+        uint4 x[P];
+#pragma unroll
+        for (int r = 0; r < P; ++r) x[r] = ld_stream(g + r * k.stride_vec + v);
+        ring_sum<P>(c, x, acc);
+      } else {
+        ring_sum_runtime(k.P, c, g, k.stride_vec, v, acc);
+      }
+      scale_mean<P>(acc, k.P);
+      const uint4 out = pack8_rne(acc);
+      const int np = P > 0 ? P : k.P;
+#pragma unroll
+      for (int r = 0; r < (P > 0 ? P : kMaxP); ++r) {
+        if (P == 0 && r >= np) break;
+        st_stream(g + r * k.stride_vec + v, out);
+      }
+    }
+  }
+}
+
+// One CTA: merge the tile partials of [tile_begin, tile_end) in float-float in a
+// fixed order, then norm and the clip coefficient min(1, max_norm / (norm +
+// 1e-6)) in double ("Distributed Training: Data Parallel, Model Parallel and
+// FSDP Strategies", "Inside DDP": clip_grad_norm_ after the averaged gradients).
+constexpr int kFinalThreads = 1024;
+__global__ void __launch_bounds__(kFinalThreads) k_norm_finalize(KCommon k, double max_norm) {
+  if (!plan_ok(k)) return;
+  __shared__ FF warp_part[kFinalThreads / 32];
+  FF acc{0.0f, 0.0f};
+  const float2* part = reinterpret_cast<const float2*>(k.sumsq);
+  int64_t i = k.tile_begin + threadIdx.x;
+  for (; i + 3 * kFinalThreads < k.tile_end; i += 4 * kFinalThreads) {
+    float2 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) q[u] = __ldcg(part + i + u * kFinalThreads);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc = ff_merge(acc, FF{q[u].x, q[u].y});
+  }
+  for (; i < k.tile_end; i += kFinalThreads) {
+    const float2 q = __ldcg(part + i);
+    acc = ff_merge(acc, FF{q.x, q.y});
+  }
+  acc = warp_ff_sum(acc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) warp_part[warp] = acc;
+  __syncthreads();
+  if (warp == 0) {
+    acc = warp_ff_sum(warp_part[lane]);
+    if (lane == 0) {
+      const double n2 = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
+      const double norm = sqrt(n2);
+      float coef = 1.0f;
+      if (!isfinite(norm)) {
+        atomicOr(&k.hdr->status, DP_STATUS_NONFINITE);
+        if (max_norm > 0.0) coef = __int_as_float(0x7fc00000);
+      } else if (max_norm > 0.0) {
+        coef = __double2float_rn(fmin(1.0, max_norm / (norm + 1e-6)));
+      }
+      k.hdr->norm2 = n2;
+      k.hdr->norm = norm;
+      k.hdr->coef = coef;
+    }
+  }
+}
+
+int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq) {
+  const KCommon k = make_common(L);
+  return with_P(L.plan->P, [&](auto pc) {
+    constexpr int P = decltype(pc)::value;
+    return launch_tiles(L, k_reduce_scatter<P>, k, static_cast<const uint4*>(grads),
+                        reinterpret_cast<float4*>(mean), sumsq ? 1 : 0);
+  });
+}
+
+int launch_allreduce(const Launch& L, void* grads) {
+  const KCommon k = make_common(L);
+  return with_P(L.plan->P, [&](auto pc) {
+    constexpr int P = decltype(pc)::value;
+    return launch_tiles(L, k_allreduce<P>, k, static_cast<uint4*>(grads));
+  });
+}
+
+int launch_norm_finalize(const Launch& L, double max_norm) {
+  const KCommon k = make_common(L);
+  k_norm_finalize<<<1, kFinalThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(k, max_norm);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace dps

@@ -1,0 +1,99 @@
+// Host-side launch helpers shared by the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <type_traits>
+#include <utility>
+
+#include "kernels.cuh"
+
+namespace dps {
+
+inline KCommon make_common(const Launch& L) {
+  DevHeader h;
+  std::memcpy(&h, L.plan->image.data(), sizeof(h));
+  KCommon k;
+  k.hdr = reinterpret_cast<DevHeader*>(L.ws);
+  k.tiles = reinterpret_cast<const TileDesc*>(L.ws + h.off_tiles);
+  k.decay = reinterpret_cast<const uint32_t*>(L.ws + h.off_decay);
+  k.sumsq = reinterpret_cast<float*>(L.ws + h.off_sumsq);
+  k.plan_id = L.plan->id;
+  k.stride_vec = L.plan->stride / kVecElems;
+  k.tile_begin = L.tile_begin;
+  k.tile_end = L.tile_end;
+  k.P = L.plan->P;
+  return k;
+}
+
+inline float* stage_ptr(const Launch& L) {
+  DevHeader h;
+  std::memcpy(&h, L.plan->image.data(), sizeof(h));
+  return reinterpret_cast<float*>(L.ws + h.off_stage);
+}
+
+// Resident CTAs per SM for a kernel (occupancy calculator, cached per device),
+// optionally capped by DPSYNC_CTAS_PER_SM for tuning sweeps.
+template <class K>
+int resident_ctas(K kernel, int threads) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess)
+    return 0;
+  if (const char* e = std::getenv("DPSYNC_CTAS_PER_SM")) {
+    const int cap = std::atoi(e);
+    if (cap > 0 && cap < per_sm) per_sm = cap;
+  }
+  const int n = sms * (per_sm > 0 ? per_sm : 1);
+  std::lock_guard<std::mutex> g(mu);
+  cache[key] = n;
+  return n;
+}
+
+// Launch `kernel` over the tiles of L with a persistent grid.
+template <class K, class... A>
+int launch_tiles(const Launch& L, K kernel, A... args) {
+  const int64_t n = L.tile_end - L.tile_begin;
+  if (n <= 0) return cudaSuccess;
+  const int cap = resident_ctas(kernel, kThreads);
+  if (cap <= 0) {
+    const cudaError_t e = cudaGetLastError();
+    return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
+  }
+  const int grid = static_cast<int>(n < cap ? n : cap);
+  kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(args...);
+  return static_cast<int>(cudaGetLastError());
+}
+
+// Rank counts with a fully unrolled instantiation; others use the runtime-P one.
+template <class F>
+int with_P(int P, F&& f) {
+  switch (P) {
+    case 1: return f(std::integral_constant<int, 1>{});
+    case 2: return f(std::integral_constant<int, 2>{});
+    case 3: return f(std::integral_constant<int, 3>{});
+    case 4: return f(std::integral_constant<int, 4>{});
+    case 5: return f(std::integral_constant<int, 5>{});
+    case 6: return f(std::integral_constant<int, 6>{});
+    case 7: return f(std::integral_constant<int, 7>{});
+    case 8: return f(std::integral_constant<int, 8>{});
+    case 16: return f(std::integral_constant<int, 16>{});
+    default: return f(std::integral_constant<int, 0>{});
+  }
+}
+
+}  // namespace dps

@@ -1,0 +1,249 @@
+/*
+ * dpsync.h - C ABI of the GB300 data-parallel gradient synchronisation library
+ * (libdpsync.so).
+ *
+ * P "virtual ranks" are data-parallel replicas whose bf16 gradient and bf16
+ * parameter copies all live in one GPU's HBM.  The library performs, as CUDA
+ * kernels over those replicas, the synchronisation step that the pages on
+ * data parallelism define:
+ *   - gradients packed into buckets in reverse layer order
+ *     ("4.1 Data parallelism in depth", sec. 4.2 "The Bucket mechanism");
+ *   - the mean all-reduce G = sum_i G_i / N, decomposed into a reduce-scatter
+ *     and an all-gather ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 1
+ *     "The Contract" and sec. 5 "Ring All-Reduce = Reduce-Scatter + All-Gather");
+ *   - the ZeRO-1/2 step: reduce-scatter, update the owned shard with AdamW on
+ *     fp32 master/m/v, all-gather the updated bf16 parameters ("Data
+ *     Parallelism: DDP, ZeRO and FSDP", "The three stages"), with optional
+ *     global gradient-norm clipping ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies",
+ *     "Inside DDP": clip_grad_norm_(params, 1.0)).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership.  The caller owns all device memory and the stream.  The library
+ *   allocates no device memory: the workspace is a caller buffer of
+ *   dp_plan_info().workspace_bytes bytes.  A plan is host memory owned by the
+ *   library, immutable after dp_plan_buckets() and safe to share between
+ *   threads.
+ * Layout.  Element i of the "flat padded index space" [0, L) is defined by the
+ *   plan (dp_plan_tensor, dp_plan_bucket).  Replica buffers (gradients,
+ *   parameters) are bf16 arrays [P][replica_stride]: replica r's element i is at
+ *   r * replica_stride + i.  master, m, v and fp32 mean buffers are fp32 [L].
+ *   Bucket b covers [offset_b, offset_b + len_b); its shard c is
+ *   [offset_b + c*S_b, offset_b + (c+1)*S_b) with S_b = len_b / P, and rank c
+ *   owns shard c.  Padding slots (between tensors and at a bucket's end) must
+ *   hold zeros in gradients and in master/m/v; the calls keep them zero.
+ * Alignment.  Every device pointer must be 16-byte aligned (DP_EALIGN).
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Every compute call only enqueues work on it and never synchronises the
+ *   device, except dp_read_norm, which synchronises `stream`.  Kernel-side
+ *   errors surface when the caller synchronises; dp_read_norm reports the
+ *   workspace's status bits.
+ * Buckets.  [b0, b1) selects a range of buckets (0 <= b0 <= b1 <= n_buckets),
+ *   so a caller can launch per bucket (DDP's bucket-ready semantics) or once
+ *   for all buckets.
+ * Errors.  0 is success; negative values are DP_E*.  dp_last_error() returns a
+ *   thread-local message for the last failing call on this thread.
+ * Numerics.  Sums are fp32, taken for shard c of every bucket in the ring's
+ *   order: rank c+1 first, then c+2, ..., ending with rank c (indices mod P);
+ *   the mean is that sum divided by P in IEEE fp32; bf16 results round to
+ *   nearest even.  AdamW runs in fp32 without fused multiply-add.
+ */
+#ifndef DPSYNC_H
+#define DPSYNC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  DP_OK = 0,
+  DP_EINVAL = -1,      /* bad argument, size, rank or bucket range */
+  DP_EALIGN = -2,      /* a device pointer is not 16-byte aligned */
+  DP_EPLAN = -3,       /* workspace does not hold this plan's uploaded image */
+  DP_ECUDA = -4,       /* a CUDA runtime call or kernel launch failed */
+  DP_ENONFINITE = -5,  /* the global gradient norm was not finite */
+  DP_ENOMEM = -6       /* host allocation failed */
+};
+
+/* Status bits written by kernels into the workspace, read by dp_read_norm. */
+enum { DP_STATUS_PLAN_MISMATCH = 1, DP_STATUS_NONFINITE = 2 };
+
+typedef struct dp_plan dp_plan;
+
+typedef struct {
+  int64_t n_params;         /* sum of the tensor sizes */
+  int64_t padded_len;       /* L: length of the flat padded index space */
+  int64_t replica_stride;   /* elements between consecutive replicas, >= L, multiple of 128 */
+  int64_t bucket_bytes;     /* the cap the plan was made with */
+  int32_t n_tensors;
+  int32_t n_buckets;
+  int32_t P;
+  int32_t tile_elems;       /* elements per work tile (tiles never cross a bucket) */
+  int64_t n_tiles;
+  int64_t table_bytes;      /* device plan image at the start of the workspace */
+  int64_t workspace_bytes;  /* whole workspace: image + norm scratch + fp32 mean stage [L] */
+} dp_plan_info_t;
+
+/* AdamW hyperparameters for one step.  max_norm <= 0 disables clipping. */
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay, max_norm;
+  int64_t step; /* t >= 1 */
+} dp_adamw_cfg;
+
+/*
+ * Bucket planner.  "DDP packs parameter gradients into Buckets in
+ * reverse-compute order (default ~25 MB each)" ("4.1 Data parallelism in
+ * depth", sec. 4.2; bucket_cap_mb).  Rule: walk tensors n-1 ... 0; each takes a
+ * slot of ceil(size/8)*8 elements (16-byte aligned); a non-empty bucket is
+ * closed when adding the next slot would exceed bucket_bytes/2 elements; a
+ * tensor is never split (one larger than the cap forms its own bucket); a
+ * closed bucket is padded up to a multiple of 8P, so each of its P shards is a
+ * whole number of 16-byte vectors.
+ *   sizes[n_tensors]  element count of each tensor (>= 0), host memory.
+ *   decay[n_tensors]  1 = weight decay applies to the tensor, 0 = not; NULL = all.
+ *   bucket_bytes      cap in bytes of bf16 gradient (>= 2).
+ *   P                 number of virtual ranks, 1..64.
+ *   out               receives the plan; free with dp_plan_free.
+ * Returns DP_EINVAL on bad arguments, DP_ENOMEM if host memory runs out.
+ */
+int dp_plan_buckets(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
+                    int64_t bucket_bytes, int32_t P, dp_plan** out);
+
+/* Same, with an explicit replica stride (elements; 0 = the default, the
+ * smallest multiple of 128 >= L plus 128).  A stride < L or not a multiple of
+ * 128 is DP_EINVAL. */
+int dp_plan_buckets_ex(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
+                       int64_t bucket_bytes, int32_t P, int64_t replica_stride, dp_plan** out);
+
+int dp_plan_info(const dp_plan* plan, dp_plan_info_t* out);
+
+/* Tensor t lives in bucket *bucket at flat offset *offset (16-byte aligned). */
+int dp_plan_tensor(const dp_plan* plan, int32_t t, int32_t* bucket, int64_t* offset);
+
+/* Bucket b: flat offset, padded length len_b and shard length S_b = len_b / P. */
+int dp_plan_bucket(const dp_plan* plan, int32_t b, int64_t* offset, int64_t* padded_len,
+                   int64_t* shard_len);
+
+void dp_plan_free(dp_plan* plan);
+
+/*
+ * Copy the plan's device image (bucket/tile tables, decay bits) into the first
+ * table_bytes of `workspace` (device, workspace_bytes long) on `stream`.  Must
+ * run once before any compute call uses that workspace; a compute call given a
+ * workspace holding another plan's image does no work and sets
+ * DP_STATUS_PLAN_MISMATCH.
+ */
+int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream);
+
+/*
+ * Reduce-scatter + mean ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
+ * after N-1 steps every rank owns one fully reduced chunk; sec. 1: G = sum G_i / N).
+ *   grads   bf16 [P][replica_stride], read only.
+ *   mean    fp32 [L]; for each bucket in [b0,b1), shard c's slots receive the
+ *           fp32 mean that rank c owns.
+ *   want_sumsq  non-zero: also store per-tile sums of mean^2 in the workspace
+ *           for dp_clip_coef (warp-shuffle partials, fixed order).
+ */
+int dp_reduce_scatter_mean(const dp_plan* plan, void* workspace, const void* grads, float* mean,
+                           int32_t b0, int32_t b1, int32_t want_sumsq, void* stream);
+
+/*
+ * Global gradient-norm clip coefficient over buckets [b0,b1) from the partials
+ * of a preceding dp_reduce_scatter_mean(want_sumsq=1) over the same buckets
+ * ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP":
+ * clip_grad_norm_(model.parameters(), 1.0) after the averaged gradients).
+ * norm = sqrt(sum mean^2) (partials summed in double in tile order);
+ * coef = min(1, max_norm / (norm + 1e-6)), or 1 when max_norm <= 0; a
+ * non-finite norm gives coef = NaN and sets DP_STATUS_NONFINITE.  Results stay
+ * in the workspace (dp_read_norm reads them).
+ */
+int dp_clip_coef(const dp_plan* plan, void* workspace, double max_norm, int32_t b0, int32_t b1,
+                 void* stream);
+
+/*
+ * Sharded AdamW ("Data Parallelism: DDP, ZeRO and FSDP", "The three stages":
+ * each rank updates the shard it owns; "Distributed Training: Data Parallel, Model Parallel and FSDP Strategies",
+ * "Inside DDP": torch.optim.AdamW(lr, weight_decay)).  For every slot i of the
+ * shards of buckets [b0,b1), owned by rank c:
+ *   g = grad[i] * coef   (coef = the workspace's clip coefficient if
+ *                         use_clip_coef, else 1)
+ *   theta = master[i] * (1 - lr*wd)          if the slot's tensor decays
+ *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
+ *   theta -= (lr / (1-b1^t)) * (m / (sqrt(v) / sqrt(1-b2^t) + eps))
+ *   params[c][i] = bf16(theta)   (only the owner's replica is written)
+ *   grad, master, m, v  fp32 [L] (master/m/v updated in place)
+ *   params              bf16 [P][replica_stride]
+ */
+int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* grad, float* master,
+                          float* m, float* v, void* params, const dp_adamw_cfg* cfg,
+                          int32_t use_clip_coef, int32_t b0, int32_t b1, void* stream);
+
+/*
+ * All-gather, in place ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
+ * reduced shards circulate until every rank has the full tensor): for every
+ * shard c of buckets [b0,b1), copy params[c][shard c] into every other replica.
+ */
+int dp_all_gather(const dp_plan* plan, void* workspace, void* params, int32_t b0, int32_t b1,
+                  void* stream);
+
+/*
+ * Broadcast replica `src` into every other replica over buckets [b0,b1): the
+ * one-time start-up broadcast of rank 0's parameters ("4.1 Data parallelism in
+ * depth", sec. 4.1 "broadcast once, sync many times").
+ */
+int dp_broadcast(const dp_plan* plan, void* workspace, void* params, int32_t src, int32_t b0,
+                 int32_t b1, void* stream);
+
+/*
+ * Mean all-reduce in place (DDP / NO_SHARD): reduce-scatter, mean, and the
+ * all-gather of bf16(mean) fused in one pass with no shard buffer ("4.1 Data
+ * parallelism in depth", sec. 5.1 AllReduce = ReduceScatter + AllGather;
+ * sec. 2: averaged, not summed).  grads bf16 [P][replica_stride], in/out.
+ */
+int dp_allreduce_mean(const dp_plan* plan, void* workspace, void* grads, int32_t b0, int32_t b1,
+                      void* stream);
+
+/*
+ * The fused ZeRO-1/2 step over all buckets ("Data Parallelism: DDP, ZeRO and
+ * FSDP", "The three stages": reduce-scatter, update the owned shard, all-gather
+ * the updated parameters).  Without clipping it is one kernel that reads the P
+ * gradient replicas and master/m/v once and writes master/m/v and the P
+ * parameter replicas once.  With clipping (cfg->max_norm > 0) it is
+ * dp_reduce_scatter_mean(want_sumsq) into the workspace's fp32 stage, then
+ * dp_clip_coef, then one kernel fusing AdamW with the all-gather.
+ *   grads   bf16 [P][replica_stride], read only.
+ *   params  bf16 [P][replica_stride], written (every replica, bit-identical).
+ *   master, m, v  fp32 [L], in/out.
+ *   stage_events  NULL, or dp_fused_zero_step_launches(cfg)+1 cudaEvent_t
+ *           handles the call records on `stream` before its first launch and
+ *           after each launch (for per-kernel timing by the caller).
+ */
+int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, void* params,
+                       float* master, float* m, float* v, const dp_adamw_cfg* cfg,
+                       void* const* stage_events, void* stream);
+
+/* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
+int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
+
+/*
+ * Synchronise `stream` and read the workspace's last clip results: norm
+ * (double), coef (fp32) and the status bits.  Any pointer may be NULL.
+ * Returns DP_ENONFINITE if the non-finite bit is set, DP_EPLAN if a kernel saw
+ * a plan mismatch.
+ */
+int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float* coef,
+                 int32_t* status, void* stream);
+
+/* Thread-local text of the last error on this thread ("" if none). */
+const char* dp_last_error(void);
+
+/* ABI version of this header (increments on incompatible change). */
+int dp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPSYNC_H */

@@ -6,21 +6,21 @@
 // header, table or helper with the CUDA library.
 //
 // What it computes (sources are the four pages on data parallelism):
-//  * "4.1 Data parallelism in depth" (infra-guide), sec. 2: the averaged
+//  * "4.1 Data parallelism in depth", sec. 2: the averaged
 //    gradient g_bar = (1/N) sum_k g_k equals the full-batch gradient when every
 //    rank averages over an equal local batch (eqs. for L, g, g_k, g_bar); sec. 4.2:
 //    gradients are packed into ~25 MB buckets in reverse compute order; sec. 5:
 //    all-reduce = reduce-scatter + all-gather, ring volume 2(N-1)/N * Psi;
 //    sec. 6.1 and 7: the ZeRO stages and the 16-byte/parameter ledger; sec. 8.2:
 //    ZeRO-3 moves 3 Psi.
-//  * "From Parameter Server to Ring All-Reduce" (duoan), sec. 1: G = sum_i G_i / N,
+//  * "Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 1: G = sum_i G_i / N,
 //    W <- optimizer_step(W, G); sec. 5: each ring step sends one chunk clockwise,
 //    the receiver adds it into a local partial sum, N-1 steps leave each rank one
 //    fully reduced chunk; the all-gather forwards reduced chunks for N-1 more
 //    steps; per-rank traffic 2(N-1)/N * M; sec. 6: 2(N-1) steps.
-//  * "Data Parallelism: DDP, ZeRO and FSDP" (neelmishra), "The three stages": ZeRO-1/2
+//  * "Data Parallelism: DDP, ZeRO and FSDP", "The three stages": ZeRO-1/2
 //    reduce-scatter, update the owned shard, all-gather the updated parameters.
-//  * "Distributed Training: DP, MP and FSDP" (tempatgunting), "Inside DDP":
+//  * "Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP":
 //    AdamW(lr=2e-4, weight_decay=0.1) and clip_grad_norm_(params, 1.0) after the
 //    averaged gradients; "FSDP1 vs FSDP2": MixedPrecisionPolicy(param bf16,
 //    reduce fp32).
@@ -47,7 +47,8 @@
 //     double and rounded to fp32 once.
 //  R7 clipping is clip_grad_norm_: norm = ||mean||_2 over the fp32 mean
 //     gradient (summed here in double), coef = min(1, max_norm/(norm+1e-6))
-//     rounded to fp32 once; g = mean * coef.  max_norm <= 0 disables it.
+//     rounded to fp32 once; g = mean * coef.  max_norm <= 0 disables it.  A
+//     non-finite norm gives coef = NaN, so the bad step shows in every output.
 //
 // Parity status: planner, ring sums/ownership/counters, AdamW closed form at
 // t=1, ledger and volumes, least-squares identity are pinned by tests that use
@@ -98,7 +99,7 @@ struct Plan {
 };
 
 // R5.  "DDP packs parameter gradients into Buckets in reverse-compute order
-// (default ~25 MB each)" (infra-guide sec. 4.2); buckets fire in that order.
+// (default ~25 MB each)" ("4.1 Data parallelism in depth", sec. 4.2); buckets fire in that order.
 bool make_plan(const int64_t* sizes, int n, int64_t bucket_bytes, int P, Plan* pl) {
   if (n < 0 || P < 1 || P > kMaxRanks || bucket_bytes < 1) return false;
   for (int t = 0; t < n; ++t)
@@ -138,7 +139,7 @@ bool make_plan(const int64_t* sizes, int n, int64_t bucket_bytes, int P, Plan* p
   return true;
 }
 
-// Literal ring reduce-scatter over P buffers (duoan sec. 5, R1): P-1 steps, each
+// Literal ring reduce-scatter over P buffers ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5, R1): P-1 steps, each
 // rank sends one chunk to its clockwise neighbour, which adds it into its local
 // partial sum.  X is [P][len] fp32; S = len/P.
 void ring_reduce_scatter(int P, int64_t len, float* X, int64_t* sent, int64_t* steps) {
@@ -162,7 +163,7 @@ void ring_reduce_scatter(int P, int64_t len, float* X, int64_t* sent, int64_t* s
   }
 }
 
-// Literal ring all-gather (duoan sec. 5): P-1 steps, each rank forwards the
+// Literal ring all-gather ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5): P-1 steps, each rank forwards the
 // reduced chunk it received last (its own chunk at step 0).  Y is [P][len] bf16.
 void ring_all_gather(int P, int64_t len, uint16_t* Y, int64_t* sent, int64_t* steps) {
   const int64_t S = len / P;
@@ -228,7 +229,7 @@ AdamScalars adam_scalars(const orc_adamw& c) {
   return s;
 }
 
-// R6: one element of AdamW (tempatgunting "Inside DDP": torch.optim.AdamW).
+// R6: one element of AdamW ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP": torch.optim.AdamW).
 void adamw_element(float g, float& theta, float& m, float& v, bool decay, const AdamScalars& s) {
   if (decay) theta = theta * s.wd_factor;
   m = s.b1 * m + s.omb1 * g;
@@ -242,6 +243,7 @@ float clip_coef(double sumsq, double max_norm, double* norm_out) {
   const double norm = std::sqrt(sumsq);
   if (norm_out) *norm_out = norm;
   if (!(max_norm > 0.0)) return 1.0f;
+  if (!std::isfinite(norm)) return std::nanf("");  // a non-finite norm poisons the step
   return static_cast<float>(std::min(1.0, max_norm / (norm + 1e-6)));
 }
 
@@ -430,7 +432,7 @@ int orc_bucket_sumsq(const int64_t* sizes, int32_t n, int64_t bucket_bytes, int3
 
 // ---- the fused ZeRO-1/2 step ------------------------------------------------
 // "ZeRO-1 and ZeRO-2 simply stop after the reduce-scatter, update the shard each
-// rank owns, and all-gather the updated parameters" (neelmishra, "The three
+// rank owns, and all-gather the updated parameters" ("Data Parallelism: DDP, ZeRO and FSDP", "The three
 // stages").  grads [P][n_params] bf16 (in), master/m/v [n_params] fp32 (in/out),
 // params [P][n_params] bf16 (out, all replicas), mean_out [n_params] (nullable,
 // pre-clip fp32 mean).  sumsq_total < 0: the clip norm is taken over this
@@ -460,7 +462,7 @@ int orc_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t
     bsum[b] = sumsq_of(means[b]);
   });
 
-  // global norm and clip coefficient (tempatgunting "Inside DDP": clip after the
+  // global norm and clip coefficient ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP": clip after the
   // gradients are averaged)
   double sumsq = 0.0;
   for (int b = 0; b < nb; ++b) sumsq += bsum[b];
@@ -538,7 +540,7 @@ int orc_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t
 
 // ---- ledger and volumes ------------------------------------------------------
 // Per-rank model-state bytes for `psi` parameters on P ranks, summing the
-// buffers each stage keeps (infra-guide sec. 6.1 table and sec. 7; neelmishra
+// buffers each stage keeps ("4.1 Data parallelism in depth", sec. 6.1 table and sec. 7; "Data Parallelism: DDP, ZeRO and FSDP",
 // "The three stages").  comp[5] = bytes per parameter of (params, grads,
 // master, m, v).  stage: 0 DDP, 1 ZeRO-1 (optimizer state sharded), 2 ZeRO-2
 // (+ gradients), 3 ZeRO-3 (+ parameters).
@@ -555,7 +557,7 @@ double orc_ledger_bytes(int32_t stage, double psi, int32_t P, const double* comp
 // with the ring primitives on M elements: DDP / ZeRO-1 / ZeRO-2 run one
 // reduce-scatter and one all-gather; ZeRO-3 runs an all-gather before the
 // forward, another before the backward, and a reduce-scatter of the gradients
-// (infra-guide sec. 8.2; neelmishra "The three stages").
+// ("4.1 Data parallelism in depth", sec. 8.2; "Data Parallelism: DDP, ZeRO and FSDP", "The three stages").
 int orc_stage_traffic(int32_t stage, int32_t P, int64_t M, int64_t* sent, int64_t* steps) {
   if (P < 1 || P > kMaxRanks || M % P) return -1;
   std::vector<float> X(static_cast<size_t>(P) * M, 1.0f);
@@ -573,7 +575,7 @@ int orc_stage_traffic(int32_t stage, int32_t P, int64_t M, int64_t* sent, int64_
   return 0;
 }
 
-// ---- least-squares identity (infra-guide sec. 2) ----------------------------
+// ---- least-squares identity ("4.1 Data parallelism in depth", sec. 2) ----------------------------
 // l_i = 1/2 (x_i . theta - y_i)^2, grad_i = (x_i . theta - y_i) x_i, in double.
 // Ranks take consecutive blocks of split[k] samples.  Outputs (each [F]):
 // g_full = (1/B) sum_i grad_i; g_k[k][F] = (1/|D_k|) sum_{i in D_k} grad_i

@@ -112,7 +112,7 @@ def pin_plan_invariants(orc):
 # --------------------------------------------------------------------------- ring
 def pin_ring_ownership(orc):
     """Rank r contributes 10**r: after the reduce-scatter exactly one chunk per
-    rank carries every contribution, and rank c holds chunk c (duoan sec. 5:
+    rank carries every contribution, and rank c holds chunk c ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
     'every rank owns one fully reduced chunk')."""
     for P in range(2, 7):
         S = 3
@@ -158,7 +158,7 @@ def pin_ring_sum_exact(orc):
 
 def pin_ring_traffic(orc):
     """Per-rank volume (N-1)M/N per phase, 2(N-1)/N*M in total, 2(N-1) steps
-    (duoan sec. 5 and 6; infra-guide sec. 5.2)."""
+    ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5 and 6; "4.1 Data parallelism in depth", sec. 5.2)."""
     for P in (1, 2, 3, 4, 8, 16):
         M = 8 * P * 3
         _, s1, k1 = orc.ring_reduce_scatter(np.zeros((P, M), np.float32))
@@ -183,7 +183,7 @@ def pin_ring_allgather_payload(orc):
 
 def pin_stage_traffic(orc):
     """DDP, ZeRO-1 and ZeRO-2 move 2(P-1)/P*M per rank, ZeRO-3 3(P-1)/P*M:
-    1.5x (neelmishra 'The three stages'; infra-guide sec. 8)."""
+    1.5x ("Data Parallelism: DDP, ZeRO and FSDP", 'The three stages'; "4.1 Data parallelism in depth", sec. 8)."""
     g = golden("ledger_pages.json")["comm_per_step"]["value"]
     for P in (2, 4, 8, 16):
         M = 8 * P * 5
@@ -233,7 +233,7 @@ def _pack_ok(orc, sizes, cap, P, rng, scale=1e-3):
 
 
 def pin_allreduce_identical(orc):
-    """Identical replicas average to themselves (average, not sum: infra-guide sec. 2)."""
+    """Identical replicas average to themselves (average, not sum: "4.1 Data parallelism in depth", sec. 2)."""
     rng = np.random.default_rng(3)
     sizes, cap = [13, 256, 1000, 7], 1024
     for P in (2, 3, 4, 8):
@@ -338,7 +338,7 @@ def pin_adamw_two_steps(orc):
 
 # --------------------------------------------------------------------------- clip
 def pin_clip_coef(orc):
-    """clip_grad_norm_(params, 1.0) after averaging (tempatgunting 'Inside DDP'):
+    """clip_grad_norm_(params, 1.0) after averaging ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", 'Inside DDP'):
     norm over all buckets, coef = min(1, max/(norm+1e-6)); library cross-check."""
     rng = np.random.default_rng(9)
     parts = rng.random(17) * 3.0
@@ -462,7 +462,7 @@ def lsq_data():
 
 def pin_lsq_identity(orc):
     """g_bar = (1/N) sum_k g_k equals the full-batch gradient for an equal split
-    (infra-guide sec. 2); summing gives N g; an uneven split with per-shard means
+    ("4.1 Data parallelism in depth", sec. 2); summing gives N g; an uneven split with per-shard means
     breaks the equality (sec. 2 note)."""
     x, y, th = lsq_data()
     g_full, g_k, g_bar, g_sum = orc.lsq_identity(x, y, th, [16, 16, 16, 16])

@@ -1,0 +1,161 @@
+"""The C ABI on the CPU: the library loads, exports every entry point the
+header declares, its host planner agrees with the oracle's planner bit for bit,
+and bad arguments are rejected before any device work."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import gradient_sync_zero_gb300 as dps
+from gradient_sync_zero_gb300 import build as dbuild
+from oracle_pins import check_plan_invariants
+from workloads import configs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    dbuild.build()
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "dpsync.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    syms = header_symbols()
+    assert len(syms) >= 18
+    lib = C.CDLL(dps.LIB_PATH)
+    missing = [s for s in syms if not hasattr(lib, s)]
+    assert not missing, missing
+    assert dps.dp_version() == 1
+
+
+def test_declared_entry_points_are_bound():
+    lib = dps.lib()
+    for s in header_symbols():
+        assert getattr(lib, s).restype is not None or s == "dp_plan_free"
+
+
+def _compare(sizes, cap, P, orc, decay=None):
+    p = dps.Plan(sizes, cap, P, decay=decay)
+    o = orc.plan(sizes, cap, P)
+    assert p.n_buckets == o["n_buckets"]
+    assert p.L == o["L"]
+    assert [p.tensor(t) for t in range(len(sizes))] == list(zip(o["t_bucket"].tolist(),
+                                                                 o["t_off"].tolist()))
+    for b in range(p.n_buckets):
+        off, ln, sh = p.bucket(b)
+        assert (off, ln) == (o["b_off"][b], o["b_len"][b])
+        assert sh * P == ln
+    assert p.stride >= p.L and p.stride % 128 == 0
+    assert p.info.n_params == sum(sizes)
+    return p
+
+
+@pytest.mark.parametrize("wl", [configs.tiny_plumbing(), configs.gpt2_small_allreduce(),
+                                configs.llama_1b1_zero2(), configs.gpt_2b5_clip()],
+                         ids=lambda w: w.name)
+def test_planner_matches_oracle_on_workloads(wl, orc):
+    p = _compare(wl.sizes, wl.bucket_bytes, wl.P, orc, wl.decay)
+    tiles = -(-np.array([p.bucket(b)[1] for b in range(p.n_buckets)]) // p.info.tile_elems)
+    assert p.info.n_tiles == int(tiles.sum())
+
+
+@pytest.mark.parametrize("cap", configs.SWEEP_BUCKETS)
+def test_planner_matches_oracle_on_sweep(cap, orc):
+    wl = configs.sweep_small_tensors(cap)
+    _compare(wl.sizes, cap, wl.P, orc)
+
+
+def test_planner_matches_oracle_random(orc):
+    rng = np.random.default_rng(17)
+    for _ in range(200):
+        n = int(rng.integers(0, 40))
+        sizes = rng.integers(0, 3000, size=n).tolist()
+        if n and rng.random() < 0.3:
+            sizes[int(rng.integers(0, n))] = int(rng.integers(10000, 50000))
+        P = int(rng.integers(1, 65))
+        cap = int(rng.choice([2, 16, 100, 4096, 65536]))
+        p = _compare(sizes, cap, P, orc)
+        check_plan_invariants(sizes, cap, P, orc.plan(sizes, cap, P))
+        assert p.L % (8 * P) == 0
+
+
+def test_tiny_plan_golden():
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "plan_tiny_P4_1MiB.json")) as f:
+        g = json.load(f)
+    p = dps.Plan(g["sizes"], g["bucket_bytes"], g["P"])
+    assert [p.tensor(t)[1] for t in range(7)] == g["t_off"]
+    assert [p.bucket(b)[:2] for b in range(3)] == list(zip(g["b_off"], g["b_len"]))
+
+
+def test_empty_and_degenerate_plans():
+    p = dps.Plan([], 1024, 4)
+    assert (p.n_buckets, p.L, p.info.n_tiles) == (0, 0, 0)
+    p = dps.Plan([0, 0], 1024, 4)
+    assert (p.n_buckets, p.L) == (1, 0)
+    p = dps.Plan([1], 2, 1)
+    assert (p.n_buckets, p.L) == (1, 8)
+    p = dps.Plan([100], 2, 64)
+    assert p.L == 512 and p.bucket(0)[2] == 8
+
+
+def test_explicit_stride():
+    p = dps.Plan([1000, 24], 1 << 20, 4, replica_stride=4096)
+    assert p.stride == 4096
+    with pytest.raises(dps.DPError) as e:
+        dps.Plan([1000, 24], 1 << 20, 4, replica_stride=1000)
+    assert e.value.code == dps.DP_EINVAL
+
+
+@pytest.mark.parametrize("sizes,cap,P", [([4], 1024, 0), ([4], 1024, 65), ([-1], 1024, 2),
+                                         ([4], 1, 2)])
+def test_planner_rejects_bad_arguments(sizes, cap, P):
+    with pytest.raises(dps.DPError) as e:
+        dps.Plan(sizes, cap, P)
+    assert e.value.code == dps.DP_EINVAL
+    assert dps.lib().dp_last_error().decode()
+
+
+def test_query_ranges():
+    p = dps.Plan([10, 20], 1024, 2)
+    with pytest.raises(dps.DPError):
+        p.tensor(2)
+    with pytest.raises(dps.DPError):
+        p.bucket(1)
+
+
+def test_compute_calls_validate_before_any_device_work():
+    """Bad ranges, NULL and misaligned pointers are refused on the host, so no
+    kernel is launched (these calls run without a GPU)."""
+    lib = dps.lib()
+    p = dps.Plan([1000, 24], 1 << 20, 4)
+    nb = p.n_buckets
+    ws, ok, odd = C.c_void_p(1 << 20), C.c_void_p(1 << 21), C.c_void_p((1 << 21) + 8)
+    assert lib.dp_allreduce_mean(p.handle, ws, ok, 0, nb + 1, None) == dps.DP_EINVAL
+    assert lib.dp_allreduce_mean(p.handle, ws, ok, 1, 0, None) == dps.DP_EINVAL
+    assert lib.dp_allreduce_mean(p.handle, ws, odd, 0, nb, None) == dps.DP_EALIGN
+    assert lib.dp_allreduce_mean(None, ws, ok, 0, nb, None) == dps.DP_EINVAL
+    assert lib.dp_all_gather(p.handle, None, ok, 0, nb, None) == dps.DP_EINVAL
+    assert lib.dp_broadcast(p.handle, ws, ok, 4, 0, nb, None) == dps.DP_EINVAL
+    assert lib.dp_reduce_scatter_mean(p.handle, ws, ok, None, 0, nb, 0, None) == dps.DP_EINVAL
+    cfg = dps.adamw_cfg(step=0)
+    assert lib.dp_fused_zero_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), None,
+                                  None) == dps.DP_EINVAL
+    cfg = dps.adamw_cfg(beta1=1.0)
+    assert lib.dp_sharded_adamw_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), 0, 0, nb,
+                                     None) == dps.DP_EINVAL
+    assert "range" in lib.dp_last_error().decode() or lib.dp_last_error()
+
+
+def test_launch_counts():
+    assert dps.dp_fused_zero_step_launches(dps.adamw_cfg(max_norm=0.0)) == 1
+    assert dps.dp_fused_zero_step_launches(dps.adamw_cfg(max_norm=1.0)) == 3

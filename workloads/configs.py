@@ -98,9 +98,11 @@ def gpt2_small_allreduce() -> Workload:
                     seed=1)
 
 
-def llama_1b1_zero2() -> Workload:
-    d, ffn, vocab, L, kv = 2048, 5632, 32000, 22, 256   # 4 KV heads of 64
-    names, shapes = ["embed_tokens"], [(vocab, d)]
+def llama_1b1_zero2(layers: int = 22, embeddings: bool = True) -> Workload:
+    """Llama-style 1.1B (22 layers).  `layers`/`embeddings` give the small
+    profiling variant (same tensor shapes and 25 MiB buckets, fewer layers)."""
+    d, ffn, vocab, L, kv = 2048, 5632, 32000, layers, 256   # 4 KV heads of 64
+    names, shapes = (["embed_tokens"], [(vocab, d)]) if embeddings else ([], [])
     for i in range(L):
         for n, s in (("input_layernorm", (d,)), ("q_proj", (d, d)), ("k_proj", (kv, d)),
                      ("v_proj", (kv, d)), ("o_proj", (d, d)),
@@ -108,9 +110,14 @@ def llama_1b1_zero2() -> Workload:
                      ("up_proj", (ffn, d)), ("down_proj", (d, ffn))):
             names.append(f"layers.{i}.{n}")
             shapes.append(s)
-    names += ["norm", "lm_head"]
-    shapes += [(d,), (vocab, d)]
-    return Workload(name="llama-1.1B-P8-zero2", P=8, names=names, shapes=shapes,
+    names += ["norm"]
+    shapes += [(d,)]
+    if embeddings:
+        names += ["lm_head"]
+        shapes += [(vocab, d)]
+    name = "llama-1.1B-P8-zero2" if (layers, embeddings) == (22, True) else \
+        f"llama-{layers}L-P8-zero2"
+    return Workload(name=name, P=8, names=names, shapes=shapes,
                     bucket_bytes=25 * MiB, sigma=5e-4, steps=10, mode="zero", seed=2)
 
 
