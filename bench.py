@@ -107,7 +107,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -160,9 +160,11 @@ def measured_peaks():
 
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=15.0,
-                       max_buckets=64, step=1):
-    """Time the CPU oracle's fused step on consecutive buckets (skipping the
-    first, a single oversized head matrix), enough for ~budget_s of work.
+                       max_passes=3, step=1):
+    """Time the CPU oracle's fused step on consecutive batches of buckets
+    (skipping the first, a single oversized head matrix), one batch of as many
+    buckets as host threads per call, until ~budget_s of work (at most
+    max_passes passes over the workload).
     Returns (params/s, params, seconds, threads, description)."""
     import numpy as np
     import oracle
@@ -175,7 +177,12 @@ def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=1
     used = []
     offsets = plan_sizes_offsets
     cfg = oracle.adamw_cfg(wl.adamw, step)
-    while b < nb and done_s < budget_s and len(used) < max_buckets:
+    passes = 0
+    while done_s < budget_s and passes < max_passes:
+        if b >= nb:                      # wrap around for another pass over the workload
+            b, passes = min(1, nb - 1), passes + 1
+            if passes >= max_passes:
+                break
         batch = list(range(b, min(nb, b + threads)))
         tens = [t for t in range(len(sizes)) if op["t_bucket"][t] in batch]
         tens.sort()
@@ -191,9 +198,10 @@ def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=1
         done_params += sum(sub)
         used += batch
         b = batch[-1] + 1
-    desc = (f"buckets {used[0]}..{used[-1]} of {nb} ({done_params} params, "
-            f"{100.0 * done_params / wl.n_params:.1f}% of the workload), oracle fused ZeRO step "
-            f"with its own clip norm over the sample")
+    desc = (f"{len(used)} bucket calls over buckets {min(used)}..{max(used)} of {nb} "
+            f"({done_params} params in total, {done_params / wl.n_params:.2f}x the workload), "
+            f"oracle fused ZeRO step in batches of {threads} buckets, each with its own clip "
+            f"norm, inputs copied from the GPU run")
     return done_params / done_s, done_params, done_s, threads, desc
 
 
@@ -430,7 +438,7 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-1.1B-P8-zero2")

@@ -14,7 +14,7 @@ using namespace dps;
 
 namespace {
 
-bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) != 0; }
 
 int cuda_fail(int err, const char* where) {
   return fail(DP_ECUDA, std::string(where) + ": " +
@@ -28,7 +28,7 @@ int prepare(const char* fn, const dp_plan* plan, void* ws, int32_t b0, int32_t b
   const Plan* pl = as_plan(plan);
   if (!pl) return fail(DP_EINVAL, std::string(fn) + ": NULL plan");
   if (!ws) return fail(DP_EINVAL, std::string(fn) + ": NULL workspace");
-  if (misaligned(ws)) return fail(DP_EALIGN, std::string(fn) + ": workspace not 16-byte aligned");
+  if (misaligned(ws)) return fail(DP_EALIGN, std::string(fn) + ": workspace not 32-byte aligned");
   const int nb = static_cast<int>(pl->b_off.size());
   if (b0 < 0 || b1 < b0 || b1 > nb)
     return fail(DP_EINVAL, std::string(fn) + ": bucket range [" + std::to_string(b0) + ", " +
@@ -41,10 +41,11 @@ int prepare(const char* fn, const dp_plan* plan, void* ws, int32_t b0, int32_t b
   return DP_OK;
 }
 
-int check_ptrs(const char* fn, std::initializer_list<const void*> ptrs) {
+// NULL is accepted only for an empty plan (L == 0), where nothing is accessed.
+int check_ptrs(const char* fn, const Plan* pl, std::initializer_list<const void*> ptrs) {
   for (const void* p : ptrs) {
-    if (!p) return fail(DP_EINVAL, std::string(fn) + ": NULL device pointer");
-    if (misaligned(p)) return fail(DP_EALIGN, std::string(fn) + ": device pointer not 16-byte aligned");
+    if (!p && pl->L > 0) return fail(DP_EINVAL, std::string(fn) + ": NULL device pointer");
+    if (misaligned(p)) return fail(DP_EALIGN, std::string(fn) + ": device pointer not 32-byte aligned");
   }
   return DP_OK;
 }
@@ -90,7 +91,7 @@ int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream) {
   clear_error();
   const Plan* pl = as_plan(plan);
   if (!pl || !workspace) return fail(DP_EINVAL, "dp_plan_upload: NULL argument");
-  if (misaligned(workspace)) return fail(DP_EALIGN, "dp_plan_upload: workspace not 16-byte aligned");
+  if (misaligned(workspace)) return fail(DP_EALIGN, "dp_plan_upload: workspace not 32-byte aligned");
   const cudaError_t e = cudaMemcpyAsync(workspace, pl->image.data(), pl->image.size(),
                                         cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "dp_plan_upload");
@@ -101,7 +102,7 @@ int dp_reduce_scatter_mean(const dp_plan* plan, void* workspace, const void* gra
   Launch L;
   int rc = prepare("dp_reduce_scatter_mean", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
-  if ((rc = check_ptrs("dp_reduce_scatter_mean", {grads, mean}))) return rc;
+  if ((rc = check_ptrs("dp_reduce_scatter_mean", L.plan, {grads, mean}))) return rc;
   const int e = launch_reduce_scatter(L, grads, mean, want_sumsq != 0);
   return e ? cuda_fail(e, "dp_reduce_scatter_mean") : DP_OK;
 }
@@ -121,7 +122,7 @@ int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* gra
   Launch L;
   int rc = prepare("dp_sharded_adamw_step", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
-  if ((rc = check_ptrs("dp_sharded_adamw_step", {grad, master, m, v, params}))) return rc;
+  if ((rc = check_ptrs("dp_sharded_adamw_step", L.plan, {grad, master, m, v, params}))) return rc;
   AdamScalars s;
   if ((rc = adam_scalars("dp_sharded_adamw_step", cfg, &s))) return rc;
   const int e = launch_adamw(L, grad, master, m, v, params, s, use_clip_coef != 0);
@@ -133,7 +134,7 @@ int dp_all_gather(const dp_plan* plan, void* workspace, void* params, int32_t b0
   Launch L;
   int rc = prepare("dp_all_gather", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
-  if ((rc = check_ptrs("dp_all_gather", {params}))) return rc;
+  if ((rc = check_ptrs("dp_all_gather", L.plan, {params}))) return rc;
   const int e = launch_all_gather(L, params);
   return e ? cuda_fail(e, "dp_all_gather") : DP_OK;
 }
@@ -143,7 +144,7 @@ int dp_broadcast(const dp_plan* plan, void* workspace, void* params, int32_t src
   Launch L;
   int rc = prepare("dp_broadcast", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
-  if ((rc = check_ptrs("dp_broadcast", {params}))) return rc;
+  if ((rc = check_ptrs("dp_broadcast", L.plan, {params}))) return rc;
   if (src < 0 || src >= L.plan->P) return fail(DP_EINVAL, "dp_broadcast: src rank out of range");
   const int e = launch_broadcast(L, params, src);
   return e ? cuda_fail(e, "dp_broadcast") : DP_OK;
@@ -154,7 +155,7 @@ int dp_allreduce_mean(const dp_plan* plan, void* workspace, void* grads, int32_t
   Launch L;
   int rc = prepare("dp_allreduce_mean", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
-  if ((rc = check_ptrs("dp_allreduce_mean", {grads}))) return rc;
+  if ((rc = check_ptrs("dp_allreduce_mean", L.plan, {grads}))) return rc;
   const int e = launch_allreduce(L, grads);
   return e ? cuda_fail(e, "dp_allreduce_mean") : DP_OK;
 }
@@ -171,7 +172,7 @@ int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, 
   int rc = prepare("dp_fused_zero_step", plan, workspace, 0,
                    pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
   if (rc) return rc;
-  if ((rc = check_ptrs("dp_fused_zero_step", {grads, params, master, m, v}))) return rc;
+  if ((rc = check_ptrs("dp_fused_zero_step", L.plan, {grads, params, master, m, v}))) return rc;
   AdamScalars s;
   if ((rc = adam_scalars("dp_fused_zero_step", cfg, &s))) return rc;
   if ((rc = record(stage_events, 0, stream))) return rc;

@@ -13,6 +13,7 @@ namespace dps {
 constexpr int kThreads = 256;                 // threads per CTA
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecElems = 8;                  // bf16 elements per 16-byte vector
+constexpr int kPairElems = 16;                // bf16 elements per 32-byte (256-bit) access
 constexpr int kTileVec = 1024;                // vectors per tile (8192 elements)
 constexpr int kTileElems = kTileVec * kVecElems;
 constexpr int kMaxP = 64;

@@ -1,15 +1,19 @@
 // Device-side building blocks for the synchronisation kernels (sm_103a).
 //
-// Work decomposition.  The flat padded index space is cut into 16-byte vectors
-// (8 bf16 gradient elements); the plan groups them into tiles of <= 1024
-// vectors that never cross a bucket.  A persistent grid (a multiple of the SM
-// count) walks the tiles of the requested bucket range round-robin; each of a
-// CTA's 256 threads takes every 256th vector of the tile, so every replica
-// stream is read and written as whole 512-byte warp transactions.
+// Work decomposition.  The flat padded index space is cut into 32-byte blocks
+// of 16 bf16 gradient elements ("pairs" of 16-byte vectors); buckets are padded
+// to 16P elements, so a block never straddles two shards.  The plan groups the
+// blocks into tiles of <= 512 blocks that never cross a bucket.  A persistent
+// grid (SM count x resident CTAs) walks the tiles round-robin; each of a CTA's
+// 256 threads takes every 256th block, so every replica stream is read and
+// written in 1 KB warp transactions of 256-bit accesses (half the memory
+// instructions of 16-byte accesses, which keeps the load/store queues from
+// throttling issue).
 //
-// Every kernel is HBM-bound (<= ~0.4 flop per byte): there is no contraction,
-// so no tensor cores; the design goal is to keep enough 16-byte loads in flight
-// and touch every byte exactly once.
+// Every kernel is HBM-bound (<= ~0.6 flop per byte): there is no contraction,
+// so no tensor cores; the aim is enough bytes in flight and every byte touched
+// exactly once.  All global accesses are streaming (.cs: evict-first), since no
+// byte is reused within a step.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -27,28 +31,67 @@ struct KCommon {
   const uint32_t* __restrict__ decay;
   float* sumsq;          // per tile: sum of squares of the mean as float-float (hi, lo)
   uint64_t plan_id;
-  int64_t stride_vec;    // replica stride in 16-byte vectors
+  int64_t stride_bytes;  // replica stride in bytes
   int64_t tile_begin;
   int64_t tile_end;
   int32_t P;             // rank count (used by the runtime-P instantiation)
 };
 
-// ---- memory access: streaming (evict-first) 16-byte loads and stores ----
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
-__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
-__device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
-__device__ __forceinline__ void st_stream(float4* p, const float4& v) { __stcs(p, v); }
+// ---- 256-bit streaming accesses (sm_100-family ld/st .v8.b32) ----
+// Every global access is volatile asm, so the compiler keeps them in program
+// order (loads of a block are issued before its stores, never re-issued).
+struct Blk {  // 16 bf16 = 32 bytes
+  uint32_t w[8];
+};
+
+__device__ __forceinline__ Blk ld_blk(const uint8_t* p) {
+  Blk r;
+  asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                 "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_blk(uint8_t* p, const Blk& v) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
+               : "memory");
+}
+
+// 8 fp32 (32 bytes)
+__device__ __forceinline__ void ld_f8(const float* p, float* f) {
+  asm volatile("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]), "=f"(f[4]), "=f"(f[5]),
+                 "=f"(f[6]), "=f"(f[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void st_f8(float* p, const float* f) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(f[0]),
+               "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+               : "memory");
+}
+
+// 16 fp32 of block b of an fp32 [L] array (elements 16b .. 16b+15)
+__device__ __forceinline__ void ld_f16(const float* base, int64_t b, float (&f)[16]) {
+  ld_f8(base + 16 * b, f);
+  ld_f8(base + 16 * b + 8, f + 8);
+}
+
+__device__ __forceinline__ void st_f16(float* base, int64_t b, const float (&f)[16]) {
+  st_f8(base + 16 * b, f);
+  st_f8(base + 16 * b + 8, f + 8);
+}
 
 // ---- bf16 <-> fp32 (bf16 -> fp32 is exact; fp32 -> bf16 rounds to nearest even) ----
-__device__ __forceinline__ void unpack8(const uint4& q, float (&f)[8]) {
-  f[0] = __uint_as_float(q.x << 16);
-  f[1] = __uint_as_float(q.x & 0xffff0000u);
-  f[2] = __uint_as_float(q.y << 16);
-  f[3] = __uint_as_float(q.y & 0xffff0000u);
-  f[4] = __uint_as_float(q.z << 16);
-  f[5] = __uint_as_float(q.z & 0xffff0000u);
-  f[6] = __uint_as_float(q.w << 16);
-  f[7] = __uint_as_float(q.w & 0xffff0000u);
+__device__ __forceinline__ void unpack16(const Blk& q, float (&f)[16]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = __uint_as_float(q.w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(q.w[i] & 0xffff0000u);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack2_rne(float lo, float hi) {
@@ -58,99 +101,112 @@ __device__ __forceinline__ uint32_t pack2_rne(float lo, float hi) {
   return u;
 }
 
-__device__ __forceinline__ uint4 pack8_rne(const float (&f)[8]) {
-  return make_uint4(pack2_rne(f[0], f[1]), pack2_rne(f[2], f[3]), pack2_rne(f[4], f[5]),
-                    pack2_rne(f[6], f[7]));
-}
-
-// ---- ring-ordered reduction ----
-// The owner c of a shard receives its sum in the ring's order: rank c+1's
-// value first, then c+2, ..., ending with rank c (indices mod P) — the order in
-// which "every rank sends one chunk clockwise ... the received chunk is added
-// into a local partial sum" ("Data Parallelism: From Parameter Server to Ring All-Reduce",
-// sec. 5).  fp32 adds, no reassociation.
-template <int P, int C>
-__device__ __forceinline__ void ring_sum_fixed(const uint4 (&x)[P], float (&acc)[8]) {
-  unpack8(x[(C + 1) % P], acc);
+__device__ __forceinline__ Blk pack16_rne(const float (&f)[16]) {
+  Blk b;
 #pragma unroll
-  for (int k = 2; k <= P; ++k) {
-    float t[8];
-    unpack8(x[(C + k) % P], t);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], t[e]);
-  }
+  for (int i = 0; i < 8; ++i) b.w[i] = pack2_rne(f[2 * i], f[2 * i + 1]);
+  return b;
 }
 
-template <int P, int C = 0>
-__device__ __forceinline__ void ring_sum(int c, const uint4 (&x)[P], float (&acc)[8]) {
-  if constexpr (C + 1 < P) {
-    if (c == C) {
-      ring_sum_fixed<P, C>(x, acc);
-      return;
-    }
-    ring_sum<P, C + 1>(c, x, acc);
-  } else {
-    ring_sum_fixed<P, C>(x, acc);
-  }
-}
-
-// Runtime-P version (P not instantiated): loads inside the loop.
-__device__ __forceinline__ void ring_sum_runtime(int P, int c, const uint4* g, int64_t stride_vec,
-                                                 int64_t v, float (&acc)[8]) {
-  int r = (c + 1) % P;
-  unpack8(ld_stream(g + r * stride_vec + v), acc);
-  for (int k = 2; k <= P; ++k) {
-    r = (c + k) % P;
-    float t[8];
-    unpack8(ld_stream(g + r * stride_vec + v), t);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], t[e]);
-  }
-}
-
-// G = sum_i G_i / N ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 1): IEEE
-// division, which a multiply by 1/P reproduces exactly when P is a power of two.
+// ---- ring-ordered reduction + mean ----
+// The owner c of a shard receives its sum in the ring's order: rank c+1's value
+// first, then c+2, ..., ending with rank c (indices mod P) — the order in which
+// "every rank sends one chunk clockwise ... the received chunk is added into a
+// local partial sum" ("Data Parallelism: From Parameter Server to Ring
+// All-Reduce", sec. 5).  The replicas are loaded directly in that order (the
+// owner is known from the block index), up to 8 blocks in flight per thread,
+// and folded with fp32 adds in the same order.  Then G = sum / N (sec. 1) as an
+// IEEE division, which a multiply by 1/P reproduces exactly for P = 2^k.
 template <int P>
-__device__ __forceinline__ void scale_mean(float (&acc)[8], int p_runtime) {
+__device__ __forceinline__ void ring_fold_chunk(const uint8_t* g, int64_t stride_bytes,
+                                                int64_t byte_off, int np, int r_first, int k0,
+                                                float (&acc)[16]) {
+  constexpr int K = (P > 0 && P < 8) ? P : 8;
+  Blk x[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if (P == 0 && k0 + k >= np) break;
+    int r = r_first + k0 + k;
+    if (r >= np) r -= np;
+    x[k] = ld_blk(g + r * stride_bytes + byte_off);
+  }
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    if (P == 0 && k0 + k >= np) break;
+    if (k0 + k == 0) {
+      unpack16(x[k], acc);
+    } else {
+      float t[16];
+      unpack16(x[k], t);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] = __fadd_rn(acc[e], t[e]);
+    }
+  }
+}
+
+template <int P>
+__device__ __forceinline__ void ring_mean16(const uint8_t* g, int64_t stride_bytes,
+                                            int64_t byte_off, int c, int p_rt,
+                                            float (&acc)[16]) {
+  constexpr int K = (P > 0 && P < 8) ? P : 8;
+  const int np = P > 0 ? P : p_rt;
+  const int r_first = (c + 1 == np) ? 0 : c + 1;
+  if constexpr (P > 0) {
+#pragma unroll
+    for (int k0 = 0; k0 < P; k0 += K) ring_fold_chunk<P>(g, stride_bytes, byte_off, np, r_first, k0, acc);
+  } else {
+#pragma unroll 1
+    for (int k0 = 0; k0 < np; k0 += K) ring_fold_chunk<P>(g, stride_bytes, byte_off, np, r_first, k0, acc);
+  }
   if constexpr (P > 0 && (P & (P - 1)) == 0) {
     constexpr float inv = 1.0f / P;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fmul_rn(acc[e], inv);
+    for (int e = 0; e < 16; ++e) acc[e] = __fmul_rn(acc[e], inv);
   } else {
-    const float fp = static_cast<float>(P > 0 ? P : p_runtime);
+    const float fp = static_cast<float>(np);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = __fdiv_rn(acc[e], fp);
+    for (int e = 0; e < 16; ++e) acc[e] = __fdiv_rn(acc[e], fp);
+  }
+}
+
+// Store one block into every replica.
+template <int P>
+__device__ __forceinline__ void store_replicas(uint8_t* base, int64_t stride_bytes,
+                                               int64_t byte_off, const Blk& val, int p_rt) {
+  if constexpr (P > 0) {
+#pragma unroll
+    for (int r = 0; r < P; ++r) st_blk(base + r * stride_bytes + byte_off, val);
+  } else {
+#pragma unroll 1
+    for (int r = 0; r < p_rt; ++r) st_blk(base + r * stride_bytes + byte_off, val);
   }
 }
 
 // ---- AdamW, torch.optim.AdamW's algorithm ("Distributed Training: Data Parallel,
 // Model Parallel and FSDP Strategies", "Inside DDP"), fp32, each op rounded ----
-__device__ __forceinline__ void adamw8(const float (&g)[8], float (&th)[8], float (&m)[8],
-                                       float (&v)[8], bool decay, const AdamScalars& s) {
+__device__ __forceinline__ void adamw1(float g, float& th, float& m, float& v, bool decay,
+                                       const AdamScalars& s) {
+  float t = th;
+  if (decay) t = __fmul_rn(t, s.wd_factor);
+  m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+  v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+  const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sqrt_bc2), s.eps);
+  th = __fsub_rn(t, __fmul_rn(s.step_size, __fdiv_rn(m, denom)));
+}
+
+// 16 elements: the first 8 belong to 16-byte vector 2b, the last 8 to 2b+1,
+// each with its own decay bit.
+__device__ __forceinline__ void adamw16(const float (&g)[16], float (&th)[16], float (&m)[16],
+                                        float (&v)[16], uint32_t dec2, const AdamScalars& s) {
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    float t = th[e];
-    if (decay) t = __fmul_rn(t, s.wd_factor);
-    m[e] = __fadd_rn(__fmul_rn(s.b1, m[e]), __fmul_rn(s.omb1, g[e]));
-    v[e] = __fadd_rn(__fmul_rn(s.b2, v[e]), __fmul_rn(s.omb2, __fmul_rn(g[e], g[e])));
-    const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v[e]), s.sqrt_bc2), s.eps);
-    th[e] = __fsub_rn(t, __fmul_rn(s.step_size, __fdiv_rn(m[e], denom)));
-  }
+  for (int e = 0; e < 16; ++e) adamw1(g[e], th[e], m[e], v[e], (dec2 >> (e >> 3)) & 1u, s);
 }
 
-__device__ __forceinline__ void load8(const float4* p, int64_t v, float (&f)[8]) {
-  const float4 a = ld_stream(p + 2 * v), b = ld_stream(p + 2 * v + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
-
-__device__ __forceinline__ void store8(float4* p, int64_t v, const float (&f)[8]) {
-  st_stream(p + 2 * v, make_float4(f[0], f[1], f[2], f[3]));
-  st_stream(p + 2 * v + 1, make_float4(f[4], f[5], f[6], f[7]));
-}
-
-__device__ __forceinline__ bool decay_bit(const uint32_t* __restrict__ bits, int64_t v) {
-  return (__ldg(bits + (v >> 5)) >> (v & 31)) & 1u;
+// Decay bits of the two 16-byte vectors of block b (vector 2b is even, so both
+// bits sit in the same 32-bit word).
+__device__ __forceinline__ uint32_t decay_bits2(const uint32_t* __restrict__ bits, int64_t b) {
+  const int64_t v = 2 * b;
+  return (__ldg(bits + (v >> 5)) >> (v & 31)) & 3u;
 }
 
 // ---- float-float accumulation (value = hi + lo) for the gradient norm ----
@@ -231,9 +287,25 @@ __device__ __forceinline__ TileDesc load_tile(const KCommon& k, int64_t tile) {
   return d;
 }
 
-// Owner (shard index) of vector v in its bucket.
+// Owner (shard index) of 16-byte vector v in its bucket.
 __device__ __forceinline__ int owner_of(const TileDesc& d, int64_t v) {
   return static_cast<int>(static_cast<uint32_t>(v - d.bvoff) / static_cast<uint32_t>(d.svec));
+}
+
+// Loop over the 32-byte blocks of the CTA's tiles: f(tile, block index b,
+// owner c).  Tiles start at even 16-byte vectors and hold an even count.
+template <class F>
+__device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
+  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
+    const TileDesc d = load_tile(k, tile);
+    const int nblk = d.nvec >> 1;
+    const int64_t b0 = d.v0 >> 1;
+#pragma unroll 1
+    for (int j = threadIdx.x; j < nblk; j += kThreads) {
+      const int64_t b = b0 + j;
+      f(tile, b, owner_of(d, 2 * b));
+    }
+  }
 }
 
 }  // namespace dps

@@ -17,35 +17,28 @@ namespace dps {
 // each square is split exactly into p + q with the FMA-based TwoProduct and
 // added with Knuth's TwoSum (Ogita, Rump & Oishi, "Accurate sum and dot
 // product", SIAM J. Sci. Comput. 26(6), 2005).  The norm is then good to
-// ~1e-13 relative, so its fp32 clip coefficient rounds like one computed from
-// an exact sum.  Partials are per tile, so the norm does not depend on the grid
+// ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
+// the exact sum.  Partials are per tile, so the norm does not depend on the grid
 // size or on how the bucket range is split into launches.
 template <int P>
-__global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint4* __restrict__ g,
-                                                             float4* __restrict__ mean, int sumsq) {
+__global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint8_t* g,
+                                                             float* mean, int sumsq) {
   if (!plan_ok(k)) return;
   __shared__ FF warp_part[kWarps];
   for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
     const TileDesc d = load_tile(k, tile);
+    const int nblk = d.nvec >> 1;
+    const int64_t b0 = d.v0 >> 1;
     FF ss{0.0f, 0.0f};
 #pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t v = d.v0 + j;
-      const int c = owner_of(d, v);
-      float acc[8];
-      if constexpr (P > 0) {
-        uint4 x[P];
-#pragma unroll
-        for (int r = 0; r < P; ++r) x[r] = ld_stream(g + r * k.stride_vec + v);
-        ring_sum<P>(c, x, acc);
-      } else {
-        ring_sum_runtime(k.P, c, g, k.stride_vec, v, acc);
-      }
-      scale_mean<P>(acc, k.P);
-      store8(mean, v, acc);
+    for (int j = threadIdx.x; j < nblk; j += kThreads) {
+      const int64_t b = b0 + j;
+      float acc[16];
+      ring_mean16<P>(g, k.stride_bytes, 32 * b, owner_of(d, 2 * b), k.P, acc);
+      st_f16(mean, b, acc);
       if (sumsq) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ff_add_square(ss, acc[e]);
+        for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
       }
     }
     if (sumsq) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
@@ -55,33 +48,13 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
 // Fused mean all-reduce in place: sum in ring order, 1/P, bf16, written back to
 // every replica (the all-gather of the reduced shards).
 template <int P>
-__global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint4* g) {
+__global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint8_t* g) {
   if (!plan_ok(k)) return;
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-#pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t v = d.v0 + j;
-      const int c = owner_of(d, v);
-      float acc[8];
-      if constexpr (P > 0) {
-        uint4 x[P];
-#pragma unroll
-        for (int r = 0; r < P; ++r) x[r] = ld_stream(g + r * k.stride_vec + v);
-        ring_sum<P>(c, x, acc);
-      } else {
-        ring_sum_runtime(k.P, c, g, k.stride_vec, v, acc);
-      }
-      scale_mean<P>(acc, k.P);
-      const uint4 out = pack8_rne(acc);
-      const int np = P > 0 ? P : k.P;
-#pragma unroll
-      for (int r = 0; r < (P > 0 ? P : kMaxP); ++r) {
-        if (P == 0 && r >= np) break;
-        st_stream(g + r * k.stride_vec + v, out);
-      }
-    }
-  }
+  for_each_block(k, [&](int64_t, int64_t b, int c) {
+    float acc[16];
+    ring_mean16<P>(g, k.stride_bytes, 32 * b, c, k.P, acc);
+    store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(acc), k.P);
+  });
 }
 
 // One CTA: merge the tile partials of [tile_begin, tile_end) in float-float in a
@@ -133,8 +106,8 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
     constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_reduce_scatter<P>, k, static_cast<const uint4*>(grads),
-                        reinterpret_cast<float4*>(mean), sumsq ? 1 : 0);
+    return launch_tiles(L, k_reduce_scatter<P>, k, static_cast<const uint8_t*>(grads), mean,
+                        sumsq ? 1 : 0);
   });
 }
 
@@ -142,7 +115,7 @@ int launch_allreduce(const Launch& L, void* grads) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
     constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_allreduce<P>, k, static_cast<uint4*>(grads));
+    return launch_tiles(L, k_allreduce<P>, k, static_cast<uint8_t*>(grads));
   });
 }
 

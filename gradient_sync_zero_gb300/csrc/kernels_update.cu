@@ -3,175 +3,123 @@
 // "ZeRO-1 and ZeRO-2 simply stop after the reduce-scatter, update the shard each
 // rank owns, and all-gather the updated parameters" ("Data Parallelism: DDP,
 // ZeRO and FSDP", "The three stages").  On one GPU the P replicas are P HBM
-// buffers, so the fused kernel performs the three phases per 16-byte vector:
-// read P gradient vectors and the owner's fp32 state once, write the state and
-// P parameter vectors once.
+// buffers, so the fused kernel performs the three phases per 32-byte block:
+// read P gradient blocks and the owner's fp32 state once, write the state and
+// P parameter blocks once.
 //
 // Roofline (HBM-bound), bytes per element: fused step 2P + 12 read, 12 + 2P
-// written; AdamW alone 16 read, 12 + 2 written; all-gather 2 read, 2(P-1) written.
+// written; AdamW alone 16 read, 12 + 2 written; all-gather 2 read, 2(P-1)
+// written; AdamW fused with the all-gather (second pass of the clipped step)
+// 16 read, 12 + 2P written.
 #include "launch.cuh"
 
 namespace dps {
 
 // Sharded AdamW on an fp32 gradient [L]; the owner's replica gets bf16(theta).
 __global__ void __launch_bounds__(kThreads)
-    k_adamw(KCommon k, const float4* __restrict__ grad, float4* __restrict__ master,
-            float4* __restrict__ m, float4* __restrict__ v, uint4* __restrict__ params,
+    k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
             AdamScalars s, int use_coef) {
   if (!plan_ok(k)) return;
   const float coef = use_coef ? k.hdr->coef : 1.0f;
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-#pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t x = d.v0 + j;
-      const int c = owner_of(d, x);
-      float g[8], th[8], mm[8], vv[8];
-      load8(grad, x, g);
-      load8(master, x, th);
-      load8(m, x, mm);
-      load8(v, x, vv);
-      const bool dec = decay_bit(k.decay, x);
-      if (use_coef) {
+  for_each_block(k, [&](int64_t, int64_t b, int c) {
+    float g[16], th[16], mm[16], vv[16];
+    ld_f16(grad, b, g);
+    ld_f16(master, b, th);
+    ld_f16(m, b, mm);
+    ld_f16(v, b, vv);
+    const uint32_t dec = decay_bits2(k.decay, b);
+    if (use_coef) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) g[e] = __fmul_rn(g[e], coef);
-      }
-      adamw8(g, th, mm, vv, dec, s);
-      store8(master, x, th);
-      store8(m, x, mm);
-      store8(v, x, vv);
-      st_stream(params + c * k.stride_vec + x, pack8_rne(th));
+      for (int e = 0; e < 16; ++e) g[e] = __fmul_rn(g[e], coef);
     }
-  }
+    adamw16(g, th, mm, vv, dec, s);
+    st_f16(master, b, th);
+    st_f16(m, b, mm);
+    st_f16(v, b, vv);
+    st_blk(params + c * k.stride_bytes + 32 * b, pack16_rne(th));
+  });
 }
 
 // In-place all-gather: the owner's slice of each shard goes to every other replica.
-__global__ void __launch_bounds__(kThreads) k_all_gather(KCommon k, uint4* params) {
+__global__ void __launch_bounds__(kThreads) k_all_gather(KCommon k, uint8_t* params) {
   if (!plan_ok(k)) return;
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-#pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t x = d.v0 + j;
-      const int c = owner_of(d, x);
-      const uint4 val = ld_stream(params + c * k.stride_vec + x);
-      for (int r = 0; r < k.P; ++r)
-        if (r != c) st_stream(params + r * k.stride_vec + x, val);
-    }
-  }
+  for_each_block(k, [&](int64_t, int64_t b, int c) {
+    const Blk val = ld_blk(params + c * k.stride_bytes + 32 * b);
+    for (int r = 0; r < k.P; ++r)
+      if (r != c) st_blk(params + r * k.stride_bytes + 32 * b, val);
+  });
 }
 
 // Replica `src` to every other replica.
-__global__ void __launch_bounds__(kThreads) k_broadcast(KCommon k, uint4* params, int src) {
+__global__ void __launch_bounds__(kThreads) k_broadcast(KCommon k, uint8_t* params, int src) {
   if (!plan_ok(k)) return;
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-#pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t x = d.v0 + j;
-      const uint4 val = ld_stream(params + src * k.stride_vec + x);
-      for (int r = 0; r < k.P; ++r)
-        if (r != src) st_stream(params + r * k.stride_vec + x, val);
-    }
-  }
+  for_each_block(k, [&](int64_t, int64_t b, int) {
+    const Blk val = ld_blk(params + src * k.stride_bytes + 32 * b);
+    for (int r = 0; r < k.P; ++r)
+      if (r != src) st_blk(params + r * k.stride_bytes + 32 * b, val);
+  });
 }
 
-template <int P>
-__device__ __forceinline__ void store_replicas(uint4* params, int64_t stride_vec, int64_t x,
-                                               const uint4& val, int p_runtime) {
-  if constexpr (P > 0) {
-#pragma unroll
-    for (int r = 0; r < P; ++r) st_stream(params + r * stride_vec + x, val);
-  } else {
-    for (int r = 0; r < p_runtime; ++r) st_stream(params + r * stride_vec + x, val);
-  }
-}
-
-// The whole ZeRO-1/2 step without clipping, one pass.
+// The whole ZeRO-1/2 step without clipping, one pass.  The replica blocks are
+// loaded and folded first, then the fp32 state is loaded, which bounds the live
+// registers to one of the two groups.
 template <int P>
 __global__ void __launch_bounds__(kThreads)
-    k_zero_fused(KCommon k, const uint4* __restrict__ grads, uint4* __restrict__ params,
-                 float4* __restrict__ master, float4* __restrict__ m, float4* __restrict__ v,
-                 AdamScalars s) {
+    k_zero_fused(KCommon k, const uint8_t* grads, uint8_t* params, float* master, float* m,
+                 float* v, AdamScalars s) {
   if (!plan_ok(k)) return;
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-#pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t x = d.v0 + j;
-      const int c = owner_of(d, x);
-      float g[8];
-      float th[8], mm[8], vv[8];
-      if constexpr (P > 0) {
-        uint4 rep[P];
-#pragma unroll
-        for (int r = 0; r < P; ++r) rep[r] = ld_stream(grads + r * k.stride_vec + x);
-        load8(master, x, th);
-        load8(m, x, mm);
-        load8(v, x, vv);
-        ring_sum<P>(c, rep, g);
-      } else {
-        load8(master, x, th);
-        load8(m, x, mm);
-        load8(v, x, vv);
-        ring_sum_runtime(k.P, c, grads, k.stride_vec, x, g);
-      }
-      scale_mean<P>(g, k.P);
-      const bool dec = decay_bit(k.decay, x);
-      adamw8(g, th, mm, vv, dec, s);
-      store8(master, x, th);
-      store8(m, x, mm);
-      store8(v, x, vv);
-      store_replicas<P>(params, k.stride_vec, x, pack8_rne(th), k.P);
-    }
-  }
+  for_each_block(k, [&](int64_t, int64_t b, int c) {
+    float g[16];
+    ring_mean16<P>(grads, k.stride_bytes, 32 * b, c, k.P, g);
+    float th[16], mm[16], vv[16];
+    ld_f16(master, b, th);
+    ld_f16(m, b, mm);
+    ld_f16(v, b, vv);
+    const uint32_t dec = decay_bits2(k.decay, b);
+    adamw16(g, th, mm, vv, dec, s);
+    st_f16(master, b, th);
+    st_f16(m, b, mm);
+    st_f16(v, b, vv);
+    store_replicas<P>(params, k.stride_bytes, 32 * b, pack16_rne(th), k.P);
+  });
 }
 
 // Second pass of the clipped step: AdamW on mean*coef fused with the all-gather.
 template <int P>
 __global__ void __launch_bounds__(kThreads)
-    k_adamw_all_gather(KCommon k, const float4* __restrict__ stage, uint4* __restrict__ params,
-                       float4* __restrict__ master, float4* __restrict__ m,
-                       float4* __restrict__ v, AdamScalars s) {
+    k_adamw_all_gather(KCommon k, const float* stage, uint8_t* params, float* master, float* m,
+                       float* v, AdamScalars s) {
   if (!plan_ok(k)) return;
   const float coef = k.hdr->coef;
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-#pragma unroll 1
-    for (int j = threadIdx.x; j < d.nvec; j += kThreads) {
-      const int64_t x = d.v0 + j;
-      float g[8], th[8], mm[8], vv[8];
-      load8(stage, x, g);
-      load8(master, x, th);
-      load8(m, x, mm);
-      load8(v, x, vv);
-      const bool dec = decay_bit(k.decay, x);
+  for_each_block(k, [&](int64_t, int64_t b, int) {
+    float g[16], th[16], mm[16], vv[16];
+    ld_f16(stage, b, g);
+    ld_f16(master, b, th);
+    ld_f16(m, b, mm);
+    ld_f16(v, b, vv);
+    const uint32_t dec = decay_bits2(k.decay, b);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) g[e] = __fmul_rn(g[e], coef);
-      adamw8(g, th, mm, vv, dec, s);
-      store8(master, x, th);
-      store8(m, x, mm);
-      store8(v, x, vv);
-      store_replicas<P>(params, k.stride_vec, x, pack8_rne(th), k.P);
-    }
-  }
+    for (int e = 0; e < 16; ++e) g[e] = __fmul_rn(g[e], coef);
+    adamw16(g, th, mm, vv, dec, s);
+    st_f16(master, b, th);
+    st_f16(m, b, mm);
+    st_f16(v, b, vv);
+    store_replicas<P>(params, k.stride_bytes, 32 * b, pack16_rne(th), k.P);
+  });
 }
 
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
                  void* params, const AdamScalars& s, bool use_coef) {
-  const KCommon k = make_common(L);
-  return launch_tiles(L, k_adamw, k, reinterpret_cast<const float4*>(grad),
-                      reinterpret_cast<float4*>(master), reinterpret_cast<float4*>(m),
-                      reinterpret_cast<float4*>(v), static_cast<uint4*>(params), s,
-                      use_coef ? 1 : 0);
+  return launch_tiles(L, k_adamw, make_common(L), grad, master, m, v,
+                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0);
 }
 
 int launch_all_gather(const Launch& L, void* params) {
-  return launch_tiles(L, k_all_gather, make_common(L), static_cast<uint4*>(params));
+  return launch_tiles(L, k_all_gather, make_common(L), static_cast<uint8_t*>(params));
 }
 
 int launch_broadcast(const Launch& L, void* params, int src) {
-  return launch_tiles(L, k_broadcast, make_common(L), static_cast<uint4*>(params), src);
+  return launch_tiles(L, k_broadcast, make_common(L), static_cast<uint8_t*>(params), src);
 }
 
 int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,
@@ -179,9 +127,8 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
     constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_zero_fused<P>, k, static_cast<const uint4*>(grads),
-                        static_cast<uint4*>(params), reinterpret_cast<float4*>(master),
-                        reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), s);
+    return launch_tiles(L, k_zero_fused<P>, k, static_cast<const uint8_t*>(grads),
+                        static_cast<uint8_t*>(params), master, m, v, s);
   });
 }
 
@@ -190,9 +137,8 @@ int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, f
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
     constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_adamw_all_gather<P>, k, reinterpret_cast<const float4*>(stage),
-                        static_cast<uint4*>(params), reinterpret_cast<float4*>(master),
-                        reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), s);
+    return launch_tiles(L, k_adamw_all_gather<P>, k, stage, static_cast<uint8_t*>(params),
+                        master, m, v, s);
   });
 }
 

@@ -23,7 +23,7 @@ inline KCommon make_common(const Launch& L) {
   k.decay = reinterpret_cast<const uint32_t*>(L.ws + h.off_decay);
   k.sumsq = reinterpret_cast<float*>(L.ws + h.off_sumsq);
   k.plan_id = L.plan->id;
-  k.stride_vec = L.plan->stride / kVecElems;
+  k.stride_bytes = L.plan->stride * 2;
   k.tile_begin = L.tile_begin;
   k.tile_end = L.tile_end;
   k.P = L.plan->P;

@@ -5,8 +5,9 @@
 // bucket_cap_mb is the knob): tensors are taken from the last to the first,
 // each in a 16-byte aligned slot; a bucket that already holds data is closed
 // when the next slot would push it past the cap; tensors are never split; a
-// closed bucket is padded to a multiple of 8P so that its P shards ("split each
-// GPU's data into N chunks", sec. 5.1) are whole 16-byte vectors.
+// closed bucket is padded to a multiple of 16P so that its P shards ("split each
+// GPU's data into N chunks", sec. 5.1) are whole 32-byte blocks of 16 bf16 — the
+// unit of one 256-bit access, which therefore never straddles two owners.
 //
 // The device image lets one launch walk any bucket range: a table of work
 // tiles (<= 1024 vectors, never crossing a bucket), each bucket's first tile,
@@ -52,7 +53,7 @@ namespace {
 bool assign_buckets(Plan& pl) {
   const int n = static_cast<int>(pl.sizes.size());
   const int64_t cap_elems = pl.bucket_bytes / 2;
-  const int64_t align = static_cast<int64_t>(kVecElems) * pl.P;
+  const int64_t align = static_cast<int64_t>(kPairElems) * pl.P;
   pl.t_off.assign(n, 0);
   pl.t_bucket.assign(n, -1);
   pl.b_off.clear();

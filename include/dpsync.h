@@ -32,7 +32,8 @@
  *   [offset_b + c*S_b, offset_b + (c+1)*S_b) with S_b = len_b / P, and rank c
  *   owns shard c.  Padding slots (between tensors and at a bucket's end) must
  *   hold zeros in gradients and in master/m/v; the calls keep them zero.
- * Alignment.  Every device pointer must be 16-byte aligned (DP_EALIGN).
+ * Alignment.  Every device pointer must be 32-byte aligned (DP_EALIGN); the
+ *   kernels move 32 bytes per access.
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
  *   Every compute call only enqueues work on it and never synchronises the
  *   device, except dp_read_norm, which synchronises `stream`.  Kernel-side
@@ -60,7 +61,7 @@ extern "C" {
 enum {
   DP_OK = 0,
   DP_EINVAL = -1,      /* bad argument, size, rank or bucket range */
-  DP_EALIGN = -2,      /* a device pointer is not 16-byte aligned */
+  DP_EALIGN = -2,      /* a device pointer is not 32-byte aligned */
   DP_EPLAN = -3,       /* workspace does not hold this plan's uploaded image */
   DP_ECUDA = -4,       /* a CUDA runtime call or kernel launch failed */
   DP_ENONFINITE = -5,  /* the global gradient norm was not finite */
@@ -99,8 +100,8 @@ typedef struct {
  * slot of ceil(size/8)*8 elements (16-byte aligned); a non-empty bucket is
  * closed when adding the next slot would exceed bucket_bytes/2 elements; a
  * tensor is never split (one larger than the cap forms its own bucket); a
- * closed bucket is padded up to a multiple of 8P, so each of its P shards is a
- * whole number of 16-byte vectors.
+ * closed bucket is padded up to a multiple of 16P, so each of its P shards is a
+ * whole number of 32-byte blocks (the kernels' 256-bit access unit).
  *   sizes[n_tensors]  element count of each tensor (>= 0), host memory.
  *   decay[n_tensors]  1 = weight decay applies to the tensor, 0 = not; NULL = all.
  *   bucket_bytes      cap in bytes of bf16 gradient (>= 2).

@@ -86,6 +86,8 @@ class Oracle:
                                     C.c_double, P, C.c_int32]
         L.orc_ledger_bytes.argtypes = [C.c_int32, C.c_double, C.c_int32, P]
         L.orc_ledger_bytes.restype = C.c_double
+        L.orc_sum.argtypes = [P, C.c_int64]
+        L.orc_sum.restype = C.c_double
         L.orc_stage_traffic.argtypes = [C.c_int32, C.c_int32, C.c_int64, P, P]
         L.orc_lsq_identity.argtypes = [C.c_int32, C.c_int32, C.c_int32, P, P, P, P, P, P, P, P]
         self.L = L
@@ -175,6 +177,11 @@ class Oracle:
                                     _p(master), _p(m), _p(v), _p(params), C.byref(cfg), _p(mean),
                                     float(sumsq_total), C.byref(st), int(n_threads)), "zero step")
         return params, master, m, v, mean, st
+
+    def sum(self, x):
+        """The oracle's compensated sum of doubles (e.g. per-bucket sums of squares)."""
+        a = np.ascontiguousarray(x, np.float64)
+        return self.L.orc_sum(_p(a), len(a))
 
     def ledger_bytes(self, stage, psi, P, comp=(2, 2, 4, 4, 4)):
         c = np.asarray(comp, np.float64)

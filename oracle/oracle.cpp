@@ -35,8 +35,9 @@
 //  R4 fp32 -> bf16 rounds to nearest even.
 //  R5 bucket rule: walk tensors last to first, 8-element aligned slots, close the
 //     bucket when a non-empty bucket would exceed the cap; a tensor is never
-//     split; a bucket is padded to a multiple of 8P; shards are its P equal,
-//     contiguous parts; padding holds zeros.
+//     split; a bucket is padded to a multiple of 16P, so each of its P equal,
+//     contiguous shards is a whole number of 32-byte bf16 blocks; padding holds
+//     zeros.
 //  R6 AdamW is torch.optim.AdamW's algorithm (decoupled decay, bias-corrected
 //     Adam, eps outside the square root), with per-element op order
 //        theta *= (1 - lr*wd)                     [decayed tensors only]
@@ -46,7 +47,8 @@
 //     in fp32 without fused multiply-add; the scalar factors are formed in
 //     double and rounded to fp32 once.
 //  R7 clipping is clip_grad_norm_: norm = ||mean||_2 over the fp32 mean
-//     gradient (summed here in double), coef = min(1, max_norm/(norm+1e-6))
+//     gradient (squares summed in double with Neumaier's compensated
+//     summation), coef = min(1, max_norm/(norm+1e-6))
 //     rounded to fp32 once; g = mean * coef.  max_norm <= 0 disables it.  A
 //     non-finite norm gives coef = NaN, so the bad step shows in every output.
 //
@@ -105,7 +107,7 @@ bool make_plan(const int64_t* sizes, int n, int64_t bucket_bytes, int P, Plan* p
   for (int t = 0; t < n; ++t)
     if (sizes[t] < 0) return false;
   const int64_t cap = bucket_bytes / 2;  // bf16 elements
-  const int64_t quantum = 8 * static_cast<int64_t>(P);
+  const int64_t quantum = 16 * static_cast<int64_t>(P);
   pl->P = P;
   pl->t_off.assign(n, 0);
   pl->t_bucket.assign(n, -1);
@@ -302,10 +304,27 @@ void bucket_mean(const Plan& pl, int b, std::vector<float>& X, std::vector<float
   }
 }
 
+// Neumaier's compensated summation (an improved Kahan-Babuska sum): the running
+// compensation keeps the result within a few ulps of the exact sum, where a
+// plain running double sum of ~1e8 squares can drift by ~1e-10 relative.
+struct CompensatedSum {
+  double sum = 0.0, comp = 0.0;
+  void add(double x) {
+    const double t = sum + x;
+    if (std::fabs(sum) >= std::fabs(x))
+      comp += (sum - t) + x;
+    else
+      comp += (x - t) + sum;
+    sum = t;
+  }
+  double value() const { return sum + comp; }
+};
+
+// sum of mean^2; each square of an fp32 value is exact in double.
 double sumsq_of(const std::vector<float>& mean) {
-  double acc = 0.0;
-  for (float x : mean) acc += static_cast<double>(x) * static_cast<double>(x);
-  return acc;
+  CompensatedSum acc;
+  for (float x : mean) acc.add(static_cast<double>(x) * static_cast<double>(x));
+  return acc.value();
 }
 
 }  // namespace
@@ -353,9 +372,16 @@ void orc_adamw_element(float g, float* state, int32_t decay, const orc_adamw* cf
 }
 
 float orc_clip_coef(const double* bucket_sumsq, int32_t nb, double max_norm, double* norm) {
-  double acc = 0.0;
-  for (int b = 0; b < nb; ++b) acc += bucket_sumsq[b];
-  return clip_coef(acc, max_norm, norm);
+  CompensatedSum acc;
+  for (int b = 0; b < nb; ++b) acc.add(bucket_sumsq[b]);
+  return clip_coef(acc.value(), max_norm, norm);
+}
+
+// The compensated total of per-bucket sums (what orc_zero_step takes as sumsq_total).
+double orc_sum(const double* x, int64_t n) {
+  CompensatedSum acc;
+  for (int64_t i = 0; i < n; ++i) acc.add(x[i]);
+  return acc.value();
 }
 
 // ---- the mean all-reduce (DDP / NO_SHARD) ----------------------------------
@@ -464,8 +490,9 @@ int orc_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t
 
   // global norm and clip coefficient ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP": clip after the
   // gradients are averaged)
-  double sumsq = 0.0;
-  for (int b = 0; b < nb; ++b) sumsq += bsum[b];
+  CompensatedSum total;
+  for (int b = 0; b < nb; ++b) total.add(bsum[b]);
+  double sumsq = total.value();
   if (sumsq_total >= 0.0) sumsq = sumsq_total;
   double norm = 0.0;
   const float coef = clip_coef(sumsq, cfg->max_norm, &norm);

@@ -67,7 +67,7 @@ def check_plan_invariants(sizes, cap_bytes, P, p):
     n = len(sizes)
     cap = cap_bytes // 2
     slot = [(s + 7) // 8 * 8 for s in sizes]
-    q = 8 * P
+    q = 16 * P
     nb = p["n_buckets"]
     assert len(p["b_off"]) == nb
     off = 0
@@ -357,6 +357,20 @@ def pin_clip_coef(orc):
     tcoef = float(t.grad[0] / t.grad.new_tensor(vec[0]))
     coef, _ = orc.clip_coef(np.array([float(np.sum(vec.astype(np.float64) ** 2))]), 1.0)
     assert math.isclose(coef, tcoef, rel_tol=2e-6)
+
+
+def pin_norm_sum_is_exact(orc):
+    """The clip norm is the 2-norm of the mean: one element of 1.0 followed by
+    2**20 elements of 2**-27 gives sum(mean^2) = 1 + 2**-34 exactly, which a
+    plain running double sum loses entirely (each 2**-54 is below half an ulp)."""
+    n_small = 1 << 20
+    sizes = [n_small, 1]                       # the 1-element tensor is packed first
+    g = np.zeros((1, n_small + 1), np.uint16)
+    g[0, :n_small] = bf16_bits(np.array([2.0 ** -27], np.float32))[0]
+    g[0, n_small] = bf16_bits(np.array([1.0], np.float32))[0]
+    sums = orc.bucket_sumsq(sizes, 1 << 30, 1, g)
+    assert len(sums) == 1 and sums[0] == 1.0 + 2.0 ** -34, sums[0] - 1.0
+    assert orc.sum(np.array([1.0] + [2.0 ** -54] * 1024)) == 1.0 + 2.0 ** -44
 
 
 # --------------------------------------------------------------------------- fused step

@@ -85,7 +85,7 @@ def test_planner_matches_oracle_random(orc):
         cap = int(rng.choice([2, 16, 100, 4096, 65536]))
         p = _compare(sizes, cap, P, orc)
         check_plan_invariants(sizes, cap, P, orc.plan(sizes, cap, P))
-        assert p.L % (8 * P) == 0
+        assert p.L % (16 * P) == 0
 
 
 def test_tiny_plan_golden():
@@ -103,9 +103,9 @@ def test_empty_and_degenerate_plans():
     p = dps.Plan([0, 0], 1024, 4)
     assert (p.n_buckets, p.L) == (1, 0)
     p = dps.Plan([1], 2, 1)
-    assert (p.n_buckets, p.L) == (1, 8)
+    assert (p.n_buckets, p.L) == (1, 16)
     p = dps.Plan([100], 2, 64)
-    assert p.L == 512 and p.bucket(0)[2] == 8
+    assert p.L == 1024 and p.bucket(0)[2] == 16
 
 
 def test_explicit_stride():
@@ -139,7 +139,7 @@ def test_compute_calls_validate_before_any_device_work():
     lib = dps.lib()
     p = dps.Plan([1000, 24], 1 << 20, 4)
     nb = p.n_buckets
-    ws, ok, odd = C.c_void_p(1 << 20), C.c_void_p(1 << 21), C.c_void_p((1 << 21) + 8)
+    ws, ok, odd = C.c_void_p(1 << 20), C.c_void_p(1 << 21), C.c_void_p((1 << 21) + 16)
     assert lib.dp_allreduce_mean(p.handle, ws, ok, 0, nb + 1, None) == dps.DP_EINVAL
     assert lib.dp_allreduce_mean(p.handle, ws, ok, 1, 0, None) == dps.DP_EINVAL
     assert lib.dp_allreduce_mean(p.handle, ws, odd, 0, nb, None) == dps.DP_EALIGN
@@ -159,3 +159,14 @@ def test_compute_calls_validate_before_any_device_work():
 def test_launch_counts():
     assert dps.dp_fused_zero_step_launches(dps.adamw_cfg(max_norm=0.0)) == 1
     assert dps.dp_fused_zero_step_launches(dps.adamw_cfg(max_norm=1.0)) == 3
+
+
+def test_empty_plan_accepts_null_pointers():
+    """An empty plan touches no memory: NULL device pointers are accepted and no
+    kernel is launched."""
+    lib = dps.lib()
+    p = dps.Plan([], 1024, 4)
+    ws = C.c_void_p(1 << 20)
+    assert lib.dp_allreduce_mean(p.handle, ws, None, 0, 0, None) == dps.DP_OK
+    assert lib.dp_all_gather(p.handle, ws, None, 0, 0, None) == dps.DP_OK
+

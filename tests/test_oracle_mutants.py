@@ -34,8 +34,12 @@ MUTANTS = {
                     "const float g = means[b][i] * static_cast<float>(P) * coef;"),
     "plan_forward_order": ("for (int t = n - 1; t >= 0; --t) {\n    const int64_t slot",
                            "for (int t = 0; t < n; ++t) {\n    const int64_t slot"),
-    "plan_pad_8": ("const int64_t quantum = 8 * static_cast<int64_t>(P);",
+    "plan_pad_8": ("const int64_t quantum = 16 * static_cast<int64_t>(P);",
                    "const int64_t quantum = 8;"),
+    "plan_pad_8P": ("const int64_t quantum = 16 * static_cast<int64_t>(P);",
+                    "const int64_t quantum = 8 * static_cast<int64_t>(P);"),
+    "norm_plain_sum": ("      comp += (sum - t) + x;\n    else\n      comp += (x - t) + sum;",
+                       "      (void)0;\n    else\n      (void)0;"),
     "plan_close_ge": ("used + slot > cap", "used + slot >= cap"),
     "plan_no_align": ("const int64_t slot = (sizes[t] + 7) / 8 * 8;",
                       "const int64_t slot = sizes[t];"),

@@ -84,7 +84,7 @@ def zero_clip_sampled(orc, wl, n_random=2, batch=16):
                                      host_grads(grads, off, wl.sizes, tb)).tolist())
     assert len(sums) == nb
     coef_ref, norm_ref = orc.clip_coef(sums, wl.adamw.max_norm)
-    total = sum(sums)
+    total = orc.sum(sums)
     a = wl.adamw
     dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v,
                            dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay,
