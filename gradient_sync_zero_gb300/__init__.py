@@ -67,6 +67,7 @@ def lib():
             "dp_fused_zero_step": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
             "dp_fused_zero_step_launches": [vp],
             "dp_read_norm": [vp, vp, vp, vp, vp, vp],
+            "dp_clip_coef_noalloc": [vp, vp, vp, f64, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -268,6 +269,18 @@ def dp_read_norm(plan, ws, stream=None, raise_on_status=True):
     if raise_on_status:
         _check(rc)
     return norm.value, coef.value, status.value
+
+
+def dp_clip_coef_noalloc(plan, grads, mean, max_norm, coef_out, norm_out, stream=None):
+    """Reduce-scatter mean + clip coefficient without a workspace (library-owned
+    static device scratch; see include/dpsync.h).  coef_out: 1-element float32
+    CUDA tensor, norm_out: 1-element float64 CUDA tensor."""
+    _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
+    _need(mean, torch.float32, plan.L, "mean")
+    _need(coef_out, torch.float32, 1, "coef_out")
+    _need(norm_out, torch.float64, 1, "norm_out")
+    _check(lib().dp_clip_coef_noalloc(plan.handle, _ptr(grads), _ptr(mean), float(max_norm),
+                                      _ptr(coef_out), _ptr(norm_out), _stream(stream)))
 
 
 def dp_version():

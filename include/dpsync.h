@@ -237,6 +237,29 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
 int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float* coef,
                  int32_t* status, void* stream);
 
+/*
+ * The pages have no counterpart for this call: it is a library convenience.
+ * dp_reduce_scatter_mean(want_sumsq=1) + dp_clip_coef over all buckets,
+ * for callers that cannot allocate device memory (a plugin handed buffers by a
+ * host application that owns the memory pool, a framework whose caching
+ * allocator must account for every byte, a loop where a cudaMalloc/cudaFree
+ * that may synchronise the device is not acceptable).  Instead of a workspace
+ * it uses a 32 MiB library-owned device array, held by every GPU that loads it
+ * until the process exits; plans up to about 1.6e9 parameters fit (larger ones:
+ * DP_EINVAL with the sizes in dp_last_error()).  It allocates nothing.
+ *   grads     bf16 [P][replica_stride] (input, 32-byte aligned)
+ *   mean      fp32 [L] (output, 32-byte aligned): the reduce-scatter mean
+ *   max_norm  clip threshold (<= 0: coef = 1)
+ *   coef_out  device float (output): min(1, max_norm / (norm + 1e-6))
+ *   norm_out  device double (output): the global L2 norm of the mean
+ * Every call shares the array and overwrites it; calls whose work overlaps on
+ * the GPU (unordered streams, concurrent host threads) race and must be
+ * serialised.  The first call on a device looks up the array's address; make
+ * that first call before any stream capture.
+ */
+int dp_clip_coef_noalloc(const dp_plan* plan, const void* grads, float* mean, double max_norm,
+                         float* coef_out, double* norm_out, void* stream);
+
 /* Thread-local text of the last error on this thread ("" if none). */
 const char* dp_last_error(void);
 

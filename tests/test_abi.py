@@ -170,3 +170,15 @@ def test_empty_plan_accepts_null_pointers():
     assert lib.dp_allreduce_mean(p.handle, ws, None, 0, 0, None) == dps.DP_OK
     assert lib.dp_all_gather(p.handle, ws, None, 0, 0, None) == dps.DP_OK
 
+
+def test_noalloc_refuses_oversized_plans_on_the_host():
+    """dp_clip_coef_noalloc checks the static array's size before any device work."""
+    lib = dps.lib()
+    plan = dps.Plan([1 << 30, 1 << 30], 25 << 20, 8)
+    ok = C.c_void_p(1 << 21)
+    rc = lib.dp_clip_coef_noalloc(plan.handle, ok, ok, C.c_double(1.0), ok, ok, None)
+    assert rc == dps.DP_EINVAL
+    msg = lib.dp_last_error().decode()
+    assert "static array holds 33554432 bytes" in msg
+    assert lib.dp_clip_coef_noalloc(plan.handle, ok, ok, C.c_double(1.0), None, ok,
+                                    None) == dps.DP_EINVAL
