@@ -158,6 +158,35 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# --------------------------------------------------------------------------- ncu traffic
+KERNEL_SOURCES = ["kernels.cuh", "kernels_reduce.cu", "kernels_update.cu", "launch.cuh"]
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gradient_sync_zero_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload, kernel):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+    profiles/traffic.json, only if it was taken on the current kernel sources."""
+    tf = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tf):
+        return None, "no ncu capture recorded"
+    with open(tf) as f:
+        tdb = json.load(f)
+    rec = tdb.get(f"{workload}:{kernel}")
+    if rec is None:
+        return None, "no ncu capture for this workload and kernel"
+    if rec.get("kernel_src_sha") != kernel_source_hash():
+        return None, "kernel changed since the ncu capture"
+    return rec["bytes_per_launch"], rec.get("how", "")
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=15.0,
                        max_passes=3, step=1):
@@ -293,14 +322,7 @@ def run_gpu(args, rank, local, world):
         KERNEL_BYTES_PER_PARAM[names[0]](P)
     step_gbs = step_bytes_pp * n_params / (ms_step * 1e-3) / 1e9
 
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tf):
-        with open(tf) as f:
-            tdb = json.load(f)
-        key = f"{wl.name}:{dom_name}"
-        if key in tdb:
-            traffic = tdb[key]["bytes_per_launch"]
+    traffic, traffic_src = stored_traffic(wl.name, dom_name)
 
     result = {
         "metric": "fused ZeRO-2 step params/s and achieved HBM GB/s vs GB300 peak (P=8, 1 GPU)"
@@ -343,6 +365,7 @@ def run_gpu(args, rank, local, world):
             "unit": "GB/s",
             "frac": achieved / peak,
             "traffic": traffic,
+            "traffic_source": traffic_src,
             "bytes_per_param": KERNEL_BYTES_PER_PARAM[dom_name](P),
         },
         "gpu_launches": (n_ev - 1) * args.steps,
