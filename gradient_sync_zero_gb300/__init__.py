@@ -17,8 +17,10 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libdpsync.so")
 
-DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM = 0, -1, -2, -3, -4, -5, -6
-DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE = 1, 2
+DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ETIMEOUT = \
+    0, -1, -2, -3, -4, -5, -6, -7
+DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT = 1, 2, 4
+DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_DRY_RUN = 0, 1, 1
 
 
 class DPError(RuntimeError):
@@ -68,6 +70,12 @@ def lib():
             "dp_fused_zero_step_launches": [vp],
             "dp_read_norm": [vp, vp, vp, vp, vp, vp],
             "dp_clip_coef_noalloc": [vp, vp, vp, f64, vp, vp, vp],
+            "dp_adamw_all_gather": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
+            "dp_tracker_create": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
+            "dp_tracker_begin": [vp],
+            "dp_tracker_mark_ready": [vp, i32, vp],
+            "dp_tracker_wait": [vp, i64],
+            "dp_tracker_fired": [vp, vp, i32, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -75,6 +83,8 @@ def lib():
             f.restype = C.c_int
         L.dp_plan_free.argtypes = [vp]
         L.dp_plan_free.restype = None
+        L.dp_tracker_free.argtypes = [vp]
+        L.dp_tracker_free.restype = None
         L.dp_last_error.argtypes = []
         L.dp_last_error.restype = C.c_char_p
         L.dp_version.restype = C.c_int
@@ -233,6 +243,65 @@ def dp_allreduce_mean(plan, ws, grads, b0=0, b1=None, stream=None):
     _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
     b0, b1 = _range(plan, b0, b1)
     _check(lib().dp_allreduce_mean(plan.handle, _ws(plan, ws), _ptr(grads), b0, b1, _stream(stream)))
+
+
+def dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg, use_clip_coef=True, stream=None):
+    for t, name in ((mean, "mean"), (master, "master"), (m, "m"), (v, "v")):
+        _need(t, torch.float32, plan.L, name)
+    _need(params, torch.bfloat16, plan.P * plan.stride, "params")
+    _check(lib().dp_adamw_all_gather(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
+                                     _ptr(v), _ptr(params), C.byref(cfg), 1 if use_clip_coef else 0,
+                                     _stream(stream)))
+
+
+class Tracker:
+    """Bucket readiness tracker (streamed per-bucket synchronisation).
+
+    mode: DP_TRACK_ALLREDUCE (in place on `grads`) or DP_TRACK_REDUCE_SCATTER
+    (into `mean`, with norm partials).  dry_run=True records the firing order
+    and launches nothing (no GPU needed)."""
+
+    def __init__(self, plan, mode, ws=None, grads=None, mean=None, stream=None, max_ctas=0,
+                 dry_run=False):
+        self.plan = plan
+        self._keep = (ws, grads, mean, stream)
+        if not dry_run:
+            _ws(plan, ws)
+            _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
+            if mode == DP_TRACK_REDUCE_SCATTER:
+                _need(mean, torch.float32, plan.L, "mean")
+            s = _stream(stream)
+        else:
+            s = None
+        h = C.c_void_p()
+        _check(lib().dp_tracker_create(plan.handle, int(mode), _ptr(ws), _ptr(grads), _ptr(mean), s,
+                                       int(max_ctas), DP_TRACK_DRY_RUN if dry_run else 0,
+                                       C.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.dp_tracker_free(h)
+            self._h = None
+
+    def begin(self):
+        _check(lib().dp_tracker_begin(self._h))
+
+    def mark_ready(self, tensor, event=None):
+        """event: torch.cuda.Event recorded after the tensor's gradient was written."""
+        ev = C.c_void_p(event.cuda_event) if event is not None else None
+        _check(lib().dp_tracker_mark_ready(self._h, int(tensor), ev))
+
+    def wait(self, timeout_ms=10000):
+        _check(lib().dp_tracker_wait(self._h, int(timeout_ms)))
+
+    def fired(self):
+        n = C.c_int32()
+        cap = self.plan.n_buckets
+        arr = (C.c_int32 * max(cap, 1))()
+        _check(lib().dp_tracker_fired(self._h, arr, cap, C.byref(n)))
+        return list(arr[:n.value])
 
 
 def dp_fused_zero_step_launches(cfg):

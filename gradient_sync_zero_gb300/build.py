@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdpsync.so")
-SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "noalloc.cu"]
+SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "noalloc.cu",
+           "tracker.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

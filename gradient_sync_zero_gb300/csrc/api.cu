@@ -160,6 +160,21 @@ int dp_allreduce_mean(const dp_plan* plan, void* workspace, void* grads, int32_t
   return e ? cuda_fail(e, "dp_allreduce_mean") : DP_OK;
 }
 
+int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean, float* master,
+                        float* m, float* v, void* params, const dp_adamw_cfg* cfg,
+                        int32_t use_clip_coef, void* stream) {
+  Launch L;
+  const Plan* pl = as_plan(plan);
+  int rc = prepare("dp_adamw_all_gather", plan, workspace, 0,
+                   pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_adamw_all_gather", L.plan, {mean, master, m, v, params}))) return rc;
+  AdamScalars s;
+  if ((rc = adam_scalars("dp_adamw_all_gather", cfg, &s))) return rc;
+  const int e = launch_adamw_all_gather(L, mean, params, master, m, v, s, use_clip_coef != 0);
+  return e ? cuda_fail(e, "dp_adamw_all_gather") : DP_OK;
+}
+
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
   return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
 }
@@ -188,7 +203,7 @@ int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, 
   e = launch_norm_finalize(L, cfg->max_norm);
   if (e) return cuda_fail(e, "dp_fused_zero_step (norm)");
   if ((rc = record(stage_events, 2, stream))) return rc;
-  e = launch_adamw_all_gather(L, stage, params, master, m, v, s);
+  e = launch_adamw_all_gather(L, stage, params, master, m, v, s, true);
   if (e) return cuda_fail(e, "dp_fused_zero_step (adamw + all-gather)");
   return record(stage_events, 3, stream);
 }
@@ -207,6 +222,8 @@ int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float
   if (status) *status = h.status;
   if (h.status & DP_STATUS_PLAN_MISMATCH)
     return fail(DP_EPLAN, "dp_read_norm: a kernel found another plan's image in the workspace");
+  if (h.status & DP_STATUS_TIMEOUT)
+    return fail(DP_ETIMEOUT, "dp_read_norm: a kernel's bounded wait on its copies gave up");
   if (h.status & DP_STATUS_NONFINITE)
     return fail(DP_ENONFINITE, "dp_read_norm: the global gradient norm was not finite");
   return DP_OK;

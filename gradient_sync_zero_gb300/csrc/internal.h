@@ -92,6 +92,7 @@ struct Launch {
   int64_t tile_begin;   // [tile_begin, tile_end)
   int64_t tile_end;
   void* stream;
+  int max_ctas = 0;     // > 0: cap on the grid (leave SMs to concurrent work)
 };
 
 // Each returns a cudaError_t value (0 = success).
@@ -105,6 +106,6 @@ int launch_broadcast(const Launch& L, void* params, int src);
 int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,
                       float* v, const AdamScalars& s);
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
-                            float* m, float* v, const AdamScalars& s);
+                            float* m, float* v, const AdamScalars& s, bool use_coef);
 
 }  // namespace dps

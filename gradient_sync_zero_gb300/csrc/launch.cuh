@@ -39,7 +39,7 @@ inline float* stage_ptr(const Launch& L) {
 // Resident CTAs per SM for a kernel (occupancy calculator, cached per device),
 // optionally capped by DPSYNC_CTAS_PER_SM for tuning sweeps.
 template <class K>
-int resident_ctas(K kernel, int threads) {
+int resident_ctas(K kernel, int threads, size_t dyn_smem = 0) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> cache;
   int dev = 0;
@@ -52,7 +52,8 @@ int resident_ctas(K kernel, int threads) {
   }
   int sms = 0, per_sm = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) !=
+      cudaSuccess)
     return 0;
   if (const char* e = std::getenv("DPSYNC_CTAS_PER_SM")) {
     const int cap = std::atoi(e);
@@ -74,7 +75,9 @@ int launch_tiles(const Launch& L, K kernel, A... args) {
     const cudaError_t e = cudaGetLastError();
     return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
   }
-  const int grid = static_cast<int>(n < cap ? n : cap);
+  int64_t g = n < cap ? n : cap;
+  if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
+  const int grid = static_cast<int>(g);
   kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(args...);
   return static_cast<int>(cudaGetLastError());
 }

@@ -1,0 +1,219 @@
+// Bucket readiness tracker: streamed per-bucket synchronisation.
+//
+// DDP's core mechanism ("4.1 Data parallelism in depth", sec. 4.2): backward
+// produces gradients last layer first; a bucket's collective fires as soon as
+// every gradient in it is ready, on a separate stream ("Distributed Training:
+// Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP"), while the
+// earlier layers keep computing.  Buckets fire in plan order, the same order
+// every step, as DDP requires of all ranks ("Data Parallelism: DDP, ZeRO and
+// FSDP", "DDP, and why it works").  Where DDP hangs on a gradient that never
+// becomes ready (find_unused_parameters, sec. 4.2 note), the tracker's wait
+// times out and names the missing tensors.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <condition_variable>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace dps {
+
+struct Tracker {
+  const Plan* plan = nullptr;
+  int mode = DP_TRACK_ALLREDUCE;
+  int flags = 0;
+  uint8_t* ws = nullptr;
+  void* grads = nullptr;
+  float* mean = nullptr;
+  void* stream = nullptr;
+  int max_ctas = 0;
+  std::vector<std::vector<int32_t>> bucket_tensors;
+  std::mutex mu;
+  std::condition_variable cv;
+  std::vector<uint8_t> ready;
+  std::vector<void*> events;
+  std::vector<int32_t> pending;     // per bucket: tensors not yet marked
+  int32_t next = 0;                 // next bucket to fire, in plan order
+  std::vector<int32_t> fired;
+  int error = DP_OK;                // sticky launch error of this step
+  std::string error_text;
+};
+
+namespace {
+
+void reset(Tracker& tr) {
+  const Plan& pl = *tr.plan;
+  std::fill(tr.ready.begin(), tr.ready.end(), 0);
+  std::fill(tr.events.begin(), tr.events.end(), nullptr);
+  for (size_t b = 0; b < tr.bucket_tensors.size(); ++b)
+    tr.pending[b] = static_cast<int32_t>(tr.bucket_tensors[b].size());
+  tr.next = 0;
+  tr.fired.clear();
+  tr.error = DP_OK;
+  tr.error_text.clear();
+  (void)pl;
+}
+
+// Launch bucket b on the tracker's stream (lock held).
+int fire(Tracker& tr, int32_t b) {
+  tr.fired.push_back(b);
+  if (tr.flags & DP_TRACK_DRY_RUN) return DP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(tr.stream);
+  for (int32_t t : tr.bucket_tensors[b]) {
+    if (!tr.events[t]) continue;
+    const cudaError_t e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(tr.events[t]), 0);
+    if (e != cudaSuccess) {
+      tr.error_text = std::string("dp_tracker: cudaStreamWaitEvent: ") + cudaGetErrorString(e);
+      return DP_ECUDA;
+    }
+  }
+  Launch L;
+  L.plan = tr.plan;
+  L.ws = tr.ws;
+  L.tile_begin = tr.plan->b_tile0[b];
+  L.tile_end = tr.plan->b_tile0[b + 1];
+  L.stream = tr.stream;
+  L.max_ctas = tr.max_ctas;
+  const int e = tr.mode == DP_TRACK_ALLREDUCE ? launch_allreduce(L, tr.grads)
+                                              : launch_reduce_scatter(L, tr.grads, tr.mean, true);
+  if (e) {
+    tr.error_text = std::string("dp_tracker: bucket launch: ") +
+                    cudaGetErrorString(static_cast<cudaError_t>(e));
+    return DP_ECUDA;
+  }
+  return DP_OK;
+}
+
+}  // namespace
+}  // namespace dps
+
+using namespace dps;
+
+extern "C" {
+
+int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* grads, float* mean,
+                      void* comm_stream, int32_t max_ctas, int32_t flags, dp_tracker** out) {
+  clear_error();
+  if (!out) return fail(DP_EINVAL, "dp_tracker_create: out is NULL");
+  *out = nullptr;
+  const Plan* pl = as_plan(plan);
+  if (!pl) return fail(DP_EINVAL, "dp_tracker_create: NULL plan");
+  if (mode != DP_TRACK_ALLREDUCE && mode != DP_TRACK_REDUCE_SCATTER)
+    return fail(DP_EINVAL, "dp_tracker_create: unknown mode");
+  if (max_ctas < 0) return fail(DP_EINVAL, "dp_tracker_create: max_ctas must be >= 0");
+  const bool dry = (flags & DP_TRACK_DRY_RUN) != 0;
+  if (!dry) {
+    if (!workspace || (pl->L > 0 && (!grads || (mode == DP_TRACK_REDUCE_SCATTER && !mean))))
+      return fail(DP_EINVAL, "dp_tracker_create: NULL workspace, grads or mean");
+    const uintptr_t a = reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(grads) |
+                        reinterpret_cast<uintptr_t>(mean);
+    if (a & 31u) return fail(DP_EALIGN, "dp_tracker_create: device pointers must be 32-byte aligned");
+  }
+  Tracker* tr = new (std::nothrow) Tracker();
+  if (!tr) return fail(DP_ENOMEM, "dp_tracker_create: out of host memory");
+  try {
+    tr->plan = pl;
+    tr->mode = mode;
+    tr->flags = flags;
+    tr->ws = static_cast<uint8_t*>(workspace);
+    tr->grads = grads;
+    tr->mean = mean;
+    tr->stream = comm_stream;
+    tr->max_ctas = max_ctas;
+    const size_t nb = pl->b_off.size(), nt = pl->sizes.size();
+    tr->bucket_tensors.assign(nb, {});
+    for (size_t t = 0; t < nt; ++t) tr->bucket_tensors[pl->t_bucket[t]].push_back(static_cast<int32_t>(t));
+    tr->ready.assign(nt, 0);
+    tr->events.assign(nt, nullptr);
+    tr->pending.assign(nb, 0);
+    reset(*tr);
+  } catch (const std::bad_alloc&) {
+    delete tr;
+    return fail(DP_ENOMEM, "dp_tracker_create: out of host memory");
+  }
+  *out = reinterpret_cast<dp_tracker*>(tr);
+  return DP_OK;
+}
+
+int dp_tracker_begin(dp_tracker* tracker) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_begin: NULL tracker");
+  std::lock_guard<std::mutex> g(tr->mu);
+  reset(*tr);
+  return DP_OK;
+}
+
+int dp_tracker_mark_ready(dp_tracker* tracker, int32_t tensor, void* ready_event) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_mark_ready: NULL tracker");
+  std::unique_lock<std::mutex> g(tr->mu);
+  const int32_t nt = static_cast<int32_t>(tr->ready.size());
+  if (tensor < 0 || tensor >= nt) return fail(DP_EINVAL, "dp_tracker_mark_ready: tensor out of range");
+  if (tr->ready[tensor])
+    return fail(DP_EINVAL, "dp_tracker_mark_ready: tensor " + std::to_string(tensor) +
+                               " already marked in this step");
+  tr->ready[tensor] = 1;
+  tr->events[tensor] = ready_event;
+  --tr->pending[tr->plan->t_bucket[tensor]];
+  const int32_t nb = static_cast<int32_t>(tr->pending.size());
+  int rc = DP_OK;
+  while (tr->next < nb && tr->pending[tr->next] == 0 && tr->error == DP_OK) {
+    rc = fire(*tr, tr->next);
+    if (rc) {
+      tr->error = rc;
+      break;
+    }
+    ++tr->next;
+  }
+  const bool done = tr->next == nb || tr->error != DP_OK;
+  const std::string text = tr->error_text;
+  g.unlock();
+  if (done) tr->cv.notify_all();
+  return rc ? fail(rc, text) : DP_OK;
+}
+
+int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_wait: NULL tracker");
+  std::unique_lock<std::mutex> g(tr->mu);
+  const int32_t nb = static_cast<int32_t>(tr->pending.size());
+  const bool ok = tr->cv.wait_for(g, std::chrono::milliseconds(std::max<int64_t>(timeout_ms, 0)),
+                                  [&] { return tr->next == nb || tr->error != DP_OK; });
+  if (tr->error != DP_OK) return fail(tr->error, tr->error_text);
+  if (ok) return DP_OK;
+  std::string missing;
+  int count = 0;
+  for (size_t t = 0; t < tr->ready.size(); ++t) {
+    if (tr->ready[t]) continue;
+    if (count < 16) missing += (count ? ", " : "") + std::to_string(t);
+    ++count;
+  }
+  return fail(DP_ETIMEOUT, "dp_tracker_wait: " + std::to_string(count) +
+                               " tensor(s) never marked ready: " + missing +
+                               (count > 16 ? ", ..." : "") + "; bucket " +
+                               std::to_string(tr->next) + " of " + std::to_string(nb) +
+                               " is the first not launched");
+}
+
+int dp_tracker_fired(const dp_tracker* tracker, int32_t* order, int32_t cap, int32_t* n_fired) {
+  clear_error();
+  Tracker* tr = const_cast<Tracker*>(reinterpret_cast<const Tracker*>(tracker));
+  if (!tr || cap < 0 || (cap > 0 && !order)) return fail(DP_EINVAL, "dp_tracker_fired: bad arguments");
+  std::lock_guard<std::mutex> g(tr->mu);
+  const int32_t n = static_cast<int32_t>(tr->fired.size());
+  for (int32_t i = 0; i < std::min(n, cap); ++i) order[i] = tr->fired[i];
+  if (n_fired) *n_fired = n;
+  return DP_OK;
+}
+
+void dp_tracker_free(dp_tracker* tracker) { delete reinterpret_cast<Tracker*>(tracker); }
+
+}  // extern "C"

@@ -65,11 +65,12 @@ enum {
   DP_EPLAN = -3,       /* workspace does not hold this plan's uploaded image */
   DP_ECUDA = -4,       /* a CUDA runtime call or kernel launch failed */
   DP_ENONFINITE = -5,  /* the global gradient norm was not finite */
-  DP_ENOMEM = -6       /* host allocation failed */
+  DP_ENOMEM = -6,      /* host allocation failed */
+  DP_ETIMEOUT = -7     /* a kernel's bounded wait on its own copies gave up */
 };
 
 /* Status bits written by kernels into the workspace, read by dp_read_norm. */
-enum { DP_STATUS_PLAN_MISMATCH = 1, DP_STATUS_NONFINITE = 2 };
+enum { DP_STATUS_PLAN_MISMATCH = 1, DP_STATUS_NONFINITE = 2, DP_STATUS_TIMEOUT = 4 };
 
 typedef struct dp_plan dp_plan;
 
@@ -225,14 +226,69 @@ int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, 
                        float* master, float* m, float* v, const dp_adamw_cfg* cfg,
                        void* const* stage_events, void* stream);
 
+/*
+ * The clipped step's second pass on its own: AdamW on mean * coef fused with
+ * the all-gather of bf16(theta) into every replica, over all buckets ("Data
+ * Parallelism: DDP, ZeRO and FSDP", "The three stages").  Use after per-bucket
+ * reduce-scatters (e.g. from a tracker) and dp_clip_coef.
+ *   mean     fp32 [L] (input: the reduce-scatter mean of every bucket)
+ *   master, m, v fp32 [L] (in/out);  params bf16 [P][replica_stride] (out)
+ *   use_clip_coef  non-zero: multiply by the workspace's clip coefficient.
+ */
+int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean, float* master,
+                        float* m, float* v, void* params, const dp_adamw_cfg* cfg,
+                        int32_t use_clip_coef, void* stream);
+
 /* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
+
+/*
+ * Streamed per-bucket synchronisation: DDP's bucket readiness.  "When every
+ * gradient in a Bucket is ready, immediately AllReduce that Bucket" while
+ * earlier layers keep running backward ("4.1 Data parallelism in depth",
+ * sec. 4.2); the collective fires "on a separate stream" ("Distributed
+ * Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP");
+ * buckets fire in the same order every step ("Data Parallelism: DDP, ZeRO and
+ * FSDP", "DDP, and why it works": bucket order must match).
+ *
+ * A tracker belongs to one plan and one set of buffers.  Each step: begin, then
+ * mark every tensor ready (from any host thread) as its gradient is written,
+ * passing a CUDA event recorded after that write (or NULL when the write is
+ * already ordered before comm_stream's work).  When bucket b and every bucket
+ * before it in plan order are complete, the tracker makes comm_stream wait for
+ * the bucket's events and launches the bucket's reduction there:
+ *   DP_TRACK_ALLREDUCE       the in-place mean all-reduce of `grads`;
+ *   DP_TRACK_REDUCE_SCATTER  the reduce-scatter mean into `mean` with norm
+ *                            partials (follow with dp_clip_coef and
+ *                            dp_adamw_all_gather on comm_stream).
+ * dp_tracker_wait returns once every bucket has been launched, or DP_ETIMEOUT
+ * after timeout_ms naming tensors never marked (DDP would hang there).  It does
+ * not synchronise the GPU: order later work after comm_stream.
+ *   max_ctas   cap on each launch's grid (0 = the full persistent grid), to leave
+ *              SMs to the backward running beside it.
+ *   flags      DP_TRACK_DRY_RUN: record the firing order, launch nothing.
+ * Events are the caller's: keep them alive and unrecorded until their bucket
+ * fires.  Marking a tensor twice in one step is DP_EINVAL.
+ */
+typedef struct dp_tracker dp_tracker;
+enum { DP_TRACK_ALLREDUCE = 0, DP_TRACK_REDUCE_SCATTER = 1 };
+enum { DP_TRACK_DRY_RUN = 1 };
+
+int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* grads, float* mean,
+                      void* comm_stream, int32_t max_ctas, int32_t flags, dp_tracker** out);
+int dp_tracker_begin(dp_tracker* tracker);
+int dp_tracker_mark_ready(dp_tracker* tracker, int32_t tensor, void* ready_event);
+int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms);
+/* Buckets launched so far this step, in launch order (up to cap entries). */
+int dp_tracker_fired(const dp_tracker* tracker, int32_t* order, int32_t cap, int32_t* n_fired);
+void dp_tracker_free(dp_tracker* tracker);
 
 /*
  * Synchronise `stream` and read the workspace's last clip results: norm
  * (double), coef (fp32) and the status bits.  Any pointer may be NULL.
  * Returns DP_ENONFINITE if the non-finite bit is set, DP_EPLAN if a kernel saw
- * a plan mismatch.
+ * a plan mismatch, DP_ETIMEOUT if a kernel's bounded wait for its own
+ * asynchronous copies gave up (its results for that step are not valid).
  */
 int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float* coef,
                  int32_t* status, void* stream);

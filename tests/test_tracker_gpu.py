@@ -1,0 +1,97 @@
+"""Streamed per-bucket synchronisation on the GPU: a producer stream writes each
+tensor's gradients in backward order (last tensor first) and records an event;
+the tracker fires each complete bucket on a separate communication stream.
+Results must equal the single-launch path and the oracle, bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_zero_gb300 as dps
+from harness import Case, assert_replicas_equal, small_workload
+from workloads import configs, device as wdev
+
+pytestmark = pytest.mark.gpu
+
+
+def produce(c, g_u16, grads, tracker, producer, n_ranks):
+    """Backward-order producer: copy tensor t of every replica, then mark it ready."""
+    src = torch.from_numpy(g_u16.view(np.int16)).view(torch.bfloat16).cuda()
+    base = wdev.tensor_bases(c.sizes)
+    events = []
+    with torch.cuda.stream(producer):
+        for t in reversed(range(len(c.sizes))):
+            o, s = c.off[t], c.sizes[t]
+            if s:
+                grads[:n_ranks, o:o + s].copy_(src[:, base[t]:base[t] + s])
+            ev = torch.cuda.Event()
+            ev.record(producer)
+            events.append(ev)
+            tracker.mark_ready(t, ev)
+    return events
+
+
+@pytest.mark.parametrize("P,max_ctas", [(8, 0), (5, 16), (16, 4)])
+def test_streamed_allreduce_equals_oracle(orc, P, max_ctas):
+    wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910, 9000], P, 32 * 1024, seed=P)
+    c = Case(wl)
+    assert c.plan.n_buckets >= 3
+    g = c.host_grads(1)
+    grads = c.plan.new_replicas()
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    tr = dps.Tracker(c.plan, dps.DP_TRACK_ALLREDUCE, c.ws, grads, stream=comm, max_ctas=max_ctas)
+    for step in range(2):                                   # the tracker is reused across steps
+        grads.zero_()
+        torch.cuda.synchronize()
+        tr.begin()
+        keep = produce(c, g, grads, tr, producer, P)
+        tr.wait(10000)
+        assert tr.fired() == list(range(c.plan.n_buckets))
+        torch.cuda.synchronize()
+        want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+        assert np.array_equal(c.from_replicas(grads), want)
+        assert_replicas_equal(grads, c.plan.L)
+        del keep
+
+
+def test_streamed_zero_step_equals_fused(orc):
+    """Tracker reduce-scatters bucket by bucket; then the clip coefficient and the
+    fused AdamW + all-gather on the same stream == dp_fused_zero_step."""
+    wl = configs.tiny_plumbing()
+    wl.adamw = configs.AdamW(max_norm=0.3)                 # clip active
+    c = Case(wl)
+    g = c.host_grads(1)
+    master0 = c.host_master()
+    a = wl.adamw
+    cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1)
+    # reference: one fused call
+    p_ref = c.plan.new_replicas()
+    s_ref = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    dps.dp_fused_zero_step(c.plan, c.ws, c.to_replicas(g), p_ref, *s_ref, cfg)
+    n_ref = dps.dp_read_norm(c.plan, c.ws)
+    # streamed
+    ws2 = c.plan.new_workspace()
+    grads, mean = c.plan.new_replicas(), c.plan.new_state()
+    params = c.plan.new_replicas()
+    st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    tr = dps.Tracker(c.plan, dps.DP_TRACK_REDUCE_SCATTER, ws2, grads, mean, stream=comm)
+    tr.begin()
+    keep = produce(c, g, grads, tr, producer, wl.P)
+    tr.wait(10000)
+    dps.dp_clip_coef(c.plan, ws2, a.max_norm, stream=comm)
+    dps.dp_adamw_all_gather(c.plan, ws2, mean, *st, params, cfg, use_clip_coef=True, stream=comm)
+    n2 = dps.dp_read_norm(c.plan, ws2, stream=comm)
+    assert n2 == n_ref and n_ref[1] < 1.0
+    assert torch.equal(params, p_ref)
+    for x, y in zip(st, s_ref):
+        assert torch.equal(x, y)
+    del keep
+    # and the oracle agrees
+    z = np.zeros_like(master0)
+    import oracle
+    p_o, m_o, _, _, _, sto = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, wl.P, g, master0, z,
+                                           z, oracle.adamw_cfg(a, 1))
+    assert sto.coef == n2[1]
+    assert np.array_equal(c.from_replicas(params), p_o)
+    assert np.array_equal(c.from_flat(st[0]).view(np.uint32), m_o.view(np.uint32))

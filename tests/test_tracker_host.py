@@ -1,0 +1,138 @@
+"""Bucket readiness tracker, host logic (dry run: no launches, no GPU).
+
+DDP fires a bucket's collective once every gradient in it is ready, buckets in
+the same order every step; a gradient that never becomes ready hangs DDP — the
+tracker reports it instead ("4.1 Data parallelism in depth", sec. 4.2)."""
+import random
+import threading
+
+import pytest
+
+import gradient_sync_zero_gb300 as dps
+from gradient_sync_zero_gb300 import build as dbuild
+from workloads import configs
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    dbuild.build()
+
+
+def dry(sizes, cap, P):
+    plan = dps.Plan(sizes, cap, P)
+    return plan, dps.Tracker(plan, dps.DP_TRACK_ALLREDUCE, dry_run=True)
+
+
+def test_backward_order_fires_every_bucket_in_plan_order():
+    wl = configs.gpt2_small_allreduce()
+    plan, tr = dry(wl.sizes, wl.bucket_bytes, wl.P)
+    tr.begin()
+    for t in reversed(range(len(wl.sizes))):          # backward: last layer first
+        tr.mark_ready(t)
+    tr.wait(1000)
+    assert tr.fired() == list(range(plan.n_buckets))
+
+
+def test_bucket_fires_exactly_when_complete():
+    sizes = [1000, 1000, 1000, 1000]                   # reverse packing: buckets {3,2}, {1,0}
+    plan, tr = dry(sizes, 4000, 2)
+    assert plan.n_buckets == 2 and [plan.tensor(t)[0] for t in range(4)] == [1, 1, 0, 0]
+    tr.begin()
+    tr.mark_ready(3)
+    assert tr.fired() == []
+    tr.mark_ready(2)
+    assert tr.fired() == [0]
+    tr.mark_ready(0)
+    assert tr.fired() == [0]
+    tr.mark_ready(1)
+    assert tr.fired() == [0, 1]
+
+
+def test_later_bucket_waits_for_earlier_ones():
+    """A later bucket that completes first is held until the buckets before it
+    have fired, so the launch order is the same every step."""
+    sizes = [1000, 1000, 1000, 1000]
+    plan, tr = dry(sizes, 4000, 2)
+    tr.begin()
+    tr.mark_ready(0)
+    tr.mark_ready(1)                                   # bucket 1 complete, bucket 0 not
+    assert tr.fired() == []
+    tr.mark_ready(3)
+    tr.mark_ready(2)
+    assert tr.fired() == [0, 1]
+
+
+def test_missing_gradient_times_out_with_its_name():
+    sizes = [10, 20, 30, 40]
+    plan, tr = dry(sizes, 64, 1)
+    tr.begin()
+    for t in (3, 2, 0):
+        tr.mark_ready(t)
+    with pytest.raises(dps.DPError) as e:
+        tr.wait(50)
+    assert e.value.code == dps.DP_ETIMEOUT
+    msg = str(e.value)
+    assert "1 tensor(s) never marked ready: 1" in msg
+
+
+def test_double_mark_and_range_are_rejected_and_begin_resets():
+    plan, tr = dry([10, 20], 1 << 20, 2)
+    tr.begin()
+    tr.mark_ready(1)
+    with pytest.raises(dps.DPError) as e:
+        tr.mark_ready(1)
+    assert e.value.code == dps.DP_EINVAL
+    with pytest.raises(dps.DPError):
+        tr.mark_ready(2)
+    tr.mark_ready(0)
+    tr.wait(100)
+    assert tr.fired() == [0]
+    tr.begin()
+    assert tr.fired() == []
+    tr.mark_ready(0)
+    tr.mark_ready(1)
+    tr.wait(100)
+    assert tr.fired() == [0]
+
+
+def test_concurrent_marking_from_many_threads():
+    wl = configs.sweep_small_tensors(64 * 1024)
+    plan, tr = dry(wl.sizes, wl.bucket_bytes, wl.P)
+    order = list(range(len(wl.sizes)))
+    random.Random(3).shuffle(order)
+    chunks = [order[i::8] for i in range(8)]
+    errors = []
+
+    def work(ts):
+        try:
+            for t in ts:
+                tr.mark_ready(t)
+        except Exception as e:  # noqa: BLE001
+            errors.append(e)
+
+    for step in range(2):
+        tr.begin()
+        th = [threading.Thread(target=work, args=(c,)) for c in chunks]
+        for x in th:
+            x.start()
+        for x in th:
+            x.join()
+        assert not errors
+        tr.wait(5000)
+        assert tr.fired() == list(range(plan.n_buckets))
+
+
+def test_create_validates_buffers():
+    plan = dps.Plan([1000], 1 << 20, 4)
+    lib = dps.lib()
+    import ctypes as C
+    h = C.c_void_p()
+    assert lib.dp_tracker_create(plan.handle, 0, None, None, None, None, 0, 0,
+                                 C.byref(h)) == dps.DP_EINVAL
+    ok, odd = C.c_void_p(1 << 20), C.c_void_p((1 << 20) + 8)
+    assert lib.dp_tracker_create(plan.handle, 0, ok, odd, None, None, 0, 0,
+                                 C.byref(h)) == dps.DP_EALIGN
+    assert lib.dp_tracker_create(plan.handle, 1, ok, ok, None, None, 0, 0,
+                                 C.byref(h)) == dps.DP_EINVAL    # reduce-scatter needs `mean`
+    assert lib.dp_tracker_create(plan.handle, 7, ok, ok, ok, None, 0, 0,
+                                 C.byref(h)) == dps.DP_EINVAL
