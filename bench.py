@@ -453,19 +453,17 @@ def run_streamed(args):
     tr = dps.Tracker(plan, mode, ws, grads, mean if zero else None, stream=comm,
                      max_ctas=args.comm_ctas)
 
+    events = [torch.cuda.Event() for _ in wl.sizes]
+
     def backward(stream, mark):
-        evs = []
         with torch.cuda.stream(stream):
             for t in reversed(range(len(wl.sizes))):
                 if mats[t] is not None:
                     dy, x, dw = mats[t]
                     torch.matmul(dy.t(), x, out=dw)
                 if mark:
-                    ev = torch.cuda.Event()
-                    ev.record(stream)
-                    evs.append(ev)
-                    tr.mark_ready(t, ev)
-        return evs
+                    events[t].record(stream)
+                    tr.mark_ready(t, events[t])
 
     def finish(stream):
         if zero:
@@ -498,11 +496,10 @@ def run_streamed(args):
 
     def streamed():
         tr.begin()
-        keep = backward(compute, True)
+        backward(compute, True)
         tr.wait(60000)
         finish(comm)
         comm.synchronize()
-        del keep
 
     def only_sync():
         sync_all(compute)

@@ -47,6 +47,13 @@ class Stats(C.Structure):
                 ("rs_sent", C.c_int64 * MAX_RANKS), ("ag_sent", C.c_int64 * MAX_RANKS)]
 
 
+class MeshStats(C.Structure):
+    _fields_ = [("rs_sent", C.c_int64 * MAX_RANKS), ("ag_sent", C.c_int64 * MAX_RANKS),
+                ("cross_sent", C.c_int64 * MAX_RANKS), ("groups_equal", C.c_int32),
+                ("replicas_equal", C.c_int32), ("sumsq", C.c_double), ("norm", C.c_double),
+                ("coef", C.c_float), ("pad_", C.c_int32)]
+
+
 def adamw_cfg(adamw, step):
     return AdamWCfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
                     adamw.max_norm, int(step))
@@ -86,6 +93,10 @@ class Oracle:
                                     C.c_double, P, C.c_int32]
         L.orc_ledger_bytes.argtypes = [C.c_int32, C.c_double, C.c_int32, P]
         L.orc_ledger_bytes.restype = C.c_double
+        L.orc_mesh_allreduce_mean.argtypes = [P, C.c_int32, C.c_int64, C.c_int32, C.c_int32, P,
+                                              P, P]
+        L.orc_mesh_zero_step.argtypes = [P, P, C.c_int32, C.c_int64, C.c_int32, C.c_int32, P, P,
+                                         P, P, P, P, P]
         L.orc_sum.argtypes = [P, C.c_int64]
         L.orc_sum.restype = C.c_double
         L.orc_stage_traffic.argtypes = [C.c_int32, C.c_int32, C.c_int64, P, P]
@@ -182,6 +193,31 @@ class Oracle:
         """The oracle's compensated sum of doubles (e.g. per-bucket sums of squares)."""
         a = np.ascontiguousarray(x, np.float64)
         return self.L.orc_sum(_p(a), len(a))
+
+    def mesh_allreduce_mean(self, sizes, bucket_bytes, R, S, grads_u16):
+        """Mean all-reduce on an R x S mesh (rank = g*S + s). Returns (out, mean, stats)."""
+        s = _i64(sizes)
+        g = np.array(grads_u16, dtype=np.uint16, copy=True, order="C")
+        mean = np.zeros(g.shape[1], np.float32)
+        st = MeshStats()
+        _check(self.L.orc_mesh_allreduce_mean(_p(s), len(s), int(bucket_bytes), int(R), int(S),
+                                              _p(g), _p(mean), C.byref(st)), "mesh allreduce")
+        return g, mean, st
+
+    def mesh_zero_step(self, sizes, decay, bucket_bytes, R, S, grads_u16, master, m, v, cfg):
+        """ZeRO-2 step on an R x S mesh. Returns (params, master, m, v, stats)."""
+        s = _i64(sizes)
+        d = np.ascontiguousarray(decay, dtype=np.uint8)
+        g = np.ascontiguousarray(grads_u16, dtype=np.uint16)
+        master = np.array(master, dtype=np.float32, copy=True)
+        m = np.array(m, dtype=np.float32, copy=True)
+        v = np.array(v, dtype=np.float32, copy=True)
+        params = np.zeros_like(g)
+        st = MeshStats()
+        _check(self.L.orc_mesh_zero_step(_p(s), _p(d), len(s), int(bucket_bytes), int(R), int(S),
+                                         _p(g), _p(master), _p(m), _p(v), _p(params), C.byref(cfg),
+                                         C.byref(st)), "mesh zero step")
+        return params, master, m, v, st
 
     def ledger_bytes(self, stage, psi, P, comp=(2, 2, 4, 4, 4)):
         c = np.asarray(comp, np.float64)

@@ -187,6 +187,28 @@ void ring_all_gather(int P, int64_t len, uint16_t* Y, int64_t* sent, int64_t* st
   }
 }
 
+// The same ring all-gather carrying fp32 partial results (used by the
+// cross-group all-reduce of the hybrid mesh).
+void ring_all_gather_f32(int P, int64_t len, float* Y, int64_t* sent, int64_t* steps) {
+  const int64_t S = len / P;
+  std::vector<float> msg(static_cast<size_t>(P) * S);
+  for (int s = 0; s + 1 < P; ++s) {
+    for (int r = 0; r < P; ++r) {
+      const int c = mod(r - s, P);
+      std::memcpy(&msg[static_cast<size_t>(r) * S], Y + static_cast<size_t>(r) * len + c * S,
+                  sizeof(float) * S);
+      sent[r] += S;
+    }
+    for (int r = 0; r < P; ++r) {
+      const int dst = (r + 1) % P;
+      const int c = mod(r - s, P);
+      std::memcpy(Y + static_cast<size_t>(dst) * len + c * S, &msg[static_cast<size_t>(r) * S],
+                  sizeof(float) * S);
+    }
+    ++*steps;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -562,6 +584,212 @@ int orc_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t
       st->replicas_equal &= equal[b];
     }
   }
+  return 0;
+}
+
+// ---- hybrid sharding on an R x S mesh -------------------------------------------
+// HYBRID_SHARD: shard within a group, data-parallel all-reduce across groups
+// ("4.1 Data parallelism in depth", sec. 6.3 table and tip; "Distributed Training:
+// Data Parallel, Model Parallel and FSDP Strategies", FSDP2 DeviceMesh
+// mesh_shape=(2, 4) with dims ("replicate", "shard"), and "Selecting and Tuning":
+// shard within a group, replicate across groups via data-parallel all-reduce;
+// "Data Parallelism: DDP, ZeRO and FSDP", "Hybrid sharding").  Rank (g, s) =
+// g*S + s.  Per bucket, literally:
+//   1. in every group g, a ring reduce-scatter over its S ranks: rank (g, s)
+//      holds the group's sum of shard s (S equal shards);
+//   2. for every shard s, a ring all-reduce over the R ranks (0..R-1, s):
+//      reduce-scatter over R sub-chunks of the shard, then all-gather;
+//   3. mean = sum / P; rank (g, s) updates shard s (every group the same);
+//   4. in every group, a ring all-gather of the bf16 shards.
+// rs_sent counts steps 1 and the cross reduce-scatter, ag_sent the cross
+// all-gather and step 4; cross_sent only the cross-group (step 2) traffic.
+struct orc_mesh_stats {
+  int64_t rs_sent[kMaxRanks];
+  int64_t ag_sent[kMaxRanks];
+  int64_t cross_sent[kMaxRanks];
+  int32_t groups_equal;     // 1 when every group's updated shard state agreed
+  int32_t replicas_equal;   // 1 when all P replicas are bit-identical afterwards
+  double sumsq;
+  double norm;
+  float coef;
+  int32_t pad_;
+};
+
+}  // extern "C"
+
+namespace {
+
+// Steps 1-2 for one bucket: X [P][len] fp32 per rank -> the total of every slot
+// as held by rank (g, s) after the cross all-reduce (identical for all g).
+void mesh_reduce(int R, int S, int64_t len, std::vector<float>& X, std::vector<float>& total,
+                 int64_t* rs_sent, int64_t* ag_sent, int64_t* cross_sent) {
+  const int P = R * S;
+  const int64_t sh = len / S;  // shard length
+  int64_t steps = 0;
+  std::vector<float> G(static_cast<size_t>(S) * len);
+  for (int g = 0; g < R; ++g) {  // 1. ring reduce-scatter inside group g
+    std::memcpy(G.data(), X.data() + static_cast<size_t>(g) * S * len, sizeof(float) * S * len);
+    int64_t sent[kMaxRanks] = {0};
+    ring_reduce_scatter(S, len, G.data(), sent, &steps);
+    std::memcpy(X.data() + static_cast<size_t>(g) * S * len, G.data(), sizeof(float) * S * len);
+    for (int s = 0; s < S; ++s) rs_sent[g * S + s] += sent[s];
+  }
+  total.assign(len, 0.0f);
+  std::vector<float> C(static_cast<size_t>(R) * sh);
+  for (int s = 0; s < S; ++s) {  // 2. ring all-reduce of shard s across the groups
+    for (int g = 0; g < R; ++g)
+      std::memcpy(C.data() + static_cast<size_t>(g) * sh,
+                  X.data() + static_cast<size_t>(g * S + s) * len + s * sh, sizeof(float) * sh);
+    int64_t sent_rs[kMaxRanks] = {0}, sent_ag[kMaxRanks] = {0};
+    ring_reduce_scatter(R, sh, C.data(), sent_rs, &steps);
+    ring_all_gather_f32(R, sh, C.data(), sent_ag, &steps);
+    for (int g = 0; g < R; ++g) {
+      rs_sent[g * S + s] += sent_rs[g];
+      ag_sent[g * S + s] += sent_ag[g];
+      cross_sent[g * S + s] += sent_rs[g] + sent_ag[g];
+    }
+    for (int g = 1; g < R; ++g)  // every group now holds the same totals
+      if (std::memcmp(C.data(), C.data() + static_cast<size_t>(g) * sh, sizeof(float) * sh))
+        total.assign(len, std::nanf(""));
+    std::memcpy(total.data() + s * sh, C.data(), sizeof(float) * sh);
+  }
+  (void)P;
+}
+
+// Step 4: ring all-gather of bf16 shards inside every group; Y [P][len].
+void mesh_all_gather(int R, int S, int64_t len, std::vector<uint16_t>& Y, int64_t* ag_sent) {
+  int64_t steps = 0;
+  std::vector<uint16_t> G(static_cast<size_t>(S) * len);
+  for (int g = 0; g < R; ++g) {
+    std::memcpy(G.data(), Y.data() + static_cast<size_t>(g) * S * len, 2 * S * len);
+    int64_t sent[kMaxRanks] = {0};
+    ring_all_gather(S, len, G.data(), sent, &steps);
+    std::memcpy(Y.data() + static_cast<size_t>(g) * S * len, G.data(), 2 * S * len);
+    for (int s = 0; s < S; ++s) ag_sent[g * S + s] += sent[s];
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// Mean all-reduce on the R x S mesh (HYBRID with NO_SHARD state): every replica
+// ends with bf16(mean).  grads [P][n_params] in/out, mean_out nullable.
+int orc_mesh_allreduce_mean(const int64_t* sizes, int32_t n, int64_t bucket_bytes, int32_t R,
+                            int32_t S, uint16_t* grads, float* mean_out, orc_mesh_stats* st) {
+  const int P = R * S;
+  Plan pl;
+  if (R < 1 || S < 1 || !make_plan(sizes, n, bucket_bytes, P, &pl)) return -1;
+  int64_t n_params = 0;
+  const std::vector<int64_t> base = tensor_bases(sizes, n, &n_params);
+  orc_mesh_stats acc;
+  std::memset(&acc, 0, sizeof(acc));
+  acc.groups_equal = 1;
+  acc.replicas_equal = 1;
+  for (size_t b = 0; b < pl.b_off.size(); ++b) {
+    const int64_t len = pl.b_len[b], sh = len / S;
+    std::vector<float> X, total;
+    pack_bucket(pl, static_cast<int>(b), sizes, base, n_params, grads, X);
+    mesh_reduce(R, S, len, X, total, acc.rs_sent, acc.ag_sent, acc.cross_sent);
+    std::vector<uint16_t> Y(static_cast<size_t>(P) * len, 0);
+    for (int g = 0; g < R; ++g)
+      for (int s = 0; s < S; ++s)
+        for (int64_t i = s * sh; i < (s + 1) * sh; ++i)
+          Y[static_cast<size_t>(g * S + s) * len + i] = f32_to_bf16_rne(total[i] / static_cast<float>(P));
+    mesh_all_gather(R, S, len, Y, acc.ag_sent);
+    for (int r = 1; r < P; ++r)
+      if (std::memcmp(Y.data(), Y.data() + static_cast<size_t>(r) * len, 2 * len)) acc.replicas_equal = 0;
+    for (int t : pl.b_tensors[b]) {
+      const int64_t o = pl.t_off[t] - pl.b_off[b];
+      for (int r = 0; r < P; ++r)
+        std::memcpy(grads + static_cast<size_t>(r) * n_params + base[t],
+                    Y.data() + static_cast<size_t>(r) * len + o, 2 * sizes[t]);
+      if (mean_out)
+        for (int64_t j = 0; j < sizes[t]; ++j) mean_out[base[t] + j] = total[o + j] / static_cast<float>(P);
+    }
+  }
+  if (st) *st = acc;
+  return 0;
+}
+
+// The ZeRO-2 step on the R x S mesh: every group's rank (g, s) updates shard s
+// of its own copy of master/m/v (they must agree across groups) and the bf16
+// parameters are all-gathered inside every group.  Clip norm over the mean,
+// as in orc_zero_step.
+int orc_mesh_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t bucket_bytes,
+                       int32_t R, int32_t S, const uint16_t* grads, float* master, float* m,
+                       float* v, uint16_t* params, const orc_adamw* cfg, orc_mesh_stats* st) {
+  const int P = R * S;
+  Plan pl;
+  if (R < 1 || S < 1 || !make_plan(sizes, n, bucket_bytes, P, &pl) || cfg->step < 1) return -1;
+  int64_t n_params = 0;
+  const std::vector<int64_t> base = tensor_bases(sizes, n, &n_params);
+  const int nb = static_cast<int>(pl.b_off.size());
+  orc_mesh_stats acc;
+  std::memset(&acc, 0, sizeof(acc));
+  acc.groups_equal = 1;
+  acc.replicas_equal = 1;
+  std::vector<std::vector<float>> means(nb);
+  CompensatedSum total_sq;
+  for (int b = 0; b < nb; ++b) {
+    std::vector<float> X, total;
+    pack_bucket(pl, b, sizes, base, n_params, grads, X);
+    mesh_reduce(R, S, pl.b_len[b], X, total, acc.rs_sent, acc.ag_sent, acc.cross_sent);
+    means[b].resize(pl.b_len[b]);
+    for (int64_t i = 0; i < pl.b_len[b]; ++i) means[b][i] = total[i] / static_cast<float>(P);
+    total_sq.add(sumsq_of(means[b]));
+  }
+  acc.sumsq = total_sq.value();
+  acc.coef = clip_coef(acc.sumsq, cfg->max_norm, &acc.norm);
+  const AdamScalars sc = adam_scalars(*cfg);
+  for (int b = 0; b < nb; ++b) {
+    const int64_t len = pl.b_len[b], sh = len / S;
+    std::vector<int32_t> slot_t(len, -1);
+    std::vector<int64_t> slot_j(len, 0);
+    for (int t : pl.b_tensors[b]) {
+      const int64_t o = pl.t_off[t] - pl.b_off[b];
+      for (int64_t j = 0; j < sizes[t]; ++j) {
+        slot_t[o + j] = t;
+        slot_j[o + j] = j;
+      }
+    }
+    std::vector<uint16_t> Y(static_cast<size_t>(P) * len, 0);
+    for (int s = 0; s < S; ++s) {
+      for (int64_t i = s * sh; i < (s + 1) * sh; ++i) {
+        const int t = slot_t[i];
+        const int64_t e = t >= 0 ? base[t] + slot_j[i] : -1;
+        float first[3] = {0, 0, 0};
+        for (int g = 0; g < R; ++g) {  // each group's owner of shard s, own state copy
+          float th = t >= 0 ? master[e] : 0.0f, mm = t >= 0 ? m[e] : 0.0f, vv = t >= 0 ? v[e] : 0.0f;
+          adamw_element(means[b][i] * acc.coef, th, mm, vv, t >= 0 && decay[t] != 0, sc);
+          if (g == 0) {
+            first[0] = th;
+            first[1] = mm;
+            first[2] = vv;
+          } else if (std::memcmp(first, &th, 4) || std::memcmp(first + 1, &mm, 4) ||
+                     std::memcmp(first + 2, &vv, 4)) {
+            acc.groups_equal = 0;
+          }
+          Y[static_cast<size_t>(g * S + s) * len + i] = f32_to_bf16_rne(th);
+        }
+        if (t >= 0) {
+          master[e] = first[0];
+          m[e] = first[1];
+          v[e] = first[2];
+        }
+      }
+    }
+    mesh_all_gather(R, S, len, Y, acc.ag_sent);
+    for (int r = 1; r < P; ++r)
+      if (std::memcmp(Y.data(), Y.data() + static_cast<size_t>(r) * len, 2 * len)) acc.replicas_equal = 0;
+    for (int t : pl.b_tensors[b]) {
+      const int64_t o = pl.t_off[t] - pl.b_off[b];
+      for (int r = 0; r < P; ++r)
+        std::memcpy(params + static_cast<size_t>(r) * n_params + base[t],
+                    Y.data() + static_cast<size_t>(r) * len + o, 2 * sizes[t]);
+    }
+  }
+  if (st) *st = acc;
   return 0;
 }
 

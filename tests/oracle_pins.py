@@ -464,6 +464,72 @@ def pin_zero_multi_step_state(orc):
         assert (mst[i], m[i], v[i]) == tuple(np.float32(x) for x in ref[k])
 
 
+# --------------------------------------------------------------------------- hybrid mesh
+def pin_mesh_degenerate_equals_flat(orc):
+    """An R x S mesh with R = 1 or S = 1 is the flat ring over P = R*S ranks."""
+    rng = np.random.default_rng(41)
+    sizes, cap = [13, 900, 2600, 77], 4096
+    for P in (2, 4, 8):
+        g = rand_bf16(rng, (P, sum(sizes)), 1e-3)
+        flat, mflat, _ = orc.allreduce_mean(sizes, cap, P, g)
+        for R, S in ((1, P), (P, 1)):
+            out, mean, st = orc.mesh_allreduce_mean(sizes, cap, R, S, g)
+            assert np.array_equal(out, flat) and np.array_equal(mean, mflat), (P, R, S)
+            assert st.replicas_equal == 1
+
+
+def pin_mesh_order(orc):
+    """Hierarchical association: for shard 0 / sub-chunk 0 of a (2, 2) mesh the
+    total is (g[1,1] + g[1,0]) + (g[0,1] + g[0,0]): with 2^24, 1, -2^24, 1 it is 1,
+    where the flat ring's fold g1 + g2 + g3 + g0 gives 2."""
+    P, R, S = 4, 2, 2
+    n = 16 * P                                    # one bucket, shard = 32, sub-chunk = 16
+    vals = {(1, 1): 2.0 ** 24, (1, 0): 1.0, (0, 1): -(2.0 ** 24), (0, 0): 1.0}
+    X = np.zeros((P, n), np.float32)
+    for (gi, si), val in vals.items():
+        X[gi * S + si, :16] = val
+    g16 = bf16_bits(X.ravel()).reshape(P, n)
+    _, mean, _ = orc.mesh_allreduce_mean([n], 1 << 20, R, S, g16)
+    _, mflat, _ = orc.allreduce_mean([n], 1 << 20, P, g16)
+    assert mean[0] == 1.0 / P and mflat[0] == 2.0 / P
+
+
+def pin_mesh_traffic(orc):
+    """Per rank, per bucket of M elements: the in-group ring moves (S-1)/S*M twice,
+    the cross-group all-reduce of one shard 2(R-1)/R * M/S; only the latter crosses
+    groups ("4.1 Data parallelism in depth", sec. 5.2 ring volume, applied per level)."""
+    rng = np.random.default_rng(43)
+    for R, S in ((2, 4), (4, 2), (2, 2), (3, 2)):
+        P = R * S
+        M = 16 * P * 5
+        g = rand_bf16(rng, (P, M), 1e-3)
+        _, _, st = orc.mesh_allreduce_mean([M], 1 << 20, R, S, g)
+        for r in range(P):
+            assert Fraction(st.cross_sent[r]) == Fraction(2 * (R - 1) * M, R * S)
+            assert Fraction(st.rs_sent[r] + st.ag_sent[r]) == \
+                Fraction(2 * (S - 1) * M, S) + Fraction(2 * (R - 1) * M, R * S)
+        flat_cross = Fraction(2 * (P - 1) * M, P)      # a flat ring over all P ranks
+        assert Fraction(st.cross_sent[0]) < flat_cross
+
+
+def pin_mesh_zero_step(orc):
+    """Every group's owner of a shard applies the same update; all replicas equal;
+    the (1, P) mesh is the flat step bit for bit, a (2, P/2) mesh within fp32
+    reassociation of it."""
+    rng = np.random.default_rng(47)
+    P = 8
+    sizes, cap, g, master = _zero_case(rng, P, sizes=(3, 1000, 655, 2621, 40), cap=4096)
+    n = sum(sizes)
+    z = np.zeros(n, np.float32)
+    cfg = cfg_struct(1, max_norm=0.5)
+    pf, mf, _, _, _, stf = orc.zero_step(sizes, [1] * 5, cap, P, g, master, z, z, cfg)
+    p1, m1, _, _, st1 = orc.mesh_zero_step(sizes, [1] * 5, cap, 1, P, g, master, z, z, cfg)
+    assert np.array_equal(p1, pf) and np.array_equal(m1, mf) and st1.coef == stf.coef
+    p2, m2, _, _, st2 = orc.mesh_zero_step(sizes, [1] * 5, cap, 2, 4, g, master, z, z, cfg)
+    assert st2.groups_equal == 1 and st2.replicas_equal == 1
+    assert np.all(np.abs(m2 - mf) <= 1e-6 * np.abs(mf) + 1e-9)
+
+
 # --------------------------------------------------------------------------- identity
 def lsq_data():
     from workloads.gen import small_ints

@@ -46,6 +46,11 @@ MUTANTS = {
     "bf16_truncate": ("u += 0x7fffu + lsb;", "(void)lsb;"),
     "lsq_sum_not_mean": ("g_bar[f] = acc / N;", "g_bar[f] = acc;"),
     "ledger_zero2_keeps_grads": ("shard_grads = stage >= 2", "shard_grads = stage >= 3"),
+    "mesh_rank_layout": ("X.data() + static_cast<size_t>(g * S + s) * len + s * sh, sizeof(float) * sh);",
+                         "X.data() + static_cast<size_t>(s * R + g) * len + s * sh, sizeof(float) * sh);"),
+    "mesh_no_cross_reduce": ("    ring_reduce_scatter(R, sh, C.data(), sent_rs, &steps);\n",
+                             "    (void)sent_rs;\n"),
+    "mesh_cross_ag_skipped": ("    ring_all_gather_f32(R, sh, C.data(), sent_ag, &steps);\n", "    (void)sent_ag;\n"),
     "zero3_one_gather": ("    ring_all_gather(P, M, Y.data(), sent, steps);\n    ring_all_gather(P, M, Y.data(), sent, steps);\n",
                          "    ring_all_gather(P, M, Y.data(), sent, steps);\n"),
 }
