@@ -240,7 +240,8 @@ def run_gpu(args, rank, local, world):
 
     torch.cuda.set_device(local)
     wl = workload_by_name(args.workload)
-    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    mesh = tuple(int(x) for x in args.mesh.split(",")) if args.mesh else None
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay, mesh=mesh)
     P, L, stride = plan.P, plan.L, plan.stride
     off = plan.tensor_offsets()
     ws = plan.new_workspace()
@@ -350,6 +351,7 @@ def run_gpu(args, rank, local, world):
             "bucket_bytes": wl.bucket_bytes,
             "clip_max_norm": wl.adamw.max_norm if zero else None,
             "parallelism": f"{P} virtual ranks per GPU x {world} GPU(s), independent replicas",
+            "mesh": f"{plan.info.R}x{plan.info.S} (replicate x shard)",
             "l2": "inputs larger than L2 (no flush): "
                   f"{step_bytes_pp * n_params / 1e9:.1f} GB moved per step vs 0.13 GB L2",
         },
@@ -579,6 +581,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--mesh", default="",
+                    help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
     ap.add_argument("--streamed", action="store_true",
                     help="measure the overlap of per-bucket sync with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=4096, help="GEMM rows of the synthetic backward")

@@ -32,7 +32,8 @@ class DPError(RuntimeError):
 class PlanInfo(C.Structure):
     _fields_ = [("n_params", C.c_int64), ("padded_len", C.c_int64), ("replica_stride", C.c_int64),
                 ("bucket_bytes", C.c_int64), ("n_tensors", C.c_int32), ("n_buckets", C.c_int32),
-                ("P", C.c_int32), ("tile_elems", C.c_int32), ("n_tiles", C.c_int64),
+                ("P", C.c_int32), ("tile_elems", C.c_int32), ("R", C.c_int32), ("S", C.c_int32),
+                ("pad_", C.c_int32), ("n_tiles", C.c_int64),
                 ("table_bytes", C.c_int64), ("workspace_bytes", C.c_int64)]
 
 
@@ -56,6 +57,7 @@ def lib():
         sig = {
             "dp_plan_buckets": [vp, vp, i32, i64, i32, vp],
             "dp_plan_buckets_ex": [vp, vp, i32, i64, i32, i64, vp],
+            "dp_plan_buckets_mesh": [vp, vp, i32, i64, i32, i32, i64, vp],
             "dp_plan_info": [vp, vp],
             "dp_plan_tensor": [vp, i32, vp, vp],
             "dp_plan_bucket": [vp, i32, vp, vp, vp],
@@ -124,7 +126,8 @@ def _need(t, dtype, numel, name):
 class Plan:
     """A bucket plan (host object of the library)."""
 
-    def __init__(self, sizes, bucket_bytes, P, decay=None, replica_stride=0):
+    def __init__(self, sizes, bucket_bytes, P, decay=None, replica_stride=0, mesh=None):
+        """mesh=(R, S) with R*S == P gives a hybrid R x S plan (R groups of S shards)."""
         sizes = [int(s) for s in sizes]
         n = len(sizes)
         arr = (C.c_int64 * max(n, 1))(*sizes)
@@ -132,8 +135,15 @@ class Plan:
         if decay is not None:
             dec = (C.c_uint8 * max(n, 1))(*[1 if d else 0 for d in decay])
         h = C.c_void_p()
-        _check(lib().dp_plan_buckets_ex(arr, dec, n, int(bucket_bytes), int(P), int(replica_stride),
-                                        C.byref(h)))
+        if mesh is None:
+            _check(lib().dp_plan_buckets_ex(arr, dec, n, int(bucket_bytes), int(P),
+                                            int(replica_stride), C.byref(h)))
+        else:
+            R, S = (int(x) for x in mesh)
+            if R * S != int(P):
+                raise ValueError(f"mesh {mesh} does not multiply to P={P}")
+            _check(lib().dp_plan_buckets_mesh(arr, dec, n, int(bucket_bytes), R, S,
+                                              int(replica_stride), C.byref(h)))
         self._h = h
         info = PlanInfo()
         _check(lib().dp_plan_info(h, C.byref(info)))

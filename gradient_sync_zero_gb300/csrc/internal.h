@@ -24,7 +24,7 @@ struct TileDesc {
   int64_t v0;      // first vector (flat vector index)
   int64_t bvoff;   // first vector of the tile's bucket
   int32_t nvec;    // vectors in the tile
-  int32_t svec;    // shard length of the bucket, in vectors (>= 1)
+  int32_t svec;    // shard length of the bucket (len / S), in vectors (>= 2)
   int32_t bucket;
   int32_t pad_;
 };
@@ -39,12 +39,13 @@ struct DevHeader {
   int64_t n_tiles;
   int32_t n_buckets;
   int32_t P;
+  int32_t R, S;
   int64_t off_tiles;      // byte offsets of the arrays inside the workspace
   int64_t off_btile;      // int64 [n_buckets+1]: first tile of each bucket
   int64_t off_decay;      // uint32 [ceil(n_vec/32)]
   int64_t off_sumsq;      // float2 [n_tiles]: per-tile sum of mean^2, hi + lo (scratch)
   int64_t off_stage;      // float [L] (scratch)
-  int64_t reserved_[4];
+  int64_t reserved_[3];
   // ---- written by kernels ----
   double norm2;
   double norm;
@@ -56,6 +57,7 @@ static_assert(sizeof(DevHeader) % 64 == 0, "header keeps the arrays aligned");
 
 struct Plan {
   int32_t P = 0;
+  int32_t R = 1, S = 0;   // mesh: R groups x S shard ranks (P = R * S)
   int64_t bucket_bytes = 0;
   int64_t n_params = 0;
   int64_t L = 0;

@@ -35,6 +35,8 @@ struct KCommon {
   int64_t tile_begin;
   int64_t tile_end;
   int32_t P;             // rank count (used by the runtime-P instantiation)
+  int32_t R;             // mesh: replicate groups (1 = flat ring)
+  int32_t S;             // mesh: shard ranks per group (P = R * S)
 };
 
 // ---- 256-bit streaming accesses (sm_100-family ld/st .v8.b32) ----
@@ -166,6 +168,82 @@ __device__ __forceinline__ void ring_mean16(const uint8_t* g, int64_t stride_byt
     const float fp = static_cast<float>(np);
 #pragma unroll
     for (int e = 0; e < 16; ++e) acc[e] = __fdiv_rn(acc[e], fp);
+  }
+}
+
+// Hybrid R x S mesh: the sum of element i of shard s in sub-chunk j is
+//   sum over groups g = j+1, ..., j (mod R) of
+//     [sum over members s' = s+1, ..., s (mod S) of grad(g*S + s')[i]]
+// — a ring reduce-scatter inside each group, then a ring all-reduce of the shard
+// across groups ("4.1 Data parallelism in depth", sec. 6.3 HYBRID_SHARD).  The P
+// blocks are loaded in that order (8 in flight per thread) and folded left to
+// right, the inner sum restarting at each group boundary.
+template <int P>
+__device__ __forceinline__ void mesh_mean16(const uint8_t* g, int64_t stride_bytes,
+                                            int64_t byte_off, int s, int j, int R, int S,
+                                            int p_rt, float (&acc)[16]) {
+  const int np = P > 0 ? P : p_rt;
+  float inner[16];
+  int gi = 0, si = 0;
+  int grp = (j + 1 == R) ? 0 : j + 1;    // current group in fold order
+  int mem = (s + 1 == S) ? 0 : s + 1;    // current member in fold order
+#pragma unroll 1
+  for (int k0 = 0; k0 < np; k0 += 8) {
+    Blk x[8];
+    int gg = grp, mm = mem, sii = si;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k0 + k >= np) break;
+      x[k] = ld_blk(g + (gg * S + mm) * stride_bytes + byte_off);
+      if (++sii == S) {
+        sii = 0;
+        gg = (gg + 1 == R) ? 0 : gg + 1;
+      }
+      mm = (mm + 1 == S) ? 0 : mm + 1;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k0 + k >= np) break;
+      float t[16];
+      unpack16(x[k], t);
+      if (si == 0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) inner[e] = t[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) inner[e] = __fadd_rn(inner[e], t[e]);
+      }
+      if (++si == S) {
+        si = 0;
+        if (gi == 0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = inner[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = __fadd_rn(acc[e], inner[e]);
+        }
+        ++gi;
+      }
+    }
+    grp = gg;
+    mem = mm;
+  }
+  const float fp = static_cast<float>(np);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = __fdiv_rn(acc[e], fp);
+}
+
+// The mean of block b for its owner, flat ring or hybrid mesh.  s = shard index
+// in the bucket (the owner rank on a flat ring).
+template <int P, bool MESH>
+__device__ __forceinline__ void block_mean16(const KCommon& k, const uint8_t* g, int64_t b,
+                                             const TileDesc& d, int s, float (&acc)[16]) {
+  if constexpr (!MESH) {
+    ring_mean16<P>(g, k.stride_bytes, 32 * b, s, k.P, acc);
+  } else {
+    const uint32_t within = static_cast<uint32_t>(2 * b - d.bvoff) % static_cast<uint32_t>(d.svec);
+    const int j = static_cast<int>(within / (static_cast<uint32_t>(d.svec) / k.R));
+    mesh_mean16<P>(g, k.stride_bytes, 32 * b, s, j, k.R, k.S, k.P, acc);
   }
 }
 
@@ -373,6 +451,21 @@ __device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
     for (int j = threadIdx.x; j < nblk; j += kThreads) {
       const int64_t b = b0 + j;
       f(tile, b, owner_of(d, 2 * b));
+    }
+  }
+}
+
+// Same loop, giving the body the tile descriptor: f(desc, block b, owner c).
+template <class F>
+__device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
+  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
+    const TileDesc d = load_tile(k, tile);
+    const int nblk = d.nvec >> 1;
+    const int64_t b0 = d.v0 >> 1;
+#pragma unroll 1
+    for (int j = threadIdx.x; j < nblk; j += kThreads) {
+      const int64_t b = b0 + j;
+      f(d, b, owner_of(d, 2 * b));
     }
   }
 }

@@ -20,7 +20,7 @@ namespace dps {
 // ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
 // the exact sum.  Partials are per tile, so the norm does not depend on the grid
 // size or on how the bucket range is split into launches.
-template <int P>
+template <int P, bool MESH>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint8_t* g,
                                                              float* mean, int sumsq) {
   if (!plan_ok(k)) return;
@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
     for (int j = threadIdx.x; j < nblk; j += kThreads) {
       const int64_t b = b0 + j;
       float acc[16];
-      ring_mean16<P>(g, k.stride_bytes, 32 * b, owner_of(d, 2 * b), k.P, acc);
+      block_mean16<P, MESH>(k, g, b, d, owner_of(d, 2 * b), acc);
       st_f16(mean, b, acc);
       if (sumsq) {
 #pragma unroll
@@ -47,12 +47,12 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
 
 // Fused mean all-reduce in place: sum in ring order, 1/P, bf16, written back to
 // every replica (the all-gather of the reduced shards).
-template <int P>
+template <int P, bool MESH>
 __global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint8_t* g) {
   if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int c) {
+  for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
     float acc[16];
-    ring_mean16<P>(g, k.stride_bytes, 32 * b, c, k.P, acc);
+    block_mean16<P, MESH>(k, g, b, d, c, acc);
     store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(acc), k.P);
   });
 }
@@ -105,17 +105,23 @@ __global__ void __launch_bounds__(kFinalThreads) k_norm_finalize(KCommon k, doub
 int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
-    constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_reduce_scatter<P>, k, static_cast<const uint8_t*>(grads), mean,
-                        sumsq ? 1 : 0);
+    return with_mesh(L.plan, [&](auto mc) {
+      constexpr int P = decltype(pc)::value;
+      constexpr bool M = decltype(mc)::value;
+      return launch_tiles(L, k_reduce_scatter<P, M>, k, static_cast<const uint8_t*>(grads), mean,
+                          sumsq ? 1 : 0);
+    });
   });
 }
 
 int launch_allreduce(const Launch& L, void* grads) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
-    constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_allreduce<P>, k, static_cast<uint8_t*>(grads));
+    return with_mesh(L.plan, [&](auto mc) {
+      constexpr int P = decltype(pc)::value;
+      constexpr bool M = decltype(mc)::value;
+      return launch_tiles(L, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
+    });
   });
 }
 

@@ -36,7 +36,9 @@ __global__ void __launch_bounds__(kThreads)
     st_f16(master, b, th);
     st_f16(m, b, mm);
     st_f16(v, b, vv);
-    st_blk(params + c * k.stride_bytes + 32 * b, pack16_rne(th));
+    // the owner of shard c in every group (rank c on a flat ring)
+    const Blk val = pack16_rne(th);
+    for (int g = 0; g < k.R; ++g) st_blk(params + (g * k.S + c) * k.stride_bytes + 32 * b, val);
   });
 }
 
@@ -44,9 +46,10 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads) k_all_gather(KCommon k, uint8_t* params) {
   if (!plan_ok(k)) return;
   for_each_block(k, [&](int64_t, int64_t b, int c) {
+    // ranks (g, c) own shard c; every other rank of each group receives it
     const Blk val = ld_blk(params + c * k.stride_bytes + 32 * b);
     for (int r = 0; r < k.P; ++r)
-      if (r != c) st_blk(params + r * k.stride_bytes + 32 * b, val);
+      if (r % k.S != c) st_blk(params + r * k.stride_bytes + 32 * b, val);
   });
 }
 
@@ -63,14 +66,14 @@ __global__ void __launch_bounds__(kThreads) k_broadcast(KCommon k, uint8_t* para
 // The whole ZeRO-1/2 step without clipping, one pass.  The replica blocks are
 // loaded and folded first, then the fp32 state is loaded, which bounds the live
 // registers to one of the two groups.
-template <int P>
+template <int P, bool MESH>
 __global__ void __launch_bounds__(kThreads)
     k_zero_fused(KCommon k, const uint8_t* grads, uint8_t* params, float* master, float* m,
                  float* v, AdamScalars s) {
   if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int c) {
+  for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
     float g[16];
-    ring_mean16<P>(grads, k.stride_bytes, 32 * b, c, k.P, g);
+    block_mean16<P, MESH>(k, grads, b, d, c, g);
     float th[16], mm[16], vv[16];
     ld_f16(master, b, th);
     ld_f16(m, b, mm);
@@ -213,9 +216,12 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
                       float* v, const AdamScalars& s) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
-    constexpr int P = decltype(pc)::value;
-    return launch_tiles(L, k_zero_fused<P>, k, static_cast<const uint8_t*>(grads),
-                        static_cast<uint8_t*>(params), master, m, v, s);
+    return with_mesh(L.plan, [&](auto mc) {
+      constexpr int P = decltype(pc)::value;
+      constexpr bool M = decltype(mc)::value;
+      return launch_tiles(L, k_zero_fused<P, M>, k, static_cast<const uint8_t*>(grads),
+                          static_cast<uint8_t*>(params), master, m, v, s);
+    });
   });
 }
 

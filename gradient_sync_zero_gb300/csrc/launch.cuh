@@ -27,6 +27,8 @@ inline KCommon make_common(const Launch& L) {
   k.tile_begin = L.tile_begin;
   k.tile_end = L.tile_end;
   k.P = L.plan->P;
+  k.R = L.plan->R;
+  k.S = L.plan->S;
   return k;
 }
 
@@ -97,6 +99,12 @@ int with_P(int P, F&& f) {
     case 16: return f(std::integral_constant<int, 16>{});
     default: return f(std::integral_constant<int, 0>{});
   }
+}
+
+// Flat ring or hybrid mesh instantiation.
+template <class F>
+int with_mesh(const Plan* pl, F&& f) {
+  return pl->R > 1 ? f(std::true_type{}) : f(std::false_type{});
 }
 
 }  // namespace dps

@@ -92,7 +92,7 @@ void build_tiles(Plan& pl) {
     pl.b_tile0[b] = static_cast<int64_t>(pl.tiles.size());
     const int64_t bv = pl.b_off[b] / kVecElems;
     const int64_t nv = pl.b_len[b] / kVecElems;
-    const int32_t sv = static_cast<int32_t>(nv / pl.P);
+    const int32_t sv = static_cast<int32_t>(nv / pl.S);
     for (int64_t v = 0; v < nv; v += kTileVec) {
       TileDesc d{};
       d.v0 = bv + v;
@@ -125,6 +125,8 @@ void build_image(Plan& pl) {
   h.n_tiles = static_cast<int64_t>(pl.tiles.size());
   h.n_buckets = static_cast<int32_t>(pl.b_off.size());
   h.P = pl.P;
+  h.R = pl.R;
+  h.S = pl.S;
   int64_t off = round_up(sizeof(DevHeader), 256);
   h.off_tiles = off;
   off = round_up(off + h.n_tiles * static_cast<int64_t>(sizeof(TileDesc)), 256);
@@ -156,19 +158,24 @@ using namespace dps;
 
 extern "C" {
 
-int dp_plan_buckets_ex(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
-                       int64_t bucket_bytes, int32_t P, int64_t replica_stride, dp_plan** out) {
+int dp_plan_buckets_mesh(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
+                         int64_t bucket_bytes, int32_t R, int32_t S, int64_t replica_stride,
+                         dp_plan** out) {
   clear_error();
   if (!out) return fail(DP_EINVAL, "dp_plan_buckets: out is NULL");
   *out = nullptr;
   if (n_tensors < 0 || (n_tensors > 0 && !sizes))
     return fail(DP_EINVAL, "dp_plan_buckets: bad tensor list");
-  if (P < 1 || P > kMaxP) return fail(DP_EINVAL, "dp_plan_buckets: P must be in 1..64");
+  if (R < 1 || S < 1 || static_cast<int64_t>(R) * S > kMaxP)
+    return fail(DP_EINVAL, "dp_plan_buckets: need R, S >= 1 and P = R*S in 1..64");
+  const int32_t P = R * S;
   if (bucket_bytes < 2) return fail(DP_EINVAL, "dp_plan_buckets: bucket_bytes must be >= 2");
   Plan* pl = new (std::nothrow) Plan();
   if (!pl) return fail(DP_ENOMEM, "dp_plan_buckets: out of host memory");
   try {
     pl->P = P;
+    pl->R = R;
+    pl->S = S;
     pl->bucket_bytes = bucket_bytes;
     pl->sizes.assign(sizes, sizes + n_tensors);
     pl->decay.assign(n_tensors, 1);
@@ -209,6 +216,16 @@ int dp_plan_buckets_ex(const int64_t* sizes, const uint8_t* decay, int32_t n_ten
   return DP_OK;
 }
 
+int dp_plan_buckets_ex(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
+                       int64_t bucket_bytes, int32_t P, int64_t replica_stride, dp_plan** out) {
+  if (P < 1 || P > kMaxP) {
+    clear_error();
+    if (out) *out = nullptr;
+    return fail(DP_EINVAL, "dp_plan_buckets: P must be in 1..64");
+  }
+  return dp_plan_buckets_mesh(sizes, decay, n_tensors, bucket_bytes, 1, P, replica_stride, out);
+}
+
 int dp_plan_buckets(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
                     int64_t bucket_bytes, int32_t P, dp_plan** out) {
   return dp_plan_buckets_ex(sizes, decay, n_tensors, bucket_bytes, P, 0, out);
@@ -226,6 +243,9 @@ int dp_plan_info(const dp_plan* plan, dp_plan_info_t* out) {
   out->n_buckets = static_cast<int32_t>(pl->b_off.size());
   out->P = pl->P;
   out->tile_elems = kTileElems;
+  out->R = pl->R;
+  out->S = pl->S;
+  out->pad_ = 0;
   out->n_tiles = static_cast<int64_t>(pl->tiles.size());
   out->table_bytes = pl->table_bytes;
   out->workspace_bytes = pl->workspace_bytes;
@@ -252,7 +272,7 @@ int dp_plan_bucket(const dp_plan* plan, int32_t b, int64_t* offset, int64_t* pad
     return fail(DP_EINVAL, "dp_plan_bucket: bucket index out of range");
   if (offset) *offset = pl->b_off[b];
   if (padded_len) *padded_len = pl->b_len[b];
-  if (shard_len) *shard_len = pl->b_len[b] / pl->P;
+  if (shard_len) *shard_len = pl->b_len[b] / pl->S;
   return DP_OK;
 }
 

@@ -30,7 +30,8 @@
  *   r * replica_stride + i.  master, m, v and fp32 mean buffers are fp32 [L].
  *   Bucket b covers [offset_b, offset_b + len_b); its shard c is
  *   [offset_b + c*S_b, offset_b + (c+1)*S_b) with S_b = len_b / P, and rank c
- *   owns shard c.  Padding slots (between tensors and at a bucket's end) must
+ *   owns shard c (on a hybrid mesh, see dp_plan_buckets_mesh: S shards, shard s
+ *   owned by rank (g, s) of every group g).  Padding slots (between tensors and at a bucket's end) must
  *   hold zeros in gradients and in master/m/v; the calls keep them zero.
  * Alignment.  Every device pointer must be 32-byte aligned (DP_EALIGN); the
  *   kernels move 32 bytes per access.
@@ -83,6 +84,8 @@ typedef struct {
   int32_t n_buckets;
   int32_t P;
   int32_t tile_elems;       /* elements per work tile (tiles never cross a bucket) */
+  int32_t R, S;             /* mesh: R replicate groups x S shards (flat plans: 1 x P) */
+  int32_t pad_;
   int64_t n_tiles;
   int64_t table_bytes;      /* device plan image at the start of the workspace */
   int64_t workspace_bytes;  /* whole workspace: image + norm scratch + fp32 mean stage [L] */
@@ -119,12 +122,32 @@ int dp_plan_buckets(const int64_t* sizes, const uint8_t* decay, int32_t n_tensor
 int dp_plan_buckets_ex(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
                        int64_t bucket_bytes, int32_t P, int64_t replica_stride, dp_plan** out);
 
+/*
+ * Same, on a hybrid R x S device mesh (P = R * S ranks; rank (g, s) = g*S + s):
+ * HYBRID_SHARD, "FULL_SHARD inside a node + data parallel across nodes" ("4.1
+ * Data parallelism in depth", sec. 6.3); FSDP2's DeviceMesh mesh_shape=(2, 4)
+ * with dims ("replicate", "shard") ("Distributed Training: Data Parallel, Model
+ * Parallel and FSDP Strategies", "FSDP1 vs FSDP2"); "Data Parallelism: DDP, ZeRO
+ * and FSDP", "Hybrid sharding".  Each bucket is split into S shards, shard s
+ * owned by rank (g, s) in every group g.  The sums follow the hierarchical
+ * rings: a ring reduce-scatter inside each group of S ranks, then a ring
+ * all-reduce of each shard across the R groups (R sub-chunks); so element i of
+ * shard s in sub-chunk j (of R) is
+ *   sum over groups g = j+1, ..., j (mod R) of
+ *     [sum over members s' = s+1, ..., s (mod S) of grad(g, s')[i]]
+ * in fp32, left to right.  R = 1 is the flat ring over P = S ranks.
+ */
+int dp_plan_buckets_mesh(const int64_t* sizes, const uint8_t* decay, int32_t n_tensors,
+                         int64_t bucket_bytes, int32_t R, int32_t S, int64_t replica_stride,
+                         dp_plan** out);
+
 int dp_plan_info(const dp_plan* plan, dp_plan_info_t* out);
 
 /* Tensor t lives in bucket *bucket at flat offset *offset (16-byte aligned). */
 int dp_plan_tensor(const dp_plan* plan, int32_t t, int32_t* bucket, int64_t* offset);
 
-/* Bucket b: flat offset, padded length len_b and shard length S_b = len_b / P. */
+/* Bucket b: flat offset, padded length len_b and shard length len_b / S (S = P
+ * for flat plans). */
 int dp_plan_bucket(const dp_plan* plan, int32_t b, int64_t* offset, int64_t* padded_len,
                    int64_t* shard_len);
 

@@ -182,3 +182,24 @@ def test_noalloc_refuses_oversized_plans_on_the_host():
     assert "static array holds 33554432 bytes" in msg
     assert lib.dp_clip_coef_noalloc(plan.handle, ok, ok, C.c_double(1.0), None, ok,
                                     None) == dps.DP_EINVAL
+
+
+@pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (8, 1), (1, 8), (3, 2)])
+def test_mesh_plan_layout(orc, R, S):
+    """A mesh plan has the flat P = R*S layout; its shards are len/S."""
+    wl = configs.tiny_plumbing()
+    P = R * S
+    p = dps.Plan(wl.sizes, wl.bucket_bytes, P, mesh=(R, S))
+    q = dps.Plan(wl.sizes, wl.bucket_bytes, P)
+    assert (p.info.R, p.info.S, p.P) == (R, S, P) and (q.info.R, q.info.S) == (1, P)
+    assert p.tensor_offsets() == q.tensor_offsets() and p.L == q.L
+    for b in range(p.n_buckets):
+        off, ln, sh = p.bucket(b)
+        assert sh * S == ln and (ln // S) % (16 * R) == 0 or R == 1
+
+
+def test_mesh_plan_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        dps.Plan([10], 1024, 8, mesh=(3, 2))
+    with pytest.raises(dps.DPError):
+        dps.Plan([10], 1024, 128, mesh=(16, 8))

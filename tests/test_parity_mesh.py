@@ -1,0 +1,88 @@
+"""Hybrid R x S mesh on the GPU against the oracle's literal hierarchical rings:
+all-reduce, fused ZeRO-2 (with and without clipping) and the staged path, bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_zero_gb300 as dps
+import oracle as oracle_mod
+from harness import Case, assert_replicas_equal, small_workload
+from workloads import configs
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [3, 1000, 65536, 13107, 26214, 4097, 27910]
+MESHES = [(2, 4), (4, 2), (2, 2), (8, 1), (3, 2), (2, 3), (2, 8), (5, 2)]
+
+
+def mesh_case(R, S, sigma=1e-3, cap=64 * 1024):
+    wl = small_workload(SIZES, R * S, cap, sigma=sigma, seed=10 * R + S)
+    c = Case.__new__(Case)
+    c.wl, c.P, c.sizes, c.decay = wl, wl.P, wl.sizes, list(wl.decay)
+    c.plan = dps.Plan(c.sizes, cap, c.P, c.decay, mesh=(R, S))
+    c.off = c.plan.tensor_offsets()
+    c.device = "cuda"
+    c.ws = c.plan.new_workspace()
+    return c
+
+
+@pytest.mark.parametrize("R,S", MESHES)
+def test_mesh_allreduce_matches_oracle(orc, R, S):
+    c = mesh_case(R, S)
+    g = c.host_grads(1)
+    dev = c.to_replicas(g)
+    dps.dp_allreduce_mean(c.plan, c.ws, dev)
+    torch.cuda.synchronize()
+    want, _, st = orc.mesh_allreduce_mean(c.sizes, c.wl.bucket_bytes, R, S, g)
+    assert st.replicas_equal == 1
+    assert np.array_equal(c.from_replicas(dev), want)
+    assert_replicas_equal(dev, c.plan.L)
+
+
+@pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (3, 2), (2, 8)])
+@pytest.mark.parametrize("max_norm", [0.0, 1.0])
+def test_mesh_fused_zero_matches_oracle(orc, R, S, max_norm):
+    c = mesh_case(R, S, sigma=0.05)
+    adamw = configs.AdamW(max_norm=max_norm)
+    master = c.host_master()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    params = c.plan.new_replicas()
+    st = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    for step in (1, 2):
+        g = c.host_grads(step)
+        cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
+                            adamw.max_norm, step)
+        dps.dp_fused_zero_step(c.plan, c.ws, c.to_replicas(g), params, *st, cfg)
+        p_o, master, m, v, so = orc.mesh_zero_step(c.sizes, c.decay, c.wl.bucket_bytes, R, S, g,
+                                                   master, m, v, oracle_mod.adamw_cfg(adamw, step))
+        assert so.groups_equal == 1 and so.replicas_equal == 1
+        if max_norm > 0:
+            norm, coef, _ = dps.dp_read_norm(c.plan, c.ws)
+            assert coef == so.coef and so.coef < 1.0
+        torch.cuda.synchronize()
+        assert np.array_equal(c.from_replicas(params), p_o)
+        for dev, ref in zip(st, (master, m, v)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("R,S", [(2, 4), (3, 2)])
+def test_mesh_staged_equals_fused(R, S):
+    """reduce-scatter -> sharded AdamW (owners of shard s in every group) ->
+    in-group all-gather == the fused step."""
+    c = mesh_case(R, S)
+    g = c.to_replicas(c.host_grads(1))
+    master = c.host_master()
+    cfg = dps.adamw_cfg(max_norm=0.0)
+    p1, p2 = c.plan.new_replicas(), c.plan.new_replicas()
+    s1 = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    s2 = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    dps.dp_fused_zero_step(c.plan, c.ws, g, p1, *s1, cfg)
+    mean = c.plan.new_state()
+    dps.dp_reduce_scatter_mean(c.plan, c.ws, g, mean)
+    dps.dp_sharded_adamw_step(c.plan, c.ws, mean, *s2, p2, cfg)
+    dps.dp_all_gather(c.plan, c.ws, p2)
+    torch.cuda.synchronize()
+    assert torch.equal(p1, p2)
+    for a, b in zip(s1, s2):
+        assert torch.equal(a, b)
