@@ -54,6 +54,12 @@ class MeshStats(C.Structure):
                 ("coef", C.c_float), ("pad_", C.c_int32)]
 
 
+class Zero3Stats(C.Structure):
+    _fields_ = [("ag_fwd_sent", C.c_int64 * MAX_RANKS), ("ag_bwd_sent", C.c_int64 * MAX_RANKS),
+                ("rs_sent", C.c_int64 * MAX_RANKS), ("gathered_ok", C.c_int32), ("pad_", C.c_int32),
+                ("norm", C.c_double), ("coef", C.c_float), ("pad2_", C.c_int32)]
+
+
 def adamw_cfg(adamw, step):
     return AdamWCfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
                     adamw.max_norm, int(step))
@@ -97,6 +103,7 @@ class Oracle:
                                               P, P]
         L.orc_mesh_zero_step.argtypes = [P, P, C.c_int32, C.c_int64, C.c_int32, C.c_int32, P, P,
                                          P, P, P, P, P]
+        L.orc_zero3_step.argtypes = [P, P, C.c_int32, C.c_int64, C.c_int32, P, P, P, P, P, P, P]
         L.orc_sum.argtypes = [P, C.c_int64]
         L.orc_sum.restype = C.c_double
         L.orc_stage_traffic.argtypes = [C.c_int32, C.c_int32, C.c_int64, P, P]
@@ -218,6 +225,22 @@ class Oracle:
                                          _p(g), _p(master), _p(m), _p(v), _p(params), C.byref(cfg),
                                          C.byref(st)), "mesh zero step")
         return params, master, m, v, st
+
+    def zero3_step(self, sizes, decay, bucket_bytes, P, grads_u16, param_shards, master, m, v,
+                   cfg):
+        """ZeRO-3 unit flow. Returns (param_shards, master, m, v, stats)."""
+        s = _i64(sizes)
+        d = np.ascontiguousarray(decay, dtype=np.uint8)
+        g = np.ascontiguousarray(grads_u16, dtype=np.uint16)
+        ps = np.array(param_shards, dtype=np.uint16, copy=True)
+        master = np.array(master, dtype=np.float32, copy=True)
+        m = np.array(m, dtype=np.float32, copy=True)
+        v = np.array(v, dtype=np.float32, copy=True)
+        st = Zero3Stats()
+        _check(self.L.orc_zero3_step(_p(s), _p(d), len(s), int(bucket_bytes), int(P), _p(g), _p(ps),
+                                     _p(master), _p(m), _p(v), C.byref(cfg), C.byref(st)),
+               "zero3 step")
+        return ps, master, m, v, st
 
     def ledger_bytes(self, stage, psi, P, comp=(2, 2, 4, 4, 4)):
         c = np.asarray(comp, np.float64)

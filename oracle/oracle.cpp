@@ -793,6 +793,86 @@ int orc_mesh_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, in
   return 0;
 }
 
+// ---- ZeRO-3 / FULL_SHARD unit flow ------------------------------------------
+// "FSDP is ZeRO-3 organized around units"; per unit: forward all-gathers the
+// unit's parameter shards into a full set, backward all-gathers them again and
+// reduce-scatters the weight gradients, then "each rank steps only the shard it
+// owns" ("Data Parallelism: DDP, ZeRO and FSDP", "How FSDP actually runs" and
+// "The three stages": 3N; "4.1 Data parallelism in depth", sec. 6.2 and 8.2).
+// Units are the plan's buckets; forward visits them from the last bucket to the
+// first (buckets hold layers in reverse), backward from the first to the last.
+// param_shards [n_params] bf16: each element as held by its shard owner (in/out);
+// grads [P][n_params]: every rank's full gradients of this step.  Outputs the
+// same master/m/v and bf16 values as orc_zero_step.
+struct orc_zero3_stats {
+  int64_t ag_fwd_sent[kMaxRanks];
+  int64_t ag_bwd_sent[kMaxRanks];
+  int64_t rs_sent[kMaxRanks];
+  int32_t gathered_ok;   // 1 when every rank's gathered unit equals the shards' values
+  int32_t pad_;
+  double norm;
+  float coef;
+  int32_t pad2_;
+};
+
+int orc_zero3_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t bucket_bytes,
+                   int32_t P, const uint16_t* grads, uint16_t* param_shards, float* master,
+                   float* m, float* v, const orc_adamw* cfg, orc_zero3_stats* st) {
+  Plan pl;
+  if (!make_plan(sizes, n, bucket_bytes, P, &pl) || cfg->step < 1) return -1;
+  int64_t n_params = 0;
+  const std::vector<int64_t> base = tensor_bases(sizes, n, &n_params);
+  const int nb = static_cast<int>(pl.b_off.size());
+  orc_zero3_stats acc;
+  std::memset(&acc, 0, sizeof(acc));
+  acc.gathered_ok = 1;
+  // the unit's bf16 shards laid out flat in the bucket (padding 0)
+  auto unit_values = [&](int b, std::vector<uint16_t>& u) {
+    u.assign(pl.b_len[b], 0);
+    for (int t : pl.b_tensors[b]) {
+      const int64_t o = pl.t_off[t] - pl.b_off[b];
+      for (int64_t j = 0; j < sizes[t]; ++j) u[o + j] = param_shards[base[t] + j];
+    }
+  };
+  // one all-gather of unit b: rank c starts with only its shard; check the result
+  auto gather = [&](int b, int64_t* sent) {
+    const int64_t len = pl.b_len[b], S = len / P;
+    std::vector<uint16_t> u, Y(static_cast<size_t>(P) * len, 0);
+    unit_values(b, u);
+    for (int c = 0; c < P; ++c)
+      std::memcpy(Y.data() + static_cast<size_t>(c) * len + c * S, u.data() + c * S, 2 * S);
+    int64_t steps = 0;
+    ring_all_gather(P, len, Y.data(), sent, &steps);
+    for (int r = 0; r < P; ++r)
+      if (std::memcmp(Y.data() + static_cast<size_t>(r) * len, u.data(), 2 * len)) acc.gathered_ok = 0;
+  };
+  for (int b = nb - 1; b >= 0; --b) gather(b, acc.ag_fwd_sent);     // forward
+  std::vector<std::vector<float>> means(nb);
+  CompensatedSum total;
+  for (int b = 0; b < nb; ++b) {                                    // backward
+    gather(b, acc.ag_bwd_sent);
+    std::vector<float> X;
+    int64_t steps = 0;
+    pack_bucket(pl, b, sizes, base, n_params, grads, X);
+    bucket_mean(pl, b, X, means[b], acc.rs_sent, &steps);
+    total.add(sumsq_of(means[b]));
+  }
+  acc.coef = clip_coef(total.value(), cfg->max_norm, &acc.norm);
+  const AdamScalars sc = adam_scalars(*cfg);
+  for (int b = 0; b < nb; ++b) {                                    // each owner's shard
+    for (int t : pl.b_tensors[b]) {
+      const int64_t o = pl.t_off[t] - pl.b_off[b];
+      for (int64_t j = 0; j < sizes[t]; ++j) {
+        const int64_t e = base[t] + j;
+        adamw_element(means[b][o + j] * acc.coef, master[e], m[e], v[e], decay[t] != 0, sc);
+        param_shards[e] = f32_to_bf16_rne(master[e]);
+      }
+    }
+  }
+  if (st) *st = acc;
+  return 0;
+}
+
 // ---- ledger and volumes ------------------------------------------------------
 // Per-rank model-state bytes for `psi` parameters on P ranks, summing the
 // buffers each stage keeps ("4.1 Data parallelism in depth", sec. 6.1 table and sec. 7; "Data Parallelism: DDP, ZeRO and FSDP",

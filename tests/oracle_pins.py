@@ -530,6 +530,33 @@ def pin_mesh_zero_step(orc):
     assert np.all(np.abs(m2 - mf) <= 1e-6 * np.abs(mf) + 1e-9)
 
 
+# --------------------------------------------------------------------------- ZeRO-3
+def pin_zero3_flow(orc):
+    """ZeRO-3 moves 3(P-1)/P * M per rank (two all-gathers of the parameters and
+    one reduce-scatter of the gradients: "Data Parallelism: DDP, ZeRO and FSDP",
+    "The three stages"), every rank gathers exactly the shards' values, and the
+    update equals the ZeRO-2 step's, since only where the parameters live differs."""
+    rng = np.random.default_rng(53)
+    for P in (2, 4, 8):
+        sizes, cap, g, master = _zero_case(rng, P, sizes=(3, 1000, 655, 2621, 40), cap=4096)
+        n = sum(sizes)
+        z = np.zeros(n, np.float32)
+        shards = bf16_bits(master)
+        cfg = cfg_struct(1, max_norm=0.5)
+        ps, m3, mm3, vv3, st = orc.zero3_step(sizes, [1, 0, 1, 1, 0], cap, P, g, shards, master, z,
+                                              z, cfg)
+        p2, m2, mm2, vv2, _, st2 = orc.zero_step(sizes, [1, 0, 1, 1, 0], cap, P, g, master, z, z,
+                                                 cfg)
+        assert st.gathered_ok == 1
+        assert np.array_equal(m3, m2) and np.array_equal(mm3, mm2) and np.array_equal(vv3, vv2)
+        assert np.array_equal(ps, p2[0]) and st.coef == st2.coef
+        L = orc.plan(sizes, cap, P)["L"]
+        for r in range(P):
+            vol = st.ag_fwd_sent[r] + st.ag_bwd_sent[r] + st.rs_sent[r]
+            assert Fraction(vol * P, (P - 1) * L) == 3
+            assert st.ag_fwd_sent[r] == st.ag_bwd_sent[r] == st.rs_sent[r]
+
+
 # --------------------------------------------------------------------------- identity
 def lsq_data():
     from workloads.gen import small_ints

@@ -51,6 +51,10 @@ MUTANTS = {
     "mesh_no_cross_reduce": ("    ring_reduce_scatter(R, sh, C.data(), sent_rs, &steps);\n",
                              "    (void)sent_rs;\n"),
     "mesh_cross_ag_skipped": ("    ring_all_gather_f32(R, sh, C.data(), sent_ag, &steps);\n", "    (void)sent_ag;\n"),
+    "zero3_fwd_gather_skipped": ("  for (int b = nb - 1; b >= 0; --b) gather(b, acc.ag_fwd_sent);     // forward",
+                                 "  // forward gathers skipped"),
+    "zero3_shard_not_updated": ("        param_shards[e] = f32_to_bf16_rne(master[e]);",
+                                "        (void)e;"),
     "zero3_one_gather": ("    ring_all_gather(P, M, Y.data(), sent, steps);\n    ring_all_gather(P, M, Y.data(), sent, steps);\n",
                          "    ring_all_gather(P, M, Y.data(), sent, steps);\n"),
 }
