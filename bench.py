@@ -521,6 +521,74 @@ def run_streamed(args):
     }
 
 
+def run_zero3(args):
+    """ZeRO-3 unit flow on the bench workload: per step, every unit's forward
+    all-gather (last bucket first), its backward all-gather and gradient
+    reduce-scatter (first bucket first), the clip coefficient and the shard
+    update.  Persistent state 18 B/param over all ranks; one [P][max unit]
+    transient buffer."""
+    import gradient_sync_zero_gb300 as dps
+
+    torch.cuda.set_device(0)
+    wl = workload_by_name(args.workload)
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    off = plan.tensor_offsets()
+    ws = plan.new_workspace()
+    grads = plan.new_replicas()
+    wdev.fill_grads(grads, off, wl, step=1)
+    master = plan.new_state()
+    wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
+    shards = master.to(torch.bfloat16)
+    m, v, mean = plan.new_state(), plan.new_state(), plan.new_state()
+    nb, P = plan.n_buckets, plan.P
+    buckets = [plan.bucket(b) for b in range(nb)]
+    unit_buf = torch.empty(P, max(ln for _, ln, _ in buckets), dtype=torch.bfloat16, device="cuda")
+    a = wl.adamw
+    stream = torch.cuda.current_stream()
+
+    def step(t, evs=None):
+        cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
+        if evs:
+            evs[0].record(stream)
+        for b in reversed(range(nb)):
+            dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
+        if evs:
+            evs[1].record(stream)
+        for b in range(nb):
+            o, ln, _ = buckets[b]
+            dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
+            dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+        if evs:
+            evs[2].record(stream)
+        dps.dp_clip_coef(plan, ws, a.max_norm)
+        dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
+        if evs:
+            evs[3].record(stream)
+
+    for t in range(1, args.warmup + 1):
+        step(t)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        step(args.warmup + 1 + k, evs[k])
+    torch.cuda.synchronize()
+    parts = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i in range(3)]
+    ms = sum(parts)
+    n = wl.n_params
+    bytes_pp = 2 * (2 + 2 * P) + (2 * P + 4) + 30          # 2 all-gathers, reduce-scatter, update
+    return {
+        "metric": "ZeRO-3 unit flow (2 all-gathers + reduce-scatter + shard update) params/s",
+        "value": n / (ms * 1e-3), "unit": "params/s", "higher_is_better": True,
+        "ms_per_step": ms,
+        "stage_ms": {"forward_all_gather": parts[0], "backward_all_gather_reduce_scatter": parts[1],
+                     "clip_and_update": parts[2]},
+        "gbs": bytes_pp * n / (ms * 1e-3) / 1e9, "bytes_per_param": bytes_pp,
+        "resident_bytes_per_param_all_ranks": 2 + 4 + 12,
+        "transient_bytes": unit_buf.numel() * 2,
+        "config": {"workload": wl.name, "P": P, "n_units": nb},
+    }
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded sample."""
     import numpy as np
@@ -583,6 +651,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--mesh", default="",
                     help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
+    ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
     ap.add_argument("--streamed", action="store_true",
                     help="measure the overlap of per-bucket sync with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=4096, help="GEMM rows of the synthetic backward")
@@ -602,6 +671,9 @@ def main(argv=None):
         return
     if args.streamed:
         print(json.dumps(run_streamed(args)), flush=True)
+        return
+    if args.zero3:
+        print(json.dumps(run_zero3(args)), flush=True)
         return
     rank, local, world = dist_setup()
     res = run_gpu(args, rank, local, world)

@@ -74,6 +74,9 @@ def lib():
             "dp_clip_coef_noalloc": [vp, vp, vp, f64, vp, vp, vp],
             "dp_adamw_all_gather": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
             "dp_tracker_create": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
+            "dp_unit_all_gather": [vp, vp, vp, i32, vp, i64, vp],
+            "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
+            "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
             "dp_tracker_begin": [vp],
             "dp_tracker_mark_ready": [vp, i32, vp],
             "dp_tracker_wait": [vp, i64],
@@ -262,6 +265,38 @@ def dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg, use_clip_coef
     _check(lib().dp_adamw_all_gather(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
                                      _ptr(v), _ptr(params), C.byref(cfg), 1 if use_clip_coef else 0,
                                      _stream(stream)))
+
+
+def dp_unit_all_gather(plan, ws, param_shards, unit, unit_buf, stream=None):
+    """ZeRO-3: every rank's row of unit_buf [P][>= len] gets unit `unit`'s values."""
+    _need(param_shards, torch.bfloat16, plan.L, "param_shards")
+    if unit_buf.dim() != 2 or unit_buf.shape[0] < plan.P or not unit_buf.is_contiguous():
+        raise ValueError("unit_buf must be a contiguous [P][unit_stride] tensor")
+    _need(unit_buf, torch.bfloat16, plan.P * unit_buf.shape[1], "unit_buf")
+    _check(lib().dp_unit_all_gather(plan.handle, _ws(plan, ws), _ptr(param_shards), int(unit),
+                                    _ptr(unit_buf), int(unit_buf.shape[1]), _stream(stream)))
+
+
+def dp_unit_reduce_scatter(plan, ws, unit_grads, unit, mean, want_sumsq=False, stream=None):
+    """ZeRO-3: unit_grads [P][>= len] (a 2-D view, rows may be strided) -> mean shards."""
+    if unit_grads.dim() != 2 or unit_grads.shape[0] < plan.P or unit_grads.stride(1) != 1:
+        raise ValueError("unit_grads must be a [P][stride] view with unit element stride")
+    if unit_grads.dtype != torch.bfloat16 or not unit_grads.is_cuda:
+        raise TypeError("unit_grads must be a CUDA bf16 tensor")
+    _need(mean, torch.float32, plan.L, "mean")
+    _check(lib().dp_unit_reduce_scatter(plan.handle, _ws(plan, ws), _ptr(unit_grads),
+                                        int(unit_grads.stride(0)), int(unit), _ptr(mean),
+                                        1 if want_sumsq else 0, _stream(stream)))
+
+
+def dp_shard_adamw_step(plan, ws, mean, master, m, v, param_shards, cfg, use_clip_coef=False,
+                        stream=None):
+    for t, name in ((mean, "mean"), (master, "master"), (m, "m"), (v, "v")):
+        _need(t, torch.float32, plan.L, name)
+    _need(param_shards, torch.bfloat16, plan.L, "param_shards")
+    _check(lib().dp_shard_adamw_step(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
+                                     _ptr(v), _ptr(param_shards), C.byref(cfg),
+                                     1 if use_clip_coef else 0, _stream(stream)))
 
 
 class Tracker:

@@ -175,6 +175,52 @@ int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean,
   return e ? cuda_fail(e, "dp_adamw_all_gather") : DP_OK;
 }
 
+int dp_unit_all_gather(const dp_plan* plan, void* workspace, const void* param_shards, int32_t unit,
+                       void* unit_buf, int64_t unit_stride, void* stream) {
+  Launch L;
+  int rc = prepare("dp_unit_all_gather", plan, workspace, unit, unit + 1, stream, &L);
+  if (rc) return rc;
+  if (unit < 0 || unit >= static_cast<int32_t>(L.plan->b_off.size()))
+    return fail(DP_EINVAL, "dp_unit_all_gather: unit out of range");
+  if ((rc = check_ptrs("dp_unit_all_gather", L.plan, {param_shards, unit_buf}))) return rc;
+  if (unit_stride < L.plan->b_len[unit] || unit_stride % 16)
+    return fail(DP_EINVAL, "dp_unit_all_gather: unit_stride must be >= the unit length and a multiple of 16");
+  const int e = launch_unit_all_gather(L, param_shards, unit_buf, unit_stride,
+                                       L.plan->b_off[unit] / kPairElems);
+  return e ? cuda_fail(e, "dp_unit_all_gather") : DP_OK;
+}
+
+int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* unit_grads,
+                           int64_t unit_stride, int32_t unit, float* mean, int32_t want_sumsq,
+                           void* stream) {
+  Launch L;
+  int rc = prepare("dp_unit_reduce_scatter", plan, workspace, unit, unit + 1, stream, &L);
+  if (rc) return rc;
+  if (unit < 0 || unit >= static_cast<int32_t>(L.plan->b_off.size()))
+    return fail(DP_EINVAL, "dp_unit_reduce_scatter: unit out of range");
+  if ((rc = check_ptrs("dp_unit_reduce_scatter", L.plan, {unit_grads, mean}))) return rc;
+  if (unit_stride < L.plan->b_len[unit] || unit_stride % 16)
+    return fail(DP_EINVAL, "dp_unit_reduce_scatter: unit_stride must be >= the unit length and a multiple of 16");
+  const int e = launch_reduce_scatter(L, unit_grads, mean, want_sumsq != 0, unit_stride,
+                                      L.plan->b_off[unit] / kPairElems);
+  return e ? cuda_fail(e, "dp_unit_reduce_scatter") : DP_OK;
+}
+
+int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean, float* master,
+                        float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
+                        int32_t use_clip_coef, void* stream) {
+  Launch L;
+  const Plan* pl = as_plan(plan);
+  int rc = prepare("dp_shard_adamw_step", plan, workspace, 0,
+                   pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_shard_adamw_step", L.plan, {mean, master, m, v, param_shards}))) return rc;
+  AdamScalars s;
+  if ((rc = adam_scalars("dp_shard_adamw_step", cfg, &s))) return rc;
+  const int e = launch_adamw(L, mean, master, m, v, param_shards, s, use_clip_coef != 0, true);
+  return e ? cuda_fail(e, "dp_shard_adamw_step") : DP_OK;
+}
+
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
   return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
 }

@@ -98,11 +98,14 @@ struct Launch {
 };
 
 // Each returns a cudaError_t value (0 = success).
-int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq);
+int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq,
+                          int64_t rep_stride = 0, int64_t rep_block0 = 0);
+int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
+                           int64_t block0);
 int launch_allreduce(const Launch& L, void* grads);
 int launch_norm_finalize(const Launch& L, double max_norm);
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef);
+                 void* params, const AdamScalars& s, bool use_coef, bool flat_params = false);
 int launch_all_gather(const Launch& L, void* params);
 int launch_broadcast(const Launch& L, void* params, int src);
 int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,

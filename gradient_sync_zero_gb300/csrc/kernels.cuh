@@ -37,6 +37,7 @@ struct KCommon {
   int32_t P;             // rank count (used by the runtime-P instantiation)
   int32_t R;             // mesh: replicate groups (1 = flat ring)
   int32_t S;             // mesh: shard ranks per group (P = R * S)
+  int64_t rep_block0;    // replica buffers start at this 32-byte block (unit buffers)
 };
 
 // ---- 256-bit streaming accesses (sm_100-family ld/st .v8.b32) ----
@@ -239,11 +240,11 @@ template <int P, bool MESH>
 __device__ __forceinline__ void block_mean16(const KCommon& k, const uint8_t* g, int64_t b,
                                              const TileDesc& d, int s, float (&acc)[16]) {
   if constexpr (!MESH) {
-    ring_mean16<P>(g, k.stride_bytes, 32 * b, s, k.P, acc);
+    ring_mean16<P>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, k.P, acc);
   } else {
     const uint32_t within = static_cast<uint32_t>(2 * b - d.bvoff) % static_cast<uint32_t>(d.svec);
     const int j = static_cast<int>(within / (static_cast<uint32_t>(d.svec) / k.R));
-    mesh_mean16<P>(g, k.stride_bytes, 32 * b, s, j, k.R, k.S, k.P, acc);
+    mesh_mean16<P>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, j, k.R, k.S, k.P, acc);
   }
 }
 

@@ -102,8 +102,11 @@ __global__ void __launch_bounds__(kFinalThreads) k_norm_finalize(KCommon k, doub
   }
 }
 
-int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq) {
-  const KCommon k = make_common(L);
+int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq,
+                          int64_t rep_stride, int64_t rep_block0) {
+  KCommon k = make_common(L);
+  if (rep_stride > 0) k.stride_bytes = 2 * rep_stride;   // replicas in a unit buffer
+  k.rep_block0 = rep_block0;
   return with_P(L.plan->P, [&](auto pc) {
     return with_mesh(L.plan, [&](auto mc) {
       constexpr int P = decltype(pc)::value;

@@ -18,7 +18,7 @@ namespace dps {
 // Sharded AdamW on an fp32 gradient [L]; the owner's replica gets bf16(theta).
 __global__ void __launch_bounds__(kThreads)
     k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
-            AdamScalars s, int use_coef) {
+            AdamScalars s, int use_coef, int flat_params) {
   if (!plan_ok(k)) return;
   const float coef = use_coef ? k.hdr->coef : 1.0f;
   for_each_block(k, [&](int64_t, int64_t b, int c) {
@@ -36,9 +36,24 @@ __global__ void __launch_bounds__(kThreads)
     st_f16(master, b, th);
     st_f16(m, b, mm);
     st_f16(v, b, vv);
-    // the owner of shard c in every group (rank c on a flat ring)
     const Blk val = pack16_rne(th);
-    for (int g = 0; g < k.R; ++g) st_blk(params + (g * k.S + c) * k.stride_bytes + 32 * b, val);
+    if (flat_params) {  // ZeRO-3: one flat array of shards
+      st_blk(params + 32 * b, val);
+    } else {            // the owner of shard c in every group (rank c on a flat ring)
+      for (int g = 0; g < k.R; ++g) st_blk(params + (g * k.S + c) * k.stride_bytes + 32 * b, val);
+    }
+  });
+}
+
+// ZeRO-3 unit all-gather: every rank's row of the unit buffer receives the unit's
+// shard values (the flat shard array holds each element once, at its owner).
+__global__ void __launch_bounds__(kThreads)
+    k_unit_all_gather(KCommon k, const uint8_t* shards, uint8_t* out, int64_t out_stride_bytes,
+                      int64_t block0) {
+  if (!plan_ok(k)) return;
+  for_each_block(k, [&](int64_t, int64_t b, int) {
+    const Blk val = ld_blk(shards + 32 * b);
+    for (int r = 0; r < k.P; ++r) st_blk(out + r * out_stride_bytes + 32 * (b - block0), val);
   });
 }
 
@@ -199,9 +214,15 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef) {
+                 void* params, const AdamScalars& s, bool use_coef, bool flat_params) {
   return launch_tiles(L, k_adamw, make_common(L), grad, master, m, v,
-                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0);
+                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
+}
+
+int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
+                           int64_t block0) {
+  return launch_tiles(L, k_unit_all_gather, make_common(L), static_cast<const uint8_t*>(shards),
+                      static_cast<uint8_t*>(out), 2 * out_stride, block0);
 }
 
 int launch_all_gather(const Launch& L, void* params) {

@@ -29,6 +29,7 @@ inline KCommon make_common(const Launch& L) {
   k.P = L.plan->P;
   k.R = L.plan->R;
   k.S = L.plan->S;
+  k.rep_block0 = 0;
   return k;
 }
 

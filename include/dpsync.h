@@ -262,6 +262,35 @@ int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean,
                         float* m, float* v, void* params, const dp_adamw_cfg* cfg,
                         int32_t use_clip_coef, void* stream);
 
+/*
+ * ZeRO-3 / FULL_SHARD unit flow ("Data Parallelism: DDP, ZeRO and FSDP", "How
+ * FSDP actually runs": per unit, all-gather the parameter shards before the
+ * forward, again before the backward, reduce-scatter the gradients after it,
+ * then each rank steps only its shard; "4.1 Data parallelism in depth",
+ * sec. 6.2).  Units are the plan's buckets.  Persistent state is sharded: one
+ * flat bf16 [L] array of parameter shards (element i held by its shard owner),
+ * fp32 [L] master/m/v and an fp32 [L] mean (the gradient shards): 18 bytes per
+ * parameter across all P ranks.  The unit buffers are transient:
+ * [P][unit_stride] bf16 (unit_stride >= the unit's padded length, a multiple of
+ * 16), one row per rank.
+ *
+ * dp_unit_all_gather: every rank's full copy of unit `unit`:
+ *   unit_buf[r][i] = param_shards[offset_unit + i], r < P, i < len_unit.
+ * dp_unit_reduce_scatter: the unit's gradients, rank r's in unit_grads[r][0..len),
+ *   reduced in ring order to the fp32 mean of each owner's shard:
+ *   mean[offset_unit + i]; want_sumsq also stores the unit's norm partials.
+ * dp_shard_adamw_step: AdamW over all buckets on mean (times the clip
+ *   coefficient if use_clip_coef), writing bf16(theta) to param_shards.
+ */
+int dp_unit_all_gather(const dp_plan* plan, void* workspace, const void* param_shards, int32_t unit,
+                       void* unit_buf, int64_t unit_stride, void* stream);
+int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* unit_grads,
+                           int64_t unit_stride, int32_t unit, float* mean, int32_t want_sumsq,
+                           void* stream);
+int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean, float* master,
+                        float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
+                        int32_t use_clip_coef, void* stream);
+
 /* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
 

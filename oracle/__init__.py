@@ -104,6 +104,9 @@ class Oracle:
         L.orc_mesh_zero_step.argtypes = [P, P, C.c_int32, C.c_int64, C.c_int32, C.c_int32, P, P,
                                          P, P, P, P, P]
         L.orc_zero3_step.argtypes = [P, P, C.c_int32, C.c_int64, C.c_int32, P, P, P, P, P, P, P]
+        L.orc_accumulate.argtypes = [C.c_int32, C.c_int64, P, P]
+        L.orc_accumulate.restype = None
+        L.orc_allreduce_mean_bf16wire.argtypes = [P, C.c_int32, C.c_int64, C.c_int32, P, P]
         L.orc_sum.argtypes = [P, C.c_int64]
         L.orc_sum.restype = C.c_double
         L.orc_stage_traffic.argtypes = [C.c_int32, C.c_int32, C.c_int64, P, P]
@@ -241,6 +244,23 @@ class Oracle:
                                      _p(master), _p(m), _p(v), C.byref(cfg), C.byref(st)),
                "zero3 step")
         return ps, master, m, v, st
+
+    def accumulate(self, acc_u16, micro_u16):
+        """acc = bf16(acc + micro), element by element ([P][n] bf16 bits)."""
+        acc = np.array(acc_u16, dtype=np.uint16, copy=True, order="C")
+        micro = np.ascontiguousarray(micro_u16, dtype=np.uint16)
+        P, n = acc.shape
+        self.L.orc_accumulate(P, n, _p(acc), _p(micro))
+        return acc
+
+    def allreduce_mean_bf16wire(self, sizes, bucket_bytes, P, grads_u16):
+        """The ring with bf16 partial sums. Returns (out, fp32 quotient)."""
+        s = _i64(sizes)
+        g = np.array(grads_u16, dtype=np.uint16, copy=True, order="C")
+        q = np.zeros(g.shape[1], np.float32)
+        _check(self.L.orc_allreduce_mean_bf16wire(_p(s), len(s), int(bucket_bytes), int(P), _p(g),
+                                                  _p(q)), "bf16 wire allreduce")
+        return g, q
 
     def ledger_bytes(self, stage, psi, P, comp=(2, 2, 4, 4, 4)):
         c = np.asarray(comp, np.float64)

@@ -873,6 +873,70 @@ int orc_zero3_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_
   return 0;
 }
 
+// ---- gradient accumulation and the bf16 wire ----------------------------------
+// "Gradient accumulation to keep global batch size large without increasing
+// memory - sync only on final micro-batch" ("Distributed Training: Data Parallel,
+// Model Parallel and FSDP Strategies", "Selecting and Tuning": no_sync on every
+// micro-batch but the last).  Each rank's bf16 gradient buffer accumulates the
+// micro-batch gradients as autograd does for bf16 gradients: acc = bf16(acc + g),
+// the add in fp32.  acc, micro: [P][n] bf16 bits.
+void orc_accumulate(int32_t P, int64_t n, uint16_t* acc, const uint16_t* micro) {
+  for (int64_t i = 0; i < static_cast<int64_t>(P) * n; ++i)
+    acc[i] = f32_to_bf16_rne(bf16_bits_to_f32(acc[i]) + bf16_bits_to_f32(micro[i]));
+}
+
+// "Precision: gradient dtype and communication hooks change both bandwidth and
+// numerical behavior" ("Data Parallelism: From Parameter Server to Ring
+// All-Reduce", sec. 8).  The ring with bf16 on the wire: every hop's partial sum
+// is rounded to bf16 before it is sent (the receiver adds in fp32 and rounds),
+// the owner's final sum is divided by P in fp32 and rounded to bf16 for the
+// all-gather.  grads [P][n_params] in/out; mean_out: the fp32 quotient before
+// its bf16 rounding (nullable).
+int orc_allreduce_mean_bf16wire(const int64_t* sizes, int32_t n, int64_t bucket_bytes, int32_t P,
+                                uint16_t* grads, float* mean_out) {
+  Plan pl;
+  if (!make_plan(sizes, n, bucket_bytes, P, &pl)) return -1;
+  int64_t n_params = 0;
+  const std::vector<int64_t> base = tensor_bases(sizes, n, &n_params);
+  for (size_t b = 0; b < pl.b_off.size(); ++b) {
+    const int64_t len = pl.b_len[b], S = len / P;
+    std::vector<float> X;
+    pack_bucket(pl, static_cast<int>(b), sizes, base, n_params, grads, X);
+    std::vector<uint16_t> W(static_cast<size_t>(P) * len);   // what each rank holds, bf16
+    for (size_t i = 0; i < W.size(); ++i) W[i] = f32_to_bf16_rne(X[i]);
+    std::vector<uint16_t> msg(static_cast<size_t>(P) * S);
+    for (int s = 0; s + 1 < P; ++s) {
+      for (int r = 0; r < P; ++r) {
+        const int c = mod(r - 1 - s, P);
+        std::memcpy(&msg[static_cast<size_t>(r) * S], W.data() + static_cast<size_t>(r) * len + c * S, 2 * S);
+      }
+      for (int r = 0; r < P; ++r) {
+        const int dst = (r + 1) % P, c = mod(r - 1 - s, P);
+        uint16_t* mine = W.data() + static_cast<size_t>(dst) * len + c * S;
+        for (int64_t i = 0; i < S; ++i)
+          mine[i] = f32_to_bf16_rne(bf16_bits_to_f32(mine[i]) + bf16_bits_to_f32(msg[static_cast<size_t>(r) * S + i]));
+      }
+    }
+    std::vector<float> q(len);
+    std::vector<uint16_t> Y(static_cast<size_t>(P) * len, 0);
+    for (int c = 0; c < P; ++c)
+      for (int64_t i = c * S; i < (c + 1) * S; ++i) {
+        q[i] = bf16_bits_to_f32(W[static_cast<size_t>(c) * len + i]) / static_cast<float>(P);
+        Y[static_cast<size_t>(c) * len + i] = f32_to_bf16_rne(q[i]);
+      }
+    int64_t sent[kMaxRanks] = {0}, steps = 0;
+    ring_all_gather(P, len, Y.data(), sent, &steps);
+    for (int t : pl.b_tensors[b]) {
+      const int64_t o = pl.t_off[t] - pl.b_off[b];
+      for (int r = 0; r < P; ++r)
+        std::memcpy(grads + static_cast<size_t>(r) * n_params + base[t],
+                    Y.data() + static_cast<size_t>(r) * len + o, 2 * sizes[t]);
+      if (mean_out) std::memcpy(mean_out + base[t], q.data() + o, 4 * sizes[t]);
+    }
+  }
+  return 0;
+}
+
 // ---- ledger and volumes ------------------------------------------------------
 // Per-rank model-state bytes for `psi` parameters on P ranks, summing the
 // buffers each stage keeps ("4.1 Data parallelism in depth", sec. 6.1 table and sec. 7; "Data Parallelism: DDP, ZeRO and FSDP",

@@ -557,6 +557,45 @@ def pin_zero3_flow(orc):
             assert st.ag_fwd_sent[r] == st.ag_bwd_sent[r] == st.rs_sent[r]
 
 
+# --------------------------------------------------------------------------- accumulation / bf16 wire
+def pin_accumulate(orc):
+    """bf16 accumulation is fp32 add + round-to-nearest-even (torch's bf16 add
+    as a library cross-check); small integers accumulate exactly."""
+    rng = np.random.default_rng(59)
+    a = rand_bf16(rng, (3, 4000), 1e-2)
+    b = rand_bf16(rng, (3, 4000), 1e-2)
+    got = orc.accumulate(a, b)
+    ta = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+    want = (ta + tb).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    ints = bf16_bits(np.arange(-50, 50, dtype=np.float32)).reshape(1, -1)
+    assert np.array_equal(bf16_to_f32(orc.accumulate(ints, ints)), 2 * bf16_to_f32(ints))
+
+
+def pin_bf16_wire(orc):
+    """P = 2: one rounded add, the same as the fp32 reduction; P >= 3: bf16 partial
+    sums absorb small terms (2^8 + 1 = 2^8 in bf16), bounded by (P-1) 2^-8 sum|g|."""
+    rng = np.random.default_rng(61)
+    sizes, cap = [1000, 333, 77], 4096
+    g = rand_bf16(rng, (2, sum(sizes)), 1e-3)
+    w, _ = orc.allreduce_mean_bf16wire(sizes, cap, 2, g)
+    f, _, _ = orc.allreduce_mean(sizes, cap, 2, g)
+    assert np.array_equal(w, f)
+    P, n = 4, 64
+    X = np.ones((P, n), np.float32)
+    X[1, :] = 256.0                                     # first in the fold of chunk 0
+    w, q = orc.allreduce_mean_bf16wire([n], 1 << 20, P, bf16_bits(X.ravel()).reshape(P, n))
+    _, mf, _ = orc.allreduce_mean([n], 1 << 20, P, bf16_bits(X.ravel()).reshape(P, n))
+    assert q[0] == 256.0 / P and mf[0] == 259.0 / P
+    for P in (3, 5, 8):
+        g = rand_bf16(rng, (P, sum(sizes)), 1e-3)
+        _, q = orc.allreduce_mean_bf16wire(sizes, cap, P, g)
+        Xd = bf16_to_f32(g).astype(np.float64)
+        assert np.all(np.abs(q - Xd.sum(0) / P) <= (P - 1) * 2.0 ** -8 * np.abs(Xd).sum(0) / P
+                      + 2.0 ** -24 * np.abs(q) + 1e-45)
+
+
 # --------------------------------------------------------------------------- identity
 def lsq_data():
     from workloads.gen import small_ints

@@ -55,6 +55,10 @@ MUTANTS = {
                                  "  // forward gathers skipped"),
     "zero3_shard_not_updated": ("        param_shards[e] = f32_to_bf16_rne(master[e]);",
                                 "        (void)e;"),
+    "accumulate_sign": ("    acc[i] = f32_to_bf16_rne(bf16_bits_to_f32(acc[i]) + bf16_bits_to_f32(micro[i]));",
+                        "    acc[i] = f32_to_bf16_rne(bf16_bits_to_f32(acc[i]) - bf16_bits_to_f32(micro[i]));"),
+    "wire_receiver_overwrites": ("          mine[i] = f32_to_bf16_rne(bf16_bits_to_f32(mine[i]) + bf16_bits_to_f32(msg[static_cast<size_t>(r) * S + i]));",
+                                 "          mine[i] = msg[static_cast<size_t>(r) * S + i];"),
     "zero3_one_gather": ("    ring_all_gather(P, M, Y.data(), sent, steps);\n    ring_all_gather(P, M, Y.data(), sent, steps);\n",
                          "    ring_all_gather(P, M, Y.data(), sent, steps);\n"),
 }

@@ -1,0 +1,99 @@
+"""ZeRO-3 / FULL_SHARD unit flow on the GPU against the oracle: forward all-gather
+of every unit, backward all-gather, reduce-scatter of the unit's gradients, then the
+shard update — bit for bit, for a flat plan and a hybrid mesh's flat sibling."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_zero_gb300 as dps
+import oracle as oracle_mod
+from harness import Case, small_workload, u16
+from workloads import configs, device as wdev
+
+pytestmark = pytest.mark.gpu
+
+
+def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf):
+    plan = c.plan
+    nb = plan.n_buckets
+    gathered = []
+    for b in reversed(range(nb)):                           # forward
+        dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
+        o, ln, _ = plan.bucket(b)
+        gathered.append((b, unit_buf[:, :ln].clone()))
+    for b in range(nb):                                     # backward
+        dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
+        o, ln, _ = plan.bucket(b)
+        dps.dp_unit_reduce_scatter(plan, c.ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+    dps.dp_clip_coef(plan, c.ws, cfg.max_norm)
+    dps.dp_shard_adamw_step(plan, c.ws, mean, *st, shards, cfg, use_clip_coef=True)
+    return gathered
+
+
+@pytest.mark.parametrize("P", [2, 4, 5, 8])
+def test_zero3_flow_matches_oracle(orc, P):
+    wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910], P, 64 * 1024, sigma=0.05,
+                        seed=30 + P)
+    c = Case(wl)
+    adamw = configs.AdamW(max_norm=1.0)
+    master = c.host_master()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    shards_h = u16(torch.from_numpy(master).to(torch.bfloat16))
+    shards = c.plan.new_state().to(torch.bfloat16)
+    wdev.fill_flat(shards, c.off, c.sizes, torch.from_numpy(master).to(torch.bfloat16).cuda())
+    st = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    mean = c.plan.new_state()
+    max_len = max(c.plan.bucket(b)[1] for b in range(c.plan.n_buckets))
+    unit_buf = torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda")
+    for step in (1, 2):
+        g = c.host_grads(step)
+        cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
+                            adamw.max_norm, step)
+        before = shards.clone()
+        gathered = zero3_flow(c, c.to_replicas(g), shards, mean, st, cfg, unit_buf)
+        shards_h, master, m, v, so = orc.zero3_step(c.sizes, c.decay, wl.bucket_bytes, P, g,
+                                                    shards_h, master, m, v,
+                                                    oracle_mod.adamw_cfg(adamw, step))
+        assert so.gathered_ok == 1 and so.coef < 1.0
+        norm, coef, status = dps.dp_read_norm(c.plan, c.ws)
+        assert status == 0 and coef == so.coef
+        torch.cuda.synchronize()
+        for b, copy in gathered:                             # every rank gathered the unit
+            o, ln, _ = c.plan.bucket(b)
+            for r in range(P):
+                assert torch.equal(copy[r], before[o:o + ln])
+        assert np.array_equal(u16(wdev.gather_flat(shards, c.off, c.sizes)), shards_h)
+        for dev, ref in zip(st, (master, m, v)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+
+
+def test_unit_all_gather_fills_every_rank_row():
+    wl = small_workload([3, 1000, 65536, 4097], 4, 64 * 1024, seed=3)
+    c = Case(wl)
+    vals = torch.arange(c.plan.L, dtype=torch.float32, device="cuda").to(torch.bfloat16)
+    max_len = max(c.plan.bucket(b)[1] for b in range(c.plan.n_buckets))
+    buf = torch.zeros(4, max_len + 64, dtype=torch.bfloat16, device="cuda")
+    for b in range(c.plan.n_buckets):
+        o, ln, _ = c.plan.bucket(b)
+        dps.dp_unit_all_gather(c.plan, c.ws, vals, b, buf)
+        torch.cuda.synchronize()
+        for r in range(4):
+            assert torch.equal(buf[r, :ln], vals[o:o + ln])
+
+
+def test_unit_reduce_scatter_equals_bucket_reduce_scatter():
+    wl = small_workload([3, 1000, 65536, 13107, 26214], 8, 32 * 1024, seed=4)
+    c = Case(wl)
+    g = c.to_replicas(c.host_grads(1))
+    a, b_ = c.plan.new_state(), c.plan.new_state()
+    dps.dp_reduce_scatter_mean(c.plan, c.ws, g, a, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 1.0)
+    n1 = dps.dp_read_norm(c.plan, c.ws)
+    for b in range(c.plan.n_buckets):
+        o, ln, _ = c.plan.bucket(b)
+        unit = g[:, o:o + ln].contiguous()                  # a separate [P][len] buffer
+        dps.dp_unit_reduce_scatter(c.plan, c.ws, unit, b, b_, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 1.0)
+    n2 = dps.dp_read_norm(c.plan, c.ws)
+    assert torch.equal(a, b_) and n1 == n2
