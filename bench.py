@@ -589,6 +589,94 @@ def run_zero3(args):
     }
 
 
+def run_accum(args):
+    """Gradient accumulation over k micro-batches, then the mean all-reduce: the
+    local accumulations (k-1 passes of acc = bf16(acc + g)) and the last
+    micro-batch fused with the sync, timed against the unfused last step
+    (accumulate, then all-reduce).  Also the all-reduce with bf16 partial sums on
+    the ring against the fp32 ring: time and error against an fp64 mean."""
+    import gradient_sync_zero_gb300 as dps
+
+    torch.cuda.set_device(0)
+    wl = workload_by_name(args.workload)
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    off = plan.tensor_offsets()
+    ws = plan.new_workspace()
+    k = max(2, args.accum)
+    micro = [plan.new_replicas() for _ in range(2)]
+    wdev.fill_grads(micro[0], off, wl, step=1)
+    wdev.fill_grads(micro[1], off, wl, step=2)
+    acc = plan.new_replicas()
+    stream = torch.cuda.current_stream()
+    P, n = plan.P, wl.n_params
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            ev[2 * i].record(stream)
+            fn()
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        return sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps)) / reps
+
+    def accumulate_only():
+        dps.dp_accumulate(plan, ws, acc, micro[1])
+
+    def fused_last():
+        dps.dp_allreduce_mean_accum(plan, ws, acc, micro[1])
+
+    def unfused_last():
+        dps.dp_accumulate(plan, ws, acc, micro[1])
+        dps.dp_allreduce_mean(plan, ws, acc)
+
+    def ar_fp32():
+        dps.dp_allreduce_mean(plan, ws, acc)
+
+    def ar_bf16():
+        dps.dp_allreduce_mean_bf16wire(plan, ws, acc)
+
+    acc.copy_(micro[0])
+    t_acc = timed(accumulate_only, args.steps)
+    t_fused = timed(fused_last, args.steps)
+    t_unfused = timed(unfused_last, args.steps)
+    t_ar = timed(ar_fp32, args.steps)
+    t_wire = timed(ar_bf16, args.steps)
+    step_fused = (k - 1) * t_acc + t_fused          # micro 1 is written in place, k-1 adds
+    step_unfused = k * t_acc + t_ar
+    # precision of the two rings against the fp64 mean, on the first micro-batch
+    L = plan.L
+    exact = micro[0][:, :L].double().mean(0)
+    res = {}
+    for name, fn in (("fp32_ring", dps.dp_allreduce_mean), ("bf16_wire", dps.dp_allreduce_mean_bf16wire)):
+        buf = micro[0].clone()
+        fn(plan, ws, buf)
+        err = (buf[0, :L].double() - exact).abs()
+        scale = micro[0][:, :L].double().abs().mean(0)
+        rel = err / scale.clamp_min(1e-30)
+        res[name] = {"max_err_over_mean_abs_g": float(rel.max()), "mean_err_over_mean_abs_g": float(rel.mean())}
+        del buf
+    torch.cuda.synchronize()
+    b_acc, b_fused, b_ar = 6 * P, 6 * P, 4 * P
+    return {
+        "metric": f"gradient accumulation ({k} micro-batches) + mean all-reduce, params/s",
+        "value": n / (step_fused * 1e-3), "unit": "params/s", "higher_is_better": True,
+        "ms_per_step": step_fused, "ms_per_step_unfused": step_unfused,
+        "kernel_ms": {"accumulate": t_acc, "fused_last_micro_batch": t_fused,
+                      "accumulate_then_allreduce": t_unfused, "allreduce_fp32_ring": t_ar,
+                      "allreduce_bf16_wire": t_wire},
+        "kernel_gbs": {"accumulate": b_acc * n / (t_acc * 1e-3) / 1e9,
+                       "fused_last_micro_batch": b_fused * n / (t_fused * 1e-3) / 1e9,
+                       "allreduce_fp32_ring": b_ar * n / (t_ar * 1e-3) / 1e9,
+                       "allreduce_bf16_wire": b_ar * n / (t_wire * 1e-3) / 1e9},
+        "bytes_per_param": {"accumulate": b_acc, "fused_last_micro_batch": b_fused, "allreduce": b_ar},
+        "precision_vs_fp64_mean": res,
+        "config": {"workload": wl.name, "P": P, "micro_batches": k, "l2": "inputs > L2"},
+    }
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded sample."""
     import numpy as np
@@ -652,6 +740,8 @@ def main(argv=None):
     ap.add_argument("--mesh", default="",
                     help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
     ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
+    ap.add_argument("--accum", type=int, default=0,
+                    help="time k-micro-batch gradient accumulation and the bf16-wire ring")
     ap.add_argument("--streamed", action="store_true",
                     help="measure the overlap of per-bucket sync with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=4096, help="GEMM rows of the synthetic backward")
@@ -674,6 +764,9 @@ def main(argv=None):
         return
     if args.zero3:
         print(json.dumps(run_zero3(args)), flush=True)
+        return
+    if args.accum:
+        print(json.dumps(run_accum(args)), flush=True)
         return
     rank, local, world = dist_setup()
     res = run_gpu(args, rank, local, world)

@@ -75,6 +75,9 @@ def lib():
             "dp_adamw_all_gather": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
             "dp_tracker_create": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
             "dp_unit_all_gather": [vp, vp, vp, i32, vp, i64, vp],
+            "dp_accumulate": [vp, vp, vp, vp, i32, i32, vp],
+            "dp_allreduce_mean_accum": [vp, vp, vp, vp, i32, i32, vp],
+            "dp_allreduce_mean_bf16wire": [vp, vp, vp, i32, i32, vp],
             "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
             "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
             "dp_tracker_begin": [vp],
@@ -347,6 +350,31 @@ class Tracker:
         arr = (C.c_int32 * max(cap, 1))()
         _check(lib().dp_tracker_fired(self._h, arr, cap, C.byref(n)))
         return list(arr[:n.value])
+
+
+def dp_accumulate(plan, ws, acc, micro, b0=0, b1=None, stream=None):
+    """acc[r] = bf16(acc[r] + micro[r]) (local gradient accumulation, no sync)."""
+    _need(acc, torch.bfloat16, plan.P * plan.stride, "acc")
+    _need(micro, torch.bfloat16, plan.P * plan.stride, "micro")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_accumulate(plan.handle, _ws(plan, ws), _ptr(acc), _ptr(micro), b0, b1,
+                               _stream(stream)))
+
+
+def dp_allreduce_mean_accum(plan, ws, acc, micro, b0=0, b1=None, stream=None):
+    """Last micro-batch: accumulate and mean all-reduce in one pass (result in acc)."""
+    _need(acc, torch.bfloat16, plan.P * plan.stride, "acc")
+    _need(micro, torch.bfloat16, plan.P * plan.stride, "micro")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_allreduce_mean_accum(plan.handle, _ws(plan, ws), _ptr(acc), _ptr(micro), b0,
+                                         b1, _stream(stream)))
+
+
+def dp_allreduce_mean_bf16wire(plan, ws, grads, b0=0, b1=None, stream=None):
+    _need(grads, torch.bfloat16, plan.P * plan.stride, "grads")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_allreduce_mean_bf16wire(plan.handle, _ws(plan, ws), _ptr(grads), b0, b1,
+                                            _stream(stream)))
 
 
 def dp_fused_zero_step_launches(cfg):

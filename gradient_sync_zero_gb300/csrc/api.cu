@@ -221,6 +221,38 @@ int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean,
   return e ? cuda_fail(e, "dp_shard_adamw_step") : DP_OK;
 }
 
+int dp_accumulate(const dp_plan* plan, void* workspace, void* acc, const void* micro, int32_t b0,
+                  int32_t b1, void* stream) {
+  Launch L;
+  int rc = prepare("dp_accumulate", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_accumulate", L.plan, {acc, micro}))) return rc;
+  const int e = launch_accumulate(L, acc, micro);
+  return e ? cuda_fail(e, "dp_accumulate") : DP_OK;
+}
+
+int dp_allreduce_mean_accum(const dp_plan* plan, void* workspace, void* acc, const void* micro,
+                            int32_t b0, int32_t b1, void* stream) {
+  Launch L;
+  int rc = prepare("dp_allreduce_mean_accum", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_allreduce_mean_accum", L.plan, {acc, micro}))) return rc;
+  if (L.plan->R > 1) return fail(DP_EINVAL, "dp_allreduce_mean_accum: flat plans only");
+  const int e = launch_allreduce_accum(L, acc, micro);
+  return e ? cuda_fail(e, "dp_allreduce_mean_accum") : DP_OK;
+}
+
+int dp_allreduce_mean_bf16wire(const dp_plan* plan, void* workspace, void* grads, int32_t b0,
+                               int32_t b1, void* stream) {
+  Launch L;
+  int rc = prepare("dp_allreduce_mean_bf16wire", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_allreduce_mean_bf16wire", L.plan, {grads}))) return rc;
+  if (L.plan->R > 1) return fail(DP_EINVAL, "dp_allreduce_mean_bf16wire: flat plans only");
+  const int e = launch_allreduce_bf16wire(L, grads);
+  return e ? cuda_fail(e, "dp_allreduce_mean_bf16wire") : DP_OK;
+}
+
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
   return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
 }

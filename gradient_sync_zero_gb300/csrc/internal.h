@@ -103,6 +103,9 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
                            int64_t block0);
 int launch_allreduce(const Launch& L, void* grads);
+int launch_accumulate(const Launch& L, void* acc, const void* micro);
+int launch_allreduce_accum(const Launch& L, void* acc, const void* micro);
+int launch_allreduce_bf16wire(const Launch& L, void* grads);
 int launch_norm_finalize(const Launch& L, double max_norm);
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
                  void* params, const AdamScalars& s, bool use_coef, bool flat_params = false);

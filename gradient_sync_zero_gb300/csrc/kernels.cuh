@@ -248,6 +248,82 @@ __device__ __forceinline__ void block_mean16(const KCommon& k, const uint8_t* g,
   }
 }
 
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Accumulation fused with the reduction: replica r's value is bf16(acc_r + micro_r)
+// (what dp_accumulate would have stored), folded in ring order as in ring_mean16.
+template <int P>
+__device__ __forceinline__ void ring_mean16_accum(const uint8_t* acc, const uint8_t* micro,
+                                                  int64_t stride_bytes, int64_t byte_off, int c,
+                                                  int p_rt, float (&out)[16]) {
+  constexpr int K = (P > 0 && P < 4) ? P : 4;
+  const int np = P > 0 ? P : p_rt;
+  const int r_first = (c + 1 == np) ? 0 : c + 1;
+#pragma unroll
+  for (int k0 = 0; k0 < (P > 0 ? P : kMaxP); k0 += K) {
+    if (k0 >= np) break;
+    Blk x[K], y[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (k0 + k >= np) break;
+      int r = r_first + k0 + k;
+      if (r >= np) r -= np;
+      x[k] = ld_blk(acc + r * stride_bytes + byte_off);
+      y[k] = ld_blk(micro + r * stride_bytes + byte_off);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (k0 + k >= np) break;
+      float a[16], b[16];
+      unpack16(x[k], a);
+      unpack16(y[k], b);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float t = bf16_round(__fadd_rn(a[e], b[e]));
+        out[e] = (k0 + k == 0) ? t : __fadd_rn(out[e], t);
+      }
+    }
+  }
+  const float fp = static_cast<float>(np);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) out[e] = __fdiv_rn(out[e], fp);
+}
+
+// The ring with bf16 partial sums: each hop rounds its fp32 add to bf16.
+template <int P>
+__device__ __forceinline__ void ring_mean16_bf16wire(const uint8_t* g, int64_t stride_bytes,
+                                                     int64_t byte_off, int c, int p_rt,
+                                                     float (&out)[16]) {
+  constexpr int K = (P > 0 && P < 8) ? P : 8;
+  const int np = P > 0 ? P : p_rt;
+  const int r_first = (c + 1 == np) ? 0 : c + 1;
+#pragma unroll
+  for (int k0 = 0; k0 < (P > 0 ? P : kMaxP); k0 += K) {
+    if (k0 >= np) break;
+    Blk x[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (k0 + k >= np) break;
+      int r = r_first + k0 + k;
+      if (r >= np) r -= np;
+      x[k] = ld_blk(g + r * stride_bytes + byte_off);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (k0 + k >= np) break;
+      float t[16];
+      unpack16(x[k], t);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) out[e] = (k0 + k == 0) ? t[e] : bf16_round(__fadd_rn(out[e], t[e]));
+    }
+  }
+  const float fp = static_cast<float>(np);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) out[e] = __fdiv_rn(out[e], fp);
+}
+
 // Store one block into every replica.
 template <int P>
 __device__ __forceinline__ void store_replicas(uint8_t* base, int64_t stride_bytes,

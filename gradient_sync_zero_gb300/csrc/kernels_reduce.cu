@@ -57,6 +57,47 @@ __global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint8_t* g) {
   });
 }
 
+// acc[r] = bf16(acc[r] + micro[r]) for every replica.
+__global__ void __launch_bounds__(kThreads) k_accumulate(KCommon k, uint8_t* acc,
+                                                         const uint8_t* micro) {
+  if (!plan_ok(k)) return;
+  for_each_block(k, [&](int64_t, int64_t b, int) {
+    for (int r = 0; r < k.P; ++r) {
+      const Blk x = ld_blk(acc + r * k.stride_bytes + 32 * b);
+      const Blk y = ld_blk(micro + r * k.stride_bytes + 32 * b);
+      float a[16], c[16];
+      unpack16(x, a);
+      unpack16(y, c);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a[e] = __fadd_rn(a[e], c[e]);
+      st_blk(acc + r * k.stride_bytes + 32 * b, pack16_rne(a));
+    }
+  });
+}
+
+// Last micro-batch: accumulate and mean all-reduce in one pass, result in acc.
+template <int P>
+__global__ void __launch_bounds__(kThreads) k_allreduce_accum(KCommon k, uint8_t* acc,
+                                                              const uint8_t* micro) {
+  if (!plan_ok(k)) return;
+  for_each_block(k, [&](int64_t, int64_t b, int c) {
+    float mean[16];
+    ring_mean16_accum<P>(acc, micro, k.stride_bytes, 32 * b, c, k.P, mean);
+    store_replicas<P>(acc, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
+  });
+}
+
+// Mean all-reduce with bf16 partial sums on the ring.
+template <int P>
+__global__ void __launch_bounds__(kThreads) k_allreduce_bf16wire(KCommon k, uint8_t* g) {
+  if (!plan_ok(k)) return;
+  for_each_block(k, [&](int64_t, int64_t b, int c) {
+    float mean[16];
+    ring_mean16_bf16wire<P>(g, k.stride_bytes, 32 * b, c, k.P, mean);
+    store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
+  });
+}
+
 // One CTA: merge the tile partials of [tile_begin, tile_end) in float-float in a
 // fixed order, then norm and the clip coefficient min(1, max_norm / (norm +
 // 1e-6)) in double ("Distributed Training: Data Parallel, Model Parallel and
@@ -125,6 +166,28 @@ int launch_allreduce(const Launch& L, void* grads) {
       constexpr bool M = decltype(mc)::value;
       return launch_tiles(L, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
     });
+  });
+}
+
+int launch_accumulate(const Launch& L, void* acc, const void* micro) {
+  return launch_tiles(L, k_accumulate, make_common(L), static_cast<uint8_t*>(acc),
+                      static_cast<const uint8_t*>(micro));
+}
+
+int launch_allreduce_accum(const Launch& L, void* acc, const void* micro) {
+  const KCommon k = make_common(L);
+  return with_P(L.plan->P, [&](auto pc) {
+    constexpr int P = decltype(pc)::value;
+    return launch_tiles(L, k_allreduce_accum<P>, k, static_cast<uint8_t*>(acc),
+                        static_cast<const uint8_t*>(micro));
+  });
+}
+
+int launch_allreduce_bf16wire(const Launch& L, void* grads) {
+  const KCommon k = make_common(L);
+  return with_P(L.plan->P, [&](auto pc) {
+    constexpr int P = decltype(pc)::value;
+    return launch_tiles(L, k_allreduce_bf16wire<P>, k, static_cast<uint8_t*>(grads));
   });
 }
 

@@ -291,6 +291,33 @@ int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean,
                         float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
                         int32_t use_clip_coef, void* stream);
 
+/*
+ * Gradient accumulation ("Distributed Training: Data Parallel, Model Parallel and
+ * FSDP Strategies", "Selecting and Tuning": no_sync on every micro-batch but the
+ * last, "sync only on final micro-batch").  Each rank accumulates its bf16
+ * gradients as autograd does for bf16 gradients: acc = bf16(acc + g), the add in
+ * fp32, rounding to nearest even.
+ * dp_accumulate: acc[r] = bf16(acc[r] + micro[r]) for every replica, buckets [b0,b1).
+ * dp_allreduce_mean_accum: the last micro-batch fused with the sync: every rank's
+ *   bf16(acc + micro) is reduced (ring order, fp32) and the bf16 mean written to
+ *   every replica of acc — one pass instead of dp_accumulate + dp_allreduce_mean.
+ *   acc, micro: bf16 [P][replica_stride].
+ */
+int dp_accumulate(const dp_plan* plan, void* workspace, void* acc, const void* micro, int32_t b0,
+                  int32_t b1, void* stream);
+int dp_allreduce_mean_accum(const dp_plan* plan, void* workspace, void* acc, const void* micro,
+                            int32_t b0, int32_t b1, void* stream);
+
+/*
+ * The mean all-reduce with bf16 on the wire, as a precision comparison
+ * ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 8:
+ * "gradient dtype and communication hooks change both bandwidth and numerical
+ * behavior"): every ring hop's partial sum is rounded to bf16 (the add in fp32),
+ * the owner's sum is divided by P in fp32 and rounded to bf16.  Flat plans only.
+ */
+int dp_allreduce_mean_bf16wire(const dp_plan* plan, void* workspace, void* grads, int32_t b0,
+                               int32_t b1, void* stream);
+
 /* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
 
