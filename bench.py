@@ -388,23 +388,80 @@ def run_gpu(args, rank, local, world):
             grads.copy_(host, non_blocking=True)
             step_fn(step)
         torch.cuda.synchronize()
+        # the host link's own rate on this buffer, for reading the e2e number
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        grads.copy_(host, non_blocking=True)
+        h1.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = host.numel() * host.element_size() / (h0.elapsed_time(h1) * 1e-3) / 1e9
+        # Pipelined: the host-to-device copy runs on its own stream in bucket groups
+        # of about equal size; each group's reduction starts as soon as its bytes
+        # have arrived, so only the last group's reduction and the update pass
+        # follow the copy (flat plans; a mesh plan runs copy-then-step).
+        pipelined = mesh is None
+        copy_stream = torch.cuda.Stream()
+        nb = plan.n_buckets
+        groups, lo_b, acc_len = [], 0, 0
+        target = plan.L / 16
+        for b in range(nb):
+            acc_len += plan.bucket(b)[1]
+            if acc_len >= target or b == nb - 1:
+                groups.append((lo_b, b + 1))
+                lo_b, acc_len = b + 1, 0
+        if pipelined and zero:
+            mean_buf = plan.new_state()
+
+        def e2e_step(step):
+            if not pipelined:
+                grads.copy_(host, non_blocking=True)
+                step_fn(step)
+                return
+            evs = []
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for b0, b1 in groups:
+                    o = plan.bucket(b0)[0]
+                    e = plan.bucket(b1 - 1)[0] + plan.bucket(b1 - 1)[1]
+                    for r in range(P):
+                        grads[r, o:e].copy_(host[r, o:e], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(copy_stream)
+                    evs.append(ev)
+            for (b0, b1), ev in zip(groups, evs):
+                stream.wait_event(ev)
+                if zero:
+                    dps.dp_reduce_scatter_mean(plan, ws, grads, mean_buf, b0, b1, want_sumsq=clip)
+                else:
+                    dps.dp_allreduce_mean(plan, ws, grads, b0, b1)
+            if zero:
+                if clip:
+                    dps.dp_clip_coef(plan, ws, wl.adamw.max_norm)
+                dps.dp_adamw_all_gather(plan, ws, mean_buf, master, m, v, params, cfg(step),
+                                        use_clip_coef=clip)
+
+        e2e_step(step + 1)                  # untimed: the pipelined path once
+        step += 1
+        torch.cuda.synchronize()
         barrier(world)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             step += 1
-            grads.copy_(host, non_blocking=True)
+            e2e_step(step)
             if zero:
-                step_fn(step)
                 dps.dp_read_norm(plan, ws)
             else:
-                step_fn(step)
                 torch.cuda.synchronize()
         torch.cuda.synchronize()
         e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
         result["e2e"] = {"value": n_params * world / e2e_s, "unit": "params/s",
                          "h2d_bytes_per_step": host.numel() * host.element_size(),
                          "d2h_bytes_per_step": 192 if zero else 0,
-                         "steps": e2e_steps}
+                         "steps": e2e_steps, "h2d_gbs_alone": h2d_gbs,
+                         "copy": (f"pipelined: {len(groups)} bucket groups, reduction overlapped "
+                                  "with the copy" if pipelined else "copy, then the step")}
+        if pipelined and zero:
+            del mean_buf
         del host
 
     # ---- CPU oracle baseline (rank 0, N=1 only) ----
@@ -565,6 +622,40 @@ def run_zero3(args):
         if evs:
             evs[3].record(stream)
 
+    graph = None
+    if args.graph:
+        # the two unit passes (their launches carry no step-dependent scalars) are
+        # captured once and replayed; the clip and the update stay eager
+        def passes():
+            for b in reversed(range(nb)):
+                dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
+            for b in range(nb):
+                o, ln, _ = buckets[b]
+                dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
+                dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            passes()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            passes()
+
+        def step(t, evs=None):  # noqa: F811  (graph-replay variant of the step above)
+            cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
+            if evs:
+                evs[0].record(stream)
+                evs[1].record(stream)
+            graph.replay()
+            if evs:
+                evs[2].record(stream)
+            dps.dp_clip_coef(plan, ws, a.max_norm)
+            dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
+            if evs:
+                evs[3].record(stream)
+
     for t in range(1, args.warmup + 1):
         step(t)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
@@ -585,7 +676,8 @@ def run_zero3(args):
         "gbs": bytes_pp * n / (ms * 1e-3) / 1e9, "bytes_per_param": bytes_pp,
         "resident_bytes_per_param_all_ranks": 2 + 4 + 12,
         "transient_bytes": unit_buf.numel() * 2,
-        "config": {"workload": wl.name, "P": P, "n_units": nb},
+        "config": {"workload": wl.name, "P": P, "n_units": nb,
+                   "launch": "CUDA graph (unit passes)" if graph is not None else "host launches"},
     }
 
 
@@ -677,6 +769,120 @@ def run_accum(args):
     }
 
 
+def run_sweep(args):
+    """Bucket-size sweep on the 6024-tensor P=16 case (24 matrices of 1024x4096 and
+    6000 log-uniform 4K-64K vectors): per bucket cap and mode, the bucket and launch
+    counts, the padding fraction, and the step time with one launch over the whole
+    tile table, with one launch per bucket (DDP's granularity) issued from the host,
+    and with those per-bucket launches replayed from a CUDA graph."""
+    import gradient_sync_zero_gb300 as dps
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    rows = []
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / reps
+
+    for cap in configs.SWEEP_BUCKETS:
+        for mode in ("allreduce", "zero"):
+            wl = configs.sweep_small_tensors(cap, mode)
+            plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+            off = plan.tensor_offsets()
+            ws = plan.new_workspace()
+            grads = plan.new_replicas()
+            wdev.fill_grads(grads, off, wl, step=1)
+            nb, P, n = plan.n_buckets, plan.P, wl.n_params
+            a = wl.adamw
+            cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1)
+            if mode == "zero":
+                params = plan.new_replicas()
+                master = plan.new_state()
+                wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
+                m, v, mean = plan.new_state(), plan.new_state(), plan.new_state()
+
+                def single():
+                    dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg)
+
+                def buckets():
+                    for b in range(nb):
+                        dps.dp_reduce_scatter_mean(plan, ws, grads, mean, b, b + 1, want_sumsq=True)
+
+                def tail():
+                    dps.dp_clip_coef(plan, ws, a.max_norm)
+                    dps.dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg)
+
+                launches_single = dps.dp_fused_zero_step_launches(cfg)
+                launches_bucket = nb + 2
+                bpp = 4 * P + 32
+            else:
+                def single():
+                    dps.dp_allreduce_mean(plan, ws, grads)
+
+                def buckets():
+                    for b in range(nb):
+                        dps.dp_allreduce_mean(plan, ws, grads, b, b + 1)
+
+                def tail():
+                    pass
+
+                launches_single, launches_bucket, bpp = 1, nb, 4 * P
+            reps = max(3, args.steps // 5)
+            t_single = timed(single, reps)
+
+            def per_bucket():
+                buckets()
+                tail()
+
+            t_bucket = timed(per_bucket, reps)
+            graph_ms, graph_note = None, ""
+            try:
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    buckets()                      # warm the host-side caches off capture
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g):
+                    buckets()
+
+                def graphed():
+                    g.replay()
+                    tail()
+
+                graph_ms = timed(graphed, reps)
+                del g
+            except Exception as e:  # noqa: BLE001  (reported in the line, not hidden)
+                graph_note = f"graph capture failed: {e}"
+            rows.append({
+                "bucket_bytes": cap, "mode": mode, "n_buckets": nb, "n_tiles": plan.info.n_tiles,
+                "padding_frac": (plan.L - n) / n,
+                "launches": {"single": launches_single, "per_bucket": launches_bucket},
+                "ms": {"single": t_single, "per_bucket_host": t_bucket, "per_bucket_graph": graph_ms},
+                "gbs_single": bpp * n / (t_single * 1e-3) / 1e9, "bytes_per_param": bpp,
+                **({"note": graph_note} if graph_note else {}),
+            })
+            del grads, ws
+            if mode == "zero":
+                del params, master, m, v, mean
+            torch.cuda.empty_cache()
+    return {"metric": "bucket-size sweep: ms per step, single launch vs per-bucket launches",
+            "unit": "ms", "rows": rows,
+            "config": {"workload": "sweep-P16 (6024 tensors)", "P": 16,
+                       "n_params": configs.sweep_small_tensors().n_params,
+                       "clip_max_norm": configs.sweep_small_tensors().adamw.max_norm,
+                       "l2": "inputs > L2 (7.5 GB per replica set)"}}
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded sample."""
     import numpy as np
@@ -740,6 +946,10 @@ def main(argv=None):
     ap.add_argument("--mesh", default="",
                     help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
     ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --zero3: replay the unit passes from a CUDA graph")
+    ap.add_argument("--sweep", action="store_true",
+                    help="bucket-size sweep: single launch vs per-bucket launches")
     ap.add_argument("--accum", type=int, default=0,
                     help="time k-micro-batch gradient accumulation and the bf16-wire ring")
     ap.add_argument("--streamed", action="store_true",
@@ -767,6 +977,9 @@ def main(argv=None):
         return
     if args.accum:
         print(json.dumps(run_accum(args)), flush=True)
+        return
+    if args.sweep:
+        print(json.dumps(run_sweep(args)), flush=True)
         return
     rank, local, world = dist_setup()
     res = run_gpu(args, rank, local, world)

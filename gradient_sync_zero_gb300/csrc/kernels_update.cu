@@ -47,14 +47,29 @@ __global__ void __launch_bounds__(kThreads)
 
 // ZeRO-3 unit all-gather: every rank's row of the unit buffer receives the unit's
 // shard values (the flat shard array holds each element once, at its owner).
+// A unit is one launch of a few waves, so the unit's blocks are split into equal
+// contiguous shares per CTA (not whole tiles, which would leave the last wave
+// partly idle); each thread keeps 4 loads in flight.
 __global__ void __launch_bounds__(kThreads)
     k_unit_all_gather(KCommon k, const uint8_t* shards, uint8_t* out, int64_t out_stride_bytes,
-                      int64_t block0) {
+                      int64_t block0, int64_t n_blk) {
   if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int) {
-    const Blk val = ld_blk(shards + 32 * b);
-    for (int r = 0; r < k.P; ++r) st_blk(out + r * out_stride_bytes + 32 * (b - block0), val);
-  });
+  constexpr int D = 4;
+  const int64_t G = gridDim.x;
+  const int64_t lo = block0 + n_blk * blockIdx.x / G;
+  const int64_t hi = block0 + n_blk * (blockIdx.x + 1) / G;
+  for (int64_t b0 = lo + threadIdx.x; b0 < hi; b0 += D * kThreads) {
+    Blk val[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d)
+      if (b0 + d * kThreads < hi) val[d] = ld_blk(shards + 32 * (b0 + d * kThreads));
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      const int64_t b = b0 + d * kThreads;
+      if (b >= hi) break;
+      for (int r = 0; r < k.P; ++r) st_blk(out + r * out_stride_bytes + 32 * (b - block0), val[d]);
+    }
+  }
 }
 
 // In-place all-gather: the owner's slice of each shard goes to every other replica.
@@ -220,9 +235,20 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
 }
 
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
-                           int64_t block0) {
-  return launch_tiles(L, k_unit_all_gather, make_common(L), static_cast<const uint8_t*>(shards),
-                      static_cast<uint8_t*>(out), 2 * out_stride, block0);
+                           int64_t block0, int64_t n_blk) {
+  if (n_blk <= 0) return cudaSuccess;
+  const int cap = resident_ctas(k_unit_all_gather, kThreads);
+  if (cap <= 0) {
+    const cudaError_t e = cudaGetLastError();
+    return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
+  }
+  const int64_t want = (n_blk + kThreads - 1) / kThreads;
+  int64_t g = want < cap ? want : cap;
+  if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
+  k_unit_all_gather<<<static_cast<int>(g), kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(
+      make_common(L), static_cast<const uint8_t*>(shards), static_cast<uint8_t*>(out), 2 * out_stride,
+      block0, n_blk);
+  return static_cast<int>(cudaGetLastError());
 }
 
 int launch_all_gather(const Launch& L, void* params) {
