@@ -15,12 +15,15 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libdpsync.so")
+# DPSYNC_VARIANT=checked loads the build with device index checks compiled in.
+VARIANT = os.environ.get("DPSYNC_VARIANT", "")
+LIB_PATH = os.path.join(HERE, "libdpsync_checked.so" if VARIANT == "checked" else "libdpsync.so")
 
 DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ETIMEOUT = \
     0, -1, -2, -3, -4, -5, -6, -7
 DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT = 1, 2, 4
 DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_DRY_RUN = 0, 1, 1
+DP_CKPT_HOST = 1
 
 
 class DPError(RuntimeError):
@@ -76,6 +79,9 @@ def lib():
             "dp_tracker_create": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
             "dp_unit_all_gather": [vp, vp, vp, i32, vp, i64, vp],
             "dp_accumulate": [vp, vp, vp, vp, i32, i32, vp],
+            "dp_selftest_bounded_wait": [vp, i64, vp],
+            "dp_checkpoint_save": [vp, C.c_char_p, vp, vp, vp, i64, i32, vp],
+            "dp_checkpoint_load": [vp, C.c_char_p, vp, vp, vp, C.POINTER(i64), i32, vp],
             "dp_allreduce_mean_accum": [vp, vp, vp, vp, i32, i32, vp],
             "dp_allreduce_mean_bf16wire": [vp, vp, vp, i32, i32, vp],
             "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
@@ -93,6 +99,8 @@ def lib():
         L.dp_plan_free.restype = None
         L.dp_tracker_free.argtypes = [vp]
         L.dp_tracker_free.restype = None
+        L.dp_bounds_violations.argtypes = [i32]
+        L.dp_bounds_violations.restype = i64
         L.dp_last_error.argtypes = []
         L.dp_last_error.restype = C.c_char_p
         L.dp_version.restype = C.c_int
@@ -375,6 +383,59 @@ def dp_allreduce_mean_bf16wire(plan, ws, grads, b0=0, b1=None, stream=None):
     b0, b1 = _range(plan, b0, b1)
     _check(lib().dp_allreduce_mean_bf16wire(plan.handle, _ws(plan, ws), _ptr(grads), b0, b1,
                                             _stream(stream)))
+
+
+def _state_arrays(plan, arrays, fn):
+    """The optimizer-state arrays for a checkpoint call: fp32, contiguous, >= L
+    elements, all on the host or all on the GPU.  Returns (pointers, host?)."""
+    host = None
+    for name, t in zip(("master", "m", "v"), arrays):
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError(f"{fn}: {name} must be a contiguous float32 tensor")
+        if t.numel() < plan.L:
+            raise ValueError(f"{fn}: {name} holds {t.numel()} elements, needs {plan.L}")
+        h = t.device.type == "cpu"
+        if host is not None and h != host:
+            raise ValueError(f"{fn}: arrays must all be on the host or all on the GPU")
+        host = h
+    return [_ptr(t) for t in arrays], host is None or host   # no array: refused, no CUDA call
+
+
+def dp_checkpoint_save(plan, path, master=None, m=None, v=None, step=0, stream=None):
+    """Write master/m/v (flat layout of `plan`, tensor order in the file) and t."""
+    ptrs, host = _state_arrays(plan, (master, m, v), "dp_checkpoint_save")
+    _check(lib().dp_checkpoint_save(plan.handle, os.fsencode(path), *ptrs, int(step),
+                                    DP_CKPT_HOST if host else 0,
+                                    None if host else _stream(stream)))
+
+
+def dp_checkpoint_load(plan, path, master=None, m=None, v=None, stream=None):
+    """Read a checkpoint into master/m/v (any plan over the same tensor sizes);
+    returns the saved step t."""
+    ptrs, host = _state_arrays(plan, (master, m, v), "dp_checkpoint_load")
+    step = C.c_int64(0)
+    _check(lib().dp_checkpoint_load(plan.handle, os.fsencode(path), *ptrs, C.byref(step),
+                                    DP_CKPT_HOST if host else 0,
+                                    None if host else _stream(stream)))
+    return step.value
+
+
+def dp_selftest_bounded_wait(limit_ns=1_000_000, stream=None):
+    """Run the bounded-wait failure path once; returns (status, ms waited)."""
+    st = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    _check(lib().dp_selftest_bounded_wait(_ptr(st), int(limit_ns), _stream(stream)))
+    s, ms = st.tolist()
+    return s, ms
+
+
+def dp_bounds_violations(reset=False):
+    """Failed device index checks since the last reset (-1: library built without checks)."""
+    n = lib().dp_bounds_violations(1 if reset else 0)
+    if n == -2:
+        raise DPError(DP_ECUDA, "dp_bounds_violations: cannot read the device counters")
+    return n
 
 
 def dp_fused_zero_step_launches(cfg):

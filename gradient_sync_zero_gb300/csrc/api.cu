@@ -254,6 +254,26 @@ int dp_allreduce_mean_bf16wire(const dp_plan* plan, void* workspace, void* grads
   return e ? cuda_fail(e, "dp_allreduce_mean_bf16wire") : DP_OK;
 }
 
+int dp_selftest_bounded_wait(int32_t* status_dev, int64_t limit_ns, void* stream) {
+  clear_error();
+  if (!status_dev) return fail(DP_EINVAL, "dp_selftest_bounded_wait: NULL status");
+  if (reinterpret_cast<uintptr_t>(status_dev) & 7u)
+    return fail(DP_EALIGN, "dp_selftest_bounded_wait: status must be 8-byte aligned");
+  if (limit_ns < 1000 || limit_ns > 10000000000LL)
+    return fail(DP_EINVAL, "dp_selftest_bounded_wait: limit_ns outside [1e3, 1e10]");
+  const int e = launch_selftest_wait(status_dev, static_cast<uint64_t>(limit_ns), stream);
+  return e ? cuda_fail(e, "dp_selftest_bounded_wait") : DP_OK;
+}
+
+int64_t dp_bounds_violations(int32_t reset) {
+  clear_error();
+  const int64_t a = bounds_violations_reduce(reset != 0);
+  const int64_t b = bounds_violations_update(reset != 0);
+  if (a == -1 && b == -1) return -1;
+  if (a < 0 || b < 0) return -2;
+  return a + b;
+}
+
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
   return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
 }

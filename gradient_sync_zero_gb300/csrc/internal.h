@@ -104,6 +104,11 @@ int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64
                            int64_t block0, int64_t n_blk);
 int launch_allreduce(const Launch& L, void* grads);
 int launch_accumulate(const Launch& L, void* acc, const void* micro);
+int launch_selftest_wait(int32_t* status, uint64_t limit_ns, void* stream);
+// Checked build: failed index checks counted by each kernel translation unit
+// (-1 in the normal build, -2 if the counter cannot be read).
+int64_t bounds_violations_reduce(bool reset);
+int64_t bounds_violations_update(bool reset);
 int launch_allreduce_accum(const Launch& L, void* acc, const void* micro);
 int launch_allreduce_bf16wire(const Launch& L, void* grads);
 int launch_norm_finalize(const Launch& L, double max_norm);

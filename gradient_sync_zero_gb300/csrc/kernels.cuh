@@ -40,6 +40,22 @@ struct KCommon {
   int64_t rep_block0;    // replica buffers start at this 32-byte block (unit buffers)
 };
 
+// ---- optional index checks (built with -DDPSYNC_CHECKED) ----
+// The checked build tests every tile descriptor, block index, owner and replica
+// index against the plan before the access it guards.  A failed check is counted
+// in this translation unit's device counter and the access is skipped or sent to
+// replica 0 — never a trap.  In the normal build the checks compile away.
+#ifdef DPSYNC_CHECKED
+static __device__ unsigned long long g_bounds_violations;
+__device__ __forceinline__ bool bounds_ok(bool ok) {
+  if (!ok) atomicAdd(&g_bounds_violations, 1ull);
+  return ok;
+}
+#define DP_IN_BOUNDS(cond) (::dps::bounds_ok(cond))
+#else
+#define DP_IN_BOUNDS(cond) (true)
+#endif
+
 // ---- 256-bit streaming accesses (sm_100-family ld/st .v8.b32) ----
 // Every global access is volatile asm, so the compiler keeps them in program
 // order (loads of a block are issued before its stores, never re-issued).
@@ -131,6 +147,7 @@ __device__ __forceinline__ void ring_fold_chunk(const uint8_t* g, int64_t stride
     if (P == 0 && k0 + k >= np) break;
     int r = r_first + k0 + k;
     if (r >= np) r -= np;
+    if (!DP_IN_BOUNDS(r >= 0 && r < np)) r = 0;
     x[k] = ld_blk(g + r * stride_bytes + byte_off);
   }
 #pragma unroll
@@ -195,7 +212,9 @@ __device__ __forceinline__ void mesh_mean16(const uint8_t* g, int64_t stride_byt
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       if (k0 + k >= np) break;
-      x[k] = ld_blk(g + (gg * S + mm) * stride_bytes + byte_off);
+      int rr = gg * S + mm;
+      if (!DP_IN_BOUNDS(rr >= 0 && rr < np)) rr = 0;
+      x[k] = ld_blk(g + rr * stride_bytes + byte_off);
       if (++sii == S) {
         sii = 0;
         gg = (gg + 1 == R) ? 0 : gg + 1;
@@ -270,6 +289,7 @@ __device__ __forceinline__ void ring_mean16_accum(const uint8_t* acc, const uint
       if (k0 + k >= np) break;
       int r = r_first + k0 + k;
       if (r >= np) r -= np;
+      if (!DP_IN_BOUNDS(r >= 0 && r < np)) r = 0;
       x[k] = ld_blk(acc + r * stride_bytes + byte_off);
       y[k] = ld_blk(micro + r * stride_bytes + byte_off);
     }
@@ -308,6 +328,7 @@ __device__ __forceinline__ void ring_mean16_bf16wire(const uint8_t* g, int64_t s
       if (k0 + k >= np) break;
       int r = r_first + k0 + k;
       if (r >= np) r -= np;
+      if (!DP_IN_BOUNDS(r >= 0 && r < np)) r = 0;
       x[k] = ld_blk(g + r * stride_bytes + byte_off);
     }
 #pragma unroll
@@ -448,11 +469,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Bounded wait: gives up after kMbarSpins polls (each poll may suspend briefly).
-constexpr uint32_t kMbarSpins = 1u << 24;
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMbarSpins; ++i)
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: polls until the phase completes or limit_ns of the global timer
+// have passed (1 s unless told otherwise); false on timeout.  2^32 polls end it
+// as well, should the timer not advance.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i != 0; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
   return false;
 }
 
@@ -511,6 +545,15 @@ __device__ __forceinline__ TileDesc load_tile(const KCommon& k, int64_t tile) {
   return d;
 }
 
+// Checked build: the descriptor lies inside the plan (even start and count,
+// within [0, n_vec), a shard of at least one block).  The same for every thread
+// of the CTA, so a skipped tile is skipped by all of them.
+__device__ __forceinline__ bool tile_ok(const KCommon& k, int64_t tile, const TileDesc& d) {
+  return DP_IN_BOUNDS(tile >= 0 && tile < k.hdr->n_tiles && d.v0 >= 0 && (d.v0 & 1) == 0 &&
+                      d.nvec >= 0 && (d.nvec & 1) == 0 && d.v0 + d.nvec <= k.hdr->n_vec &&
+                      d.svec >= 2 && d.bvoff >= 0 && d.bvoff <= d.v0);
+}
+
 // Owner (shard index) of 16-byte vector v in its bucket.
 __device__ __forceinline__ int owner_of(const TileDesc& d, int64_t v) {
   return static_cast<int>(static_cast<uint32_t>(v - d.bvoff) / static_cast<uint32_t>(d.svec));
@@ -522,12 +565,15 @@ template <class F>
 __device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
   for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
     const TileDesc d = load_tile(k, tile);
+    if (!tile_ok(k, tile, d)) continue;
     const int nblk = d.nvec >> 1;
     const int64_t b0 = d.v0 >> 1;
 #pragma unroll 1
     for (int j = threadIdx.x; j < nblk; j += kThreads) {
       const int64_t b = b0 + j;
-      f(tile, b, owner_of(d, 2 * b));
+      const int c = owner_of(d, 2 * b);
+      if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+      f(tile, b, c);
     }
   }
 }
@@ -537,12 +583,15 @@ template <class F>
 __device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
   for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
     const TileDesc d = load_tile(k, tile);
+    if (!tile_ok(k, tile, d)) continue;
     const int nblk = d.nvec >> 1;
     const int64_t b0 = d.v0 >> 1;
 #pragma unroll 1
     for (int j = threadIdx.x; j < nblk; j += kThreads) {
       const int64_t b = b0 + j;
-      f(d, b, owner_of(d, 2 * b));
+      const int c = owner_of(d, 2 * b);
+      if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+      f(d, b, c);
     }
   }
 }

@@ -27,14 +27,17 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
   __shared__ FF warp_part[kWarps];
   for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
     const TileDesc d = load_tile(k, tile);
+    if (!tile_ok(k, tile, d)) continue;
     const int nblk = d.nvec >> 1;
     const int64_t b0 = d.v0 >> 1;
     FF ss{0.0f, 0.0f};
 #pragma unroll 1
     for (int j = threadIdx.x; j < nblk; j += kThreads) {
       const int64_t b = b0 + j;
+      const int c = owner_of(d, 2 * b);
+      if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
       float acc[16];
-      block_mean16<P, MESH>(k, g, b, d, owner_of(d, 2 * b), acc);
+      block_mean16<P, MESH>(k, g, b, d, c, acc);
       st_f16(mean, b, acc);
       if (sumsq) {
 #pragma unroll
@@ -167,6 +170,21 @@ int launch_allreduce(const Launch& L, void* grads) {
       return launch_tiles(L, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
     });
   });
+}
+
+int64_t bounds_violations_reduce(bool reset) {
+#ifdef DPSYNC_CHECKED
+  unsigned long long n = 0;
+  if (cudaMemcpyFromSymbol(&n, g_bounds_violations, sizeof n) != cudaSuccess) return -2;
+  if (reset) {
+    const unsigned long long z = 0;
+    if (cudaMemcpyToSymbol(g_bounds_violations, &z, sizeof z) != cudaSuccess) return -2;
+  }
+  return static_cast<int64_t>(n);
+#else
+  (void)reset;
+  return -1;
+#endif
 }
 
 int launch_accumulate(const Launch& L, void* acc, const void* micro) {

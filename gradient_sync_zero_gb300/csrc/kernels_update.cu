@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kThreads)
     k_unit_all_gather(KCommon k, const uint8_t* shards, uint8_t* out, int64_t out_stride_bytes,
                       int64_t block0, int64_t n_blk) {
   if (!plan_ok(k)) return;
+  if (!DP_IN_BOUNDS(block0 >= 0 && n_blk >= 0 && 2 * (block0 + n_blk) <= k.hdr->n_vec)) return;
   constexpr int D = 4;
   const int64_t G = gridDim.x;
   const int64_t lo = block0 + n_blk * blockIdx.x / G;
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads)
                        float* v, AdamScalars s, int64_t L, int use_coef) {
   constexpr int kPer = kTmaChunk / kThreads;   // elements per thread per chunk (multiple of 4)
   if (!plan_ok(k)) return;
+  if (!DP_IN_BOUNDS(L >= 0 && L <= kVecElems * k.hdr->n_vec)) return;
   const int64_t nchunks = (L + kTmaChunk - 1) / kTmaChunk;
   if (static_cast<int64_t>(blockIdx.x) >= nchunks) return;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -226,6 +228,41 @@ __global__ void __launch_bounds__(kThreads)
     }
     bulk_wait_all();
   }
+}
+
+// Failure-path check of the bounded wait: one thread arms an mbarrier for 16
+// bytes that no copy will ever deliver, waits with the bulk-copy kernels' bounded
+// wait, and reports the timeout.  Nothing is in flight when it returns.
+__global__ void k_selftest_wait(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_arrive_expect_tx(&bar, 16u);
+  const uint64_t t0 = global_ns();
+  const bool ok = mbar_wait_bounded(&bar, 0u, limit_ns);
+  status[0] = ok ? 0 : DP_STATUS_TIMEOUT;
+  status[1] = static_cast<int32_t>((global_ns() - t0) / 1000000ull);  // ms waited
+}
+
+int launch_selftest_wait(int32_t* status, uint64_t limit_ns, void* stream) {
+  k_selftest_wait<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int64_t bounds_violations_update(bool reset) {
+#ifdef DPSYNC_CHECKED
+  unsigned long long n = 0;
+  if (cudaMemcpyFromSymbol(&n, g_bounds_violations, sizeof n) != cudaSuccess) return -2;
+  if (reset) {
+    const unsigned long long z = 0;
+    if (cudaMemcpyToSymbol(g_bounds_violations, &z, sizeof z) != cudaSuccess) return -2;
+  }
+  return static_cast<int64_t>(n);
+#else
+  (void)reset;
+  return -1;
+#endif
 }
 
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,

@@ -318,6 +318,59 @@ int dp_allreduce_mean_accum(const dp_plan* plan, void* workspace, void* acc, con
 int dp_allreduce_mean_bf16wire(const dp_plan* plan, void* workspace, void* grads, int32_t b0,
                                int32_t b1, void* stream);
 
+/*
+ * Checkpoint and resume of the optimizer state (fp32 master, m, v in the plan's
+ * flat layout, and the step t).  The pages name the optimizer state as what a
+ * ZeRO step carries between steps ("Data Parallelism: DDP, ZeRO and FSDP", "The
+ * three stages"; "4.1 Data parallelism in depth", sec. 7) and note FSDP2's clearer
+ * checkpoint semantics (sec. 6.4); the file format is this library's own.
+ * The file holds the arrays in tensor order without padding, so a checkpoint
+ * saved under one plan loads into any plan over the same tensor sizes (another
+ * bucket size, rank count or mesh).  Layout, little-endian: 80-byte header
+ * (magic "DPSYNCK1", u32 version 1, u32 arrays mask: bit 0 master, 1 m, 2 v;
+ * i64 n_tensors, n_params, step; u64 checksum; i32 P, R, S, 0; i64 bucket_bytes;
+ * 8 zero bytes), i64 sizes[n_tensors], then each present array as f32[n_params].
+ * checksum: 64-bit FNV-1a over the bytes after the header in 8-byte
+ * little-endian words (last word zero-padded).
+ *
+ * save: a NULL array is left out (at least one is required).  Writes path.tmp,
+ *   then renames it over path.  Synchronises `stream` first (device mode).
+ * load: a NULL destination skips that array; a requested array the file lacks is
+ *   DP_EINVAL; tensor sizes that differ from the plan's are DP_EPLAN (checked before
+ *   anything is written).  Padding slots are set to 0.  A checksum mismatch is
+ *   found at the end (DP_EINVAL; the destinations then hold partial data).  *step
+ *   (nullable) receives t.  Synchronous on `stream`.
+ * flags: DP_CKPT_HOST = the arrays are host memory (no CUDA call is made).
+ * Errors: DP_EINVAL (path, I/O, format), DP_EPLAN, DP_ENOMEM, DP_ECUDA.
+ */
+#define DP_CKPT_HOST 1
+int dp_checkpoint_save(const dp_plan* plan, const char* path, const float* master, const float* m,
+                       const float* v, int64_t step, int32_t flags, void* stream);
+int dp_checkpoint_load(const dp_plan* plan, const char* path, float* master, float* m, float* v,
+                       int64_t* step, int32_t flags, void* stream);
+
+/*
+ * Failure detection without a GPU fault.  The pages' hangs come from waits that
+ * never end (an unready bucket, "4.1 Data parallelism in depth", sec. 4.2 note);
+ * here every device wait is bounded.  This call checks that path: one CTA arms a
+ * shared-memory mbarrier for 16 bytes that no copy delivers, waits with the same
+ * bounded wait the bulk-copy kernels use (limit_ns of the global timer, in
+ * [1e3, 1e10]), writes status_dev[0] = DP_STATUS_TIMEOUT (0 had the wait
+ * completed) and status_dev[1] = milliseconds waited, and returns.  The context
+ * stays usable.  status_dev: device int32[2], 8-byte aligned.  Asynchronous.
+ */
+int dp_selftest_bounded_wait(int32_t* status_dev, int64_t limit_ns, void* stream);
+
+/*
+ * Index checks.  A library built with -DDPSYNC_CHECKED (libdpsync_checked.so)
+ * tests every tile descriptor, block index, shard owner and replica index against
+ * the plan before the access; a failed check is counted and the access skipped,
+ * never trapped (the stand-in for a memory checker).  Returns the count since the
+ * last reset (reset != 0 zeroes it; synchronises the device), -1 for a library
+ * built without checks, -2 if the counters cannot be read.
+ */
+int64_t dp_bounds_violations(int32_t reset);
+
 /* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
 
