@@ -24,6 +24,7 @@ parameters / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -240,6 +241,8 @@ def run_gpu(args, rank, local, world):
 
     torch.cuda.set_device(local)
     wl = workload_by_name(args.workload)
+    if args.max_norm is not None:
+        wl.adamw = dataclasses.replace(wl.adamw, max_norm=args.max_norm)
     mesh = tuple(int(x) for x in args.mesh.split(",")) if args.mesh else None
     plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay, mesh=mesh)
     P, L, stride = plan.P, plan.L, plan.stride
@@ -946,6 +949,8 @@ def main(argv=None):
     ap.add_argument("--mesh", default="",
                     help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
     ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
+    ap.add_argument("--max-norm", type=float, default=None,
+                    help="override the workload's clip threshold (0 = no clipping: one fused pass)")
     ap.add_argument("--graph", action="store_true",
                     help="with --zero3: replay the unit passes from a CUDA graph")
     ap.add_argument("--sweep", action="store_true",
