@@ -448,19 +448,35 @@ def run_gpu(args, rank, local, world):
         torch.cuda.synchronize()
         barrier(world)
         t0 = time.perf_counter()
+        step_ms = []
         for _ in range(e2e_steps):
             step += 1
+            ts = time.perf_counter()
             e2e_step(step)
             if zero:
                 dps.dp_read_norm(plan, ws)
             else:
                 torch.cuda.synchronize()
+            step_ms.append((time.perf_counter() - ts) * 1e3)
         torch.cuda.synchronize()
         e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+        # the copies alone, in the same groups, for reading the number
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for b0, b1 in groups:
+            o = plan.bucket(b0)[0]
+            e = plan.bucket(b1 - 1)[0] + plan.bucket(b1 - 1)[1]
+            for r in range(P):
+                grads[r, o:e].copy_(host[r, o:e], non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        copy_only_ms = c0.elapsed_time(c1)
         result["e2e"] = {"value": n_params * world / e2e_s, "unit": "params/s",
                          "h2d_bytes_per_step": host.numel() * host.element_size(),
                          "d2h_bytes_per_step": 192 if zero else 0,
                          "steps": e2e_steps, "h2d_gbs_alone": h2d_gbs,
+                         "step_ms": [round(x, 2) for x in step_ms],
+                         "grouped_copies_alone_ms": round(copy_only_ms, 2),
                          "copy": (f"pipelined: {len(groups)} bucket groups, reduction overlapped "
                                   "with the copy" if pipelined else "copy, then the step")}
         if pipelined and zero:

@@ -253,17 +253,73 @@ __device__ __forceinline__ void mesh_mean16(const uint8_t* g, int64_t stride_byt
   for (int e = 0; e < 16; ++e) acc[e] = __fdiv_rn(acc[e], fp);
 }
 
-// The mean of block b for its owner, flat ring or hybrid mesh.  s = shard index
-// in the bucket (the owner rank on a flat ring).
-template <int P, bool MESH>
+// The same fold with P and the group size S known at compile time (P a multiple
+// of 8 and of S): the rank order is fixed by (s, j) alone, so the loop unrolls
+// like the flat ring's, 8 blocks in flight, whole groups per batch.
+template <int P, int S>
+__device__ __forceinline__ void mesh_mean16_ct(const uint8_t* g, int64_t stride_bytes,
+                                               int64_t byte_off, int s, int j, float (&acc)[16]) {
+  static_assert(P % 8 == 0 && 8 % S == 0 && P % S == 0, "whole groups per batch of 8");
+  constexpr int R = P / S;
+  float inner[16];
+#pragma unroll
+  for (int k0 = 0; k0 < P; k0 += 8) {
+    Blk x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int q = k0 + k;                       // position in the fold order
+      int grp = j + 1 + q / S;                    // < 2R
+      grp -= (grp >= R) ? R : 0;
+      int mem = s + 1 + q % S;                    // < 2S
+      mem -= (mem >= S) ? S : 0;
+      int rr = grp * S + mem;
+      if (!DP_IN_BOUNDS(rr >= 0 && rr < P)) rr = 0;
+      x[k] = ld_blk(g + rr * stride_bytes + byte_off);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int q = k0 + k;
+      float t[16];
+      unpack16(x[k], t);
+      if (q % S == 0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) inner[e] = t[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) inner[e] = __fadd_rn(inner[e], t[e]);
+      }
+      if (q % S == S - 1) {
+        if (q / S == 0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = inner[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] = __fadd_rn(acc[e], inner[e]);
+        }
+      }
+    }
+  }
+  constexpr float inv = 1.0f / P;                 // P is a power of two: exact
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = __fmul_rn(acc[e], inv);
+}
+
+// The mean of block b for its owner: MS = 0 flat ring, MS > 0 hybrid mesh with
+// group size MS fixed at compile time, MS < 0 hybrid mesh with the shape read
+// at run time.  s = shard index in the bucket (the owner rank on a flat ring).
+template <int P, int MS>
 __device__ __forceinline__ void block_mean16(const KCommon& k, const uint8_t* g, int64_t b,
                                              const TileDesc& d, int s, float (&acc)[16]) {
-  if constexpr (!MESH) {
+  if constexpr (MS == 0) {
     ring_mean16<P>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, k.P, acc);
   } else {
     const uint32_t within = static_cast<uint32_t>(2 * b - d.bvoff) % static_cast<uint32_t>(d.svec);
     const int j = static_cast<int>(within / (static_cast<uint32_t>(d.svec) / k.R));
-    mesh_mean16<P>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, j, k.R, k.S, k.P, acc);
+    if constexpr (MS > 0) {
+      mesh_mean16_ct<P, MS>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, j, acc);
+    } else {
+      mesh_mean16<P>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, j, k.R, k.S, k.P, acc);
+    }
   }
 }
 

@@ -20,7 +20,7 @@ namespace dps {
 // ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
 // the exact sum.  Partials are per tile, so the norm does not depend on the grid
 // size or on how the bucket range is split into launches.
-template <int P, bool MESH>
+template <int P, int MS>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint8_t* g,
                                                              float* mean, int sumsq) {
   if (!plan_ok(k)) return;
@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
       const int c = owner_of(d, 2 * b);
       if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
       float acc[16];
-      block_mean16<P, MESH>(k, g, b, d, c, acc);
+      block_mean16<P, MS>(k, g, b, d, c, acc);
       st_f16(mean, b, acc);
       if (sumsq) {
 #pragma unroll
@@ -50,12 +50,12 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
 
 // Fused mean all-reduce in place: sum in ring order, 1/P, bf16, written back to
 // every replica (the all-gather of the reduced shards).
-template <int P, bool MESH>
+template <int P, int MS>
 __global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint8_t* g) {
   if (!plan_ok(k)) return;
   for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
     float acc[16];
-    block_mean16<P, MESH>(k, g, b, d, c, acc);
+    block_mean16<P, MS>(k, g, b, d, c, acc);
     store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(acc), k.P);
   });
 }
@@ -152,9 +152,9 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
   if (rep_stride > 0) k.stride_bytes = 2 * rep_stride;   // replicas in a unit buffer
   k.rep_block0 = rep_block0;
   return with_P(L.plan->P, [&](auto pc) {
-    return with_mesh(L.plan, [&](auto mc) {
-      constexpr int P = decltype(pc)::value;
-      constexpr bool M = decltype(mc)::value;
+    constexpr int P = decltype(pc)::value;
+    return with_mesh<P>(L.plan, [&](auto mc) {
+      constexpr int M = decltype(mc)::value;
       return launch_tiles(L, k_reduce_scatter<P, M>, k, static_cast<const uint8_t*>(grads), mean,
                           sumsq ? 1 : 0);
     });
@@ -164,9 +164,9 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
 int launch_allreduce(const Launch& L, void* grads) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
-    return with_mesh(L.plan, [&](auto mc) {
-      constexpr int P = decltype(pc)::value;
-      constexpr bool M = decltype(mc)::value;
+    constexpr int P = decltype(pc)::value;
+    return with_mesh<P>(L.plan, [&](auto mc) {
+      constexpr int M = decltype(mc)::value;
       return launch_tiles(L, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
     });
   });

@@ -97,14 +97,14 @@ __global__ void __launch_bounds__(kThreads) k_broadcast(KCommon k, uint8_t* para
 // The whole ZeRO-1/2 step without clipping, one pass.  The replica blocks are
 // loaded and folded first, then the fp32 state is loaded, which bounds the live
 // registers to one of the two groups.
-template <int P, bool MESH>
+template <int P, int MS>
 __global__ void __launch_bounds__(kThreads)
     k_zero_fused(KCommon k, const uint8_t* grads, uint8_t* params, float* master, float* m,
                  float* v, AdamScalars s) {
   if (!plan_ok(k)) return;
   for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
     float g[16];
-    block_mean16<P, MESH>(k, grads, b, d, c, g);
+    block_mean16<P, MS>(k, grads, b, d, c, g);
     float th[16], mm[16], vv[16];
     ld_f16(master, b, th);
     ld_f16(m, b, mm);
@@ -300,9 +300,9 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
                       float* v, const AdamScalars& s) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
-    return with_mesh(L.plan, [&](auto mc) {
-      constexpr int P = decltype(pc)::value;
-      constexpr bool M = decltype(mc)::value;
+    constexpr int P = decltype(pc)::value;
+    return with_mesh<P>(L.plan, [&](auto mc) {
+      constexpr int M = decltype(mc)::value;
       return launch_tiles(L, k_zero_fused<P, M>, k, static_cast<const uint8_t*>(grads),
                           static_cast<uint8_t*>(params), master, m, v, s);
     });

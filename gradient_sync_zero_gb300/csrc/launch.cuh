@@ -102,10 +102,21 @@ int with_P(int P, F&& f) {
   }
 }
 
-// Flat ring or hybrid mesh instantiation.
-template <class F>
+// Flat ring (0), hybrid mesh with the group size S known at compile time (S,
+// for the common shapes of 8 and 16 ranks), or with S read at run time (-1).
+template <int P, class F>
 int with_mesh(const Plan* pl, F&& f) {
-  return pl->R > 1 ? f(std::true_type{}) : f(std::false_type{});
+  if (pl->R == 1) return f(std::integral_constant<int, 0>{});
+  if constexpr (P == 8) {
+    if (pl->S == 2) return f(std::integral_constant<int, 2>{});
+    if (pl->S == 4) return f(std::integral_constant<int, 4>{});
+  }
+  if constexpr (P == 16) {
+    if (pl->S == 2) return f(std::integral_constant<int, 2>{});
+    if (pl->S == 4) return f(std::integral_constant<int, 4>{});
+    if (pl->S == 8) return f(std::integral_constant<int, 8>{});
+  }
+  return f(std::integral_constant<int, -1>{});
 }
 
 }  // namespace dps

@@ -1,7 +1,7 @@
 """GPU path against the CPU oracle, element by element, at sizes the oracle
 finishes in seconds (several tiles per bucket, ragged tails, zero-size tensors,
-oversized tensors, P from 1 to 16 and a rank count without a dedicated
-instantiation).
+oversized tensors, P from 1 to 16, rank counts without a dedicated
+instantiation, and P = 64, the largest the planner accepts).
 
 Tolerances (stated by the target): reduced fp32 gradients <= 1e-6 relative,
 fp32 master/m/v <= 1e-5 relative after 3 steps, bf16 parameters within 1 ulp,
@@ -28,7 +28,7 @@ SIZE_SETS = {
     "zeros": [0, 517, 0, 9000, 1, 0],
     "oversized": [70000, 12, 130000, 5],
 }
-RANKS = [1, 2, 3, 4, 5, 7, 8, 11, 16]
+RANKS = [1, 2, 3, 4, 5, 7, 8, 11, 16, 64]   # 64: the largest rank count the planner accepts
 
 
 def case_for(sizes_key, P, cap=64 * 1024, sigma=1e-3, seed=0, decay=None):

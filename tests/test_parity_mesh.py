@@ -12,7 +12,7 @@ from workloads import configs
 pytestmark = pytest.mark.gpu
 
 SIZES = [3, 1000, 65536, 13107, 26214, 4097, 27910]
-MESHES = [(2, 4), (4, 2), (2, 2), (8, 1), (3, 2), (2, 3), (2, 8), (5, 2)]
+MESHES = [(2, 4), (4, 2), (2, 2), (8, 1), (3, 2), (2, 3), (2, 8), (4, 4), (8, 2), (5, 2)]
 
 
 def mesh_case(R, S, sigma=1e-3, cap=64 * 1024):
@@ -39,7 +39,7 @@ def test_mesh_allreduce_matches_oracle(orc, R, S):
     assert_replicas_equal(dev, c.plan.L)
 
 
-@pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (3, 2), (2, 8)])
+@pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (3, 2), (2, 8), (4, 4), (8, 2)])
 @pytest.mark.parametrize("max_norm", [0.0, 1.0])
 def test_mesh_fused_zero_matches_oracle(orc, R, S, max_norm):
     c = mesh_case(R, S, sigma=0.05)
