@@ -902,6 +902,86 @@ def run_sweep(args):
                        "l2": "inputs > L2 (7.5 GB per replica set)"}}
 
 
+def run_kernels(args):
+    """Every entry point's kernel(s) on the workload, one after another: average
+    time per launch (CUDA events on the launching stream, after warm-up) and the
+    HBM rate of its algorithmic bytes against the measured copy peak.  The unit
+    kernels of the ZeRO-3 flow are timed as one pass over all units."""
+    import gradient_sync_zero_gb300 as dps
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    wl = workload_by_name(args.workload)
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    off = plan.tensor_offsets()
+    ws = plan.new_workspace()
+    P, n, nb = plan.P, wl.n_params, plan.n_buckets
+    grads, params, micro = plan.new_replicas(), plan.new_replicas(), plan.new_replicas()
+    wdev.fill_grads(grads, off, wl, step=1)
+    wdev.fill_grads(micro, off, wl, step=2)
+    master = plan.new_state()
+    wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
+    m, v, mean = plan.new_state(), plan.new_state(), plan.new_state()
+    shards = master.to(torch.bfloat16)
+    buckets = [plan.bucket(b) for b in range(nb)]
+    unit_buf = torch.empty(P, max(ln for _, ln, _ in buckets), dtype=torch.bfloat16, device="cuda")
+    a = wl.adamw
+    cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, 1.0, 1)
+    cfg0 = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, 0.0, 1)
+
+    def unit_ag_pass():
+        for b in range(nb):
+            dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
+
+    def unit_rs_pass():
+        for b in range(nb):
+            dps.dp_unit_reduce_scatter(plan, ws, unit_buf[:, :buckets[b][1]], b, mean, want_sumsq=True)
+
+    table = [  # name, kernel, bytes per parameter, call
+        ("dp_reduce_scatter_mean", "k_reduce_scatter", 2 * P + 4,
+         lambda: dps.dp_reduce_scatter_mean(plan, ws, grads, mean, want_sumsq=True)),
+        ("dp_clip_coef", "k_norm_finalize", 0, lambda: dps.dp_clip_coef(plan, ws, 1.0)),
+        ("dp_sharded_adamw_step", "k_adamw", 30,
+         lambda: dps.dp_sharded_adamw_step(plan, ws, mean, master, m, v, params, cfg, use_clip_coef=True)),
+        ("dp_all_gather", "k_all_gather", 2 * P, lambda: dps.dp_all_gather(plan, ws, params)),
+        ("dp_broadcast", "k_broadcast", 2 * P, lambda: dps.dp_broadcast(plan, ws, params, 0)),
+        ("dp_adamw_all_gather", "k_adamw_all_gather", 28 + 2 * P,
+         lambda: dps.dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg)),
+        ("dp_fused_zero_step (no clip)", "k_zero_fused", 4 * P + 24,
+         lambda: dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg0)),
+        ("dp_allreduce_mean", "k_allreduce", 4 * P, lambda: dps.dp_allreduce_mean(plan, ws, grads)),
+        ("dp_allreduce_mean_bf16wire", "k_allreduce_bf16wire", 4 * P,
+         lambda: dps.dp_allreduce_mean_bf16wire(plan, ws, grads)),
+        ("dp_accumulate", "k_accumulate", 6 * P, lambda: dps.dp_accumulate(plan, ws, grads, micro)),
+        ("dp_allreduce_mean_accum", "k_allreduce_accum", 6 * P,
+         lambda: dps.dp_allreduce_mean_accum(plan, ws, grads, micro)),
+        ("dp_unit_all_gather (all units)", "k_unit_all_gather", 2 + 2 * P, unit_ag_pass),
+        ("dp_unit_reduce_scatter (all units)", "k_reduce_scatter", 2 * P + 4, unit_rs_pass),
+        ("dp_shard_adamw_step", "k_adamw", 30,
+         lambda: dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)),
+    ]
+    peak, peak_src = measured_peaks()
+    rows = []
+    for name, kern, bpp, fn in table:
+        for _ in range(args.warmup):
+            fn()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            evs[2 * i].record(stream)
+            fn()
+            evs[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        ms = sum(evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)) / args.steps
+        gbs = bpp * n / (ms * 1e-3) / 1e9
+        rows.append({"entry": name, "kernel": kern, "ms": round(ms, 4), "bytes_per_param": bpp,
+                     "gbs": round(gbs, 1), "frac": round(gbs / peak, 4) if bpp else None})
+    return {"metric": "per-kernel time and HBM rate of algorithmic bytes", "unit": "GB/s",
+            "peak": peak, "peak_source": peak_src, "rows": rows,
+            "config": {"workload": wl.name, "P": P, "n_params": n, "n_buckets": nb,
+                       "l2": "inputs larger than L2"}}
+
+
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is a bounded sample."""
     import numpy as np
@@ -969,6 +1049,8 @@ def main(argv=None):
                     help="override the workload's clip threshold (0 = no clipping: one fused pass)")
     ap.add_argument("--graph", action="store_true",
                     help="with --zero3: replay the unit passes from a CUDA graph")
+    ap.add_argument("--kernels", action="store_true",
+                    help="time every entry point's kernel on the workload")
     ap.add_argument("--sweep", action="store_true",
                     help="bucket-size sweep: single launch vs per-bucket launches")
     ap.add_argument("--accum", type=int, default=0,
@@ -1001,6 +1083,9 @@ def main(argv=None):
         return
     if args.sweep:
         print(json.dumps(run_sweep(args)), flush=True)
+        return
+    if args.kernels:
+        print(json.dumps(run_kernels(args)), flush=True)
         return
     rank, local, world = dist_setup()
     res = run_gpu(args, rank, local, world)
