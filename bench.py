@@ -641,6 +641,55 @@ def run_zero3(args):
         if evs:
             evs[3].record(stream)
 
+    if args.prefetch:
+        # FSDP-style prefetch: two unit buffers and two streams.  Forward gathers
+        # alternate streams and buffers, so one unit's gather overlaps the next;
+        # in backward the gather of unit b+1 runs while unit b's gradients are
+        # reduce-scattered (the reduce-scatter waits for its unit's gather, which
+        # stands in for the backward compute that needs those parameters, and a
+        # buffer is reused only after the unit that last held it is done).
+        unit_bufs = [unit_buf, torch.empty_like(unit_buf)]
+        s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def step(t, evs=None):  # noqa: F811  (prefetching variant of the step above)
+            cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
+            if evs:
+                evs[0].record(stream)
+            s_a.wait_stream(stream)
+            s_b.wait_stream(stream)
+            for i, b in enumerate(reversed(range(nb))):
+                with torch.cuda.stream(s_a if i % 2 == 0 else s_b):
+                    dps.dp_unit_all_gather(plan, ws, shards, b, unit_bufs[i % 2])
+            stream.wait_stream(s_a)
+            stream.wait_stream(s_b)
+            if evs:
+                evs[1].record(stream)
+            s_a.wait_stream(stream)
+            s_b.wait_stream(stream)
+            released = [None, None]
+            for i, b in enumerate(range(nb)):
+                o, ln, _ = buckets[b]
+                with torch.cuda.stream(s_a):
+                    if released[i % 2] is not None:
+                        s_a.wait_event(released[i % 2])
+                    dps.dp_unit_all_gather(plan, ws, shards, b, unit_bufs[i % 2])
+                    gathered = torch.cuda.Event()
+                    gathered.record(s_a)
+                with torch.cuda.stream(s_b):
+                    s_b.wait_event(gathered)
+                    dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+                    done = torch.cuda.Event()
+                    done.record(s_b)
+                    released[i % 2] = done
+            stream.wait_stream(s_a)
+            stream.wait_stream(s_b)
+            if evs:
+                evs[2].record(stream)
+            dps.dp_clip_coef(plan, ws, a.max_norm)
+            dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
+            if evs:
+                evs[3].record(stream)
+
     graph = None
     if args.graph:
         # the two unit passes (their launches carry no step-dependent scalars) are
@@ -696,7 +745,8 @@ def run_zero3(args):
         "resident_bytes_per_param_all_ranks": 2 + 4 + 12,
         "transient_bytes": unit_buf.numel() * 2,
         "config": {"workload": wl.name, "P": P, "n_units": nb,
-                   "launch": "CUDA graph (unit passes)" if graph is not None else "host launches"},
+                   "launch": "CUDA graph (unit passes)" if graph is not None else
+                   ("host launches, prefetch on two streams" if args.prefetch else "host launches")},
     }
 
 
@@ -1047,6 +1097,8 @@ def main(argv=None):
     ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
     ap.add_argument("--max-norm", type=float, default=None,
                     help="override the workload's clip threshold (0 = no clipping: one fused pass)")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="with --zero3: gather the next unit while the current one reduce-scatters")
     ap.add_argument("--graph", action="store_true",
                     help="with --zero3: replay the unit passes from a CUDA graph")
     ap.add_argument("--kernels", action="store_true",

@@ -186,8 +186,7 @@ int dp_unit_all_gather(const dp_plan* plan, void* workspace, const void* param_s
   if (unit_stride < L.plan->b_len[unit] || unit_stride % 16)
     return fail(DP_EINVAL, "dp_unit_all_gather: unit_stride must be >= the unit length and a multiple of 16");
   const int e = launch_unit_all_gather(L, param_shards, unit_buf, unit_stride,
-                                       L.plan->b_off[unit] / kPairElems,
-                                       L.plan->b_len[unit] / kPairElems);
+                                       L.plan->b_off[unit] / kPairElems);
   return e ? cuda_fail(e, "dp_unit_all_gather") : DP_OK;
 }
 

@@ -101,7 +101,7 @@ struct Launch {
 int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq,
                           int64_t rep_stride = 0, int64_t rep_block0 = 0);
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
-                           int64_t block0, int64_t n_blk);
+                           int64_t block0);
 int launch_allreduce(const Launch& L, void* grads);
 int launch_accumulate(const Launch& L, void* acc, const void* micro);
 int launch_selftest_wait(int32_t* status, uint64_t limit_ns, void* stream);

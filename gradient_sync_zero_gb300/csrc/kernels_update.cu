@@ -45,53 +45,130 @@ __global__ void __launch_bounds__(kThreads)
   });
 }
 
-// ZeRO-3 unit all-gather: every rank's row of the unit buffer receives the unit's
-// shard values (the flat shard array holds each element once, at its owner).
-// A unit is one launch of a few waves, so the unit's blocks are split into equal
-// contiguous shares per CTA (not whole tiles, which would leave the last wave
-// partly idle); each thread keeps 4 loads in flight.
-__global__ void __launch_bounds__(kThreads)
-    k_unit_all_gather(KCommon k, const uint8_t* shards, uint8_t* out, int64_t out_stride_bytes,
-                      int64_t block0, int64_t n_blk) {
+// ---- replica write-back with bulk copies: all-gather, broadcast, unit all-gather ----
+// Each tile (<= 8192 elements, inside one bucket) is one job: one thread streams
+// the tile's source segments into a shared-memory stage (bulk loads counted on an
+// mbarrier) and writes the stage to every destination row with bulk stores.
+// Written with per-thread 32-byte accesses, one load feeds P-1 stores and the
+// LSU queue limits the kernel (lg_throttle 23 stalls per issue at P = 8); a bulk
+// store moves a whole segment per instruction.  3 stages in flight per CTA;
+// every wait is bounded (DP_STATUS_TIMEOUT, the CTA still drains its copies).
+//   all-gather: the owner's row of each shard -> every row r with r mod S != owner
+//   broadcast:  row src -> every other row
+//   unit:       the flat bf16 shard array -> all P rows of a unit buffer
+enum RepMode : int { kRepAllGather = 0, kRepBroadcast = 1, kRepUnit = 2 };
+constexpr int kRepStages = 3;
+constexpr uint32_t kRepStageBytes = static_cast<uint32_t>(kTileElems) * 2;   // 16 KB
+constexpr size_t kRepSmem = kRepStages * static_cast<size_t>(kRepStageBytes) +
+                            kRepStages * sizeof(uint64_t);
+
+struct RepArgs {
+  const uint8_t* src;     // replicas (all-gather, broadcast) or the flat shards (unit)
+  uint8_t* dst;           // replicas or the unit buffer
+  int64_t dst_stride;     // bytes between destination rows
+  int64_t dst_vec0;       // unit: the unit's first 16-byte vector (destination column 0)
+  int64_t dst_vec_limit;  // unit: 16-byte vectors per destination row
+  int mode;
+  int src_rank;           // broadcast
+};
+
+__global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
   if (!plan_ok(k)) return;
-  if (!DP_IN_BOUNDS(block0 >= 0 && n_blk >= 0 && 2 * (block0 + n_blk) <= k.hdr->n_vec)) return;
-  constexpr int D = 4;
-  const int64_t G = gridDim.x;
-  const int64_t lo = block0 + n_blk * blockIdx.x / G;
-  const int64_t hi = block0 + n_blk * (blockIdx.x + 1) / G;
-  for (int64_t b0 = lo + threadIdx.x; b0 < hi; b0 += D * kThreads) {
-    Blk val[D];
-#pragma unroll
-    for (int d = 0; d < D; ++d)
-      if (b0 + d * kThreads < hi) val[d] = ld_blk(shards + 32 * (b0 + d * kThreads));
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-      const int64_t b = b0 + d * kThreads;
-      if (b >= hi) break;
-      for (int r = 0; r < k.P; ++r) st_blk(out + r * out_stride_bytes + 32 * (b - block0), val[d]);
+  if (threadIdx.x != 0) return;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + kRepStages * kRepStageBytes);
+  for (int q = 0; q < kRepStages; ++q) mbar_init(&bar[q]);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const int64_t first = k.tile_begin + blockIdx.x, step = gridDim.x;
+  const int64_t mine = first < k.tile_end ? (k.tile_end - first + step - 1) / step : 0;
+
+  // f(x, e, c) for each run [x, e) of 16-byte vectors of the tile with one source row
+  auto segments = [&](const TileDesc& d, auto&& f) {
+    const int64_t end = d.v0 + d.nvec;
+    if (a.mode != kRepAllGather) {
+      f(d.v0, end, a.src_rank);
+      return;
     }
+    for (int64_t x = d.v0; x < end;) {
+      const int c = owner_of(d, x);
+      int64_t e = d.bvoff + static_cast<int64_t>(c + 1) * d.svec;
+      if (e > end) e = end;
+      f(x, e, c);
+      x = e;
+    }
+  };
+  auto issue_load = [&](int64_t i) {
+    if (i >= mine) return;
+    const int64_t tile = first + i * step;
+    const TileDesc d = load_tile(k, tile);
+    uint64_t* q = &bar[i % kRepStages];
+    if (!tile_ok(k, tile, d)) {
+      mbar_arrive_expect_tx(q, 0u);   // checked build: the stage completes empty
+      return;
+    }
+    uint8_t* stage = smem_raw + (i % kRepStages) * kRepStageBytes;
+    mbar_arrive_expect_tx(q, 16u * static_cast<uint32_t>(d.nvec));
+    segments(d, [&](int64_t x, int64_t e, int c) {
+      const uint8_t* src = a.mode == kRepUnit ? a.src + 16 * x : a.src + c * k.stride_bytes + 16 * x;
+      bulk_load(stage + 16 * (x - d.v0), src, 16u * static_cast<uint32_t>(e - x), q);
+    });
+  };
+  auto issue_stores = [&](int64_t i) {
+    const int64_t tile = first + i * step;
+    const TileDesc d = load_tile(k, tile);
+    if (!tile_ok(k, tile, d)) return;
+    const uint8_t* stage = smem_raw + (i % kRepStages) * kRepStageBytes;
+    segments(d, [&](int64_t x, int64_t e, int c) {
+      const uint32_t bytes = 16u * static_cast<uint32_t>(e - x);
+      const uint8_t* sm = stage + 16 * (x - d.v0);
+      for (int r = 0; r < k.P; ++r) {
+        if (a.mode == kRepAllGather && r % k.S == c) continue;
+        if (a.mode == kRepBroadcast && r == a.src_rank) continue;
+        const int64_t col = a.mode == kRepUnit ? x - a.dst_vec0 : x;
+        if (a.mode == kRepUnit && !DP_IN_BOUNDS(col >= 0 && col + (e - x) <= a.dst_vec_limit)) continue;
+        bulk_store(a.dst + r * a.dst_stride + 16 * col, sm, bytes);
+      }
+    });
+  };
+
+  issue_load(0);
+  issue_load(1);
+  bool timed_out = false;
+  int64_t i = 0;
+  for (; i < mine; ++i) {
+    if (!mbar_wait_bounded(&bar[i % kRepStages], static_cast<uint32_t>((i / kRepStages) & 1))) {
+      timed_out = true;
+      break;
+    }
+    issue_stores(i);
+    bulk_commit();
+    bulk_wait_read<1>();   // tile i-1's stores have left its stage ...
+    issue_load(i + 2);     // ... which now receives tile i+2
   }
+  if (timed_out) {
+    atomicOr(&k.hdr->status, DP_STATUS_TIMEOUT);
+    for (int64_t q = i; q < i + 2 && q < mine; ++q)   // loads still in flight (bounded)
+      mbar_wait_bounded(&bar[q % kRepStages], static_cast<uint32_t>((q / kRepStages) & 1));
+  }
+  bulk_wait_all();
 }
 
-// In-place all-gather: the owner's slice of each shard goes to every other replica.
-__global__ void __launch_bounds__(kThreads) k_all_gather(KCommon k, uint8_t* params) {
-  if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int c) {
-    // ranks (g, c) own shard c; every other rank of each group receives it
-    const Blk val = ld_blk(params + c * k.stride_bytes + 32 * b);
-    for (int r = 0; r < k.P; ++r)
-      if (r % k.S != c) st_blk(params + r * k.stride_bytes + 32 * b, val);
-  });
-}
-
-// Replica `src` to every other replica.
-__global__ void __launch_bounds__(kThreads) k_broadcast(KCommon k, uint8_t* params, int src) {
-  if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int) {
-    const Blk val = ld_blk(params + src * k.stride_bytes + 32 * b);
-    for (int r = 0; r < k.P; ++r)
-      if (r != src) st_blk(params + r * k.stride_bytes + 32 * b, val);
-  });
+int launch_replicate(const Launch& L, const RepArgs& a) {
+  if (L.tile_end <= L.tile_begin) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_replicate, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kRepSmem));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  const int64_t cap = resident_ctas(k_replicate, 32, kRepSmem);
+  if (cap <= 0) {
+    e = cudaGetLastError();
+    return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
+  }
+  const int64_t n = L.tile_end - L.tile_begin;
+  int64_t g = n < cap ? n : cap;
+  if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
+  k_replicate<<<static_cast<int>(g), 32, kRepSmem, static_cast<cudaStream_t>(L.stream)>>>(
+      make_common(L), a);
+  return static_cast<int>(cudaGetLastError());
 }
 
 // The whole ZeRO-1/2 step without clipping, one pass.  The replica blocks are
@@ -272,28 +349,22 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
 }
 
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
-                           int64_t block0, int64_t n_blk) {
-  if (n_blk <= 0) return cudaSuccess;
-  const int cap = resident_ctas(k_unit_all_gather, kThreads);
-  if (cap <= 0) {
-    const cudaError_t e = cudaGetLastError();
-    return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
-  }
-  const int64_t want = (n_blk + kThreads - 1) / kThreads;
-  int64_t g = want < cap ? want : cap;
-  if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
-  k_unit_all_gather<<<static_cast<int>(g), kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(
-      make_common(L), static_cast<const uint8_t*>(shards), static_cast<uint8_t*>(out), 2 * out_stride,
-      block0, n_blk);
-  return static_cast<int>(cudaGetLastError());
+                           int64_t block0) {
+  RepArgs a{static_cast<const uint8_t*>(shards), static_cast<uint8_t*>(out), 2 * out_stride,
+            2 * block0, out_stride / kVecElems, kRepUnit, 0};
+  return launch_replicate(L, a);
 }
 
 int launch_all_gather(const Launch& L, void* params) {
-  return launch_tiles(L, k_all_gather, make_common(L), static_cast<uint8_t*>(params));
+  RepArgs a{static_cast<const uint8_t*>(params), static_cast<uint8_t*>(params), 2 * L.plan->stride,
+            0, 0, kRepAllGather, 0};
+  return launch_replicate(L, a);
 }
 
 int launch_broadcast(const Launch& L, void* params, int src) {
-  return launch_tiles(L, k_broadcast, make_common(L), static_cast<uint8_t*>(params), src);
+  RepArgs a{static_cast<const uint8_t*>(params), static_cast<uint8_t*>(params), 2 * L.plan->stride,
+            0, 0, kRepBroadcast, src};
+  return launch_replicate(L, a);
 }
 
 int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,

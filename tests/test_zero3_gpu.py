@@ -97,3 +97,71 @@ def test_unit_reduce_scatter_equals_bucket_reduce_scatter():
     dps.dp_clip_coef(c.plan, c.ws, 1.0)
     n2 = dps.dp_read_norm(c.plan, c.ws)
     assert torch.equal(a, b_) and n1 == n2
+
+
+def test_prefetch_schedule_on_two_streams_equals_sequential():
+    """The FSDP-style prefetch schedule — the next unit's gather on one stream while
+    the current unit's gradients reduce-scatter on another, two unit buffers —
+    shares the workspace between concurrent launches and must give the sequential
+    flow's mean, norm, state and gathered units bit for bit."""
+    wl = configs.llama_1b1_zero2(layers=2, embeddings=False)
+    wl.bucket_bytes = 4 << 20                                 # many units
+    c = Case(wl)
+    plan, nb, P = c.plan, c.plan.n_buckets, wl.P
+    assert nb >= 8
+    grads = plan.new_replicas()
+    wdev.fill_grads(grads, c.off, wl, 1)
+    master0 = torch.randn(plan.L, device="cuda") * 0.02
+    cfg = dps.adamw_cfg(2e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, 1)
+    max_len = max(plan.bucket(b)[1] for b in range(nb))
+
+    def run(prefetch):
+        shards = master0.to(torch.bfloat16)
+        st = [master0.clone(), plan.new_state(), plan.new_state()]
+        mean = plan.new_state()
+        ws = plan.new_workspace()
+        bufs = [torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        seen = []
+        if not prefetch:
+            for b in range(nb):
+                o, ln, _ = plan.bucket(b)
+                dps.dp_unit_all_gather(plan, ws, shards, b, bufs[0])
+                seen.append(bufs[0][:, :ln].clone())
+                dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+        else:
+            main = torch.cuda.current_stream()
+            s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+            s_a.wait_stream(main)
+            s_b.wait_stream(main)
+            released = [None, None]
+            for i, b in enumerate(range(nb)):
+                o, ln, _ = plan.bucket(b)
+                with torch.cuda.stream(s_a):
+                    if released[i % 2] is not None:
+                        s_a.wait_event(released[i % 2])
+                    dps.dp_unit_all_gather(plan, ws, shards, b, bufs[i % 2])
+                    ev = torch.cuda.Event()
+                    ev.record(s_a)
+                with torch.cuda.stream(s_b):
+                    s_b.wait_event(ev)
+                    seen.append(bufs[i % 2][:, :ln].clone())   # the unit's "backward" reads it
+                    dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+                    done = torch.cuda.Event()
+                    done.record(s_b)
+                    released[i % 2] = done
+            main.wait_stream(s_a)
+            main.wait_stream(s_b)
+        dps.dp_clip_coef(plan, ws, 1.0)
+        dps.dp_shard_adamw_step(plan, ws, mean, *st, shards, cfg, use_clip_coef=True)
+        torch.cuda.synchronize()
+        return mean, dps.dp_read_norm(plan, ws), st, shards, seen
+
+    m1, n1, st1, sh1, seen1 = run(False)
+    m2, n2, st2, sh2, seen2 = run(True)
+    assert n1 == n2 and n1[2] == 0
+    assert torch.equal(m1.view(torch.int32), m2.view(torch.int32))
+    assert torch.equal(sh1, sh2)
+    for a, b in zip(st1, st2):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    for a, b in zip(seen1, seen2):
+        assert torch.equal(a, b)
