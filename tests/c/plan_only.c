@@ -1,0 +1,31 @@
+/* A C99 caller of the library's planner (no GPU needed): plans three tensors
+ * into 4 ranks and prints the layout the planner chose, one value per line. */
+#include <stdint.h>
+#include <stdio.h>
+
+#include "dpsync.h"
+
+int main(void) {
+  const int64_t sizes[3] = {1000, 70000, 12};
+  const uint8_t decay[3] = {1, 1, 0};
+  dp_plan* plan = NULL;
+  if (dp_plan_buckets(sizes, decay, 3, 64 * 1024, 4, &plan) != DP_OK) {
+    fprintf(stderr, "plan: %s\n", dp_last_error());
+    return 1;
+  }
+  dp_plan_info_t info;
+  if (dp_plan_info(plan, &info) != DP_OK) return 2;
+  printf("%lld\n%lld\n%d\n", (long long)info.n_params, (long long)info.padded_len, info.n_buckets);
+  for (int32_t t = 0; t < 3; ++t) {
+    int32_t b = -1;
+    int64_t off = -1;
+    if (dp_plan_tensor(plan, t, &b, &off) != DP_OK) return 3;
+    printf("%d %lld\n", b, (long long)off);
+  }
+  /* a refused call leaves a message and no plan */
+  dp_plan* bad = NULL;
+  const int rc = dp_plan_buckets(sizes, decay, 3, 64 * 1024, 0, &bad);
+  printf("%d %d\n", rc == DP_EINVAL, bad == NULL);
+  dp_plan_free(plan);
+  return 0;
+}
