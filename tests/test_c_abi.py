@@ -41,3 +41,38 @@ def test_c_program_plans_like_the_binding(tmp_path):
         b, off = (int(x) for x in lines[3 + t].split())
         assert (b, off) == plan.tensor(t)
     assert lines[6] == "1 1"
+
+
+def _cuda_home():
+    return os.environ.get("CUDA_HOME", "/usr/local/cuda")
+
+
+def _build_gpu_program(tmp_path):
+    lib = dbuild.build()
+    cuda = _cuda_home()
+    exe = tmp_path / "allreduce_gpu"
+    r = subprocess.run([CC, "-std=c99", "-Wall", "-Werror", "-I", INC, "-I", os.path.join(cuda, "include"),
+                        os.path.join(ROOT, "tests", "c", "allreduce_gpu.c"), "-o", str(exe), lib,
+                        f"-Wl,-rpath,{os.path.dirname(lib)}", "-L", os.path.join(cuda, "lib64"),
+                        "-lcudart", f"-Wl,-rpath,{os.path.join(cuda, 'lib64')}"],
+                       capture_output=True, text=True)
+    return exe, r
+
+
+def test_c_gpu_program_builds(tmp_path):
+    """The GPU caller compiles and links as C99 against the library and cudart."""
+    if not os.path.exists(os.path.join(_cuda_home(), "include", "cuda_runtime.h")):
+        pytest.skip("no CUDA headers")
+    _, r = _build_gpu_program(tmp_path)
+    assert r.returncode == 0, r.stderr
+
+
+@pytest.mark.gpu
+def test_c_program_allreduces_on_the_gpu(tmp_path):
+    """A C99 process with no Python in it: plan, cudaMalloc, upload, all-reduce;
+    every replica holds the exact mean."""
+    exe, r = _build_gpu_program(tmp_path)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "mismatches 0" in run.stdout
