@@ -1005,6 +1005,8 @@ def run_kernels(args):
         ("dp_accumulate", "k_accumulate", 6 * P, lambda: dps.dp_accumulate(plan, ws, grads, micro)),
         ("dp_allreduce_mean_accum", "k_allreduce_accum", 6 * P,
          lambda: dps.dp_allreduce_mean_accum(plan, ws, grads, micro)),
+        ("dp_reduce_scatter_mean_accum", "k_reduce_scatter (accumulating)", 4 * P + 4,
+         lambda: dps.dp_reduce_scatter_mean_accum(plan, ws, grads, micro, mean, want_sumsq=True)),
         ("dp_unit_all_gather (all units)", "k_unit_all_gather", 2 + 2 * P, unit_ag_pass),
         ("dp_unit_reduce_scatter (all units)", "k_reduce_scatter", 2 * P + 4, unit_rs_pass),
         ("dp_shard_adamw_step", "k_adamw", 30,

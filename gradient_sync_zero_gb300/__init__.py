@@ -83,6 +83,7 @@ def lib():
             "dp_checkpoint_save": [vp, C.c_char_p, vp, vp, vp, i64, i32, vp],
             "dp_checkpoint_load": [vp, C.c_char_p, vp, vp, vp, C.POINTER(i64), i32, vp],
             "dp_allreduce_mean_accum": [vp, vp, vp, vp, i32, i32, vp],
+            "dp_reduce_scatter_mean_accum": [vp, vp, vp, vp, vp, i32, i32, i32, vp],
             "dp_allreduce_mean_bf16wire": [vp, vp, vp, i32, i32, vp],
             "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
             "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
@@ -376,6 +377,18 @@ def dp_allreduce_mean_accum(plan, ws, acc, micro, b0=0, b1=None, stream=None):
     b0, b1 = _range(plan, b0, b1)
     _check(lib().dp_allreduce_mean_accum(plan.handle, _ws(plan, ws), _ptr(acc), _ptr(micro), b0,
                                          b1, _stream(stream)))
+
+
+def dp_reduce_scatter_mean_accum(plan, ws, acc, micro, mean, b0=0, b1=None, want_sumsq=False,
+                                 stream=None):
+    """Last micro-batch (ZeRO): reduce-scatter every rank's bf16(acc + micro) into mean."""
+    _need(acc, torch.bfloat16, plan.P * plan.stride, "acc")
+    _need(micro, torch.bfloat16, plan.P * plan.stride, "micro")
+    _need(mean, torch.float32, plan.L, "mean")
+    b0, b1 = _range(plan, b0, b1)
+    _check(lib().dp_reduce_scatter_mean_accum(plan.handle, _ws(plan, ws), _ptr(acc), _ptr(micro),
+                                              _ptr(mean), b0, b1, 1 if want_sumsq else 0,
+                                              _stream(stream)))
 
 
 def dp_allreduce_mean_bf16wire(plan, ws, grads, b0=0, b1=None, stream=None):

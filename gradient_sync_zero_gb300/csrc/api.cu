@@ -242,6 +242,18 @@ int dp_allreduce_mean_accum(const dp_plan* plan, void* workspace, void* acc, con
   return e ? cuda_fail(e, "dp_allreduce_mean_accum") : DP_OK;
 }
 
+int dp_reduce_scatter_mean_accum(const dp_plan* plan, void* workspace, const void* acc,
+                                 const void* micro, float* mean, int32_t b0, int32_t b1,
+                                 int32_t want_sumsq, void* stream) {
+  Launch L;
+  int rc = prepare("dp_reduce_scatter_mean_accum", plan, workspace, b0, b1, stream, &L);
+  if (rc) return rc;
+  if ((rc = check_ptrs("dp_reduce_scatter_mean_accum", L.plan, {acc, micro, mean}))) return rc;
+  if (L.plan->R > 1) return fail(DP_EINVAL, "dp_reduce_scatter_mean_accum: flat plans only");
+  const int e = launch_reduce_scatter_accum(L, acc, micro, mean, want_sumsq != 0);
+  return e ? cuda_fail(e, "dp_reduce_scatter_mean_accum") : DP_OK;
+}
+
 int dp_allreduce_mean_bf16wire(const dp_plan* plan, void* workspace, void* grads, int32_t b0,
                                int32_t b1, void* stream) {
   Launch L;

@@ -110,6 +110,8 @@ int launch_selftest_wait(int32_t* status, uint64_t limit_ns, void* stream);
 int64_t bounds_violations_reduce(bool reset);
 int64_t bounds_violations_update(bool reset);
 int launch_allreduce_accum(const Launch& L, void* acc, const void* micro);
+int launch_reduce_scatter_accum(const Launch& L, const void* acc, const void* micro, float* mean,
+                                bool sumsq);
 int launch_allreduce_bf16wire(const Launch& L, void* grads);
 int launch_norm_finalize(const Launch& L, double max_norm);
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,

@@ -20,9 +20,12 @@ namespace dps {
 // ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
 // the exact sum.  Partials are per tile, so the norm does not depend on the grid
 // size or on how the bucket range is split into launches.
-template <int P, int MS>
+// ACC: the last micro-batch of gradient accumulation fused in — replica r's
+// value is bf16(g_r + micro_r), formed in registers (flat plans).
+template <int P, int MS, bool ACC>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint8_t* g,
-                                                             float* mean, int sumsq) {
+                                                             float* mean, int sumsq,
+                                                             const uint8_t* micro) {
   if (!plan_ok(k)) return;
   __shared__ FF warp_part[kWarps];
   for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
@@ -37,7 +40,11 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
       const int c = owner_of(d, 2 * b);
       if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
       float acc[16];
-      block_mean16<P, MS>(k, g, b, d, c, acc);
+      if constexpr (ACC) {
+        ring_mean16_accum<P>(g, micro, k.stride_bytes, 32 * b, c, k.P, acc);
+      } else {
+        block_mean16<P, MS>(k, g, b, d, c, acc);
+      }
       st_f16(mean, b, acc);
       if (sumsq) {
 #pragma unroll
@@ -155,9 +162,19 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      return launch_tiles(L, k_reduce_scatter<P, M>, k, static_cast<const uint8_t*>(grads), mean,
-                          sumsq ? 1 : 0);
+      return launch_tiles(L, k_reduce_scatter<P, M, false>, k, static_cast<const uint8_t*>(grads),
+                          mean, sumsq ? 1 : 0, static_cast<const uint8_t*>(nullptr));
     });
+  });
+}
+
+int launch_reduce_scatter_accum(const Launch& L, const void* acc, const void* micro, float* mean,
+                                bool sumsq) {
+  const KCommon k = make_common(L);
+  return with_P(L.plan->P, [&](auto pc) {
+    constexpr int P = decltype(pc)::value;
+    return launch_tiles(L, k_reduce_scatter<P, 0, true>, k, static_cast<const uint8_t*>(acc), mean,
+                        sumsq ? 1 : 0, static_cast<const uint8_t*>(micro));
   });
 }
 

@@ -307,6 +307,12 @@ int dp_accumulate(const dp_plan* plan, void* workspace, void* acc, const void* m
                   int32_t b1, void* stream);
 int dp_allreduce_mean_accum(const dp_plan* plan, void* workspace, void* acc, const void* micro,
                             int32_t b0, int32_t b1, void* stream);
+/* The ZeRO form of the same fusion: the last micro-batch's bf16(acc + micro) of
+ * every rank reduce-scattered into the fp32 mean (as dp_reduce_scatter_mean, with
+ * the optional norm partials); acc and micro are only read.  Flat plans only. */
+int dp_reduce_scatter_mean_accum(const dp_plan* plan, void* workspace, const void* acc,
+                                 const void* micro, float* mean, int32_t b0, int32_t b1,
+                                 int32_t want_sumsq, void* stream);
 
 /*
  * The mean all-reduce with bf16 on the wire, as a precision comparison

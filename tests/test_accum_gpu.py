@@ -145,3 +145,62 @@ def test_full_size_gpt2_accumulation_sampled(orc):
         b = np.stack([u16(m1[r, o:o + s]) for r in range(wl.P)])
         assert np.array_equal(np.stack([u16(summed[r, o:o + s]) for r in range(wl.P)]),
                               orc.accumulate(a, b))
+
+
+@pytest.mark.parametrize("P", [2, 5, 8, 16])
+def test_last_micro_batch_reduce_scatter_equals_oracle(orc, P):
+    """ZeRO form: the fused last micro-batch reduce-scatter gives the oracle's fp32
+    mean of the accumulated gradients bit for bit, the same norm partials as the
+    unfused path, and leaves acc and micro unchanged."""
+    wl = small_workload(SIZES, P, 32 * 1024, seed=40 + P, outlier_frac=0.01)
+    c = Case(wl)
+    m = micro_batches(c, 3)
+    acc = c.to_replicas(m[0])
+    dps.dp_accumulate(c.plan, c.ws, acc, c.to_replicas(m[1]))
+    last = c.to_replicas(m[2])
+    acc0, last0 = acc.clone(), last.clone()
+    mean = c.plan.new_state()
+    dps.dp_reduce_scatter_mean_accum(c.plan, c.ws, acc, last, mean, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 1.0)
+    n_fused = dps.dp_read_norm(c.plan, c.ws)
+    ws2 = c.plan.new_workspace()
+    two, mean2 = acc.clone(), c.plan.new_state()
+    dps.dp_accumulate(c.plan, ws2, two, last)
+    dps.dp_reduce_scatter_mean(c.plan, ws2, two, mean2, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, ws2, 1.0)
+    n_two = dps.dp_read_norm(c.plan, ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, acc0) and torch.equal(last, last0)
+    assert torch.equal(mean.view(torch.int32), mean2.view(torch.int32)) and n_fused == n_two
+    want = orc.accumulate(orc.accumulate(m[0], m[1]), m[2])
+    _, omean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, want)
+    assert np.array_equal(c.from_flat(mean).view(np.uint32), omean.view(np.uint32))
+
+
+def test_accumulated_zero_step_equals_oracle(orc):
+    """Two micro-batches, then the fused last-micro-batch reduce-scatter, the clip
+    coefficient and the AdamW + all-gather pass: the oracle's ZeRO step on the
+    accumulated gradients, bit for bit."""
+    import oracle as oracle_mod
+    wl = configs.tiny_plumbing()
+    wl.adamw = configs.AdamW(max_norm=0.3)
+    c = Case(wl)
+    m0, m1 = c.host_grads(1), c.host_grads(2)
+    acc, last = c.to_replicas(m0), c.to_replicas(m1)
+    master0 = c.host_master()
+    st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    params, mean = c.plan.new_replicas(), c.plan.new_state()
+    a = wl.adamw
+    cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1)
+    dps.dp_reduce_scatter_mean_accum(c.plan, c.ws, acc, last, mean, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, a.max_norm)
+    dps.dp_adamw_all_gather(c.plan, c.ws, mean, *st, params, cfg)
+    norm, coef, status = dps.dp_read_norm(c.plan, c.ws)
+    g = orc.accumulate(m0, m1)
+    z = np.zeros_like(master0)
+    p_o, m_o, mo, vo, _, so = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, wl.P, g, master0, z, z,
+                                            oracle_mod.adamw_cfg(a, 1))
+    assert status == 0 and coef == so.coef < 1.0
+    assert np.array_equal(c.from_replicas(params), p_o)
+    for dev, ref in zip(st, (m_o, mo, vo)):
+        assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
