@@ -602,7 +602,13 @@ def run_zero3(args):
     all-gather (last bucket first), its backward all-gather and gradient
     reduce-scatter (first bucket first), the clip coefficient and the shard
     update.  Persistent state 18 B/param over all ranks; one [P][max unit]
-    transient buffer."""
+    transient buffer (two with --prefetch).  --prefetch: the next unit is
+    gathered on a second stream while the current one reduce-scatters (FSDP's
+    prefetch; the reduce-scatter waits for its unit's gather, which stands in for
+    the backward compute that needs those parameters, and a buffer is reused only
+    after the unit that last held it is done).  --graph: the whole step is
+    captured once with cfg=None and replayed, the step's AdamW scalars written
+    into the workspace before each replay."""
     import gradient_sync_zero_gb300 as dps
 
     torch.cuda.set_device(0)
@@ -619,110 +625,94 @@ def run_zero3(args):
     nb, P = plan.n_buckets, plan.P
     buckets = [plan.bucket(b) for b in range(nb)]
     unit_buf = torch.empty(P, max(ln for _, ln, _ in buckets), dtype=torch.bfloat16, device="cuda")
+    unit_bufs = [unit_buf, torch.empty_like(unit_buf)] if args.prefetch else [unit_buf]
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
     a = wl.adamw
     stream = torch.cuda.current_stream()
 
-    def step(t, evs=None):
-        cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
-        if evs:
-            evs[0].record(stream)
-        for b in reversed(range(nb)):
-            dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
-        if evs:
-            evs[1].record(stream)
-        for b in range(nb):
-            o, ln, _ = buckets[b]
-            dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
-            dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
-        if evs:
-            evs[2].record(stream)
-        dps.dp_clip_coef(plan, ws, a.max_norm)
-        dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
-        if evs:
-            evs[3].record(stream)
+    def cfg_of(t):
+        return dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
 
-    if args.prefetch:
-        # FSDP-style prefetch: two unit buffers and two streams.  Forward gathers
-        # alternate streams and buffers, so one unit's gather overlaps the next;
-        # in backward the gather of unit b+1 runs while unit b's gradients are
-        # reduce-scattered (the reduce-scatter waits for its unit's gather, which
-        # stands in for the backward compute that needs those parameters, and a
-        # buffer is reused only after the unit that last held it is done).
-        unit_bufs = [unit_buf, torch.empty_like(unit_buf)]
-        s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
-
-        def step(t, evs=None):  # noqa: F811  (prefetching variant of the step above)
-            cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
-            if evs:
-                evs[0].record(stream)
-            s_a.wait_stream(stream)
-            s_b.wait_stream(stream)
-            for i, b in enumerate(reversed(range(nb))):
-                with torch.cuda.stream(s_a if i % 2 == 0 else s_b):
-                    dps.dp_unit_all_gather(plan, ws, shards, b, unit_bufs[i % 2])
-            stream.wait_stream(s_a)
-            stream.wait_stream(s_b)
-            if evs:
-                evs[1].record(stream)
-            s_a.wait_stream(stream)
-            s_b.wait_stream(stream)
-            released = [None, None]
-            for i, b in enumerate(range(nb)):
-                o, ln, _ = buckets[b]
-                with torch.cuda.stream(s_a):
-                    if released[i % 2] is not None:
-                        s_a.wait_event(released[i % 2])
-                    dps.dp_unit_all_gather(plan, ws, shards, b, unit_bufs[i % 2])
-                    gathered = torch.cuda.Event()
-                    gathered.record(s_a)
-                with torch.cuda.stream(s_b):
-                    s_b.wait_event(gathered)
-                    dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
-                    done = torch.cuda.Event()
-                    done.record(s_b)
-                    released[i % 2] = done
-            stream.wait_stream(s_a)
-            stream.wait_stream(s_b)
-            if evs:
-                evs[2].record(stream)
-            dps.dp_clip_coef(plan, ws, a.max_norm)
-            dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
-            if evs:
-                evs[3].record(stream)
-
-    graph = None
-    if args.graph:
-        # the two unit passes (their launches carry no step-dependent scalars) are
-        # captured once and replayed; the clip and the update stay eager
-        def passes():
+    def forward():
+        if not args.prefetch:
             for b in reversed(range(nb)):
                 dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
+            return
+        cur = torch.cuda.current_stream()
+        s_a.wait_stream(cur)
+        s_b.wait_stream(cur)
+        for i, b in enumerate(reversed(range(nb))):
+            with torch.cuda.stream(s_a if i % 2 == 0 else s_b):
+                dps.dp_unit_all_gather(plan, ws, shards, b, unit_bufs[i % 2])
+        cur.wait_stream(s_a)
+        cur.wait_stream(s_b)
+
+    def backward():
+        if not args.prefetch:
             for b in range(nb):
                 o, ln, _ = buckets[b]
                 dps.dp_unit_all_gather(plan, ws, shards, b, unit_buf)
                 dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+            return
+        cur = torch.cuda.current_stream()
+        s_a.wait_stream(cur)
+        s_b.wait_stream(cur)
+        released = [None, None]
+        for i, b in enumerate(range(nb)):
+            o, ln, _ = buckets[b]
+            with torch.cuda.stream(s_a):
+                if released[i % 2] is not None:
+                    s_a.wait_event(released[i % 2])
+                dps.dp_unit_all_gather(plan, ws, shards, b, unit_bufs[i % 2])
+                gathered = torch.cuda.Event()
+                gathered.record(s_a)
+            with torch.cuda.stream(s_b):
+                s_b.wait_event(gathered)
+                dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+                done = torch.cuda.Event()
+                done.record(s_b)
+                released[i % 2] = done
+        cur.wait_stream(s_a)
+        cur.wait_stream(s_b)
 
+    def update(cfg):
+        dps.dp_clip_coef(plan, ws, a.max_norm)
+        dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
+
+    graph = None
+    if args.graph:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            passes()
+            dps.dp_set_adamw_cfg(plan, ws, cfg_of(1))
+            forward()                       # one eager step first: launcher setup off capture
+            backward()
+            update(None)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            passes()
+            forward()
+            backward()
+            update(None)
 
-        def step(t, evs=None):  # noqa: F811  (graph-replay variant of the step above)
-            cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, t)
+    def step(t, evs=None):
+        def mark(i):
             if evs:
-                evs[0].record(stream)
-                evs[1].record(stream)
+                evs[i].record(stream)
+        mark(0)
+        if graph is not None:
+            dps.dp_set_adamw_cfg(plan, ws, cfg_of(t))
+            mark(1)
+            mark(2)
             graph.replay()
-            if evs:
-                evs[2].record(stream)
-            dps.dp_clip_coef(plan, ws, a.max_norm)
-            dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)
-            if evs:
-                evs[3].record(stream)
+            mark(3)
+            return
+        forward()
+        mark(1)
+        backward()
+        mark(2)
+        update(cfg_of(t))
+        mark(3)
 
     for t in range(1, args.warmup + 1):
         step(t)
@@ -743,10 +733,10 @@ def run_zero3(args):
                      "clip_and_update": parts[2]},
         "gbs": bytes_pp * n / (ms * 1e-3) / 1e9, "bytes_per_param": bytes_pp,
         "resident_bytes_per_param_all_ranks": 2 + 4 + 12,
-        "transient_bytes": unit_buf.numel() * 2,
+        "transient_bytes": sum(x.numel() * 2 for x in unit_bufs),
         "config": {"workload": wl.name, "P": P, "n_units": nb,
-                   "launch": "CUDA graph (unit passes)" if graph is not None else
-                   ("host launches, prefetch on two streams" if args.prefetch else "host launches")},
+                   "launch": ("CUDA graph of the whole step" if graph is not None else "host launches")
+                   + (", prefetch on two streams" if args.prefetch else "")},
     }
 
 

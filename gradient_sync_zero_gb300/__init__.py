@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(HERE, "libdpsync_checked.so" if VARIANT == "checked" els
 
 DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ETIMEOUT = \
     0, -1, -2, -3, -4, -5, -6, -7
-DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT = 1, 2, 4
+DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT, DP_STATUS_NO_SCALARS = 1, 2, 4, 8
 DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_DRY_RUN = 0, 1, 1
 DP_CKPT_HOST = 1
 
@@ -80,6 +80,7 @@ def lib():
             "dp_unit_all_gather": [vp, vp, vp, i32, vp, i64, vp],
             "dp_accumulate": [vp, vp, vp, vp, i32, i32, vp],
             "dp_selftest_bounded_wait": [vp, i64, vp],
+            "dp_set_adamw_cfg": [vp, vp, vp, vp],
             "dp_checkpoint_save": [vp, C.c_char_p, vp, vp, vp, i64, i32, vp],
             "dp_checkpoint_load": [vp, C.c_char_p, vp, vp, vp, C.POINTER(i64), i32, vp],
             "dp_allreduce_mean_accum": [vp, vp, vp, vp, i32, i32, vp],
@@ -119,6 +120,11 @@ def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _cfg_ref(cfg):
+    """cfg=None: the update reads the scalars set by dp_set_adamw_cfg (graph capture)."""
+    return None if cfg is None else C.byref(cfg)
 
 
 def _ptr(t):
@@ -247,7 +253,7 @@ def dp_sharded_adamw_step(plan, ws, grad, master, m, v, params, cfg, use_clip_co
     _need(params, torch.bfloat16, plan.P * plan.stride, "params")
     b0, b1 = _range(plan, b0, b1)
     _check(lib().dp_sharded_adamw_step(plan.handle, _ws(plan, ws), _ptr(grad), _ptr(master), _ptr(m),
-                                       _ptr(v), _ptr(params), C.byref(cfg),
+                                       _ptr(v), _ptr(params), _cfg_ref(cfg),
                                        1 if use_clip_coef else 0, b0, b1, _stream(stream)))
 
 
@@ -275,7 +281,7 @@ def dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg, use_clip_coef
         _need(t, torch.float32, plan.L, name)
     _need(params, torch.bfloat16, plan.P * plan.stride, "params")
     _check(lib().dp_adamw_all_gather(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
-                                     _ptr(v), _ptr(params), C.byref(cfg), 1 if use_clip_coef else 0,
+                                     _ptr(v), _ptr(params), _cfg_ref(cfg), 1 if use_clip_coef else 0,
                                      _stream(stream)))
 
 
@@ -307,7 +313,7 @@ def dp_shard_adamw_step(plan, ws, mean, master, m, v, param_shards, cfg, use_cli
         _need(t, torch.float32, plan.L, name)
     _need(param_shards, torch.bfloat16, plan.L, "param_shards")
     _check(lib().dp_shard_adamw_step(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
-                                     _ptr(v), _ptr(param_shards), C.byref(cfg),
+                                     _ptr(v), _ptr(param_shards), _cfg_ref(cfg),
                                      1 if use_clip_coef else 0, _stream(stream)))
 
 
@@ -449,6 +455,13 @@ def dp_bounds_violations(reset=False):
     if n == -2:
         raise DPError(DP_ECUDA, "dp_bounds_violations: cannot read the device counters")
     return n
+
+
+def dp_set_adamw_cfg(plan, ws, cfg, stream=None):
+    """Store this step's AdamW scalars in the workspace; updates called with cfg=None
+    (e.g. inside a captured CUDA graph) use them.  Call outside the graph, before
+    each replay."""
+    _check(lib().dp_set_adamw_cfg(plan.handle, _ws(plan, ws), C.byref(cfg), _stream(stream)))
 
 
 def dp_fused_zero_step_launches(cfg):

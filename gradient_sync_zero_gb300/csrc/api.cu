@@ -3,6 +3,8 @@
 // call only enqueues work on the caller's stream (dp_read_norm also syncs it).
 #include <cuda_runtime.h>
 
+#include <cstddef>
+
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -123,9 +125,9 @@ int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* gra
   int rc = prepare("dp_sharded_adamw_step", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
   if ((rc = check_ptrs("dp_sharded_adamw_step", L.plan, {grad, master, m, v, params}))) return rc;
-  AdamScalars s;
-  if ((rc = adam_scalars("dp_sharded_adamw_step", cfg, &s))) return rc;
-  const int e = launch_adamw(L, grad, master, m, v, params, s, use_clip_coef != 0);
+  AdamScalars s{};
+  if (cfg && (rc = adam_scalars("dp_sharded_adamw_step", cfg, &s))) return rc;
+  const int e = launch_adamw(L, grad, master, m, v, params, s, use_clip_coef != 0, false, !cfg);
   return e ? cuda_fail(e, "dp_sharded_adamw_step") : DP_OK;
 }
 
@@ -169,9 +171,9 @@ int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean,
                    pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
   if (rc) return rc;
   if ((rc = check_ptrs("dp_adamw_all_gather", L.plan, {mean, master, m, v, params}))) return rc;
-  AdamScalars s;
-  if ((rc = adam_scalars("dp_adamw_all_gather", cfg, &s))) return rc;
-  const int e = launch_adamw_all_gather(L, mean, params, master, m, v, s, use_clip_coef != 0);
+  AdamScalars s{};
+  if (cfg && (rc = adam_scalars("dp_adamw_all_gather", cfg, &s))) return rc;
+  const int e = launch_adamw_all_gather(L, mean, params, master, m, v, s, use_clip_coef != 0, !cfg);
   return e ? cuda_fail(e, "dp_adamw_all_gather") : DP_OK;
 }
 
@@ -215,9 +217,9 @@ int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean,
                    pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
   if (rc) return rc;
   if ((rc = check_ptrs("dp_shard_adamw_step", L.plan, {mean, master, m, v, param_shards}))) return rc;
-  AdamScalars s;
-  if ((rc = adam_scalars("dp_shard_adamw_step", cfg, &s))) return rc;
-  const int e = launch_adamw(L, mean, master, m, v, param_shards, s, use_clip_coef != 0, true);
+  AdamScalars s{};
+  if (cfg && (rc = adam_scalars("dp_shard_adamw_step", cfg, &s))) return rc;
+  const int e = launch_adamw(L, mean, master, m, v, param_shards, s, use_clip_coef != 0, true, !cfg);
   return e ? cuda_fail(e, "dp_shard_adamw_step") : DP_OK;
 }
 
@@ -285,6 +287,26 @@ int64_t dp_bounds_violations(int32_t reset) {
   return a + b;
 }
 
+int dp_set_adamw_cfg(const dp_plan* plan, void* workspace, const dp_adamw_cfg* cfg, void* stream) {
+  clear_error();
+  const Plan* pl = as_plan(plan);
+  if (!pl || !workspace) return fail(DP_EINVAL, "dp_set_adamw_cfg: NULL plan or workspace");
+  if (misaligned(workspace)) return fail(DP_EALIGN, "dp_set_adamw_cfg: workspace not 32-byte aligned");
+  struct {
+    AdamScalars s;
+    uint32_t tag;
+  } blob{};
+  int rc = adam_scalars("dp_set_adamw_cfg", cfg, &blob.s);
+  if (rc) return rc;
+  blob.tag = kAdamTag;
+  static_assert(offsetof(DevHeader, adam_tag) == offsetof(DevHeader, adam) + sizeof(AdamScalars),
+                "scalars and tag are adjacent");
+  const cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(workspace) + offsetof(DevHeader, adam),
+                                        &blob, sizeof(AdamScalars) + sizeof(uint32_t),
+                                        cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DP_OK : cuda_fail(e, "dp_set_adamw_cfg");
+}
+
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
   return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
 }
@@ -336,6 +358,8 @@ int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float
     return fail(DP_ETIMEOUT, "dp_read_norm: a kernel's bounded wait on its copies gave up");
   if (h.status & DP_STATUS_NONFINITE)
     return fail(DP_ENONFINITE, "dp_read_norm: the global gradient norm was not finite");
+  if (h.status & DP_STATUS_NO_SCALARS)
+    return fail(DP_EINVAL, "dp_read_norm: an update ran with cfg = NULL before dp_set_adamw_cfg");
   return DP_OK;
 }
 

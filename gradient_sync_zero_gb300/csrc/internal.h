@@ -30,6 +30,12 @@ struct TileDesc {
 };
 static_assert(sizeof(TileDesc) == 32, "TileDesc is one 32-byte sector");
 
+// AdamW's per-step scalars, formed on the host (in double, rounded once).
+struct AdamScalars {
+  float wd_factor, b1, omb1, b2, omb2, step_size, sqrt_bc2, eps;
+};
+constexpr uint32_t kAdamTag = 0x574d4441u;   // "ADMW": the header holds scalars
+
 // Header at the start of the workspace (device).  The first part is uploaded
 // with the plan; the results part is written by kernels.
 struct DevHeader {
@@ -51,7 +57,10 @@ struct DevHeader {
   double norm;
   float coef;
   int32_t status;
-  int64_t reserved2_[7];
+  AdamScalars adam;       // set by dp_set_adamw_cfg, read by the update kernels when
+  uint32_t adam_tag;      // called without a cfg (graph-captured steps); kAdamTag
+  int32_t pad3_;
+  int64_t reserved2_[2];
 };
 static_assert(sizeof(DevHeader) % 64 == 0, "header keeps the arrays aligned");
 
@@ -84,10 +93,6 @@ const char* last_error_text();
 const Plan* as_plan(const dp_plan* p);
 
 // ---- kernel launchers (kernels_*.cu) ----
-struct AdamScalars {
-  float wd_factor, b1, omb1, b2, omb2, step_size, sqrt_bc2, eps;
-};
-
 struct Launch {
   const Plan* plan;
   uint8_t* ws;          // workspace base (device)
@@ -115,12 +120,14 @@ int launch_reduce_scatter_accum(const Launch& L, const void* acc, const void* mi
 int launch_allreduce_bf16wire(const Launch& L, void* grads);
 int launch_norm_finalize(const Launch& L, double max_norm);
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef, bool flat_params = false);
+                 void* params, const AdamScalars& s, bool use_coef, bool flat_params = false,
+                 bool dev_scalars = false);
 int launch_all_gather(const Launch& L, void* params);
 int launch_broadcast(const Launch& L, void* params, int src);
 int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,
                       float* v, const AdamScalars& s);
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
-                            float* m, float* v, const AdamScalars& s, bool use_coef);
+                            float* m, float* v, const AdamScalars& s, bool use_coef,
+                            bool dev_scalars = false);
 
 }  // namespace dps

@@ -16,10 +16,22 @@
 namespace dps {
 
 // Sharded AdamW on an fp32 gradient [L]; the owner's replica gets bf16(theta).
+// dev_s: take the step's scalars from the workspace header (dp_set_adamw_cfg), so a
+// captured graph of the step replays with the scalars of the current step.
+__device__ __forceinline__ bool header_scalars(const KCommon& k, AdamScalars& s) {
+  if (k.hdr->adam_tag != kAdamTag) {
+    if (threadIdx.x == 0) atomicOr(&k.hdr->status, DP_STATUS_NO_SCALARS);
+    return false;
+  }
+  s = k.hdr->adam;
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads)
     k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
-            AdamScalars s, int use_coef, int flat_params) {
+            AdamScalars s, int use_coef, int flat_params, int dev_s) {
   if (!plan_ok(k)) return;
+  if (dev_s && !header_scalars(k, s)) return;
   const float coef = use_coef ? k.hdr->coef : 1.0f;
   for_each_block(k, [&](int64_t, int64_t b, int c) {
     float g[16], th[16], mm[16], vv[16];
@@ -155,8 +167,7 @@ __global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
 
 int launch_replicate(const Launch& L, const RepArgs& a) {
   if (L.tile_end <= L.tile_begin) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_replicate, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kRepSmem));
+  cudaError_t e = ensure_dyn_smem(k_replicate, kRepSmem);
   if (e != cudaSuccess) return static_cast<int>(e);
   const int64_t cap = resident_ctas(k_replicate, 32, kRepSmem);
   if (cap <= 0) {
@@ -219,9 +230,10 @@ constexpr size_t kTmaSmem = kTmaStages * sizeof(TmaStage) + kTmaStages * sizeof(
 
 __global__ void __launch_bounds__(kThreads)
     k_adamw_all_gather(KCommon k, const float* mean, uint8_t* params, float* master, float* m,
-                       float* v, AdamScalars s, int64_t L, int use_coef) {
+                       float* v, AdamScalars s, int64_t L, int use_coef, int dev_s) {
   constexpr int kPer = kTmaChunk / kThreads;   // elements per thread per chunk (multiple of 4)
   if (!plan_ok(k)) return;
+  if (dev_s && !header_scalars(k, s)) return;
   if (!DP_IN_BOUNDS(L >= 0 && L <= kVecElems * k.hdr->n_vec)) return;
   const int64_t nchunks = (L + kTmaChunk - 1) / kTmaChunk;
   if (static_cast<int64_t>(blockIdx.x) >= nchunks) return;
@@ -343,9 +355,11 @@ int64_t bounds_violations_update(bool reset) {
 }
 
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef, bool flat_params) {
+                 void* params, const AdamScalars& s, bool use_coef, bool flat_params,
+                 bool dev_scalars) {
   return launch_tiles(L, k_adamw, make_common(L), grad, master, m, v,
-                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
+                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0,
+                      dev_scalars ? 1 : 0);
 }
 
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
@@ -381,12 +395,12 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
 }
 
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
-                            float* m, float* v, const AdamScalars& s, bool use_coef) {
+                            float* m, float* v, const AdamScalars& s, bool use_coef,
+                            bool dev_scalars) {
   const KCommon k = make_common(L);
   const int64_t Lp = L.plan->L;
   if (Lp == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_adamw_all_gather, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kTmaSmem));
+  cudaError_t e = ensure_dyn_smem(k_adamw_all_gather, kTmaSmem);
   if (e != cudaSuccess) return static_cast<int>(e);
   const int64_t cap = resident_ctas(k_adamw_all_gather, kThreads, kTmaSmem);
   if (cap <= 0) {
@@ -398,7 +412,8 @@ int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, f
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
   const int grid = static_cast<int>(g);
   k_adamw_all_gather<<<grid, kThreads, kTmaSmem, static_cast<cudaStream_t>(L.stream)>>>(
-      k, stage, static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0);
+      k, stage, static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0,
+      dev_scalars ? 1 : 0);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -39,6 +39,24 @@ inline float* stage_ptr(const Launch& L) {
   return reinterpret_cast<float*>(L.ws + h.off_stage);
 }
 
+// Opt a kernel in to `bytes` of dynamic shared memory, once per device (so that
+// launches inside a CUDA graph capture make no attribute call).
+template <class K>
+cudaError_t ensure_dyn_smem(K kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  std::lock_guard<std::mutex> g(mu);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done[key] = bytes;
+  return e;
+}
+
 // Resident CTAs per SM for a kernel (occupancy calculator, cached per device),
 // optionally capped by DPSYNC_CTAS_PER_SM for tuning sweeps.
 template <class K>

@@ -71,7 +71,12 @@ enum {
 };
 
 /* Status bits written by kernels into the workspace, read by dp_read_norm. */
-enum { DP_STATUS_PLAN_MISMATCH = 1, DP_STATUS_NONFINITE = 2, DP_STATUS_TIMEOUT = 4 };
+enum {
+  DP_STATUS_PLAN_MISMATCH = 1,
+  DP_STATUS_NONFINITE = 2,
+  DP_STATUS_TIMEOUT = 4,
+  DP_STATUS_NO_SCALARS = 8   /* an update ran without a cfg before dp_set_adamw_cfg */
+};
 
 typedef struct dp_plan dp_plan;
 
@@ -376,6 +381,20 @@ int dp_selftest_bounded_wait(int32_t* status_dev, int64_t limit_ns, void* stream
  * built without checks, -2 if the counters cannot be read.
  */
 int64_t dp_bounds_violations(int32_t reset);
+
+/*
+ * CUDA-graph capture of whole steps.  The update kernels take AdamW's per-step
+ * scalars as launch arguments, which a captured graph would freeze.  This call
+ * forms them from cfg on the host (exactly as the per-call path does) and copies
+ * them into the workspace on `stream`; dp_sharded_adamw_step, dp_adamw_all_gather
+ * and dp_shard_adamw_step called with cfg = NULL then read them from there when
+ * they run.  So: capture the step once with cfg = NULL, and before each replay call
+ * dp_set_adamw_cfg with that step's cfg (outside the graph).  An update that runs
+ * with cfg = NULL before any dp_set_adamw_cfg on this workspace skips its work and
+ * sets DP_STATUS_NO_SCALARS.  dp_plan_upload clears the scalars.  The host copy is
+ * staged by the driver before this call returns (cfg need not outlive it).
+ */
+int dp_set_adamw_cfg(const dp_plan* plan, void* workspace, const dp_adamw_cfg* cfg, void* stream);
 
 /* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);

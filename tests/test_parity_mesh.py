@@ -12,7 +12,7 @@ from workloads import configs
 pytestmark = pytest.mark.gpu
 
 SIZES = [3, 1000, 65536, 13107, 26214, 4097, 27910]
-MESHES = [(2, 4), (4, 2), (2, 2), (8, 1), (3, 2), (2, 3), (2, 8), (4, 4), (8, 2), (5, 2)]
+MESHES = [(2, 4), (4, 2), (2, 2), (8, 1), (3, 2), (2, 3), (2, 8), (4, 4), (8, 2), (5, 2), (8, 8)]
 
 
 def mesh_case(R, S, sigma=1e-3, cap=64 * 1024):

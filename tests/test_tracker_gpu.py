@@ -53,6 +53,29 @@ def test_streamed_allreduce_equals_oracle(orc, P, max_ctas):
         del keep
 
 
+def test_streamed_mesh_allreduce_equals_oracle(orc):
+    """The tracker on a hybrid 2 x 4 plan fires the mesh all-reduce bucket by bucket."""
+    P, R, S = 8, 2, 4
+    wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910, 9000], P, 32 * 1024, seed=77)
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, P, mesh=(R, S))
+    c = Case(wl)
+    c.plan, c.off, c.ws = plan, plan.tensor_offsets(), plan.new_workspace()
+    g = c.host_grads(1)
+    grads = plan.new_replicas()
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    tr = dps.Tracker(plan, dps.DP_TRACK_ALLREDUCE, c.ws, grads, stream=comm)
+    tr.begin()
+    keep = produce(c, g, grads, tr, producer, P)
+    tr.wait(10000)
+    assert tr.fired() == list(range(plan.n_buckets))
+    torch.cuda.synchronize()
+    want = orc.mesh_allreduce_mean(c.sizes, wl.bucket_bytes, R, S, g)
+    want = want[0] if isinstance(want, tuple) else want
+    assert np.array_equal(c.from_replicas(grads), want)
+    assert_replicas_equal(grads, plan.L)
+    del keep
+
+
 def test_streamed_zero_step_equals_fused(orc):
     """Tracker reduce-scatters bucket by bucket; then the clip coefficient and the
     fused AdamW + all-gather on the same stream == dp_fused_zero_step."""

@@ -165,3 +165,84 @@ def test_prefetch_schedule_on_two_streams_equals_sequential():
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     for a, b in zip(seen1, seen2):
         assert torch.equal(a, b)
+
+
+def test_captured_prefetch_step_equals_eager():
+    """The whole ZeRO-3 backward + update with the two-stream prefetch schedule,
+    captured once as a CUDA graph (cfg=None, scalars from dp_set_adamw_cfg) and
+    replayed for steps 1 and 2, equals the eager sequential flow bit for bit."""
+    wl = configs.llama_1b1_zero2(layers=2, embeddings=False)
+    wl.bucket_bytes = 4 << 20
+    c = Case(wl)
+    plan, nb, P = c.plan, c.plan.n_buckets, wl.P
+    grads = plan.new_replicas()
+    wdev.fill_grads(grads, c.off, wl, 1)
+    master0 = torch.randn(plan.L, device="cuda") * 0.02
+    max_len = max(plan.bucket(b)[1] for b in range(nb))
+
+    def cfg(t):
+        return dps.adamw_cfg(2e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, t)
+
+    # eager, sequential
+    sh_e = master0.to(torch.bfloat16)
+    st_e = [master0.clone(), plan.new_state(), plan.new_state()]
+    mean_e, ws_e = plan.new_state(), plan.new_workspace()
+    buf = torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda")
+    for t in (1, 2):
+        for b in range(nb):
+            o, ln, _ = plan.bucket(b)
+            dps.dp_unit_all_gather(plan, ws_e, sh_e, b, buf)
+            dps.dp_unit_reduce_scatter(plan, ws_e, grads[:, o:o + ln], b, mean_e, want_sumsq=True)
+        dps.dp_clip_coef(plan, ws_e, 1.0)
+        dps.dp_shard_adamw_step(plan, ws_e, mean_e, *st_e, sh_e, cfg(t), use_clip_coef=True)
+    # captured prefetch schedule
+    sh_g = master0.to(torch.bfloat16)
+    st_g = [master0.clone(), plan.new_state(), plan.new_state()]
+    mean_g, ws_g = plan.new_state(), plan.new_workspace()
+    bufs = [torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def body():
+        cur = torch.cuda.current_stream()
+        s_a.wait_stream(cur)
+        s_b.wait_stream(cur)
+        released = [None, None]
+        for i, b in enumerate(range(nb)):
+            o, ln, _ = plan.bucket(b)
+            with torch.cuda.stream(s_a):
+                if released[i % 2] is not None:
+                    s_a.wait_event(released[i % 2])
+                dps.dp_unit_all_gather(plan, ws_g, sh_g, b, bufs[i % 2])
+                ev = torch.cuda.Event()
+                ev.record(s_a)
+            with torch.cuda.stream(s_b):
+                s_b.wait_event(ev)
+                dps.dp_unit_reduce_scatter(plan, ws_g, grads[:, o:o + ln], b, mean_g, want_sumsq=True)
+                done = torch.cuda.Event()
+                done.record(s_b)
+                released[i % 2] = done
+        cur.wait_stream(s_a)
+        cur.wait_stream(s_b)
+        dps.dp_clip_coef(plan, ws_g, 1.0)
+        dps.dp_shard_adamw_step(plan, ws_g, mean_g, *st_g, sh_g, None, use_clip_coef=True)
+
+    # launcher setup outside the capture, on scratch state
+    scratch = [plan.new_state() for _ in range(4)]
+    dps.dp_unit_all_gather(plan, ws_g, sh_g, 0, bufs[0])
+    o0, ln0, _ = plan.bucket(0)
+    dps.dp_unit_reduce_scatter(plan, ws_g, grads[:, o0:o0 + ln0], 0, scratch[0])
+    dps.dp_shard_adamw_step(plan, ws_g, scratch[0], *scratch[1:], plan.new_state().to(torch.bfloat16),
+                            cfg(1))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    for t in (1, 2):
+        dps.dp_set_adamw_cfg(plan, ws_g, cfg(t))
+        graph.replay()
+    torch.cuda.synchronize()
+    assert dps.dp_read_norm(plan, ws_g) == dps.dp_read_norm(plan, ws_e)
+    assert torch.equal(sh_g, sh_e)
+    assert torch.equal(mean_g.view(torch.int32), mean_e.view(torch.int32))
+    for x, y in zip(st_g, st_e):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
