@@ -27,11 +27,9 @@ __device__ __forceinline__ bool header_scalars(const KCommon& k, AdamScalars& s)
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
-            AdamScalars s, int use_coef, int flat_params, int dev_s) {
-  if (!plan_ok(k)) return;
-  if (dev_s && !header_scalars(k, s)) return;
+__device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, float* master,
+                                           float* m, float* v, uint8_t* params,
+                                           const AdamScalars& s, int use_coef, int flat_params) {
   const float coef = use_coef ? k.hdr->coef : 1.0f;
   for_each_block(k, [&](int64_t, int64_t b, int c) {
     float g[16], th[16], mm[16], vv[16];
@@ -55,6 +53,22 @@ __global__ void __launch_bounds__(kThreads)
       for (int g = 0; g < k.R; ++g) st_blk(params + (g * k.S + c) * k.stride_bytes + 32 * b, val);
     }
   });
+}
+
+// DEV_S: the scalars come from the workspace header (a separate instantiation, so
+// the per-call path keeps them in the kernel's parameter space).
+template <bool DEV_S>
+__global__ void __launch_bounds__(kThreads)
+    k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
+            AdamScalars s, int use_coef, int flat_params) {
+  if (!plan_ok(k)) return;
+  if constexpr (DEV_S) {
+    AdamScalars sd;
+    if (!header_scalars(k, sd)) return;
+    adamw_body(k, grad, master, m, v, params, sd, use_coef, flat_params);
+  } else {
+    adamw_body(k, grad, master, m, v, params, s, use_coef, flat_params);
+  }
 }
 
 // ---- replica write-back with bulk copies: all-gather, broadcast, unit all-gather ----
@@ -228,12 +242,10 @@ struct TmaStage {
 };
 constexpr size_t kTmaSmem = kTmaStages * sizeof(TmaStage) + kTmaStages * sizeof(uint64_t);
 
-__global__ void __launch_bounds__(kThreads)
-    k_adamw_all_gather(KCommon k, const float* mean, uint8_t* params, float* master, float* m,
-                       float* v, AdamScalars s, int64_t L, int use_coef, int dev_s) {
+__device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mean, uint8_t* params,
+                                              float* master, float* m, float* v,
+                                              const AdamScalars& s, int64_t L, int use_coef) {
   constexpr int kPer = kTmaChunk / kThreads;   // elements per thread per chunk (multiple of 4)
-  if (!plan_ok(k)) return;
-  if (dev_s && !header_scalars(k, s)) return;
   if (!DP_IN_BOUNDS(L >= 0 && L <= kVecElems * k.hdr->n_vec)) return;
   const int64_t nchunks = (L + kTmaChunk - 1) / kTmaChunk;
   if (static_cast<int64_t>(blockIdx.x) >= nchunks) return;
@@ -319,6 +331,21 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// DEV_S: the scalars come from the workspace header (see k_adamw).
+template <bool DEV_S>
+__global__ void __launch_bounds__(kThreads)
+    k_adamw_all_gather(KCommon k, const float* mean, uint8_t* params, float* master, float* m,
+                       float* v, AdamScalars s, int64_t L, int use_coef) {
+  if (!plan_ok(k)) return;
+  if constexpr (DEV_S) {
+    AdamScalars sd;
+    if (!header_scalars(k, sd)) return;
+    adamw_ag_body(k, mean, params, master, m, v, sd, L, use_coef);
+  } else {
+    adamw_ag_body(k, mean, params, master, m, v, s, L, use_coef);
+  }
+}
+
 // Failure-path check of the bounded wait: one thread arms an mbarrier for 16
 // bytes that no copy will ever deliver, waits with the bulk-copy kernels' bounded
 // wait, and reports the timeout.  Nothing is in flight when it returns.
@@ -357,9 +384,8 @@ int64_t bounds_violations_update(bool reset) {
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
                  void* params, const AdamScalars& s, bool use_coef, bool flat_params,
                  bool dev_scalars) {
-  return launch_tiles(L, k_adamw, make_common(L), grad, master, m, v,
-                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0,
-                      dev_scalars ? 1 : 0);
+  return launch_tiles(L, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
+                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
 }
 
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
@@ -400,9 +426,10 @@ int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, f
   const KCommon k = make_common(L);
   const int64_t Lp = L.plan->L;
   if (Lp == 0) return cudaSuccess;
-  cudaError_t e = ensure_dyn_smem(k_adamw_all_gather, kTmaSmem);
+  auto kern = dev_scalars ? k_adamw_all_gather<true> : k_adamw_all_gather<false>;
+  cudaError_t e = ensure_dyn_smem(kern, kTmaSmem);
   if (e != cudaSuccess) return static_cast<int>(e);
-  const int64_t cap = resident_ctas(k_adamw_all_gather, kThreads, kTmaSmem);
+  const int64_t cap = resident_ctas(kern, kThreads, kTmaSmem);
   if (cap <= 0) {
     e = cudaGetLastError();
     return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
@@ -411,9 +438,8 @@ int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, f
   int64_t g = nchunks < cap ? nchunks : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
   const int grid = static_cast<int>(g);
-  k_adamw_all_gather<<<grid, kThreads, kTmaSmem, static_cast<cudaStream_t>(L.stream)>>>(
-      k, stage, static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0,
-      dev_scalars ? 1 : 0);
+  kern<<<grid, kThreads, kTmaSmem, static_cast<cudaStream_t>(L.stream)>>>(
+      k, stage, static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0);
   return static_cast<int>(cudaGetLastError());
 }
 
