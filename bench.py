@@ -400,8 +400,11 @@ def run_gpu(args, rank, local, world):
         h2d_gbs = host.numel() * host.element_size() / (h0.elapsed_time(h1) * 1e-3) / 1e9
         # Pipelined: the host-to-device copy runs on its own stream in bucket groups
         # of about equal size; each group's reduction starts as soon as its bytes
-        # have arrived, so only the last group's reduction and the update pass
-        # follow the copy (flat plans; a mesh plan runs copy-then-step).
+        # have arrived.  Across steps, step t+1's copy starts as soon as step t's
+        # reductions have consumed the gradient buffer, so it overlaps step t's
+        # update pass; each step's result (the 192-byte workspace header with the
+        # norm and status) is read back asynchronously into its own pinned buffer
+        # and checked after the loop (flat plans; a mesh plan runs copy-then-step).
         pipelined = mesh is None
         copy_stream = torch.cuda.Stream()
         nb = plan.n_buckets
@@ -414,6 +417,7 @@ def run_gpu(args, rank, local, world):
                 lo_b, acc_len = b + 1, 0
         if pipelined and zero:
             mean_buf = plan.new_state()
+        consumed = [None]                    # event: the last reduction of the previous step
 
         def e2e_step(step):
             if not pipelined:
@@ -421,7 +425,10 @@ def run_gpu(args, rank, local, world):
                 step_fn(step)
                 return
             evs = []
-            copy_stream.wait_stream(stream)
+            if consumed[0] is None:
+                copy_stream.wait_stream(stream)
+            else:
+                copy_stream.wait_event(consumed[0])
             with torch.cuda.stream(copy_stream):
                 for b0, b1 in groups:
                     o = plan.bucket(b0)[0]
@@ -437,6 +444,8 @@ def run_gpu(args, rank, local, world):
                     dps.dp_reduce_scatter_mean(plan, ws, grads, mean_buf, b0, b1, want_sumsq=clip)
                 else:
                     dps.dp_allreduce_mean(plan, ws, grads, b0, b1)
+            consumed[0] = torch.cuda.Event()
+            consumed[0].record(stream)
             if zero:
                 if clip:
                     dps.dp_clip_coef(plan, ws, wl.adamw.max_norm)
@@ -446,20 +455,28 @@ def run_gpu(args, rank, local, world):
         e2e_step(step + 1)                  # untimed: the pipelined path once
         step += 1
         torch.cuda.synchronize()
+        consumed[0] = None
+        results = [torch.empty(192, dtype=torch.uint8, pin_memory=True) for _ in range(e2e_steps)]
+        done = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
         barrier(world)
         t0 = time.perf_counter()
-        step_ms = []
-        for _ in range(e2e_steps):
+        done[0].record(stream)
+        for k in range(e2e_steps):
             step += 1
-            ts = time.perf_counter()
             e2e_step(step)
             if zero:
-                dps.dp_read_norm(plan, ws)
+                results[k].copy_(ws[:192], non_blocking=True)     # this step's result, D2H
             else:
                 torch.cuda.synchronize()
-            step_ms.append((time.perf_counter() - ts) * 1e3)
+            done[k + 1].record(stream)
         torch.cuda.synchronize()
         e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+        step_ms = [done[k].elapsed_time(done[k + 1]) for k in range(e2e_steps)]
+        if zero:
+            norms = [float(r[120:128].view(torch.float64)) for r in results]   # header: norm
+            status = [int(r[132:136].view(torch.int32)) for r in results]      # header: status
+            if any(st != 0 for st in status) or norms[-1] != dps.dp_read_norm(plan, ws)[0]:
+                raise RuntimeError(f"e2e: unexpected step results {norms} {status}")
         # the copies alone, in the same groups, for reading the number
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record(stream)
@@ -477,8 +494,10 @@ def run_gpu(args, rank, local, world):
                          "steps": e2e_steps, "h2d_gbs_alone": h2d_gbs,
                          "step_ms": [round(x, 2) for x in step_ms],
                          "grouped_copies_alone_ms": round(copy_only_ms, 2),
-                         "copy": (f"pipelined: {len(groups)} bucket groups, reduction overlapped "
-                                  "with the copy" if pipelined else "copy, then the step")}
+                         "copy": (f"pipelined: {len(groups)} bucket groups, each group's reduction "
+                                  "overlapped with the copy, the next step's copy with this step's "
+                                  "update; results read back asynchronously"
+                                  if pipelined else "copy, then the step")}
         if pipelined and zero:
             del mean_buf
         del host
@@ -1081,7 +1100,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama-1.1B-P8-zero2")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--mesh", default="",
