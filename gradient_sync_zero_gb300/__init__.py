@@ -89,6 +89,7 @@ def lib():
             "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
             "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
             "dp_tracker_begin": [vp],
+            "dp_tracker_set_micro": [vp, vp],
             "dp_tracker_mark_ready": [vp, i32, vp],
             "dp_tracker_wait": [vp, i64],
             "dp_tracker_fired": [vp, vp, i32, vp],
@@ -341,6 +342,7 @@ class Tracker:
                                        int(max_ctas), DP_TRACK_DRY_RUN if dry_run else 0,
                                        C.byref(h)))
         self._h = h
+        self._dry = dry_run
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -350,6 +352,14 @@ class Tracker:
 
     def begin(self):
         _check(lib().dp_tracker_begin(self._h))
+
+    def set_micro(self, micro):
+        """Last micro-batch of accumulation: fire the fused bf16(grads + micro)
+        reduction per bucket (None: the plain reduction)."""
+        if micro is not None and not getattr(self, "_dry", False):
+            _need(micro, torch.bfloat16, self.plan.P * self.plan.stride, "micro")
+        self._micro = micro
+        _check(lib().dp_tracker_set_micro(self._h, _ptr(micro) if micro is not None else None))
 
     def mark_ready(self, tensor, event=None):
         """event: torch.cuda.Event recorded after the tensor's gradient was written."""

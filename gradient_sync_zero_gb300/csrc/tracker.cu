@@ -1,4 +1,9 @@
 // Bucket readiness tracker: streamed per-bucket synchronisation.
+// With a micro-batch buffer set (dp_tracker_set_micro), each bucket's launch is the
+// last micro-batch of gradient accumulation fused with its sync: every rank's
+// bf16(grads + micro) is reduced ("Distributed Training: Data Parallel, Model
+// Parallel and FSDP Strategies", "Selecting and Tuning": no_sync on the other
+// micro-batches, sync on the final one, bucket by bucket as backward proceeds).
 //
 // DDP's core mechanism ("4.1 Data parallelism in depth", sec. 4.2): backward
 // produces gradients last layer first; a bucket's collective fires as soon as
@@ -29,6 +34,7 @@ struct Tracker {
   int flags = 0;
   uint8_t* ws = nullptr;
   void* grads = nullptr;
+  const void* micro = nullptr;      // set: the last micro-batch of accumulation (fused add)
   float* mean = nullptr;
   void* stream = nullptr;
   int max_ctas = 0;
@@ -79,8 +85,12 @@ int fire(Tracker& tr, int32_t b) {
   L.tile_end = tr.plan->b_tile0[b + 1];
   L.stream = tr.stream;
   L.max_ctas = tr.max_ctas;
-  const int e = tr.mode == DP_TRACK_ALLREDUCE ? launch_allreduce(L, tr.grads)
-                                              : launch_reduce_scatter(L, tr.grads, tr.mean, true);
+  int e;
+  if (tr.mode == DP_TRACK_ALLREDUCE)
+    e = tr.micro ? launch_allreduce_accum(L, tr.grads, tr.micro) : launch_allreduce(L, tr.grads);
+  else
+    e = tr.micro ? launch_reduce_scatter_accum(L, tr.grads, tr.micro, tr.mean, true)
+                 : launch_reduce_scatter(L, tr.grads, tr.mean, true);
   if (e) {
     tr.error_text = std::string("dp_tracker: bucket launch: ") +
                     cudaGetErrorString(static_cast<cudaError_t>(e));
@@ -137,6 +147,20 @@ int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* 
     return fail(DP_ENOMEM, "dp_tracker_create: out of host memory");
   }
   *out = reinterpret_cast<dp_tracker*>(tr);
+  return DP_OK;
+}
+
+int dp_tracker_set_micro(dp_tracker* tracker, const void* micro) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_set_micro: NULL tracker");
+  if (micro && tr->plan->R > 1) return fail(DP_EINVAL, "dp_tracker_set_micro: flat plans only");
+  if (reinterpret_cast<uintptr_t>(micro) & 31u)
+    return fail(DP_EALIGN, "dp_tracker_set_micro: micro must be 32-byte aligned");
+  std::lock_guard<std::mutex> g(tr->mu);
+  if (tr->next != 0 && tr->next != static_cast<int32_t>(tr->pending.size()))
+    return fail(DP_EINVAL, "dp_tracker_set_micro: a step is in progress (some buckets fired)");
+  tr->micro = micro;
   return DP_OK;
 }
 

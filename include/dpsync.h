@@ -433,6 +433,14 @@ enum { DP_TRACK_DRY_RUN = 1 };
 
 int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* grads, float* mean,
                       void* comm_stream, int32_t max_ctas, int32_t flags, dp_tracker** out);
+/* Gradient accumulation: with micro set (bf16 [P][replica_stride], 32-byte
+ * aligned), each bucket's launch fuses the last micro-batch's add — grads holds the
+ * sum of the earlier micro-batches, micro the last one's gradients as backward
+ * writes them; the reduction runs on bf16(grads + micro) (dp_allreduce_mean_accum
+ * / dp_reduce_scatter_mean_accum per bucket).  NULL restores the plain reduction.
+ * Flat plans only; refused (DP_EINVAL) while a step has fired some but not all
+ * buckets. */
+int dp_tracker_set_micro(dp_tracker* tracker, const void* micro);
 int dp_tracker_begin(dp_tracker* tracker);
 int dp_tracker_mark_ready(dp_tracker* tracker, int32_t tensor, void* ready_event);
 int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms);

@@ -118,3 +118,47 @@ def test_streamed_zero_step_equals_fused(orc):
     assert sto.coef == n2[1]
     assert np.array_equal(c.from_replicas(params), p_o)
     assert np.array_equal(c.from_flat(st[0]).view(np.uint32), m_o.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode", [dps.DP_TRACK_ALLREDUCE, dps.DP_TRACK_REDUCE_SCATTER])
+def test_streamed_last_micro_batch_equals_fused_single_launch(mode):
+    """Accumulation: grads holds the earlier micro-batches' sum; the last micro-batch's
+    gradients arrive tensor by tensor in backward order into `micro`, and each bucket
+    fires the fused add + sync.  Equal, bit for bit, to one fused launch."""
+    P = 8
+    wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910, 9000], P, 32 * 1024, seed=91)
+    c = Case(wl)
+    acc0 = c.to_replicas(c.host_grads(1))
+    g_last = c.host_grads(2)
+    # reference: one fused launch over all buckets
+    ref = acc0.clone()
+    mean_ref = c.plan.new_state()
+    if mode == dps.DP_TRACK_ALLREDUCE:
+        dps.dp_allreduce_mean_accum(c.plan, c.ws, ref, c.to_replicas(g_last))
+    else:
+        dps.dp_reduce_scatter_mean_accum(c.plan, c.ws, ref, c.to_replicas(g_last), mean_ref,
+                                         want_sumsq=True)
+        dps.dp_clip_coef(c.plan, c.ws, 1.0)
+    n_ref = dps.dp_read_norm(c.plan, c.ws)
+    # streamed
+    ws2 = c.plan.new_workspace()
+    acc = acc0.clone()
+    micro = c.plan.new_replicas()
+    mean = c.plan.new_state()
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    tr = dps.Tracker(c.plan, mode, ws2, acc, mean if mode == dps.DP_TRACK_REDUCE_SCATTER else None,
+                     stream=comm)
+    tr.set_micro(micro)
+    tr.begin()
+    keep = produce(c, g_last, micro, tr, producer, P)
+    tr.wait(10000)
+    if mode == dps.DP_TRACK_REDUCE_SCATTER:
+        dps.dp_clip_coef(c.plan, ws2, 1.0, stream=comm)
+    n2 = dps.dp_read_norm(c.plan, ws2, stream=comm)
+    torch.cuda.synchronize()
+    if mode == dps.DP_TRACK_ALLREDUCE:
+        assert torch.equal(acc, ref)
+    else:
+        assert torch.equal(mean.view(torch.int32), mean_ref.view(torch.int32)) and n2 == n_ref
+    del keep

@@ -136,3 +136,25 @@ def test_create_validates_buffers():
                                  C.byref(h)) == dps.DP_EINVAL    # reduce-scatter needs `mean`
     assert lib.dp_tracker_create(plan.handle, 7, ok, ok, ok, None, 0, 0,
                                  C.byref(h)) == dps.DP_EINVAL
+
+
+def test_set_micro_rules():
+    """Accumulation mode: flat plans only, 32-byte aligned, and not in the middle
+    of a step (some but not all buckets fired)."""
+    import ctypes as C
+    sizes = [1000, 1000, 1000, 1000]
+    plan, tr = dry(sizes, 4000, 2)
+    lib = dps.lib()
+    assert lib.dp_tracker_set_micro(tr._h, C.c_void_p(1 << 20)) == dps.DP_OK
+    assert lib.dp_tracker_set_micro(tr._h, C.c_void_p((1 << 20) + 16)) == dps.DP_EALIGN
+    tr.begin()
+    tr.mark_ready(3)
+    tr.mark_ready(2)                                   # bucket 0 fired, bucket 1 not
+    assert tr.fired() == [0]
+    assert lib.dp_tracker_set_micro(tr._h, None) == dps.DP_EINVAL
+    tr.mark_ready(1)
+    tr.mark_ready(0)
+    assert lib.dp_tracker_set_micro(tr._h, None) == dps.DP_OK   # step complete
+    mesh = dps.Plan(sizes, 4000, 4, mesh=(2, 2))
+    trm = dps.Tracker(mesh, dps.DP_TRACK_ALLREDUCE, dry_run=True)
+    assert lib.dp_tracker_set_micro(trm._h, C.c_void_p(1 << 20)) == dps.DP_EINVAL
