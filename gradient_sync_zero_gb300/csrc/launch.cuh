@@ -87,20 +87,46 @@ int resident_ctas(K kernel, int threads, size_t dyn_smem = 0) {
 }
 
 // Launch `kernel` over the tiles of L with a persistent grid.
+inline int sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev] = sms;
+  return sms;
+}
+
+// Persistent grid over the launch's tiles: at most the resident CTAs, or
+// per_sm CTAs per SM when given (some read/write mixes run faster with fewer
+// loads in flight than full occupancy keeps).
 template <class K, class... A>
-int launch_tiles(const Launch& L, K kernel, A... args) {
+int launch_tiles_per_sm(const Launch& L, int per_sm, K kernel, A... args) {
   const int64_t n = L.tile_end - L.tile_begin;
   if (n <= 0) return cudaSuccess;
-  const int cap = resident_ctas(kernel, kThreads);
+  int cap = resident_ctas(kernel, kThreads);
   if (cap <= 0) {
     const cudaError_t e = cudaGetLastError();
     return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
+  }
+  if (per_sm > 0) {
+    const int sms = sm_count();
+    if (sms > 0 && cap > sms * per_sm) cap = sms * per_sm;
   }
   int64_t g = n < cap ? n : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
   const int grid = static_cast<int>(g);
   kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(args...);
   return static_cast<int>(cudaGetLastError());
+}
+
+template <class K, class... A>
+int launch_tiles(const Launch& L, K kernel, A... args) {
+  return launch_tiles_per_sm(L, 0, kernel, args...);
 }
 
 // Rank counts with a fully unrolled instantiation; others use the runtime-P one.
