@@ -38,6 +38,8 @@ struct KCommon {
   int32_t R;             // mesh: replicate groups (1 = flat ring)
   int32_t S;             // mesh: shard ranks per group (P = R * S)
   int64_t rep_block0;    // replica buffers start at this 32-byte block (unit buffers)
+  int32_t split;         // CTAs per tile (1, or 2 for launches with few tiles)
+  int32_t pad_;
 };
 
 // ---- optional index checks (built with -DDPSYNC_CHECKED) ----
@@ -616,39 +618,62 @@ __device__ __forceinline__ int owner_of(const TileDesc& d, int64_t v) {
 }
 
 // Loop over the 32-byte blocks of the CTA's tiles: f(tile, block index b,
-// owner c).  Tiles start at even 16-byte vectors and hold an even count.
-template <class F>
+// owner c).  Tiles start at even 16-byte vectors and hold an even count.  With
+// k.split = 2 (launches over few tiles) two CTAs share each tile, alternating
+// runs of kThreads blocks, so every thread of a small launch moves one block.
+template <bool SPLIT = true, class F>
 __device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-    if (!tile_ok(k, tile, d)) continue;
-    const int nblk = d.nvec >> 1;
-    const int64_t b0 = d.v0 >> 1;
+  // the common case (split 1) keeps constant strides; split 2 is for small launches
+  // (SPLIT = false: a kernel always launched unsplit compiles the first walk only)
+  auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
+    for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
+      const TileDesc d = load_tile(k, tile);
+      if (!tile_ok(k, tile, d)) continue;
+      const int nblk = d.nvec >> 1;
+      const int64_t b0 = d.v0 >> 1;
 #pragma unroll 1
-    for (int j = threadIdx.x; j < nblk; j += kThreads) {
-      const int64_t b = b0 + j;
-      const int c = owner_of(d, 2 * b);
-      if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
-      f(tile, b, c);
+      for (int j = j0; j < nblk; j += jstep) {
+        const int64_t b = b0 + j;
+        const int c = owner_of(d, 2 * b);
+        if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+        f(tile, b, c);
+      }
     }
+  };
+  if (!SPLIT || k.split == 1) {
+    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, kThreads);
+  } else {
+    const int64_t cta_tile = blockIdx.x / 2;
+    walk(k.tile_begin + cta_tile, gridDim.x / 2,
+         static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
   }
 }
 
 // Same loop, giving the body the tile descriptor: f(desc, block b, owner c).
-template <class F>
+template <bool SPLIT = true, class F>
 __device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-    if (!tile_ok(k, tile, d)) continue;
-    const int nblk = d.nvec >> 1;
-    const int64_t b0 = d.v0 >> 1;
+  // the common case (split 1) keeps constant strides; split 2 is for small launches
+  auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
+    for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
+      const TileDesc d = load_tile(k, tile);
+      if (!tile_ok(k, tile, d)) continue;
+      const int nblk = d.nvec >> 1;
+      const int64_t b0 = d.v0 >> 1;
 #pragma unroll 1
-    for (int j = threadIdx.x; j < nblk; j += kThreads) {
-      const int64_t b = b0 + j;
-      const int c = owner_of(d, 2 * b);
-      if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
-      f(d, b, c);
+      for (int j = j0; j < nblk; j += jstep) {
+        const int64_t b = b0 + j;
+        const int c = owner_of(d, 2 * b);
+        if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+        f(d, b, c);
+      }
     }
+  };
+  if (!SPLIT || k.split == 1) {
+    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, kThreads);
+  } else {
+    const int64_t cta_tile = blockIdx.x / 2;
+    walk(k.tile_begin + cta_tile, gridDim.x / 2,
+         static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
   }
 }
 

@@ -37,30 +37,41 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
                                                              const uint8_t* micro) {
   if (!plan_ok(k)) return;
   __shared__ FF warp_part[kWarps];
-  for (int64_t tile = k.tile_begin + blockIdx.x; tile < k.tile_end; tile += gridDim.x) {
-    const TileDesc d = load_tile(k, tile);
-    if (!tile_ok(k, tile, d)) continue;
-    const int nblk = d.nvec >> 1;
-    const int64_t b0 = d.v0 >> 1;
-    FF ss{0.0f, 0.0f};
+  // k.split = 2 (small launches) only without norm partials: a tile's partial has
+  // one writer.  The common case keeps constant strides.
+  auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
+    for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
+      const TileDesc d = load_tile(k, tile);
+      if (!tile_ok(k, tile, d)) continue;
+      const int nblk = d.nvec >> 1;
+      const int64_t b0 = d.v0 >> 1;
+      FF ss{0.0f, 0.0f};
 #pragma unroll 1
-    for (int j = threadIdx.x; j < nblk; j += kThreads) {
-      const int64_t b = b0 + j;
-      const int c = owner_of(d, 2 * b);
-      if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
-      float acc[16];
-      if constexpr (ACC) {
-        ring_mean16_accum<P>(g, micro, k.stride_bytes, 32 * b, c, k.P, acc);
-      } else {
-        block_mean16<P, MS>(k, g, b, d, c, acc);
-      }
-      st_f16(mean, b, acc);
-      if (sumsq) {
+      for (int j = j0; j < nblk; j += jstep) {
+        const int64_t b = b0 + j;
+        const int c = owner_of(d, 2 * b);
+        if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+        float acc[16];
+        if constexpr (ACC) {
+          ring_mean16_accum<P>(g, micro, k.stride_bytes, 32 * b, c, k.P, acc);
+        } else {
+          block_mean16<P, MS>(k, g, b, d, c, acc);
+        }
+        st_f16(mean, b, acc);
+        if (sumsq) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
+          for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
+        }
       }
+      if (sumsq) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
     }
-    if (sumsq) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
+  };
+  if (ACC || k.split == 1) {   // the accumulating form always launches unsplit
+    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, kThreads);
+  } else {
+    const int64_t cta_tile = blockIdx.x / 2;
+    walk(k.tile_begin + cta_tile, gridDim.x / 2,
+         static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
   }
 }
 
@@ -99,7 +110,7 @@ template <int P>
 __global__ void __launch_bounds__(kThreads) k_allreduce_accum(KCommon k, uint8_t* acc,
                                                               const uint8_t* micro) {
   if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int c) {
+  for_each_block<false>(k, [&](int64_t, int64_t b, int c) {
     float mean[16];
     ring_mean16_accum<P>(acc, micro, k.stride_bytes, 32 * b, c, k.P, mean);
     store_replicas<P>(acc, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
@@ -110,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_accum(KCommon k, uint8_t
 template <int P>
 __global__ void __launch_bounds__(kThreads) k_allreduce_bf16wire(KCommon k, uint8_t* g) {
   if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int c) {
+  for_each_block<false>(k, [&](int64_t, int64_t b, int c) {
     float mean[16];
     ring_mean16_bf16wire<P>(g, k.stride_bytes, 32 * b, c, k.P, mean);
     store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
@@ -171,8 +182,12 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      return launch_tiles(L, k_reduce_scatter<P, M, false>, k, static_cast<const uint8_t*>(grads),
-                          mean, sumsq ? 1 : 0, static_cast<const uint8_t*>(nullptr));
+      if (sumsq)
+        return launch_tiles(L, k_reduce_scatter<P, M, false>, k, static_cast<const uint8_t*>(grads),
+                            mean, 1, static_cast<const uint8_t*>(nullptr));
+      return launch_tiles_split(L, 0, k_reduce_scatter<P, M, false>, k,
+                                static_cast<const uint8_t*>(grads), mean, 0,
+                                static_cast<const uint8_t*>(nullptr));
     });
   });
 }
@@ -193,7 +208,7 @@ int launch_allreduce(const Launch& L, void* grads) {
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      return launch_tiles_per_sm(L, kAllreducePerSm, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
+      return launch_tiles_split(L, kAllreducePerSm, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
     });
   });
 }
@@ -214,8 +229,8 @@ int64_t bounds_violations_reduce(bool reset) {
 }
 
 int launch_accumulate(const Launch& L, void* acc, const void* micro) {
-  return launch_tiles_per_sm(L, kAccumPerSm, k_accumulate, make_common(L), static_cast<uint8_t*>(acc),
-                             static_cast<const uint8_t*>(micro));
+  return launch_tiles_split(L, kAccumPerSm, k_accumulate, make_common(L), static_cast<uint8_t*>(acc),
+                            static_cast<const uint8_t*>(micro));
 }
 
 int launch_allreduce_accum(const Launch& L, void* acc, const void* micro) {

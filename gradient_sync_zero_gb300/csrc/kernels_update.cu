@@ -391,7 +391,7 @@ int64_t bounds_violations_update(bool reset) {
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
                  void* params, const AdamScalars& s, bool use_coef, bool flat_params,
                  bool dev_scalars) {
-  return launch_tiles(L, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
+  return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
                       static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
 }
 
@@ -421,8 +421,8 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      return launch_tiles(L, k_zero_fused<P, M>, k, static_cast<const uint8_t*>(grads),
-                          static_cast<uint8_t*>(params), master, m, v, s);
+      return launch_tiles_split(L, 0, k_zero_fused<P, M>, k, static_cast<const uint8_t*>(grads),
+                                static_cast<uint8_t*>(params), master, m, v, s);
     });
   });
 }

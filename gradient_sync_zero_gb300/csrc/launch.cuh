@@ -30,6 +30,8 @@ inline KCommon make_common(const Launch& L) {
   k.R = L.plan->R;
   k.S = L.plan->S;
   k.rep_block0 = 0;
+  k.split = 1;
+  k.pad_ = 0;
   return k;
 }
 
@@ -127,6 +129,31 @@ int launch_tiles_per_sm(const Launch& L, int per_sm, K kernel, A... args) {
 template <class K, class... A>
 int launch_tiles(const Launch& L, K kernel, A... args) {
   return launch_tiles_per_sm(L, 0, kernel, args...);
+}
+
+// As launch_tiles_per_sm for kernels that loop with for_each_block(2): when the
+// launch covers at most half as many tiles as CTAs fit, two CTAs share each tile
+// (k.split = 2), halving each thread's serial chain of loads for the small
+// per-bucket launches of streamed synchronisation.
+template <class K, class... A>
+int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... args) {
+  const int64_t n = L.tile_end - L.tile_begin;
+  if (n <= 0) return cudaSuccess;
+  int cap = resident_ctas(kernel, kThreads);
+  if (cap <= 0) {
+    const cudaError_t e = cudaGetLastError();
+    return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
+  }
+  if (per_sm > 0) {
+    const int sms = sm_count();
+    if (sms > 0 && cap > sms * per_sm) cap = sms * per_sm;
+  }
+  if (L.max_ctas > 0 && cap > L.max_ctas) cap = L.max_ctas;
+  k.split = 2 * n <= cap ? 2 : 1;
+  int64_t g = n * k.split < cap ? n * k.split : cap;
+  g -= g % k.split;
+  kernel<<<static_cast<int>(g), kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(k, args...);
+  return static_cast<int>(cudaGetLastError());
 }
 
 // Rank counts with a fully unrolled instantiation; others use the runtime-P one.
