@@ -38,7 +38,7 @@ def test_accumulate_equals_oracle(orc, P):
     assert not acc[:, :c.plan.L][:, c.padding_mask().cuda()].any()   # padding stays zero
 
 
-@pytest.mark.parametrize("P", [2, 5, 8, 12, 16])
+@pytest.mark.parametrize("P", [2, 5, 8, 12, 16, 64])
 def test_last_micro_batch_fused_equals_oracle(orc, P):
     """k-1 local accumulations, then one fused accumulate + mean all-reduce =
     oracle accumulate k-1 times, then its ring all-reduce."""
@@ -147,7 +147,7 @@ def test_full_size_gpt2_accumulation_sampled(orc):
                               orc.accumulate(a, b))
 
 
-@pytest.mark.parametrize("P", [2, 5, 8, 16])
+@pytest.mark.parametrize("P", [2, 5, 8, 16, 24])
 def test_last_micro_batch_reduce_scatter_equals_oracle(orc, P):
     """ZeRO form: the fused last micro-batch reduce-scatter gives the oracle's fp32
     mean of the accumulated gradients bit for bit, the same norm partials as the

@@ -30,7 +30,7 @@ def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf):
     return gathered
 
 
-@pytest.mark.parametrize("P", [2, 4, 5, 8])
+@pytest.mark.parametrize("P", [2, 4, 5, 8, 12, 16])
 def test_zero3_flow_matches_oracle(orc, P):
     wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910], P, 64 * 1024, sigma=0.05,
                         seed=30 + P)
