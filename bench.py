@@ -173,13 +173,14 @@ def kernel_source_hash():
 
 
 def stored_traffic(workload, kernel):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-    profiles/traffic.json, only if it was taken on the current kernel sources."""
-    tf = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
+    profiles' DRAM-traffic record, only if it was taken on the current kernel sources."""
+    tf = os.path.join(ROOT, "profiles", "dram_traffic_llama-1.1B-P8-zero2.txt")
     if not os.path.exists(tf):
         return None, "no ncu capture recorded"
     with open(tf) as f:
-        tdb = json.load(f)
+        text = f.read()
+    tdb = json.loads(text[text.index("{"):])     # comment lines, then the JSON record
     rec = tdb.get(f"{workload}:{kernel}")
     if rec is None:
         return None, "no ncu capture for this workload and kernel"
