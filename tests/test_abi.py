@@ -203,3 +203,21 @@ def test_mesh_plan_rejects_bad_shapes():
         dps.Plan([10], 1024, 8, mesh=(3, 2))
     with pytest.raises(dps.DPError):
         dps.Plan([10], 1024, 128, mesh=(16, 8))
+
+
+def test_binding_rejects_wrong_buffers_before_any_call():
+    """The binding checks dtype, device, contiguity and size of every buffer and
+    raises before the library is called (no GPU needed to see it)."""
+    import torch
+    plan = dps.Plan([1000, 70000], 64 * 1024, 4)
+    ws = torch.zeros(plan.info.workspace_bytes, dtype=torch.uint8)
+    g = torch.zeros(plan.P, plan.stride, dtype=torch.bfloat16)          # host tensor
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dps.dp_allreduce_mean(plan, ws, g)
+    with pytest.raises(TypeError, match="must be a torch.Tensor"):
+        dps.dp_allreduce_mean(plan, ws, g.float().numpy())
+    with pytest.raises(ValueError, match="does not multiply"):
+        dps.Plan([1000], 1 << 20, 8, mesh=(3, 2))
+    with pytest.raises(dps.DPError) as e:
+        dps.Plan([1000], 1 << 20, 65)
+    assert e.value.code == dps.DP_EINVAL
