@@ -164,11 +164,17 @@ KERNEL_SOURCES = ["kernels.cuh", "kernels_reduce.cu", "kernels_update.cu", "laun
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and whitespace are removed first,
+    so an edit to a comment does not retire a DRAM-traffic record."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "gradient_sync_zero_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "gradient_sync_zero_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                 # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

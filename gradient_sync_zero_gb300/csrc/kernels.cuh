@@ -131,10 +131,10 @@ __device__ __forceinline__ Blk pack16_rne(const float (&f)[16]) {
 
 // ---- ring-ordered reduction + mean ----
 // The owner c of a shard receives its sum in the ring's order: rank c+1's value
-// first, then c+2, ..., ending with rank c (indices mod P) — the order in which
-// "every rank sends one chunk clockwise ... the received chunk is added into a
-// local partial sum" ("Data Parallelism: From Parameter Server to Ring
-// All-Reduce", sec. 5).  The replicas are loaded directly in that order (the
+// first, then c+2, ..., ending with rank c (indices mod P) — the order a ring
+// builds it in, each rank passing a chunk to its neighbour, which adds it to its
+// own running sum ("Data Parallelism: From Parameter Server to Ring All-Reduce",
+// sec. 5).  The replicas are loaded directly in that order (the
 // owner is known from the block index), up to 8 blocks in flight per thread,
 // and folded with fp32 adds in the same order.  Then G = sum / N (sec. 1) as an
 // IEEE division, which a multiply by 1/P reproduces exactly for P = 2^k.

@@ -1,8 +1,8 @@
 // Sharded AdamW, all-gather / broadcast write-back, and the fused ZeRO-1/2 step.
 //
-// "ZeRO-1 and ZeRO-2 simply stop after the reduce-scatter, update the shard each
-// rank owns, and all-gather the updated parameters" ("Data Parallelism: DDP,
-// ZeRO and FSDP", "The three stages").  On one GPU the P replicas are P HBM
+// ZeRO-1 and ZeRO-2 keep DDP's reduce-scatter, let each rank update only the
+// shard it owns, and all-gather the new parameters ("Data Parallelism: DDP, ZeRO
+// and FSDP", "The three stages").  On one GPU the P replicas are P HBM
 // buffers, so the fused kernel performs the three phases per 32-byte block:
 // read P gradient blocks and the owner's fp32 state once, write the state and
 // P parameter blocks once.

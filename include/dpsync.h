@@ -10,12 +10,12 @@
  *     ("4.1 Data parallelism in depth", sec. 4.2 "The Bucket mechanism");
  *   - the mean all-reduce G = sum_i G_i / N, decomposed into a reduce-scatter
  *     and an all-gather ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 1
- *     "The Contract" and sec. 5 "Ring All-Reduce = Reduce-Scatter + All-Gather");
+ *     and sec. 5, the ring's two phases);
  *   - the ZeRO-1/2 step: reduce-scatter, update the owned shard with AdamW on
  *     fp32 master/m/v, all-gather the updated bf16 parameters ("Data
  *     Parallelism: DDP, ZeRO and FSDP", "The three stages"), with optional
  *     global gradient-norm clipping ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies",
- *     "Inside DDP": clip_grad_norm_(params, 1.0)).
+ *     "Inside DDP": the gradients are clipped to norm 1.0 after averaging).
  *
  * Conventions shared by every call
  * --------------------------------
@@ -103,9 +103,9 @@ typedef struct {
 } dp_adamw_cfg;
 
 /*
- * Bucket planner.  "DDP packs parameter gradients into Buckets in
- * reverse-compute order (default ~25 MB each)" ("4.1 Data parallelism in
- * depth", sec. 4.2; bucket_cap_mb).  Rule: walk tensors n-1 ... 0; each takes a
+ * Bucket planner.  DDP groups gradients into buckets of about 25 MB, filled in
+ * the reverse of the order the forward pass computes them ("4.1 Data
+ * parallelism in depth", sec. 4.2; PyTorch's bucket_cap_mb).  Rule: walk tensors n-1 ... 0; each takes a
  * slot of ceil(size/8)*8 elements (16-byte aligned); a non-empty bucket is
  * closed when adding the next slot would exceed bucket_bytes/2 elements; a
  * tensor is never split (one larger than the cap forms its own bucket); a
@@ -129,8 +129,8 @@ int dp_plan_buckets_ex(const int64_t* sizes, const uint8_t* decay, int32_t n_ten
 
 /*
  * Same, on a hybrid R x S device mesh (P = R * S ranks; rank (g, s) = g*S + s):
- * HYBRID_SHARD, "FULL_SHARD inside a node + data parallel across nodes" ("4.1
- * Data parallelism in depth", sec. 6.3); FSDP2's DeviceMesh mesh_shape=(2, 4)
+ * HYBRID_SHARD, full sharding within a group of ranks and plain data
+ * parallelism between the groups ("4.1 Data parallelism in depth", sec. 6.3); FSDP2's DeviceMesh mesh_shape=(2, 4)
  * with dims ("replicate", "shard") ("Distributed Training: Data Parallel, Model
  * Parallel and FSDP Strategies", "FSDP1 vs FSDP2"); "Data Parallelism: DDP, ZeRO
  * and FSDP", "Hybrid sharding".  Each bucket is split into S shards, shard s
@@ -169,7 +169,8 @@ int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream);
 
 /*
  * Reduce-scatter + mean ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
- * after N-1 steps every rank owns one fully reduced chunk; sec. 1: G = sum G_i / N).
+ * the first N-1 ring steps leave each rank holding the complete sum of one
+ * chunk; sec. 1: the synchronised gradient is the ranks' average).
  *   grads   bf16 [P][replica_stride], read only.
  *   mean    fp32 [L]; for each bucket in [b0,b1), shard c's slots receive the
  *           fp32 mean that rank c owns.
@@ -183,7 +184,7 @@ int dp_reduce_scatter_mean(const dp_plan* plan, void* workspace, const void* gra
  * Global gradient-norm clip coefficient over buckets [b0,b1) from the partials
  * of a preceding dp_reduce_scatter_mean(want_sumsq=1) over the same buckets
  * ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP":
- * clip_grad_norm_(model.parameters(), 1.0) after the averaged gradients).
+ * the averaged gradients are clipped to a global norm of 1.0).
  * norm = sqrt(sum mean^2) (partials summed in double in tile order);
  * coef = min(1, max_norm / (norm + 1e-6)), or 1 when max_norm <= 0; a
  * non-finite norm gives coef = NaN and sets DP_STATUS_NONFINITE.  Results stay
@@ -212,7 +213,8 @@ int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* gra
 
 /*
  * All-gather, in place ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
- * reduced shards circulate until every rank has the full tensor): for every
+ * the second phase passes the reduced chunks around the ring so that all ranks
+ * end with the whole result): for every
  * shard c of buckets [b0,b1), copy params[c][shard c] into every other replica.
  */
 int dp_all_gather(const dp_plan* plan, void* workspace, void* params, int32_t b0, int32_t b1,
@@ -221,7 +223,8 @@ int dp_all_gather(const dp_plan* plan, void* workspace, void* params, int32_t b0
 /*
  * Broadcast replica `src` into every other replica over buckets [b0,b1): the
  * one-time start-up broadcast of rank 0's parameters ("4.1 Data parallelism in
- * depth", sec. 4.1 "broadcast once, sync many times").
+ * depth", sec. 4.1: parameters are copied from one rank once at the start,
+ * gradients are synchronised every step).
  */
 int dp_broadcast(const dp_plan* plan, void* workspace, void* params, int32_t src, int32_t b0,
                  int32_t b1, void* stream);
@@ -299,7 +302,7 @@ int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean,
 /*
  * Gradient accumulation ("Distributed Training: Data Parallel, Model Parallel and
  * FSDP Strategies", "Selecting and Tuning": no_sync on every micro-batch but the
- * last, "sync only on final micro-batch").  Each rank accumulates its bf16
+ * last, which alone is synchronised).  Each rank accumulates its bf16
  * gradients as autograd does for bf16 gradients: acc = bf16(acc + g), the add in
  * fp32, rounding to nearest even.
  * dp_accumulate: acc[r] = bf16(acc[r] + micro[r]) for every replica, buckets [b0,b1).
@@ -321,9 +324,9 @@ int dp_reduce_scatter_mean_accum(const dp_plan* plan, void* workspace, const voi
 
 /*
  * The mean all-reduce with bf16 on the wire, as a precision comparison
- * ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 8:
- * "gradient dtype and communication hooks change both bandwidth and numerical
- * behavior"): every ring hop's partial sum is rounded to bf16 (the add in fp32),
+ * ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 8: the dtype
+ * the gradients travel in affects both the bytes moved and the numerics):
+ * every ring hop's partial sum is rounded to bf16 (the add in fp32),
  * the owner's sum is divided by P in fp32 and rounded to bf16.  Flat plans only.
  */
 int dp_allreduce_mean_bf16wire(const dp_plan* plan, void* workspace, void* grads, int32_t b0,
@@ -400,10 +403,10 @@ int dp_set_adamw_cfg(const dp_plan* plan, void* workspace, const dp_adamw_cfg* c
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
 
 /*
- * Streamed per-bucket synchronisation: DDP's bucket readiness.  "When every
- * gradient in a Bucket is ready, immediately AllReduce that Bucket" while
- * earlier layers keep running backward ("4.1 Data parallelism in depth",
- * sec. 4.2); the collective fires "on a separate stream" ("Distributed
+ * Streamed per-bucket synchronisation: DDP's bucket readiness.  As soon as all
+ * of a bucket's gradients exist its all-reduce starts, while backward continues
+ * through the earlier layers ("4.1 Data parallelism in depth", sec. 4.2); the
+ * communication runs on its own stream beside the computation ("Distributed
  * Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP");
  * buckets fire in the same order every step ("Data Parallelism: DDP, ZeRO and
  * FSDP", "DDP, and why it works": bucket order must match).

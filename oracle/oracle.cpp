@@ -13,15 +13,17 @@
 //    all-reduce = reduce-scatter + all-gather, ring volume 2(N-1)/N * Psi;
 //    sec. 6.1 and 7: the ZeRO stages and the 16-byte/parameter ledger; sec. 8.2:
 //    ZeRO-3 moves 3 Psi.
-//  * "Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 1: G = sum_i G_i / N,
-//    W <- optimizer_step(W, G); sec. 5: each ring step sends one chunk clockwise,
-//    the receiver adds it into a local partial sum, N-1 steps leave each rank one
-//    fully reduced chunk; the all-gather forwards reduced chunks for N-1 more
-//    steps; per-rank traffic 2(N-1)/N * M; sec. 6: 2(N-1) steps.
+//  * "Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 1: the
+//    synchronised gradient is the average over the N ranks, and every rank applies
+//    the same optimizer step with it; sec. 5: at each ring step a rank passes one
+//    chunk to its neighbour, which adds it to its own running sum, so after N-1
+//    steps each rank holds one chunk's complete sum, and N-1 more steps pass the
+//    reduced chunks on until every rank has all of them; per-rank traffic
+//    2(N-1)/N * M; sec. 6: 2(N-1) steps.
 //  * "Data Parallelism: DDP, ZeRO and FSDP", "The three stages": ZeRO-1/2
 //    reduce-scatter, update the owned shard, all-gather the updated parameters.
 //  * "Distributed Training: Data Parallel, Model Parallel and FSDP Strategies", "Inside DDP":
-//    AdamW(lr=2e-4, weight_decay=0.1) and clip_grad_norm_(params, 1.0) after the
+//    AdamW with learning rate 2e-4 and weight decay 0.1, clipping to norm 1.0 after the
 //    averaged gradients; "FSDP1 vs FSDP2": MixedPrecisionPolicy(param bf16,
 //    reduce fp32).
 //
@@ -100,8 +102,8 @@ struct Plan {
   std::vector<std::vector<int32_t>> b_tensors;  // tensors of each bucket
 };
 
-// R5.  "DDP packs parameter gradients into Buckets in reverse-compute order
-// (default ~25 MB each)" ("4.1 Data parallelism in depth", sec. 4.2); buckets fire in that order.
+// R5.  DDP fills buckets of about 25 MB in the reverse of the forward pass's
+// order ("4.1 Data parallelism in depth", sec. 4.2); buckets fire in that order.
 bool make_plan(const int64_t* sizes, int n, int64_t bucket_bytes, int P, Plan* pl) {
   if (n < 0 || P < 1 || P > kMaxRanks || bucket_bytes < 1) return false;
   for (int t = 0; t < n; ++t)
@@ -479,9 +481,9 @@ int orc_bucket_sumsq(const int64_t* sizes, int32_t n, int64_t bucket_bytes, int3
 }
 
 // ---- the fused ZeRO-1/2 step ------------------------------------------------
-// "ZeRO-1 and ZeRO-2 simply stop after the reduce-scatter, update the shard each
-// rank owns, and all-gather the updated parameters" ("Data Parallelism: DDP, ZeRO and FSDP", "The three
-// stages").  grads [P][n_params] bf16 (in), master/m/v [n_params] fp32 (in/out),
+// ZeRO-1/2 keep DDP's reduce-scatter, have each rank update the shard it owns,
+// then all-gather the new parameters ("Data Parallelism: DDP, ZeRO and FSDP",
+// "The three stages").  grads [P][n_params] bf16 (in), master/m/v [n_params] fp32 (in/out),
 // params [P][n_params] bf16 (out, all replicas), mean_out [n_params] (nullable,
 // pre-clip fp32 mean).  sumsq_total < 0: the clip norm is taken over this
 // problem; >= 0: that value is used (a streamed problem's total from
@@ -592,7 +594,8 @@ int orc_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_t
 // ("4.1 Data parallelism in depth", sec. 6.3 table and tip; "Distributed Training:
 // Data Parallel, Model Parallel and FSDP Strategies", FSDP2 DeviceMesh
 // mesh_shape=(2, 4) with dims ("replicate", "shard"), and "Selecting and Tuning":
-// shard within a group, replicate across groups via data-parallel all-reduce;
+// sharding inside each group of ranks, an ordinary data-parallel all-reduce
+// between the groups;
 // "Data Parallelism: DDP, ZeRO and FSDP", "Hybrid sharding").  Rank (g, s) =
 // g*S + s.  Per bucket, literally:
 //   1. in every group g, a ring reduce-scatter over its S ranks: rank (g, s)
@@ -794,10 +797,11 @@ int orc_mesh_zero_step(const int64_t* sizes, const uint8_t* decay, int32_t n, in
 }
 
 // ---- ZeRO-3 / FULL_SHARD unit flow ------------------------------------------
-// "FSDP is ZeRO-3 organized around units"; per unit: forward all-gathers the
-// unit's parameter shards into a full set, backward all-gathers them again and
-// reduce-scatters the weight gradients, then "each rank steps only the shard it
-// owns" ("Data Parallelism: DDP, ZeRO and FSDP", "How FSDP actually runs" and
+// FSDP applies ZeRO-3 unit by unit: before a unit's forward its parameter shards
+// are all-gathered into the whole unit, before its backward they are gathered
+// again and afterwards its gradients are reduce-scattered, and the optimizer on
+// each rank updates only that rank's shard ("Data Parallelism: DDP, ZeRO and
+// FSDP", "How FSDP actually runs" and
 // "The three stages": 3N; "4.1 Data parallelism in depth", sec. 6.2 and 8.2).
 // Units are the plan's buckets; forward visits them from the last bucket to the
 // first (buckets hold layers in reverse), backward from the first to the last.
@@ -874,10 +878,10 @@ int orc_zero3_step(const int64_t* sizes, const uint8_t* decay, int32_t n, int64_
 }
 
 // ---- gradient accumulation and the bf16 wire ----------------------------------
-// "Gradient accumulation to keep global batch size large without increasing
-// memory - sync only on final micro-batch" ("Distributed Training: Data Parallel,
-// Model Parallel and FSDP Strategies", "Selecting and Tuning": no_sync on every
-// micro-batch but the last).  Each rank's bf16 gradient buffer accumulates the
+// Gradient accumulation keeps the global batch large at a fixed memory cost,
+// synchronising only on the last micro-batch ("Distributed Training: Data
+// Parallel, Model Parallel and FSDP Strategies", "Selecting and Tuning": no_sync
+// on every micro-batch but the last).  Each rank's bf16 gradient buffer accumulates the
 // micro-batch gradients as autograd does for bf16 gradients: acc = bf16(acc + g),
 // the add in fp32.  acc, micro: [P][n] bf16 bits.
 void orc_accumulate(int32_t P, int64_t n, uint16_t* acc, const uint16_t* micro) {
@@ -885,9 +889,9 @@ void orc_accumulate(int32_t P, int64_t n, uint16_t* acc, const uint16_t* micro) 
     acc[i] = f32_to_bf16_rne(bf16_bits_to_f32(acc[i]) + bf16_bits_to_f32(micro[i]));
 }
 
-// "Precision: gradient dtype and communication hooks change both bandwidth and
-// numerical behavior" ("Data Parallelism: From Parameter Server to Ring
-// All-Reduce", sec. 8).  The ring with bf16 on the wire: every hop's partial sum
+// The dtype gradients are communicated in changes both the bytes moved and the
+// numerics ("Data Parallelism: From Parameter Server to Ring All-Reduce",
+// sec. 8).  The ring with bf16 on the wire: every hop's partial sum
 // is rounded to bf16 before it is sent (the receiver adds in fp32 and rounds),
 // the owner's final sum is divided by P in fp32 and rounded to bf16 for the
 // all-gather.  grads [P][n_params] in/out; mean_out: the fp32 quotient before

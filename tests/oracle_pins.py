@@ -112,8 +112,9 @@ def pin_plan_invariants(orc):
 # --------------------------------------------------------------------------- ring
 def pin_ring_ownership(orc):
     """Rank r contributes 10**r: after the reduce-scatter exactly one chunk per
-    rank carries every contribution, and rank c holds chunk c ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
-    'every rank owns one fully reduced chunk')."""
+    rank carries every contribution, and rank c holds chunk c ("Data Parallelism: From
+    Parameter Server to Ring All-Reduce", sec. 5: each rank ends the reduce-scatter
+    holding one chunk's complete sum)."""
     for P in range(2, 7):
         S = 3
         X = np.zeros((P, P * S), np.float32)
