@@ -639,7 +639,8 @@ def run_zero3(args):
 
     torch.cuda.set_device(0)
     wl = workload_by_name(args.workload)
-    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    mesh = tuple(int(x) for x in args.mesh.split(",")) if args.mesh else None
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay, mesh=mesh)
     off = plan.tensor_offsets()
     ws = plan.new_workspace()
     grads = plan.new_replicas()
@@ -761,6 +762,7 @@ def run_zero3(args):
         "resident_bytes_per_param_all_ranks": 2 + 4 + 12,
         "transient_bytes": sum(x.numel() * 2 for x in unit_bufs),
         "config": {"workload": wl.name, "P": P, "n_units": nb,
+                   "mesh": f"{plan.info.R}x{plan.info.S} (replicate x shard)",
                    "launch": ("CUDA graph of the whole step" if graph is not None else "host launches")
                    + (", prefetch on two streams" if args.prefetch else "")},
     }

@@ -6,8 +6,8 @@ import torch
 
 import gradient_sync_zero_gb300 as dps
 import oracle as oracle_mod
-from harness import Case, assert_replicas_equal, small_workload
-from workloads import configs
+from harness import Case, assert_replicas_equal, small_workload, u16
+from workloads import configs, device as wdev
 
 pytestmark = pytest.mark.gpu
 
@@ -86,3 +86,48 @@ def test_mesh_staged_equals_fused(R, S):
     assert torch.equal(p1, p2)
     for a, b in zip(s1, s2):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (3, 2)])
+def test_hybrid_full_shard_unit_flow_matches_oracle(orc, R, S):
+    """HYBRID_SHARD proper: full sharding inside each group and data parallelism
+    between groups ("4.1 Data parallelism in depth", sec. 6.3) — the ZeRO-3 unit
+    flow on a mesh plan.  Each unit is gathered from the flat shard array, its
+    gradients are reduce-scattered with the two-level fold, and each shard is
+    updated; master/m/v and the shards equal the oracle's mesh step bit for bit
+    (the update is elementwise, so where the parameters live does not change it)."""
+    c = mesh_case(R, S, sigma=0.05)
+    adamw = configs.AdamW(max_norm=1.0)
+    master = c.host_master()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    plan, nb, P = c.plan, c.plan.n_buckets, R * S
+    shards = c.plan.new_state().to(torch.bfloat16)
+    wdev.fill_flat(shards, c.off, c.sizes, torch.from_numpy(master).to(torch.bfloat16).cuda())
+    st = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    mean = c.plan.new_state()
+    unit_buf = torch.zeros(P, max(plan.bucket(b)[1] for b in range(nb)), dtype=torch.bfloat16,
+                           device="cuda")
+    for step in (1, 2):
+        g = c.host_grads(step)
+        grads = c.to_replicas(g)
+        cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
+                            adamw.max_norm, step)
+        before = shards.clone()
+        for b in range(nb):
+            o, ln, _ = plan.bucket(b)
+            dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
+            torch.cuda.synchronize()
+            for r in range(P):
+                assert torch.equal(unit_buf[r, :ln], before[o:o + ln])
+            dps.dp_unit_reduce_scatter(plan, c.ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+        dps.dp_clip_coef(plan, c.ws, adamw.max_norm)
+        dps.dp_shard_adamw_step(plan, c.ws, mean, *st, shards, cfg, use_clip_coef=True)
+        p_o, master, m, v, so = orc.mesh_zero_step(c.sizes, c.decay, c.wl.bucket_bytes, R, S, g,
+                                                   master, m, v, oracle_mod.adamw_cfg(adamw, step))
+        norm, coef, status = dps.dp_read_norm(plan, c.ws)
+        assert status == 0 and coef == so.coef
+        torch.cuda.synchronize()
+        assert np.array_equal(u16(wdev.gather_flat(shards, c.off, c.sizes)), p_o[0])
+        for dev, ref in zip(st, (master, m, v)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
