@@ -1,0 +1,80 @@
+"""Seeded random plans against the oracle: tensor counts and sizes (zero-size,
+one-element, larger than the cap), bucket caps, rank counts 1..64 and mesh shapes
+drawn at random; the mean all-reduce, the clipped ZeRO-2 step and, on mesh plans,
+the hybrid all-reduce must match the oracle bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_sync_zero_gb300 as dps
+import oracle as oracle_mod
+from harness import Case, small_workload
+from workloads import configs
+
+pytestmark = pytest.mark.gpu
+
+
+def random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    n = int(rng.integers(1, 12))
+    kinds = rng.integers(0, 4, size=n)
+    sizes = [int(x) for x in np.where(kinds == 0, rng.integers(0, 3, size=n),
+                                      np.where(kinds == 1, rng.integers(1, 300, size=n),
+                                               rng.integers(300, 40000, size=n)))]
+    P = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 24, 32, 64]))
+    cap = int(rng.choice([64, 1024, 8192, 65536, 1 << 20]))
+    wl = small_workload(sizes, P, cap, sigma=float(rng.choice([1e-3, 0.05])), seed=seed,
+                        outlier_frac=0.01)
+    return wl, rng
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_plan_allreduce(orc, seed):
+    wl, _ = random_case(seed)
+    c = Case(wl)
+    g = c.host_grads(1)
+    buf = c.to_replicas(g)
+    dps.dp_allreduce_mean(c.plan, c.ws, buf)
+    torch.cuda.synchronize()
+    want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
+    assert np.array_equal(c.from_replicas(buf), want)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_plan_zero_step_clipped(orc, seed):
+    wl, _ = random_case(seed)
+    wl.adamw = configs.AdamW(max_norm=0.05)
+    c = Case(wl)
+    g = c.host_grads(1)
+    master0 = c.host_master()
+    params = c.plan.new_replicas()
+    st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    a = wl.adamw
+    cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1)
+    dps.dp_fused_zero_step(c.plan, c.ws, c.to_replicas(g), params, *st, cfg)
+    norm, coef, status = dps.dp_read_norm(c.plan, c.ws)
+    z = np.zeros_like(master0)
+    p_o, m_o, mo, vo, _, so = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, wl.P, g, master0, z,
+                                            z, oracle_mod.adamw_cfg(a, 1))
+    assert status == 0 and coef == so.coef
+    assert np.array_equal(c.from_replicas(params), p_o)
+    for dev, ref in zip(st, (m_o, mo, vo)):
+        assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_mesh_allreduce(orc, seed):
+    wl, rng = random_case(seed)
+    shapes = [(R, S) for R in (2, 3, 4, 8) for S in (1, 2, 3, 4, 8) if R * S <= 64]
+    R, S = shapes[int(rng.integers(0, len(shapes)))]
+    wl = small_workload(wl.sizes, R * S, wl.bucket_bytes, sigma=1e-3, seed=seed)
+    c = Case.__new__(Case)
+    c.wl, c.P, c.sizes, c.decay = wl, wl.P, wl.sizes, list(wl.decay)
+    c.plan = dps.Plan(c.sizes, wl.bucket_bytes, c.P, c.decay, mesh=(R, S))
+    c.off, c.device, c.ws = c.plan.tensor_offsets(), "cuda", c.plan.new_workspace()
+    g = c.host_grads(1)
+    buf = c.to_replicas(g)
+    dps.dp_allreduce_mean(c.plan, c.ws, buf)
+    torch.cuda.synchronize()
+    want, _, _ = orc.mesh_allreduce_mean(c.sizes, wl.bucket_bytes, R, S, g)
+    assert np.array_equal(c.from_replicas(buf), want)
