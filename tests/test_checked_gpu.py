@@ -25,14 +25,15 @@ def test_parity_suites_under_index_checks():
     dbuild.build(checked=True)
     env = dict(os.environ, DPSYNC_VARIANT="checked")
     suites = ["tests/test_parity_gpu.py", "tests/test_parity_mesh.py", "tests/test_zero3_gpu.py",
-              "tests/test_accum_gpu.py", "tests/test_tracker_gpu.py", "tests/test_checked_gpu.py"]
+              "tests/test_accum_gpu.py", "tests/test_tracker_gpu.py", "tests/test_graph_gpu.py",
+              "tests/test_fuzz_gpu.py", "tests/test_checked_gpu.py"]
     r = subprocess.run([sys.executable, "-m", "pytest", "-m", "gpu", "-x", "-q",
                         "-p", "no:cacheprovider", *suites],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1800)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
     import re
     m = re.search(r"(\d+) passed", r.stdout)
-    assert m and int(m.group(1)) >= 60 and " failed" not in r.stdout, r.stdout[-2000:]
+    assert m and int(m.group(1)) >= 150 and " failed" not in r.stdout, r.stdout[-2000:]
 
 
 @pytest.mark.plants_bad_descriptor
