@@ -429,6 +429,11 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  *   flags      DP_TRACK_DRY_RUN: record the firing order, launch nothing.
  * Events are the caller's: keep them alive and unrecorded until their bucket
  * fires.  Marking a tensor twice in one step is DP_EINVAL.
+ * Parameters that a step does not use (a skipped branch) never get a gradient,
+ * so their bucket would never fire ("4.1 Data parallelism in depth", sec. 4.2
+ * note).  DDP's find_unused_parameters marks them ready after the forward pass;
+ * here the caller does the same: zero their gradient slots and mark them ready
+ * (event NULL) as soon as it knows they are unused.
  */
 typedef struct dp_tracker dp_tracker;
 enum { DP_TRACK_ALLREDUCE = 0, DP_TRACK_REDUCE_SCATTER = 1 };

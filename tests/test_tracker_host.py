@@ -158,3 +158,19 @@ def test_set_micro_rules():
     mesh = dps.Plan(sizes, 4000, 4, mesh=(2, 2))
     trm = dps.Tracker(mesh, dps.DP_TRACK_ALLREDUCE, dry_run=True)
     assert lib.dp_tracker_set_micro(trm._h, C.c_void_p(1 << 20)) == dps.DP_EINVAL
+
+
+def test_unused_parameters_marked_after_forward_let_the_bucket_fire():
+    """find_unused_parameters: a tensor the step did not use is marked ready up
+    front (its gradient slots zeroed by the caller); its bucket then fires as soon
+    as the used tensors are ready, instead of timing out."""
+    sizes = [1000, 1000, 1000, 1000]
+    plan, tr = dry(sizes, 4000, 2)                      # buckets {3,2}, {1,0}
+    tr.begin()
+    tr.mark_ready(2)                                   # tensor 2 unused this step
+    tr.mark_ready(3)
+    assert tr.fired() == [0]
+    tr.mark_ready(1)
+    tr.mark_ready(0)
+    tr.wait(100)
+    assert tr.fired() == [0, 1]
