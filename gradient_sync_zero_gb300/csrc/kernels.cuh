@@ -584,7 +584,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Plan check: a workspace holding another plan's image is refused.
+//
+// Every library kernel starts here.  The kernels are launched as programmatic
+// dependents of the previous kernel in their stream, so the launch is prepared
+// while that kernel runs and its CTAs are dispatched as that kernel's CTAs exit
+// (no early trigger: a persistent grid is never placed on SMs still busy with
+// its predecessor).  The wait below returns once the predecessor has finished
+// and its writes are visible (at once for an ordinary launch), and only then is
+// global memory touched.
 __device__ __forceinline__ bool plan_ok(const KCommon& k) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (k.hdr->plan_id == k.plan_id) return true;
   if (threadIdx.x == 0) atomicOr(&k.hdr->status, DP_STATUS_PLAN_MISMATCH);
   return false;

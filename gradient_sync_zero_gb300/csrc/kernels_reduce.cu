@@ -253,8 +253,7 @@ int launch_allreduce_bf16wire(const Launch& L, void* grads) {
 
 int launch_norm_finalize(const Launch& L, double max_norm) {
   const KCommon k = make_common(L);
-  k_norm_finalize<<<1, kFinalThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(k, max_norm);
-  return static_cast<int>(cudaGetLastError());
+  return launch_k(k_norm_finalize, 1, kFinalThreads, 0, L.stream, k, max_norm);
 }
 
 }  // namespace dps

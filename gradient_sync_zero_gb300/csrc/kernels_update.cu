@@ -193,9 +193,7 @@ int launch_replicate(const Launch& L, const RepArgs& a) {
   const int64_t n = L.tile_end - L.tile_begin;
   int64_t g = n < cap ? n : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
-  k_replicate<<<static_cast<int>(g), 32, kRepSmem, static_cast<cudaStream_t>(L.stream)>>>(
-      make_common(L), a);
-  return static_cast<int>(cudaGetLastError());
+  return launch_k(k_replicate, static_cast<int>(g), 32, kRepSmem, L.stream, make_common(L), a);
 }
 
 // The whole ZeRO-1/2 step without clipping, one pass.  The replica blocks are
@@ -443,9 +441,8 @@ int launch_ag(const Launch& L, const KCommon& k, const float* stage, void* param
   const int64_t nchunks = (Lp + CH - 1) / CH;
   int64_t g = nchunks < cap ? nchunks : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
-  kern<<<static_cast<int>(g), kThreads, smem, static_cast<cudaStream_t>(L.stream)>>>(
-      k, stage, static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0);
-  return static_cast<int>(cudaGetLastError());
+  return launch_k(kern, static_cast<int>(g), kThreads, smem, L.stream, k, stage,
+                  static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0);
 }
 
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,

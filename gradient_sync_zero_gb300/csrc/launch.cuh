@@ -88,6 +88,37 @@ int resident_ctas(K kernel, int threads, size_t dyn_smem = 0) {
   return n;
 }
 
+// Programmatic dependent launch (on unless DPSYNC_PDL=0): a kernel's CTAs may be
+// scheduled while the previous kernel in the stream drains; each kernel waits
+// for that kernel's completion (griddepcontrol.wait in plan_ok) before its first
+// global access, so stream order and visibility are as for plain launches.
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("DPSYNC_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+// Launch through cudaLaunchKernelEx with the programmatic-serialisation
+// attribute; returns the launch's error (and clears the thread's last error).
+template <class K, class... A>
+int launch_k(K kernel, int grid, int threads, size_t smem, void* stream, A... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  const cudaError_t last = cudaGetLastError();
+  return static_cast<int>(e != cudaSuccess ? e : last);
+}
+
 // Launch `kernel` over the tiles of L with a persistent grid.
 inline int sm_count() {
   static std::mutex mu;
@@ -121,9 +152,7 @@ int launch_tiles_per_sm(const Launch& L, int per_sm, K kernel, A... args) {
   }
   int64_t g = n < cap ? n : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
-  const int grid = static_cast<int>(g);
-  kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(args...);
-  return static_cast<int>(cudaGetLastError());
+  return launch_k(kernel, static_cast<int>(g), kThreads, 0, L.stream, args...);
 }
 
 template <class K, class... A>
@@ -152,8 +181,7 @@ int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... ar
   k.split = 2 * n <= cap ? 2 : 1;
   int64_t g = n * k.split < cap ? n * k.split : cap;
   g -= g % k.split;
-  kernel<<<static_cast<int>(g), kThreads, 0, static_cast<cudaStream_t>(L.stream)>>>(k, args...);
-  return static_cast<int>(cudaGetLastError());
+  return launch_k(kernel, static_cast<int>(g), kThreads, 0, L.stream, k, args...);
 }
 
 // Rank counts with a fully unrolled instantiation; others use the runtime-P one.
