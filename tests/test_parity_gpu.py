@@ -188,6 +188,39 @@ def test_staged_clip_equals_fused_clip():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("P", [3, 8])
+def test_chained_per_bucket_launches_match_oracle(orc, P):
+    """Hundreds of tiny launches back to back, each reading what the launch just
+    before it wrote (per bucket: reduce-scatter -> AdamW on its mean -> all-gather
+    of its shard), with the mean stage and the parameter replicas filled with
+    garbage before every step.  A kernel that read its input before its
+    predecessor's writes were visible would leave garbage or the previous
+    step's values behind; the result must equal the oracle's bit for bit."""
+    rng = np.random.default_rng(11)
+    sizes = [int(s) for s in rng.integers(1, 3000, size=160)]
+    wl = small_workload(sizes, P, 8 * 1024, sigma=1e-3, seed=40 + P)
+    c = Case(wl)
+    assert c.plan.n_buckets >= 50
+    adamw = configs.AdamW(max_norm=0.0)
+    master0 = c.host_master()
+    grads = [c.host_grads(s) for s in (1, 2)]
+    ref = run_oracle_steps(orc, c, grads, master0, [ocfg(adamw, s) for s in (1, 2)])
+    params = c.plan.new_replicas()
+    st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    mean = c.plan.new_state()
+    for s, g in zip((1, 2), grads):
+        dev = c.to_replicas(g)
+        mean.fill_(1.0e30)
+        params.fill_(7.0)
+        torch.cuda.synchronize()
+        for b in reversed(range(c.plan.n_buckets)):      # the order backward fills them
+            dps.dp_reduce_scatter_mean(c.plan, c.ws, dev, mean, b, b + 1)
+            dps.dp_sharded_adamw_step(c.plan, c.ws, mean, *st, params, dcfg(adamw, s), b0=b, b1=b + 1)
+            dps.dp_all_gather(c.plan, c.ws, params, b, b + 1)
+        torch.cuda.synchronize()
+        check_state(c, params, st, ref[s - 1], exact=True)
+
+
 def test_per_bucket_allreduce_equals_single_launch():
     c = case_for("ragged", 8, cap=16 * 1024)
     assert c.plan.n_buckets > 3
