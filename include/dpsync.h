@@ -39,7 +39,13 @@
  *   Every compute call only enqueues work on it and never synchronises the
  *   device, except dp_read_norm, which synchronises `stream`.  Kernel-side
  *   errors surface when the caller synchronises; dp_read_norm reports the
- *   workspace's status bits.
+ *   workspace's status bits.  Kernels are launched as programmatic dependents
+ *   of the previous kernel in the stream: a launch is prepared while that
+ *   kernel runs, but no kernel of the library reads or writes memory before
+ *   its predecessor has finished and its writes are visible, so the stream's
+ *   ordering is that of plain launches, with other libraries' kernels too.
+ *   The environment variable DPSYNC_PDL=0 (read once per process) gives plain
+ *   launches.
  * Buckets.  [b0, b1) selects a range of buckets (0 <= b0 <= b1 <= n_buckets),
  *   so a caller can launch per bucket (DDP's bucket-ready semantics) or once
  *   for all buckets.
