@@ -252,6 +252,8 @@ def run_gpu(args, rank, local, world):
         wl.adamw = dataclasses.replace(wl.adamw, max_norm=args.max_norm)
     mesh = tuple(int(x) for x in args.mesh.split(",")) if args.mesh else None
     plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay, mesh=mesh)
+    if world > 1:
+        dps.check_plans_match(plan)      # every process built the same buckets (else DP_EPLAN)
     P, L, stride = plan.P, plan.L, plan.stride
     off = plan.tensor_offsets()
     ws = plan.new_workspace()

@@ -93,6 +93,8 @@ def lib():
             "dp_tracker_mark_ready": [vp, i32, vp],
             "dp_tracker_wait": [vp, i64],
             "dp_tracker_fired": [vp, vp, i32, vp],
+            "dp_plan_fingerprint": [vp, vp],
+            "dp_plan_check_match": [vp, vp, i32],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -200,6 +202,19 @@ class Plan:
     def tensor_offsets(self):
         return [self.tensor(t)[1] for t in range(len(self.sizes))]
 
+    @property
+    def fingerprint(self):
+        """64-bit layout fingerprint (dp_plan_fingerprint), as a Python int."""
+        out = C.c_uint64()
+        _check(lib().dp_plan_fingerprint(self._h, C.byref(out)))
+        return out.value
+
+    def check_match(self, fingerprints):
+        """dp_plan_check_match over a list of fingerprints (one per rank)."""
+        fps = [int(f) for f in fingerprints]
+        arr = (C.c_uint64 * max(len(fps), 1))(*fps)
+        _check(lib().dp_plan_check_match(self._h, arr, len(fps)))
+
     # ---- device buffers (torch plumbing) ----
     def new_replicas(self, device="cuda", dtype=torch.bfloat16):
         return torch.zeros(self.P, self.stride, dtype=dtype, device=device)
@@ -211,6 +226,22 @@ class Plan:
         ws = torch.empty(self.info.workspace_bytes, dtype=torch.uint8, device=device)
         self.upload(ws, stream)
         return ws
+
+
+def check_plans_match(plan, group=None):
+    """Gather every process's plan fingerprint over torch.distributed and check
+    them with dp_plan_check_match: raises DPError (DP_EPLAN) on every rank when
+    one rank built a different bucket layout, instead of the mismatched
+    collectives hanging.  Without an initialised process group only this plan
+    is checked."""
+    import torch.distributed as dist
+    fp = plan.fingerprint
+    if dist.is_available() and dist.is_initialized():
+        fps = [None] * dist.get_world_size(group)
+        dist.all_gather_object(fps, fp, group=group)
+    else:
+        fps = [fp]
+    plan.check_match(fps)
 
 
 def adamw_cfg(lr=2e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.0, step=1):

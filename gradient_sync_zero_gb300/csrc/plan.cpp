@@ -15,6 +15,7 @@
 #include <algorithm>
 #include <atomic>
 #include <chrono>
+#include <cstdio>
 #include <cstring>
 #include <new>
 #include <random>
@@ -151,6 +152,45 @@ void build_image(Plan& pl) {
     std::memcpy(pl.image.data() + h.off_decay, pl.decay_bits.data(), pl.decay_bits.size() * 4);
 }
 
+// 64-bit FNV-1a over the layout, each value as 8 little-endian bytes, so the
+// result does not depend on the host's byte order or word size.
+class LayoutHash {
+ public:
+  void add(int64_t v) {
+    const uint64_t u = static_cast<uint64_t>(v);
+    for (int i = 0; i < 8; ++i) {
+      h_ ^= (u >> (8 * i)) & 0xffu;
+      h_ *= 0x100000001b3ull;   // FNV-1a 64-bit prime
+    }
+  }
+  uint64_t value() const { return h_; }
+
+ private:
+  uint64_t h_ = 0xcbf29ce484222325ull;   // FNV-1a 64-bit offset basis
+};
+
+uint64_t layout_fingerprint(const Plan& pl) {
+  LayoutHash h;
+  h.add(0x31544e4946504c44ll);   // format tag ("DLPFINT1")
+  h.add(pl.P);
+  h.add(pl.R);
+  h.add(pl.S);
+  h.add(pl.L);
+  h.add(static_cast<int64_t>(pl.sizes.size()));
+  for (size_t t = 0; t < pl.sizes.size(); ++t) {
+    h.add(pl.sizes[t]);
+    h.add(pl.decay[t]);
+    h.add(pl.t_off[t]);
+    h.add(pl.t_bucket[t]);
+  }
+  h.add(static_cast<int64_t>(pl.b_off.size()));
+  for (size_t b = 0; b < pl.b_off.size(); ++b) {
+    h.add(pl.b_off[b]);
+    h.add(pl.b_len[b]);
+  }
+  return h.value();
+}
+
 }  // namespace
 }  // namespace dps
 
@@ -273,6 +313,35 @@ int dp_plan_bucket(const dp_plan* plan, int32_t b, int64_t* offset, int64_t* pad
   if (offset) *offset = pl->b_off[b];
   if (padded_len) *padded_len = pl->b_len[b];
   if (shard_len) *shard_len = pl->b_len[b] / pl->S;
+  return DP_OK;
+}
+
+int dp_plan_fingerprint(const dp_plan* plan, uint64_t* out) {
+  clear_error();
+  const Plan* pl = as_plan(plan);
+  if (!pl || !out) return fail(DP_EINVAL, "dp_plan_fingerprint: NULL argument");
+  *out = layout_fingerprint(*pl);
+  return DP_OK;
+}
+
+int dp_plan_check_match(const dp_plan* plan, const uint64_t* fingerprints, int32_t n_ranks) {
+  clear_error();
+  const Plan* pl = as_plan(plan);
+  if (!pl) return fail(DP_EINVAL, "dp_plan_check_match: NULL plan");
+  if (n_ranks < 0 || (n_ranks > 0 && !fingerprints))
+    return fail(DP_EINVAL, "dp_plan_check_match: bad fingerprint list");
+  const uint64_t mine = layout_fingerprint(*pl);
+  for (int32_t r = 0; r < n_ranks; ++r) {
+    if (fingerprints[r] != mine) {
+      char buf[160];
+      std::snprintf(buf, sizeof(buf),
+                    "dp_plan_check_match: rank %d's bucket layout differs (fingerprint %016llx, "
+                    "this plan %016llx)",
+                    r, static_cast<unsigned long long>(fingerprints[r]),
+                    static_cast<unsigned long long>(mine));
+      return fail(DP_EPLAN, buf);
+    }
+  }
   return DP_OK;
 }
 

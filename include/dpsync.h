@@ -165,6 +165,29 @@ int dp_plan_bucket(const dp_plan* plan, int32_t b, int64_t* offset, int64_t* pad
 void dp_plan_free(dp_plan* plan);
 
 /*
+ * Cross-process plan check.  Every rank must pack its gradients into the same
+ * buckets in the same order, or the collectives of different ranks no longer
+ * line up and the job hangs ("4.1 Data parallelism in depth", sec. 4.2 on the
+ * bucket mechanism; "Data Parallelism: DDP, ZeRO and FSDP", "DDP, and why it
+ * works").  Processes that each build their own plan compare them before the
+ * first step and get an error instead of a hang.
+ *
+ * dp_plan_fingerprint: *out = a 64-bit FNV-1a hash of the layout, identical on
+ *   every platform: P, the mesh shape (R, S), the padded length L, and per
+ *   tensor its size, decay flag, flat offset and bucket, per bucket its offset
+ *   and padded length (each as 8 little-endian bytes, in that order, after a
+ *   format tag).  The bucket cap and the replica stride are not part of it: two
+ *   caps that give the same buckets give the same fingerprint, and each
+ *   process's replica buffers are its own.  Host only; DP_EINVAL on NULL.
+ * dp_plan_check_match: fingerprints[0..n_ranks) are the values every rank
+ *   computed (gathered by the caller, e.g. over torch.distributed); DP_OK if all
+ *   equal this plan's, else DP_EPLAN naming the first rank that differs.
+ *   DP_EINVAL for NULL fingerprints with n_ranks > 0 or n_ranks < 0.
+ */
+int dp_plan_fingerprint(const dp_plan* plan, uint64_t* out);
+int dp_plan_check_match(const dp_plan* plan, const uint64_t* fingerprints, int32_t n_ranks);
+
+/*
  * Copy the plan's device image (bucket/tile tables, decay bits) into the first
  * table_bytes of `workspace` (device, workspace_bytes long) on `stream`.  Must
  * run once before any compute call uses that workspace; a compute call given a
