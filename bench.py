@@ -1043,7 +1043,7 @@ def run_kernels(args):
          lambda: dps.dp_reduce_scatter_mean_accum(plan, ws, grads, micro, mean, want_sumsq=True)),
         ("dp_unit_all_gather (all units)", "k_unit_all_gather", 2 + 2 * P, unit_ag_pass),
         ("dp_unit_reduce_scatter (all units)", "k_reduce_scatter", 2 * P + 4, unit_rs_pass),
-        ("dp_shard_adamw_step", "k_adamw", 30,
+        ("dp_shard_adamw_step", "k_adamw_all_gather (1 row)", 30,
          lambda: dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)),
     ]
     peak, peak_src = measured_peaks()

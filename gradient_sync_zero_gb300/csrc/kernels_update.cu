@@ -249,7 +249,8 @@ constexpr int kTmaStages = 2;
 template <int CH, int ST>
 __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mean, uint8_t* params,
                                               float* master, float* m, float* v,
-                                              const AdamScalars& s, int64_t L, int use_coef) {
+                                              const AdamScalars& s, int64_t L, int use_coef,
+                                              int rows, int64_t row_bytes) {
   using Stage = TmaStageT<CH>;
   constexpr int kPer = CH / kThreads;   // elements per thread per chunk (multiple of 4)
   static_assert(kPer % 4 == 0 && ST >= 2, "float4 lanes; at least double buffering");
@@ -319,7 +320,7 @@ __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mea
       bulk_store(master + e0, b.in[1], 4u * n);
       bulk_store(m + e0, b.in[2], 4u * n);
       bulk_store(v + e0, b.in[3], 4u * n);
-      for (int r = 0; r < k.P; ++r) bulk_store(params + r * k.stride_bytes + 2 * e0, b.out, 2u * n);
+      for (int r = 0; r < rows; ++r) bulk_store(params + r * row_bytes + 2 * e0, b.out, 2u * n);
       bulk_commit();
       bulk_wait_read<1>();    // the previous chunk's stores have left its stage ...
       issue_load(i + ST - 1); // ... which now receives the chunk ST-1 ahead
@@ -340,14 +341,15 @@ __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mea
 template <bool DEV_S, int CH = kTmaChunk, int ST = kTmaStages>
 __global__ void __launch_bounds__(kThreads)
     k_adamw_all_gather(KCommon k, const float* mean, uint8_t* params, float* master, float* m,
-                       float* v, AdamScalars s, int64_t L, int use_coef) {
+                       float* v, AdamScalars s, int64_t L, int use_coef, int rows,
+                       int64_t row_bytes) {
   if (!plan_ok(k)) return;
   if constexpr (DEV_S) {
     AdamScalars sd;
     if (!header_scalars(k, sd)) return;
-    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, sd, L, use_coef);
+    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, sd, L, use_coef, rows, row_bytes);
   } else {
-    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, s, L, use_coef);
+    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, s, L, use_coef, rows, row_bytes);
   }
 }
 
@@ -386,13 +388,6 @@ int64_t bounds_violations_update(bool reset) {
 #endif
 }
 
-int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef, bool flat_params,
-                 bool dev_scalars) {
-  return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
-                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
-}
-
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
                            int64_t block0) {
   RepArgs a{static_cast<const uint8_t*>(shards), static_cast<uint8_t*>(out), 2 * out_stride,
@@ -425,9 +420,13 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
   });
 }
 
+// rows = P, row_bytes = the replica stride: every replica gets the parameters
+// (the all-gather); rows = 1, row_bytes = 0: one flat bf16 array [L] (the ZeRO-3
+// shard update).
 template <bool DEV_S, int CH, int ST>
 int launch_ag(const Launch& L, const KCommon& k, const float* stage, void* params,
-                      float* master, float* m, float* v, const AdamScalars& s, bool use_coef) {
+              float* master, float* m, float* v, const AdamScalars& s, bool use_coef, int rows,
+              int64_t row_bytes) {
   const int64_t Lp = L.plan->L;
   auto kern = k_adamw_all_gather<DEV_S, CH, ST>;
   constexpr size_t smem = tma_smem<CH, ST>();
@@ -442,7 +441,26 @@ int launch_ag(const Launch& L, const KCommon& k, const float* stage, void* param
   int64_t g = nchunks < cap ? nchunks : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
   return launch_k(kern, static_cast<int>(g), kThreads, smem, L.stream, k, stage,
-                  static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0);
+                  static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0, rows,
+                  row_bytes);
+}
+
+int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
+                 void* params, const AdamScalars& s, bool use_coef, bool flat_params,
+                 bool dev_scalars) {
+  // The ZeRO-3 shard update covers the whole plan and writes one flat bf16 array:
+  // the bulk-copy pass with a single output row streams it (no owner rows needed).
+  if (flat_params && L.tile_begin == 0 &&
+      L.tile_end == static_cast<int64_t>(L.plan->tiles.size())) {
+    if (L.plan->L == 0) return cudaSuccess;
+    const KCommon k = make_common(L);
+    return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, grad, params, master, m, v,
+                                                                s, use_coef, 1, 0)
+                       : launch_ag<false, kTmaChunk, kTmaStages>(L, k, grad, params, master, m,
+                                                                 v, s, use_coef, 1, 0);
+  }
+  return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
+                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
 }
 
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
@@ -450,10 +468,12 @@ int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, f
                             bool dev_scalars) {
   const KCommon k = make_common(L);
   if (L.plan->L == 0) return cudaSuccess;
-  return dev_scalars
-             ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v, s, use_coef)
-             : launch_ag<false, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v, s,
-                                                               use_coef);
+  const int rows = L.plan->P;
+  const int64_t rb = k.stride_bytes;
+  return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v, s,
+                                                              use_coef, rows, rb)
+                     : launch_ag<false, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v,
+                                                               s, use_coef, rows, rb);
 }
 
 }  // namespace dps
