@@ -26,7 +26,7 @@ def test_parity_suites_under_index_checks():
     env = dict(os.environ, DPSYNC_VARIANT="checked")
     suites = ["tests/test_parity_gpu.py", "tests/test_parity_mesh.py", "tests/test_zero3_gpu.py",
               "tests/test_accum_gpu.py", "tests/test_tracker_gpu.py", "tests/test_graph_gpu.py",
-              "tests/test_fuzz_gpu.py", "tests/test_checked_gpu.py"]
+              "tests/test_fuzz_gpu.py", "tests/test_staged_owner_rows_gpu.py", "tests/test_checked_gpu.py"]
     r = subprocess.run([sys.executable, "-m", "pytest", "-m", "gpu", "-x", "-q",
                         "-p", "no:cacheprovider", *suites],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1800)
