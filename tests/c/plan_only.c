@@ -22,6 +22,15 @@ int main(void) {
     if (dp_plan_tensor(plan, t, &b, &off) != DP_OK) return 3;
     printf("%d %lld\n", b, (long long)off);
   }
+  /* the layout fingerprint, and the cross-process check against a second rank's */
+  uint64_t fp = 0;
+  if (dp_plan_fingerprint(plan, &fp) != DP_OK) return 4;
+  printf("%016llx\n", (unsigned long long)fp);
+  uint64_t ranks[2] = {fp, fp};
+  const int same = dp_plan_check_match(plan, ranks, 2);
+  ranks[1] = fp ^ 1u;
+  const int differ = dp_plan_check_match(plan, ranks, 2);
+  printf("%d %d\n", same == DP_OK, differ == DP_EPLAN);
   /* a refused call leaves a message and no plan */
   dp_plan* bad = NULL;
   const int rc = dp_plan_buckets(sizes, decay, 3, 64 * 1024, 0, &bad);

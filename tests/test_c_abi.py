@@ -40,7 +40,9 @@ def test_c_program_plans_like_the_binding(tmp_path):
     for t in range(3):
         b, off = (int(x) for x in lines[3 + t].split())
         assert (b, off) == plan.tensor(t)
-    assert lines[6] == "1 1"
+    assert int(lines[6], 16) == plan.fingerprint
+    assert lines[7] == "1 1"
+    assert lines[8] == "1 1"
 
 
 def _cuda_home():
