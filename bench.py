@@ -442,6 +442,21 @@ def run_gpu(args, rank, local, world):
             mean_buf = plan.new_state()
         consumed = [None]                    # event: the last reduction of the previous step
 
+        def grouped_copies_ms():
+            # the copies alone, in the step's bucket groups (for reading the e2e number)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for b0, b1 in groups:
+                o = plan.bucket(b0)[0]
+                e = plan.bucket(b1 - 1)[0] + plan.bucket(b1 - 1)[1]
+                for r in range(P):
+                    grads[r, o:e].copy_(host[r, o:e], non_blocking=True)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            return c0.elapsed_time(c1)
+
+        copy_before_ms = grouped_copies_ms()
+
         def e2e_step(step):
             if not pipelined:
                 grads.copy_(host, non_blocking=True)
@@ -500,23 +515,14 @@ def run_gpu(args, rank, local, world):
             status = [int(r[132:136].view(torch.int32)) for r in results]      # header: status
             if any(st != 0 for st in status) or norms[-1] != dps.dp_read_norm(plan, ws)[0]:
                 raise RuntimeError(f"e2e: unexpected step results {norms} {status}")
-        # the copies alone, in the same groups, for reading the number
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(stream)
-        for b0, b1 in groups:
-            o = plan.bucket(b0)[0]
-            e = plan.bucket(b1 - 1)[0] + plan.bucket(b1 - 1)[1]
-            for r in range(P):
-                grads[r, o:e].copy_(host[r, o:e], non_blocking=True)
-        c1.record(stream)
-        torch.cuda.synchronize()
-        copy_only_ms = c0.elapsed_time(c1)
+        copy_only_ms = grouped_copies_ms()
         result["e2e"] = {"value": n_params * world / e2e_s, "unit": "params/s",
                          "h2d_bytes_per_step": host.numel() * host.element_size(),
                          "d2h_bytes_per_step": 192 if zero else 0,
                          "steps": e2e_steps, "h2d_gbs_alone": h2d_gbs,
                          "step_ms": [round(x, 2) for x in step_ms],
                          "grouped_copies_alone_ms": round(copy_only_ms, 2),
+                         "grouped_copies_before_ms": round(copy_before_ms, 2),
                          "copy": (f"pipelined: {len(groups)} bucket groups, each group's reduction "
                                   "overlapped with the copy, the next step's copy with this step's "
                                   "update; results read back asynchronously"
