@@ -546,12 +546,17 @@ def run_streamed(args):
     stream marks each tensor ready; the tracker fires every complete bucket's
     reduction on a high-priority communication stream with a capped grid.
     Compared with the backward alone and with backward-then-sync on one stream.
-    The GEMMs only model the backward's time; the gradients are the workload's
-    synthetic ones, already resident."""
+    ZeRO without clipping (--max-norm 0) fires each bucket's whole step
+    (DP_TRACK_ZERO_STEP); with clipping the tracker reduce-scatters per bucket and
+    the clip and the AdamW + all-gather pass follow the backward.  The GEMMs only
+    model the backward's time; the gradients are the workload's synthetic ones,
+    already resident."""
     import gradient_sync_zero_gb300 as dps
 
     torch.cuda.set_device(0)
     wl = workload_by_name(args.workload)
+    if args.max_norm is not None:
+        wl.adamw = dataclasses.replace(wl.adamw, max_norm=args.max_norm)
     plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
     off = plan.tensor_offsets()
     ws = plan.new_workspace()
@@ -559,6 +564,7 @@ def run_streamed(args):
     wdev.fill_grads(grads, off, wl, step=1)
     zero = wl.mode == "zero"
     a = wl.adamw
+    whole = zero and not (a.max_norm > 0)    # each bucket's whole step fires on readiness
     cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1)
     if zero:
         mean, params = plan.new_state(), plan.new_replicas()
@@ -575,7 +581,8 @@ def run_streamed(args):
             mats.append(None)
     compute = torch.cuda.Stream()
     comm = torch.cuda.Stream(priority=-1)
-    mode = dps.DP_TRACK_REDUCE_SCATTER if zero else dps.DP_TRACK_ALLREDUCE
+    mode = (dps.DP_TRACK_ZERO_STEP if whole else
+            dps.DP_TRACK_REDUCE_SCATTER if zero else dps.DP_TRACK_ALLREDUCE)
     tr = dps.Tracker(plan, mode, ws, grads, mean if zero else None, stream=comm,
                      max_ctas=args.comm_ctas)
 
@@ -592,11 +599,14 @@ def run_streamed(args):
                     tr.mark_ready(t, events[t])
 
     def finish(stream):
-        if zero:
+        if zero and not whole:
             dps.dp_clip_coef(plan, ws, a.max_norm, stream=stream)
             dps.dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg, stream=stream)
 
     def sync_all(stream):
+        if whole:
+            dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg, stream=stream)
+            return
         if zero:
             dps.dp_reduce_scatter_mean(plan, ws, grads, mean, want_sumsq=True, stream=stream)
         else:
@@ -621,6 +631,8 @@ def run_streamed(args):
         sync_all(compute)
 
     def streamed():
+        if whole:
+            tr.set_zero_step(params, master, m, v, cfg)
         tr.begin()
         backward(compute, True)
         tr.wait(60000)
@@ -641,7 +653,10 @@ def run_streamed(args):
         "value": hidden, "unit": "fraction", "higher_is_better": True,
         "ms": {"backward": t_b, "sync": t_s, "backward_then_sync": t_seq, "streamed": t_str},
         "config": {"workload": wl.name, "tokens": T, "comm_ctas": args.comm_ctas,
-                   "n_buckets": plan.n_buckets, "mode": wl.mode},
+                   "n_buckets": plan.n_buckets, "mode": wl.mode, "clip_max_norm": a.max_norm,
+                   "tracker_mode": ("whole zero step per bucket" if whole else
+                                    "reduce-scatter per bucket" if zero else
+                                    "all-reduce per bucket")},
     }
 
 

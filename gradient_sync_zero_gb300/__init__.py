@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(HERE, "libdpsync_checked.so" if VARIANT == "checked" els
 DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ETIMEOUT = \
     0, -1, -2, -3, -4, -5, -6, -7
 DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT, DP_STATUS_NO_SCALARS = 1, 2, 4, 8
-DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_DRY_RUN = 0, 1, 1
+DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_ZERO_STEP, DP_TRACK_DRY_RUN = 0, 1, 2, 1
 DP_CKPT_HOST = 1
 
 
@@ -95,6 +95,7 @@ def lib():
             "dp_tracker_fired": [vp, vp, i32, vp],
             "dp_plan_fingerprint": [vp, vp],
             "dp_plan_check_match": [vp, vp, i32],
+            "dp_tracker_set_zero_step": [vp, vp, vp, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -352,9 +353,10 @@ def dp_shard_adamw_step(plan, ws, mean, master, m, v, param_shards, cfg, use_cli
 class Tracker:
     """Bucket readiness tracker (streamed per-bucket synchronisation).
 
-    mode: DP_TRACK_ALLREDUCE (in place on `grads`) or DP_TRACK_REDUCE_SCATTER
-    (into `mean`, with norm partials).  dry_run=True records the firing order
-    and launches nothing (no GPU needed)."""
+    mode: DP_TRACK_ALLREDUCE (in place on `grads`), DP_TRACK_REDUCE_SCATTER
+    (into `mean`, with norm partials) or DP_TRACK_ZERO_STEP (each bucket's whole
+    unclipped ZeRO step; targets from set_zero_step).  dry_run=True records the
+    firing order and launches nothing (no GPU needed)."""
 
     def __init__(self, plan, mode, ws=None, grads=None, mean=None, stream=None, max_ctas=0,
                  dry_run=False):
@@ -391,6 +393,17 @@ class Tracker:
             _need(micro, torch.bfloat16, self.plan.P * self.plan.stride, "micro")
         self._micro = micro
         _check(lib().dp_tracker_set_micro(self._h, _ptr(micro) if micro is not None else None))
+
+    def set_zero_step(self, params, master, m, v, cfg):
+        """DP_TRACK_ZERO_STEP: the replicas and fp32 state each bucket's step
+        updates, and this step's AdamW settings (cfg.max_norm must be <= 0)."""
+        if not getattr(self, "_dry", False):
+            _need(params, torch.bfloat16, self.plan.P * self.plan.stride, "params")
+            for t, name in ((master, "master"), (m, "m"), (v, "v")):
+                _need(t, torch.float32, self.plan.L, name)
+        self._zero = (params, master, m, v)
+        _check(lib().dp_tracker_set_zero_step(self._h, _ptr(params), _ptr(master), _ptr(m), _ptr(v),
+                                              _cfg_ref(cfg)))
 
     def mark_ready(self, tensor, event=None):
         """event: torch.cuda.Event recorded after the tensor's gradient was written."""

@@ -12,6 +12,30 @@
 
 #include "internal.h"
 
+namespace dps {
+
+int adam_scalars(const char* fn, const dp_adamw_cfg* cfg, AdamScalars* s) {
+  if (!cfg) return fail(DP_EINVAL, std::string(fn) + ": NULL cfg");
+  if (cfg->step < 1) return fail(DP_EINVAL, std::string(fn) + ": step must be >= 1");
+  if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
+    return fail(DP_EINVAL, std::string(fn) + ": betas must be in [0, 1)");
+  // Scalar factors formed once in double and rounded to fp32 (torch.optim.AdamW
+  // forms them as Python floats): decay factor 1 - lr*wd, 1-b1, 1-b2,
+  // step size lr / (1 - b1^t) and sqrt(1 - b2^t).
+  const double t = static_cast<double>(cfg->step);
+  s->wd_factor = static_cast<float>(1.0 - cfg->lr * cfg->weight_decay);
+  s->b1 = static_cast<float>(cfg->beta1);
+  s->omb1 = static_cast<float>(1.0 - cfg->beta1);
+  s->b2 = static_cast<float>(cfg->beta2);
+  s->omb2 = static_cast<float>(1.0 - cfg->beta2);
+  s->step_size = static_cast<float>(cfg->lr / (1.0 - std::pow(cfg->beta1, t)));
+  s->sqrt_bc2 = static_cast<float>(std::sqrt(1.0 - std::pow(cfg->beta2, t)));
+  s->eps = static_cast<float>(cfg->eps);
+  return DP_OK;
+}
+
+}  // namespace dps
+
 using namespace dps;
 
 namespace {
@@ -49,26 +73,6 @@ int check_ptrs(const char* fn, const Plan* pl, std::initializer_list<const void*
     if (!p && pl->L > 0) return fail(DP_EINVAL, std::string(fn) + ": NULL device pointer");
     if (misaligned(p)) return fail(DP_EALIGN, std::string(fn) + ": device pointer not 32-byte aligned");
   }
-  return DP_OK;
-}
-
-int adam_scalars(const char* fn, const dp_adamw_cfg* cfg, AdamScalars* s) {
-  if (!cfg) return fail(DP_EINVAL, std::string(fn) + ": NULL cfg");
-  if (cfg->step < 1) return fail(DP_EINVAL, std::string(fn) + ": step must be >= 1");
-  if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
-    return fail(DP_EINVAL, std::string(fn) + ": betas must be in [0, 1)");
-  // Scalar factors formed once in double and rounded to fp32 (torch.optim.AdamW
-  // forms them as Python floats): decay factor 1 - lr*wd, 1-b1, 1-b2,
-  // step size lr / (1 - b1^t) and sqrt(1 - b2^t).
-  const double t = static_cast<double>(cfg->step);
-  s->wd_factor = static_cast<float>(1.0 - cfg->lr * cfg->weight_decay);
-  s->b1 = static_cast<float>(cfg->beta1);
-  s->omb1 = static_cast<float>(1.0 - cfg->beta1);
-  s->b2 = static_cast<float>(cfg->beta2);
-  s->omb2 = static_cast<float>(1.0 - cfg->beta2);
-  s->step_size = static_cast<float>(cfg->lr / (1.0 - std::pow(cfg->beta1, t)));
-  s->sqrt_bc2 = static_cast<float>(std::sqrt(1.0 - std::pow(cfg->beta2, t)));
-  s->eps = static_cast<float>(cfg->eps);
   return DP_OK;
 }
 

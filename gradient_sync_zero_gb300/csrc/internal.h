@@ -86,6 +86,9 @@ struct Plan {
   std::vector<uint8_t> image;       // host copy of the device image (table_bytes)
 };
 
+// AdamW's per-step scalars from a cfg (checked; DP_EINVAL with a message naming fn).
+int adam_scalars(const char* fn, const dp_adamw_cfg* cfg, AdamScalars* s);
+
 // Thread-local last-error text (dp_last_error); fail() records and returns code.
 int fail(int code, const std::string& msg);
 void clear_error();

@@ -37,6 +37,13 @@ struct Tracker {
   const void* micro = nullptr;      // set: the last micro-batch of accumulation (fused add)
   float* mean = nullptr;
   void* stream = nullptr;
+  // DP_TRACK_ZERO_STEP: the step's targets and AdamW scalars (dp_tracker_set_zero_step)
+  void* params = nullptr;
+  float* master = nullptr;
+  float* m = nullptr;
+  float* v = nullptr;
+  AdamScalars adam{};
+  bool zero_set = false;
   int max_ctas = 0;
   std::vector<std::vector<int32_t>> bucket_tensors;
   std::mutex mu;
@@ -86,7 +93,14 @@ int fire(Tracker& tr, int32_t b) {
   L.stream = tr.stream;
   L.max_ctas = tr.max_ctas;
   int e;
-  if (tr.mode == DP_TRACK_ALLREDUCE)
+  if (tr.mode == DP_TRACK_ZERO_STEP) {
+    if (!tr.zero_set) {
+      tr.error_text = "dp_tracker: bucket " + std::to_string(b) +
+                      " became ready before dp_tracker_set_zero_step";
+      return DP_EINVAL;
+    }
+    e = launch_zero_fused(L, tr.grads, tr.params, tr.master, tr.m, tr.v, tr.adam);
+  } else if (tr.mode == DP_TRACK_ALLREDUCE)
     e = tr.micro ? launch_allreduce_accum(L, tr.grads, tr.micro) : launch_allreduce(L, tr.grads);
   else
     e = tr.micro ? launch_reduce_scatter_accum(L, tr.grads, tr.micro, tr.mean, true)
@@ -113,7 +127,7 @@ int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* 
   *out = nullptr;
   const Plan* pl = as_plan(plan);
   if (!pl) return fail(DP_EINVAL, "dp_tracker_create: NULL plan");
-  if (mode != DP_TRACK_ALLREDUCE && mode != DP_TRACK_REDUCE_SCATTER)
+  if (mode != DP_TRACK_ALLREDUCE && mode != DP_TRACK_REDUCE_SCATTER && mode != DP_TRACK_ZERO_STEP)
     return fail(DP_EINVAL, "dp_tracker_create: unknown mode");
   if (max_ctas < 0) return fail(DP_EINVAL, "dp_tracker_create: max_ctas must be >= 0");
   const bool dry = (flags & DP_TRACK_DRY_RUN) != 0;
@@ -155,12 +169,45 @@ int dp_tracker_set_micro(dp_tracker* tracker, const void* micro) {
   Tracker* tr = reinterpret_cast<Tracker*>(tracker);
   if (!tr) return fail(DP_EINVAL, "dp_tracker_set_micro: NULL tracker");
   if (micro && tr->plan->R > 1) return fail(DP_EINVAL, "dp_tracker_set_micro: flat plans only");
+  if (micro && tr->mode == DP_TRACK_ZERO_STEP)
+    return fail(DP_EINVAL, "dp_tracker_set_micro: not with DP_TRACK_ZERO_STEP");
   if (reinterpret_cast<uintptr_t>(micro) & 31u)
     return fail(DP_EALIGN, "dp_tracker_set_micro: micro must be 32-byte aligned");
   std::lock_guard<std::mutex> g(tr->mu);
   if (tr->next != 0 && tr->next != static_cast<int32_t>(tr->pending.size()))
     return fail(DP_EINVAL, "dp_tracker_set_micro: a step is in progress (some buckets fired)");
   tr->micro = micro;
+  return DP_OK;
+}
+
+int dp_tracker_set_zero_step(dp_tracker* tracker, void* params, float* master, float* m, float* v,
+                             const dp_adamw_cfg* cfg) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_set_zero_step: NULL tracker");
+  if (tr->mode != DP_TRACK_ZERO_STEP)
+    return fail(DP_EINVAL, "dp_tracker_set_zero_step: the tracker is not in DP_TRACK_ZERO_STEP mode");
+  if (tr->micro) return fail(DP_EINVAL, "dp_tracker_set_zero_step: a micro-batch buffer is set");
+  if (tr->plan->L > 0 && (!params || !master || !m || !v))
+    return fail(DP_EINVAL, "dp_tracker_set_zero_step: NULL device pointer");
+  const uintptr_t a = reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(master) |
+                      reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(v);
+  if (a & 31u) return fail(DP_EALIGN, "dp_tracker_set_zero_step: device pointers must be 32-byte aligned");
+  AdamScalars s{};
+  const int rc = adam_scalars("dp_tracker_set_zero_step", cfg, &s);
+  if (rc) return rc;
+  if (cfg->max_norm > 0.0)
+    return fail(DP_EINVAL, "dp_tracker_set_zero_step: clipping needs the global norm of every "
+                           "bucket before any update; use DP_TRACK_REDUCE_SCATTER");
+  std::lock_guard<std::mutex> g(tr->mu);
+  if (tr->next != 0 && tr->next != static_cast<int32_t>(tr->pending.size()))
+    return fail(DP_EINVAL, "dp_tracker_set_zero_step: a step is in progress (some buckets fired)");
+  tr->params = params;
+  tr->master = master;
+  tr->m = m;
+  tr->v = v;
+  tr->adam = s;
+  tr->zero_set = true;
   return DP_OK;
 }
 

@@ -449,7 +449,16 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  *   DP_TRACK_ALLREDUCE       the in-place mean all-reduce of `grads`;
  *   DP_TRACK_REDUCE_SCATTER  the reduce-scatter mean into `mean` with norm
  *                            partials (follow with dp_clip_coef and
- *                            dp_adamw_all_gather on comm_stream).
+ *                            dp_adamw_all_gather on comm_stream);
+ *   DP_TRACK_ZERO_STEP       the whole ZeRO-1/2 step of the bucket without
+ *                            clipping: reduce-scatter, AdamW on each owner's
+ *                            shard and all-gather of the new parameters in one
+ *                            pass over the bucket (dp_fused_zero_step on
+ *                            [b, b+1)); set the targets and the step's AdamW
+ *                            settings with dp_tracker_set_zero_step.  `mean` is
+ *                            not used.  With clipping every update needs the
+ *                            global norm of all buckets first, so a clipped step
+ *                            uses DP_TRACK_REDUCE_SCATTER instead.
  * dp_tracker_wait returns once every bucket has been launched, or DP_ETIMEOUT
  * after timeout_ms naming tensors never marked (DDP would hang there).  It does
  * not synchronise the GPU: order later work after comm_stream.
@@ -465,7 +474,7 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  * (event NULL) as soon as it knows they are unused.
  */
 typedef struct dp_tracker dp_tracker;
-enum { DP_TRACK_ALLREDUCE = 0, DP_TRACK_REDUCE_SCATTER = 1 };
+enum { DP_TRACK_ALLREDUCE = 0, DP_TRACK_REDUCE_SCATTER = 1, DP_TRACK_ZERO_STEP = 2 };
 enum { DP_TRACK_DRY_RUN = 1 };
 
 int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* grads, float* mean,
@@ -478,6 +487,16 @@ int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* 
  * Flat plans only; refused (DP_EINVAL) while a step has fired some but not all
  * buckets. */
 int dp_tracker_set_micro(dp_tracker* tracker, const void* micro);
+/* DP_TRACK_ZERO_STEP: the parameter replicas (bf16 [P][replica_stride]), the fp32
+ * master, m and v [L] that each bucket's step updates, and the step's AdamW
+ * settings (copied; cfg->step is this step's t).  Call before the step's first
+ * bucket fires, again for every step (t changes).  DP_EINVAL for another mode,
+ * a NULL pointer or cfg, cfg->max_norm > 0 (clipping needs the global norm), a
+ * micro-batch buffer set, or a step that has fired some but not all buckets;
+ * DP_EALIGN for a pointer that is not 32-byte aligned.  A bucket that becomes
+ * ready before any call fails its launch with DP_EINVAL. */
+int dp_tracker_set_zero_step(dp_tracker* tracker, void* params, float* master, float* m, float* v,
+                             const dp_adamw_cfg* cfg);
 int dp_tracker_begin(dp_tracker* tracker);
 int dp_tracker_mark_ready(dp_tracker* tracker, int32_t tensor, void* ready_event);
 int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms);

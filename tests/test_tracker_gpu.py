@@ -162,3 +162,52 @@ def test_streamed_last_micro_batch_equals_fused_single_launch(mode):
     else:
         assert torch.equal(mean.view(torch.int32), mean_ref.view(torch.int32)) and n2 == n_ref
     del keep
+
+
+@pytest.mark.parametrize("P,mesh,max_ctas", [(8, None, 0), (5, None, 16), (8, (2, 4), 0)])
+def test_streamed_whole_zero_step_per_bucket_matches_oracle(orc, P, mesh, max_ctas):
+    """DP_TRACK_ZERO_STEP: each bucket's whole unclipped ZeRO step (reduce-scatter,
+    AdamW on the owners' shards, all-gather) fires as soon as the bucket is ready,
+    while the producer is still writing earlier tensors.  Three steps through one
+    tracker (the AdamW settings change with t); master/m/v and every replica equal
+    the oracle's ZeRO step bit for bit."""
+    import oracle as oracle_mod
+    wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910, 9000], P, 32 * 1024,
+                        sigma=0.05, seed=90 + P)
+    c = Case(wl)
+    if mesh:
+        c.plan = dps.Plan(wl.sizes, wl.bucket_bytes, P, c.decay, mesh=mesh)
+        c.off, c.ws = c.plan.tensor_offsets(), c.plan.new_workspace()
+    assert c.plan.n_buckets >= 3
+    adamw = configs.AdamW(max_norm=0.0)
+    master = c.host_master()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    grads, params = c.plan.new_replicas(), c.plan.new_replicas()
+    st = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    tr = dps.Tracker(c.plan, dps.DP_TRACK_ZERO_STEP, c.ws, grads, stream=comm, max_ctas=max_ctas)
+    for step in (1, 2, 3):
+        g = c.host_grads(step)
+        ocfg = oracle_mod.adamw_cfg(adamw, step)
+        if mesh:
+            p_o, master, m, v, _ = orc.mesh_zero_step(c.sizes, c.decay, wl.bucket_bytes, *mesh, g,
+                                                      master, m, v, ocfg)
+        else:
+            p_o, master, m, v, _, _ = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, P, g,
+                                                    master, m, v, ocfg)
+        cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
+                            0.0, step)
+        grads.zero_()
+        torch.cuda.synchronize()
+        tr.set_zero_step(params, *st, cfg)
+        tr.begin()
+        keep = produce(c, g, grads, tr, producer, P)
+        tr.wait(10000)
+        assert tr.fired() == list(range(c.plan.n_buckets))
+        torch.cuda.synchronize()
+        assert np.array_equal(c.from_replicas(params), p_o)
+        assert_replicas_equal(params, c.plan.L)
+        for dev, ref in zip(st, (master, m, v)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+        del keep

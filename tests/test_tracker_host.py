@@ -174,3 +174,39 @@ def test_unused_parameters_marked_after_forward_let_the_bucket_fire():
     tr.mark_ready(0)
     tr.wait(100)
     assert tr.fired() == [0, 1]
+
+
+def test_set_zero_step_rules():
+    """DP_TRACK_ZERO_STEP: the targets and AdamW settings of each bucket's whole
+    step.  Refused in another mode, with clipping (the global norm must precede
+    every update), with NULL or misaligned pointers, with a micro-batch buffer,
+    and in the middle of a step; `mean` is not needed to create the tracker."""
+    import ctypes as C
+    sizes = [1000, 1000, 1000, 1000]
+    plan = dps.Plan(sizes, 4000, 2)
+    lib = dps.lib()
+    ok, odd = C.c_void_p(1 << 20), C.c_void_p((1 << 20) + 8)
+    h = C.c_void_p()
+    assert lib.dp_tracker_create(plan.handle, dps.DP_TRACK_ZERO_STEP, ok, ok, None, None, 0, 0,
+                                 C.byref(h)) == dps.DP_OK
+    lib.dp_tracker_free(h)
+    cfg = dps.adamw_cfg(max_norm=0.0, step=1)
+    clipped = dps.adamw_cfg(max_norm=1.0, step=1)
+    _, ar = dry(sizes, 4000, 2)
+    assert lib.dp_tracker_set_zero_step(ar._h, ok, ok, ok, ok, C.byref(cfg)) == dps.DP_EINVAL
+    tr = dps.Tracker(plan, dps.DP_TRACK_ZERO_STEP, dry_run=True)
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, ok, ok, C.byref(clipped)) == dps.DP_EINVAL
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, ok, ok, None) == dps.DP_EINVAL
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, None, ok, ok, C.byref(cfg)) == dps.DP_EINVAL
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, odd, ok, C.byref(cfg)) == dps.DP_EALIGN
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, ok, ok, C.byref(cfg)) == dps.DP_OK
+    assert lib.dp_tracker_set_micro(tr._h, ok) == dps.DP_EINVAL       # no accumulation here
+    tr.begin()
+    tr.mark_ready(3)
+    tr.mark_ready(2)                                   # bucket 0 fired, bucket 1 not
+    assert tr.fired() == [0]
+    step2 = dps.adamw_cfg(max_norm=0.0, step=2)
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, ok, ok, C.byref(step2)) == dps.DP_EINVAL
+    tr.mark_ready(1)
+    tr.mark_ready(0)
+    assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, ok, ok, C.byref(step2)) == dps.DP_OK
