@@ -580,7 +580,7 @@ def run_streamed(args):
         else:
             mats.append(None)
     compute = torch.cuda.Stream()
-    comm = torch.cuda.Stream(priority=-1)
+    comm = torch.cuda.Stream(priority=args.comm_priority)
     mode = (dps.DP_TRACK_ZERO_STEP if whole else
             dps.DP_TRACK_REDUCE_SCATTER if zero else dps.DP_TRACK_ALLREDUCE)
     tr = dps.Tracker(plan, mode, ws, grads, mean if zero else None, stream=comm,
@@ -654,6 +654,7 @@ def run_streamed(args):
         "ms": {"backward": t_b, "sync": t_s, "backward_then_sync": t_seq, "streamed": t_str},
         "config": {"workload": wl.name, "tokens": T, "comm_ctas": args.comm_ctas,
                    "n_buckets": plan.n_buckets, "mode": wl.mode, "clip_max_norm": a.max_norm,
+                   "comm_priority": args.comm_priority,
                    "tracker_mode": ("whole zero step per bucket" if whole else
                                     "reduce-scatter per bucket" if zero else
                                     "all-reduce per bucket")},
@@ -1152,6 +1153,8 @@ def main(argv=None):
     ap.add_argument("--mesh", default="",
                     help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
     ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
+    ap.add_argument("--comm-priority", type=int, default=-1,
+                    help="with --streamed: CUDA priority of the communication stream (-1 high, 0 normal)")
     ap.add_argument("--max-norm", type=float, default=None,
                     help="override the workload's clip threshold (0 = no clipping: one fused pass)")
     ap.add_argument("--prefetch", action="store_true",
