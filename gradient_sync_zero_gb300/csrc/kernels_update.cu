@@ -29,7 +29,7 @@ __device__ __forceinline__ bool header_scalars(const KCommon& k, AdamScalars& s)
 
 __device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, float* master,
                                            float* m, float* v, uint8_t* params,
-                                           const AdamScalars& s, int use_coef, int flat_params) {
+                                           const AdamScalars& s, int use_coef) {
   const float coef = use_coef ? k.hdr->coef : 1.0f;
   for_each_block(k, [&](int64_t, int64_t b, int c) {
     float g[16], th[16], mm[16], vv[16];
@@ -47,11 +47,8 @@ __device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, 
     st_f16(m, b, mm);
     st_f16(v, b, vv);
     const Blk val = pack16_rne(th);
-    if (flat_params) {  // ZeRO-3: one flat array of shards
-      st_blk(params + 32 * b, val);
-    } else {            // the owner of shard c in every group (rank c on a flat ring)
-      for (int g = 0; g < k.R; ++g) st_blk(params + (g * k.S + c) * k.stride_bytes + 32 * b, val);
-    }
+    // the owner of shard c in every group (rank c on a flat ring)
+    for (int g = 0; g < k.R; ++g) st_blk(params + (g * k.S + c) * k.stride_bytes + 32 * b, val);
   });
 }
 
@@ -60,14 +57,14 @@ __device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, 
 template <bool DEV_S>
 __global__ void __launch_bounds__(kThreads)
     k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
-            AdamScalars s, int use_coef, int flat_params) {
+            AdamScalars s, int use_coef) {
   if (!plan_ok(k)) return;
   if constexpr (DEV_S) {
     AdamScalars sd;
     if (!header_scalars(k, sd)) return;
-    adamw_body(k, grad, master, m, v, params, sd, use_coef, flat_params);
+    adamw_body(k, grad, master, m, v, params, sd, use_coef);
   } else {
-    adamw_body(k, grad, master, m, v, params, s, use_coef, flat_params);
+    adamw_body(k, grad, master, m, v, params, s, use_coef);
   }
 }
 
@@ -450,8 +447,9 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
                  bool dev_scalars) {
   // The ZeRO-3 shard update covers the whole plan and writes one flat bf16 array:
   // the bulk-copy pass with a single output row streams it (no owner rows needed).
-  if (flat_params && L.tile_begin == 0 &&
-      L.tile_end == static_cast<int64_t>(L.plan->tiles.size())) {
+  if (flat_params) {
+    if (L.tile_begin != 0 || L.tile_end != static_cast<int64_t>(L.plan->tiles.size()))
+      return cudaErrorInvalidValue;   // only whole-plan flat updates exist
     if (L.plan->L == 0) return cudaSuccess;
     const KCommon k = make_common(L);
     return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, grad, params, master, m, v,
@@ -460,7 +458,7 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
                                                                  v, s, use_coef, 1, 0);
   }
   return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
-                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0, flat_params ? 1 : 0);
+                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0);
 }
 
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
