@@ -242,6 +242,31 @@ def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=1
     return done_params / done_s, done_params, done_s, threads, desc
 
 
+def oracle_allreduce_rate(wl, offsets, grads_dev, budget_s=15.0, max_passes=3):
+    """Time the CPU oracle's mean all-reduce (the literal ring over P host buffers,
+    every bucket of the plan) on the whole workload: passes until ~budget_s of work,
+    at least one and at most max_passes.
+    Returns (params/s, params, seconds, threads, description)."""
+    import numpy as np
+    import oracle
+    orc = oracle.default()
+    threads = os.cpu_count() or 1
+    g = torch.cat([grads_dev[:, offsets[t]:offsets[t] + wl.sizes[t]]
+                   for t in range(len(wl.sizes))], dim=1)
+    g = g.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    done_params, done_s, passes = 0, 0.0, 0
+    while passes < max_passes and (passes == 0 or done_s < budget_s):
+        t0 = time.perf_counter()
+        orc.allreduce_mean(wl.sizes, wl.bucket_bytes, wl.P, g, want_mean=False, n_threads=threads)
+        done_s += time.perf_counter() - t0
+        done_params += wl.n_params
+        passes += 1
+    desc = (f"{passes} pass(es) over the whole workload ({wl.n_params} params each), oracle "
+            f"mean all-reduce over all {orc.plan(wl.sizes, wl.bucket_bytes, wl.P)['n_buckets']} "
+            f"buckets with {threads} threads, inputs copied from the GPU run")
+    return done_params / done_s, done_params, done_s, threads, desc
+
+
 # --------------------------------------------------------------------------- GPU bench
 def run_gpu(args, rank, local, world):
     import gradient_sync_zero_gb300 as dps
@@ -532,9 +557,14 @@ def run_gpu(args, rank, local, world):
         del host
 
     # ---- CPU oracle baseline (rank 0, N=1 only) ----
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and zero:
-        rate, npar, secs, thr, desc = oracle_sample_rate(wl, off, grads, master,
-                                                         budget_s=args.cpu_budget)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if zero:
+            rate, npar, secs, thr, desc = oracle_sample_rate(wl, off, grads, master,
+                                                             budget_s=args.cpu_budget)
+        else:
+            wdev.fill_grads(grads, off, wl, step=1)      # fresh inputs, not the last mean
+            rate, npar, secs, thr, desc = oracle_allreduce_rate(wl, off, grads,
+                                                                budget_s=args.cpu_budget)
         result["cpu_baseline"] = {"value": rate, "unit": "params/s", "cores": thr, "kind": "oracle",
                                   "sample": desc, "seconds": secs}
     return result
@@ -1110,23 +1140,32 @@ def run_reference(args, rank, world):
                   .view(torch.int16).numpy().view(np.uint16) for r in range(wl.P)])
     mst = torch.cat([gen.master_values(wl, base[t], wl.sizes[t]) for t in tens]).numpy()
     z = np.zeros_like(mst)
+    zero = wl.mode == "zero"
+
+    def one_step(step):
+        if zero:
+            orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g, mst, z, z,
+                          oracle.adamw_cfg(wl.adamw, step), n_threads=threads)
+        else:
+            orc.allreduce_mean(sub, wl.bucket_bytes, wl.P, g, want_mean=False, n_threads=threads)
+
     step = 0
     for _ in range(args.warmup):
         step += 1
-        orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g, mst, z, z,
-                      oracle.adamw_cfg(wl.adamw, step), n_threads=threads)
+        one_step(step)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step += 1
-        orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g, mst, z, z,
-                      oracle.adamw_cfg(wl.adamw, step), n_threads=threads)
+        one_step(step)
     secs = (time.perf_counter() - t0) / args.steps
     value = sum(sub) / secs
-    desc = (f"buckets {batch[0]}..{batch[-1]} of {nb} ({sum(sub)} params per step), oracle fused "
-            f"ZeRO step with its own clip norm over the sample")
+    desc = (f"buckets {batch[0]}..{batch[-1]} of {nb} ({sum(sub)} params per step), " +
+            ("oracle fused ZeRO step with its own clip norm over the sample" if zero else
+             "oracle mean all-reduce (literal ring) over the sample"))
     return {
         "impl": "reference",
-        "metric": "fused ZeRO-2 step params/s and achieved HBM GB/s vs GB300 peak (P=8, 1 GPU)",
+        "metric": "fused ZeRO-2 step params/s and achieved HBM GB/s vs GB300 peak (P=8, 1 GPU)"
+        if zero else "bucketed mean all-reduce params/s",
         "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",

@@ -89,3 +89,27 @@ def test_workload_names_resolve():
     assert bench.workload_by_name("llama-1.1B-P8-zero2").P == 8
     with pytest.raises(SystemExit):
         bench.workload_by_name("nope")
+
+
+def test_reference_arm_times_the_allreduce_for_allreduce_workloads(monkeypatch):
+    """An all-reduce workload's reference arm times the oracle's mean all-reduce and
+    names the all-reduce metric (the plumbing shapes, switched to all-reduce mode)."""
+    import argparse
+    import dataclasses
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import configs
+    wl = dataclasses.replace(configs.tiny_plumbing(), name="tiny-P4-1M-allreduce", mode="allreduce")
+    monkeypatch.setattr(bench, "workload_by_name", lambda name: wl)
+    calls = []
+    import oracle
+    orc = oracle.default()
+    real = orc.allreduce_mean
+    monkeypatch.setattr(orc, "allreduce_mean", lambda *a, **k: calls.append(1) or real(*a, **k))
+    monkeypatch.setattr(orc, "zero_step", lambda *a, **k: pytest.fail("zero step timed"))
+    monkeypatch.setattr(oracle, "default", lambda: orc)
+    d = bench.run_reference(argparse.Namespace(steps=2, warmup=1, workload=wl.name), 0, 1)
+    assert len(calls) == 3
+    assert d["metric"] == "bucketed mean all-reduce params/s" and d["value"] > 0
+    assert "all-reduce" in d["cpu_baseline"]["sample"]
+    json.dumps(d)
