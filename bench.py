@@ -180,10 +180,11 @@ def kernel_source_hash():
 
 def stored_traffic(workload, kernel):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the
-    profiles' DRAM-traffic record, only if it was taken on the current kernel sources."""
-    tf = os.path.join(ROOT, "profiles", "dram_traffic_llama-1.1B-P8-zero2.txt")
+    profiles' DRAM-traffic record of this workload, only if it was taken on the
+    current kernel sources."""
+    tf = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.txt")
     if not os.path.exists(tf):
-        return None, "no ncu capture recorded"
+        return None, "no ncu capture recorded for this workload"
     with open(tf) as f:
         text = f.read()
     tdb = json.loads(text[text.index("{"):])     # comment lines, then the JSON record
@@ -242,7 +243,7 @@ def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=1
     return done_params / done_s, done_params, done_s, threads, desc
 
 
-def oracle_allreduce_rate(wl, offsets, grads_dev, budget_s=15.0, max_passes=3):
+def oracle_allreduce_rate(wl, offsets, grads_dev, budget_s=15.0, max_passes=40):
     """Time the CPU oracle's mean all-reduce (the literal ring over P host buffers,
     every bucket of the plan) on the whole workload: passes until ~budget_s of work,
     at least one and at most max_passes.
