@@ -5,8 +5,8 @@
 // bucket_cap_mb is the knob): tensors are taken from the last to the first,
 // each in a 16-byte aligned slot; a bucket that already holds data is closed
 // when the next slot would push it past the cap; tensors are never split; a
-// closed bucket is padded to a multiple of 16P so that its P shards ("split each
-// GPU's data into N chunks", sec. 5.1) are whole 32-byte blocks of 16 bf16 — the
+// closed bucket is padded to a multiple of 16P so that its P shards (sec. 5.1:
+// each rank's buffer is cut into one chunk per rank) are whole 32-byte blocks of 16 bf16 — the
 // unit of one 256-bit access, which therefore never straddles two owners.
 //
 // The device image lets one launch walk any bucket range: a table of work

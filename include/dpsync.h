@@ -109,9 +109,10 @@ typedef struct {
 } dp_adamw_cfg;
 
 /*
- * Bucket planner.  DDP groups gradients into buckets of about 25 MB, filled in
- * the reverse of the order the forward pass computes them ("4.1 Data
- * parallelism in depth", sec. 4.2; PyTorch's bucket_cap_mb).  Rule: walk tensors n-1 ... 0; each takes a
+ * Bucket planner.  Gradients are packed into buckets of about 25 MB (one
+ * collective per bucket), filled in the reverse of the order the forward pass
+ * computes them ("4.1 Data parallelism in depth", sec. 4.2; PyTorch's
+ * bucket_cap_mb).  Rule: walk tensors n-1 ... 0; each takes a
  * slot of ceil(size/8)*8 elements (16-byte aligned); a non-empty bucket is
  * closed when adding the next slot would exceed bucket_bytes/2 elements; a
  * tensor is never split (one larger than the cap forms its own bucket); a

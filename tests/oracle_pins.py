@@ -183,7 +183,7 @@ def pin_ring_allgather_payload(orc):
 
 
 def pin_stage_traffic(orc):
-    """DDP, ZeRO-1 and ZeRO-2 move 2(P-1)/P*M per rank, ZeRO-3 3(P-1)/P*M:
+    """DDP, ZeRO-1 and ZeRO-2 each send 2(P-1)/P*M per rank, ZeRO-3 3(P-1)/P*M:
     1.5x ("Data Parallelism: DDP, ZeRO and FSDP", 'The three stages'; "4.1 Data parallelism in depth", sec. 8)."""
     g = golden("ledger_pages.json")["comm_per_step"]["value"]
     for P in (2, 4, 8, 16):
