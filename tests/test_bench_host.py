@@ -113,3 +113,25 @@ def test_reference_arm_times_the_allreduce_for_allreduce_workloads(monkeypatch):
     assert d["metric"] == "bucketed mean all-reduce params/s" and d["value"] > 0
     assert "all-reduce" in d["cpu_baseline"]["sample"]
     json.dumps(d)
+
+
+def test_oracle_allreduce_rate_on_host_buffers():
+    """The all-reduce CPU baseline gathers the tensors out of the padded replica
+    layout and times whole passes of the oracle's ring, at least one and at most
+    max_passes."""
+    import dataclasses
+    sys.path.insert(0, ROOT)
+    import bench
+    import gradient_sync_zero_gb300 as dps
+    from workloads import configs
+    wl = dataclasses.replace(configs.tiny_plumbing(), name="tiny-P4-1M-allreduce", mode="allreduce")
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P)
+    grads = plan.new_replicas(device="cpu")
+    grads.normal_(0.0, 1e-3)
+    rate, n, secs, thr, desc = bench.oracle_allreduce_rate(wl, plan.tensor_offsets(), grads,
+                                                           budget_s=0.0, max_passes=2)
+    assert n == wl.n_params and secs > 0 and rate == n / secs and thr >= 1
+    assert desc.startswith("1 pass(es)")
+    _, _, _, _, desc2 = bench.oracle_allreduce_rate(wl, plan.tensor_offsets(), grads,
+                                                    budget_s=1e9, max_passes=2)
+    assert desc2.startswith("2 pass(es)")
