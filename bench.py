@@ -451,8 +451,8 @@ def run_gpu(args, rank, local, world):
         # of about equal size; each group's reduction starts as soon as its bytes
         # have arrived.  Across steps, step t+1's copy starts as soon as step t's
         # reductions have consumed the gradient buffer, so it overlaps step t's
-        # update pass; each step's result (the 192-byte workspace header with the
-        # norm and status) is read back asynchronously into its own pinned buffer
+        # update pass; each step's result (the workspace's norm and status fields) is
+        # read back asynchronously into its own pinned buffer
         # and checked after the loop (flat plans; a mesh plan runs copy-then-step).
         pipelined = mesh is None
         copy_stream = torch.cuda.Stream()
@@ -467,6 +467,16 @@ def run_gpu(args, rank, local, world):
         if pipelined and zero:
             mean_buf = plan.new_state()
         consumed = [None]                    # event: the last reduction of the previous step
+        # --e2e-readback: every step also reads one updated replica back to pinned
+        # host memory (the parameters; the mean gradients for an all-reduce), on its
+        # own stream, so it runs on the link's other direction beside the next
+        # step's host-to-device copy.  The next writer of that replica waits for it.
+        readback = args.e2e_readback and pipelined
+        if readback:
+            d2h_stream = torch.cuda.Stream()
+            out_rep = params if zero else grads
+            host_out = torch.empty(L, dtype=torch.bfloat16, pin_memory=True)
+        read_done = [None]                   # event: the last step's read-back finished
 
         def grouped_copies_ms():
             # the copies alone, in the step's bucket groups (for reading the e2e number)
@@ -493,6 +503,8 @@ def run_gpu(args, rank, local, world):
                 copy_stream.wait_stream(stream)
             else:
                 copy_stream.wait_event(consumed[0])
+            if readback and not zero and read_done[0] is not None:
+                copy_stream.wait_event(read_done[0])     # the mean is read before it is overwritten
             with torch.cuda.stream(copy_stream):
                 for b0, b1 in groups:
                     o = plan.bucket(b0)[0]
@@ -513,14 +525,29 @@ def run_gpu(args, rank, local, world):
             if zero:
                 if clip:
                     dps.dp_clip_coef(plan, ws, wl.adamw.max_norm)
+                if readback and read_done[0] is not None:
+                    stream.wait_event(read_done[0])      # last step's parameters are out
                 dps.dp_adamw_all_gather(plan, ws, mean_buf, master, m, v, params, cfg(step),
                                         use_clip_coef=clip)
+            if readback:
+                ready = torch.cuda.Event()
+                ready.record(stream)
+                d2h_stream.wait_event(ready)
+                with torch.cuda.stream(d2h_stream):
+                    host_out.copy_(out_rep[0, :L], non_blocking=True)
+                read_done[0] = torch.cuda.Event()
+                read_done[0].record(d2h_stream)
 
         e2e_step(step + 1)                  # untimed: the pipelined path once
         step += 1
         torch.cuda.synchronize()
         consumed[0] = None
-        results = [torch.empty(192, dtype=torch.uint8, pin_memory=True) for _ in range(e2e_steps)]
+        # the step's result: the workspace's result fields (norm, coef, status), at the
+        # offsets the library reports
+        off_n2, off_norm, off_coef, off_status = dps.workspace_result_offsets()
+        res_bytes = off_status + 4
+        results = [torch.empty(res_bytes, dtype=torch.uint8, pin_memory=True)
+                   for _ in range(e2e_steps)]
         done = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
         barrier(world)
         t0 = time.perf_counter()
@@ -529,22 +556,24 @@ def run_gpu(args, rank, local, world):
             step += 1
             e2e_step(step)
             if zero:
-                results[k].copy_(ws[:192], non_blocking=True)     # this step's result, D2H
+                results[k].copy_(ws[:res_bytes], non_blocking=True)   # this step's result, D2H
             else:
                 torch.cuda.synchronize()
             done[k + 1].record(stream)
         torch.cuda.synchronize()
         e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
         step_ms = [done[k].elapsed_time(done[k + 1]) for k in range(e2e_steps)]
+        if readback and not torch.equal(host_out, out_rep[0, :L].cpu()):
+            raise RuntimeError("e2e: the replica read back differs from the device's")
         if zero:
-            norms = [float(r[120:128].view(torch.float64)) for r in results]   # header: norm
-            status = [int(r[132:136].view(torch.int32)) for r in results]      # header: status
+            norms = [float(r[off_norm:off_norm + 8].view(torch.float64)) for r in results]
+            status = [int(r[off_status:off_status + 4].view(torch.int32)) for r in results]
             if any(st != 0 for st in status) or norms[-1] != dps.dp_read_norm(plan, ws)[0]:
                 raise RuntimeError(f"e2e: unexpected step results {norms} {status}")
         copy_only_ms = grouped_copies_ms()
         result["e2e"] = {"value": n_params * world / e2e_s, "unit": "params/s",
                          "h2d_bytes_per_step": host.numel() * host.element_size(),
-                         "d2h_bytes_per_step": 192 if zero else 0,
+                         "d2h_bytes_per_step": (res_bytes if zero else 0) + (2 * L if readback else 0),
                          "steps": e2e_steps, "h2d_gbs_alone": h2d_gbs,
                          "step_ms": [round(x, 2) for x in step_ms],
                          "grouped_copies_alone_ms": round(copy_only_ms, 2),
@@ -552,6 +581,8 @@ def run_gpu(args, rank, local, world):
                          "copy": (f"pipelined: {len(groups)} bucket groups, each group's reduction "
                                   "overlapped with the copy, the next step's copy with this step's "
                                   "update; results read back asynchronously"
+                                  + ("; one updated replica read back to pinned host memory every "
+                                     "step, beside the next step's copy" if readback else "")
                                   if pipelined else "copy, then the step")}
         if pipelined and zero:
             del mean_buf
@@ -569,6 +600,21 @@ def run_gpu(args, rank, local, world):
         result["cpu_baseline"] = {"value": rate, "unit": "params/s", "cores": thr, "kind": "oracle",
                                   "sample": desc, "seconds": secs}
     return result
+
+
+def layer_groups(names):
+    """Runs of consecutive tensors of one layer ("<block>.<i>.<rest>"), others
+    alone: [(t0, t1), ...] in tensor order."""
+    def key(n):
+        parts = n.split(".")
+        return ".".join(parts[:2]) if len(parts) > 2 and parts[1].isdigit() else n
+    out = []
+    for t, n in enumerate(names):
+        if out and key(names[out[-1][0]]) == key(n):
+            out[-1] = (out[-1][0], t + 1)
+        else:
+            out.append((t, t + 1))
+    return out
 
 
 def run_streamed(args):
@@ -618,16 +664,38 @@ def run_streamed(args):
                      max_ctas=args.comm_ctas)
 
     events = [torch.cuda.Event() for _ in wl.sizes]
+    # marking: "tensor" = an event and a mark call per tensor; "batch" = an event
+    # per tensor, one mark call per layer (the tensors "<block>.<i>.*" of one
+    # layer; others alone); "layer" = one event and one call per layer
+    groups = [(t, t + 1) for t in range(len(wl.sizes))] if args.mark == "tensor" else \
+        layer_groups(wl.names)
+    host_mark_s = [0.0]
+    dry_tr = dps.Tracker(plan, mode, dry_run=True)
 
-    def backward(stream, mark):
+    def backward(stream, mark, tracker=None):
+        tracker = tracker or tr
         with torch.cuda.stream(stream):
-            for t in reversed(range(len(wl.sizes))):
-                if mats[t] is not None:
-                    dy, x, dw = mats[t]
-                    torch.matmul(dy.t(), x, out=dw)
+            for g0, g1 in reversed(groups):
+                for t in reversed(range(g0, g1)):
+                    if mats[t] is not None:
+                        dy, x, dw = mats[t]
+                        torch.matmul(dy.t(), x, out=dw)
+                    if mark and args.mark == "batch":
+                        h0 = time.perf_counter()
+                        events[t].record(stream)
+                        host_mark_s[0] += time.perf_counter() - h0
                 if mark:
-                    events[t].record(stream)
-                    tr.mark_ready(t, events[t])
+                    h0 = time.perf_counter()
+                    if args.mark == "batch":
+                        ts = list(range(g1 - 1, g0 - 1, -1))
+                        tracker.mark_ready_batch(ts, [events[t] for t in ts])
+                    else:
+                        events[g0].record(stream)
+                        if g1 - g0 == 1:
+                            tracker.mark_ready(g0, events[g0])
+                        else:
+                            tracker.mark_ready_range(g0, g1, events[g0])
+                    host_mark_s[0] += time.perf_counter() - h0
 
     def finish(stream):
         if zero and not whole:
@@ -673,17 +741,58 @@ def run_streamed(args):
     def only_sync():
         sync_all(compute)
 
+    def concurrent():
+        # the sync of every bucket on the comm stream beside the backward, with no
+        # readiness waits (the result is not a valid step): what SM and HBM
+        # contention alone cost
+        comm.wait_stream(compute)
+        backward(compute, False)
+        if whole:
+            dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg, stream=comm)
+        elif zero:
+            dps.dp_reduce_scatter_mean(plan, ws, grads, mean, want_sumsq=True, stream=comm)
+            finish(comm)
+        else:
+            dps.dp_allreduce_mean(plan, ws, grads, stream=comm)
+        compute.wait_stream(comm)
+
+    def marks_only():
+        # the backward with its event records and marks on a dry-run tracker
+        # (no waits, no launches): what marking costs the backward
+        dry_tr.begin()
+        backward(compute, True, dry_tr)
+
+    def host_ms(fn, reps):
+        torch.cuda.synchronize()
+        host_mark_s[0] = 0.0
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        return (t1 - t0) / reps * 1e3, host_mark_s[0] / reps * 1e3
+
     reps = max(3, args.steps // 5)
     t_b = timed(only_backward, reps)
     t_s = timed(only_sync, reps)
     t_seq = timed(sequential, reps)
     t_str = timed(streamed, reps)
+    t_con = timed(concurrent, reps)
+    t_mrk = timed(marks_only, reps)
+    hb, _ = host_ms(only_backward, reps)
+    hm, hmark = host_ms(marks_only, reps)
+    n_launch, n_wait = tr.stats()                 # the last streamed step
     hidden = (t_seq - t_str) / max(t_seq - t_b, 1e-9)
     return {
         "metric": "streamed per-bucket sync: share of sync time hidden under a synthetic backward",
         "value": hidden, "unit": "fraction", "higher_is_better": True,
-        "ms": {"backward": t_b, "sync": t_s, "backward_then_sync": t_seq, "streamed": t_str},
+        "ms": {"backward": t_b, "sync": t_s, "backward_then_sync": t_seq, "streamed": t_str,
+               "backward_beside_sync_no_waits": t_con, "backward_with_marks_dry": t_mrk},
+        "host_ms": {"backward_issue": hb, "backward_issue_with_marks": hm,
+                    "in_record_and_mark_calls": hmark},
+        "per_step": {"marks": len(groups), "launches": n_launch, "stream_waits": n_wait},
         "config": {"workload": wl.name, "tokens": T, "comm_ctas": args.comm_ctas,
+                   "mark": args.mark,
                    "n_buckets": plan.n_buckets, "mode": wl.mode, "clip_max_norm": a.max_norm,
                    "comm_priority": args.comm_priority,
                    "tracker_mode": ("whole zero step per bucket" if whole else
@@ -1188,6 +1297,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama-1.1B-P8-zero2")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-readback", action="store_true",
+                    help="e2e: also read one updated replica back to the host every step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--mesh", default="",
@@ -1210,6 +1321,9 @@ def main(argv=None):
     ap.add_argument("--streamed", action="store_true",
                     help="measure the overlap of per-bucket sync with a synthetic backward")
     ap.add_argument("--tokens", type=int, default=4096, help="GEMM rows of the synthetic backward")
+    ap.add_argument("--mark", choices=["batch", "layer", "tensor"], default="batch",
+                    help="--streamed: an event per tensor and a mark call per layer (batch), "
+                         "an event and a call per layer (layer), or per tensor (tensor)")
     ap.add_argument("--comm-ctas", type=int, default=152,
                     help="grid cap of the streamed sync kernels")
     args = ap.parse_args(argv)

@@ -67,7 +67,7 @@ def lib():
             "dp_plan_upload": [vp, vp, vp],
             "dp_reduce_scatter_mean": [vp, vp, vp, vp, i32, i32, i32, vp],
             "dp_clip_coef": [vp, vp, f64, i32, i32, vp],
-            "dp_sharded_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp],
+            "dp_sharded_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, vp],
             "dp_all_gather": [vp, vp, vp, i32, i32, vp],
             "dp_broadcast": [vp, vp, vp, i32, i32, i32, vp],
             "dp_allreduce_mean": [vp, vp, vp, i32, i32, vp],
@@ -75,7 +75,7 @@ def lib():
             "dp_fused_zero_step_launches": [vp],
             "dp_read_norm": [vp, vp, vp, vp, vp, vp],
             "dp_clip_coef_noalloc": [vp, vp, vp, f64, vp, vp, vp],
-            "dp_adamw_all_gather": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
+            "dp_adamw_all_gather": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp],
             "dp_tracker_create": [vp, i32, vp, vp, vp, vp, i32, i32, vp],
             "dp_unit_all_gather": [vp, vp, vp, i32, vp, i64, vp],
             "dp_accumulate": [vp, vp, vp, vp, i32, i32, vp],
@@ -87,10 +87,14 @@ def lib():
             "dp_reduce_scatter_mean_accum": [vp, vp, vp, vp, vp, i32, i32, i32, vp],
             "dp_allreduce_mean_bf16wire": [vp, vp, vp, i32, i32, vp],
             "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
-            "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp],
+            "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp],
+            "dp_workspace_result_offsets": [vp],
             "dp_tracker_begin": [vp],
             "dp_tracker_set_micro": [vp, vp],
             "dp_tracker_mark_ready": [vp, i32, vp],
+            "dp_tracker_mark_ready_range": [vp, i32, i32, vp],
+            "dp_tracker_mark_ready_batch": [vp, vp, vp, i32],
+            "dp_tracker_stats": [vp, vp, vp],
             "dp_tracker_wait": [vp, i64],
             "dp_tracker_fired": [vp, vp, i32, vp],
             "dp_plan_fingerprint": [vp, vp],
@@ -133,6 +137,22 @@ def _cfg_ref(cfg):
 
 def _ptr(t):
     return C.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _coef(coef_dev):
+    """coef_dev: None, or a 1-element float32 CUDA tensor holding a clip
+    coefficient the caller formed itself."""
+    if coef_dev is None:
+        return None
+    _need(coef_dev, torch.float32, 1, "coef_dev")
+    return _ptr(coef_dev)
+
+
+def workspace_result_offsets():
+    """Byte offsets of (norm2, norm, coef, status) in a workspace, from the library."""
+    out = (C.c_int64 * 4)()
+    _check(lib().dp_workspace_result_offsets(out))
+    return tuple(out)
 
 
 def _need(t, dtype, numel, name):
@@ -280,14 +300,17 @@ def dp_clip_coef(plan, ws, max_norm, b0=0, b1=None, stream=None):
 
 
 def dp_sharded_adamw_step(plan, ws, grad, master, m, v, params, cfg, use_clip_coef=False, b0=0,
-                          b1=None, stream=None):
+                          b1=None, stream=None, coef_dev=None):
+    """coef_dev: a float32 CUDA tensor [1] with the caller's own clip coefficient
+    (needs use_clip_coef=True); None with use_clip_coef: the workspace's."""
     for t, name in ((grad, "grad"), (master, "master"), (m, "m"), (v, "v")):
         _need(t, torch.float32, plan.L, name)
     _need(params, torch.bfloat16, plan.P * plan.stride, "params")
     b0, b1 = _range(plan, b0, b1)
     _check(lib().dp_sharded_adamw_step(plan.handle, _ws(plan, ws), _ptr(grad), _ptr(master), _ptr(m),
                                        _ptr(v), _ptr(params), _cfg_ref(cfg),
-                                       1 if use_clip_coef else 0, b0, b1, _stream(stream)))
+                                       1 if use_clip_coef else 0, _coef(coef_dev), b0, b1,
+                                       _stream(stream)))
 
 
 def dp_all_gather(plan, ws, params, b0=0, b1=None, stream=None):
@@ -309,13 +332,14 @@ def dp_allreduce_mean(plan, ws, grads, b0=0, b1=None, stream=None):
     _check(lib().dp_allreduce_mean(plan.handle, _ws(plan, ws), _ptr(grads), b0, b1, _stream(stream)))
 
 
-def dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg, use_clip_coef=True, stream=None):
+def dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg, use_clip_coef=True, stream=None,
+                        coef_dev=None):
     for t, name in ((mean, "mean"), (master, "master"), (m, "m"), (v, "v")):
         _need(t, torch.float32, plan.L, name)
     _need(params, torch.bfloat16, plan.P * plan.stride, "params")
     _check(lib().dp_adamw_all_gather(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
                                      _ptr(v), _ptr(params), _cfg_ref(cfg), 1 if use_clip_coef else 0,
-                                     _stream(stream)))
+                                     _coef(coef_dev), _stream(stream)))
 
 
 def dp_unit_all_gather(plan, ws, param_shards, unit, unit_buf, stream=None):
@@ -341,13 +365,13 @@ def dp_unit_reduce_scatter(plan, ws, unit_grads, unit, mean, want_sumsq=False, s
 
 
 def dp_shard_adamw_step(plan, ws, mean, master, m, v, param_shards, cfg, use_clip_coef=False,
-                        stream=None):
+                        stream=None, coef_dev=None):
     for t, name in ((mean, "mean"), (master, "master"), (m, "m"), (v, "v")):
         _need(t, torch.float32, plan.L, name)
     _need(param_shards, torch.bfloat16, plan.L, "param_shards")
     _check(lib().dp_shard_adamw_step(plan.handle, _ws(plan, ws), _ptr(mean), _ptr(master), _ptr(m),
                                      _ptr(v), _ptr(param_shards), _cfg_ref(cfg),
-                                     1 if use_clip_coef else 0, _stream(stream)))
+                                     1 if use_clip_coef else 0, _coef(coef_dev), _stream(stream)))
 
 
 class Tracker:
@@ -409,6 +433,29 @@ class Tracker:
         """event: torch.cuda.Event recorded after the tensor's gradient was written."""
         ev = C.c_void_p(event.cuda_event) if event is not None else None
         _check(lib().dp_tracker_mark_ready(self._h, int(tensor), ev))
+
+    def mark_ready_range(self, t0, t1, event=None):
+        """Tensors [t0, t1) ready, all written before `event` (one call, one event)."""
+        ev = C.c_void_p(event.cuda_event) if event is not None else None
+        _check(lib().dp_tracker_mark_ready_range(self._h, int(t0), int(t1), ev))
+
+    def mark_ready_batch(self, tensors, events=None):
+        """Tensors ready, each written before its own event (events: a list of
+        torch.cuda.Event, or None), in one call."""
+        ts = [int(t) for t in tensors]
+        arr = (C.c_int32 * max(len(ts), 1))(*ts)
+        evs = None
+        if events is not None:
+            if len(events) != len(ts):
+                raise ValueError("one event per tensor")
+            evs = (C.c_void_p * max(len(ts), 1))(*[e.cuda_event for e in events])
+        _check(lib().dp_tracker_mark_ready_batch(self._h, arr, evs, len(ts)))
+
+    def stats(self):
+        """(launches, cudaStreamWaitEvent calls) of this step so far."""
+        n, w = C.c_int32(), C.c_int32()
+        _check(lib().dp_tracker_stats(self._h, C.byref(n), C.byref(w)))
+        return n.value, w.value
 
     def wait(self, timeout_ms=10000):
         _check(lib().dp_tracker_wait(self._h, int(timeout_ms)))

@@ -82,6 +82,24 @@ float* stage_of(const Plan* pl, void* ws) {
   return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + h.off_stage);
 }
 
+// The clip coefficient an update multiplies the gradient by: the caller's device
+// float (coef_dev), the workspace's last dp_clip_coef result (use_clip_coef), or
+// none (NULL: 1).
+int coef_source(const char* fn, void* ws, int32_t use_clip_coef, const float* coef_dev,
+                const float** out) {
+  *out = nullptr;
+  if (coef_dev) {
+    if (!use_clip_coef)
+      return fail(DP_EINVAL, std::string(fn) + ": coef_dev given with use_clip_coef = 0");
+    if (reinterpret_cast<uintptr_t>(coef_dev) & 3u)
+      return fail(DP_EALIGN, std::string(fn) + ": coef_dev not 4-byte aligned");
+    *out = coef_dev;
+  } else if (use_clip_coef) {
+    *out = reinterpret_cast<const float*>(static_cast<uint8_t*>(ws) + offsetof(DevHeader, coef));
+  }
+  return DP_OK;
+}
+
 int record(void* const* ev, int i, void* stream) {
   if (!ev) return DP_OK;
   const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]),
@@ -124,14 +142,17 @@ int dp_clip_coef(const dp_plan* plan, void* workspace, double max_norm, int32_t 
 
 int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* grad, float* master,
                           float* m, float* v, void* params, const dp_adamw_cfg* cfg,
-                          int32_t use_clip_coef, int32_t b0, int32_t b1, void* stream) {
+                          int32_t use_clip_coef, const float* coef_dev, int32_t b0, int32_t b1,
+                          void* stream) {
   Launch L;
   int rc = prepare("dp_sharded_adamw_step", plan, workspace, b0, b1, stream, &L);
   if (rc) return rc;
   if ((rc = check_ptrs("dp_sharded_adamw_step", L.plan, {grad, master, m, v, params}))) return rc;
+  const float* coefp = nullptr;
+  if ((rc = coef_source("dp_sharded_adamw_step", workspace, use_clip_coef, coef_dev, &coefp))) return rc;
   AdamScalars s{};
   if (cfg && (rc = adam_scalars("dp_sharded_adamw_step", cfg, &s))) return rc;
-  const int e = launch_adamw(L, grad, master, m, v, params, s, use_clip_coef != 0, false, !cfg);
+  const int e = launch_adamw(L, grad, master, m, v, params, s, coefp, false, !cfg);
   return e ? cuda_fail(e, "dp_sharded_adamw_step") : DP_OK;
 }
 
@@ -168,16 +189,18 @@ int dp_allreduce_mean(const dp_plan* plan, void* workspace, void* grads, int32_t
 
 int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean, float* master,
                         float* m, float* v, void* params, const dp_adamw_cfg* cfg,
-                        int32_t use_clip_coef, void* stream) {
+                        int32_t use_clip_coef, const float* coef_dev, void* stream) {
   Launch L;
   const Plan* pl = as_plan(plan);
   int rc = prepare("dp_adamw_all_gather", plan, workspace, 0,
                    pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
   if (rc) return rc;
   if ((rc = check_ptrs("dp_adamw_all_gather", L.plan, {mean, master, m, v, params}))) return rc;
+  const float* coefp = nullptr;
+  if ((rc = coef_source("dp_adamw_all_gather", workspace, use_clip_coef, coef_dev, &coefp))) return rc;
   AdamScalars s{};
   if (cfg && (rc = adam_scalars("dp_adamw_all_gather", cfg, &s))) return rc;
-  const int e = launch_adamw_all_gather(L, mean, params, master, m, v, s, use_clip_coef != 0, !cfg);
+  const int e = launch_adamw_all_gather(L, mean, params, master, m, v, s, coefp, !cfg);
   return e ? cuda_fail(e, "dp_adamw_all_gather") : DP_OK;
 }
 
@@ -214,16 +237,18 @@ int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* uni
 
 int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean, float* master,
                         float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
-                        int32_t use_clip_coef, void* stream) {
+                        int32_t use_clip_coef, const float* coef_dev, void* stream) {
   Launch L;
   const Plan* pl = as_plan(plan);
   int rc = prepare("dp_shard_adamw_step", plan, workspace, 0,
                    pl ? static_cast<int32_t>(pl->b_off.size()) : 0, stream, &L);
   if (rc) return rc;
   if ((rc = check_ptrs("dp_shard_adamw_step", L.plan, {mean, master, m, v, param_shards}))) return rc;
+  const float* coefp = nullptr;
+  if ((rc = coef_source("dp_shard_adamw_step", workspace, use_clip_coef, coef_dev, &coefp))) return rc;
   AdamScalars s{};
   if (cfg && (rc = adam_scalars("dp_shard_adamw_step", cfg, &s))) return rc;
-  const int e = launch_adamw(L, mean, master, m, v, param_shards, s, use_clip_coef != 0, true, !cfg);
+  const int e = launch_adamw(L, mean, master, m, v, param_shards, s, coefp, true, !cfg);
   return e ? cuda_fail(e, "dp_shard_adamw_step") : DP_OK;
 }
 
@@ -311,6 +336,16 @@ int dp_set_adamw_cfg(const dp_plan* plan, void* workspace, const dp_adamw_cfg* c
   return e == cudaSuccess ? DP_OK : cuda_fail(e, "dp_set_adamw_cfg");
 }
 
+int dp_workspace_result_offsets(int64_t* offsets) {
+  clear_error();
+  if (!offsets) return fail(DP_EINVAL, "dp_workspace_result_offsets: NULL offsets");
+  offsets[0] = static_cast<int64_t>(offsetof(DevHeader, norm2));
+  offsets[1] = static_cast<int64_t>(offsetof(DevHeader, norm));
+  offsets[2] = static_cast<int64_t>(offsetof(DevHeader, coef));
+  offsets[3] = static_cast<int64_t>(offsetof(DevHeader, status));
+  return DP_OK;
+}
+
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg) {
   return (cfg && cfg->max_norm > 0.0) ? 3 : 1;
 }
@@ -339,7 +374,9 @@ int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, 
   e = launch_norm_finalize(L, cfg->max_norm);
   if (e) return cuda_fail(e, "dp_fused_zero_step (norm)");
   if ((rc = record(stage_events, 2, stream))) return rc;
-  e = launch_adamw_all_gather(L, stage, params, master, m, v, s, true);
+  const float* ws_coef = reinterpret_cast<const float*>(static_cast<uint8_t*>(workspace) +
+                                                        offsetof(DevHeader, coef));
+  e = launch_adamw_all_gather(L, stage, params, master, m, v, s, ws_coef);
   if (e) return cuda_fail(e, "dp_fused_zero_step (adamw + all-gather)");
   return record(stage_events, 3, stream);
 }

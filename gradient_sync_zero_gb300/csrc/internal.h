@@ -2,6 +2,7 @@
 // planner, C-ABI, kernel launchers).  Not part of the public ABI.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -63,6 +64,11 @@ struct DevHeader {
   int64_t reserved2_[2];
 };
 static_assert(sizeof(DevHeader) % 64 == 0, "header keeps the arrays aligned");
+// the results part's layout is public (include/dpsync.h, DP_WS_*_OFFSET)
+static_assert(offsetof(DevHeader, norm2) == DP_WS_NORM2_OFFSET, "public offset of norm2");
+static_assert(offsetof(DevHeader, norm) == DP_WS_NORM_OFFSET, "public offset of norm");
+static_assert(offsetof(DevHeader, coef) == DP_WS_COEF_OFFSET, "public offset of coef");
+static_assert(offsetof(DevHeader, status) == DP_WS_STATUS_OFFSET, "public offset of status");
 
 struct Plan {
   int32_t P = 0;
@@ -122,15 +128,16 @@ int launch_reduce_scatter_accum(const Launch& L, const void* acc, const void* mi
                                 bool sumsq);
 int launch_allreduce_bf16wire(const Launch& L, void* grads);
 int launch_norm_finalize(const Launch& L, double max_norm);
+// coefp: device fp32 clip coefficient multiplying the gradient (NULL = 1).
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef, bool flat_params = false,
+                 void* params, const AdamScalars& s, const float* coefp, bool flat_params = false,
                  bool dev_scalars = false);
 int launch_all_gather(const Launch& L, void* params);
 int launch_broadcast(const Launch& L, void* params, int src);
 int launch_zero_fused(const Launch& L, const void* grads, void* params, float* master, float* m,
                       float* v, const AdamScalars& s);
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
-                            float* m, float* v, const AdamScalars& s, bool use_coef,
+                            float* m, float* v, const AdamScalars& s, const float* coefp,
                             bool dev_scalars = false);
 
 }  // namespace dps

@@ -40,6 +40,15 @@ struct KCommon {
   int64_t rep_block0;    // replica buffers start at this 32-byte block (unit buffers)
   int32_t split;         // CTAs per tile (1, or 2 for launches with few tiles)
   int32_t pad_;
+  // A launch inside one bucket carries that bucket in its parameters, so its
+  // tile descriptors are computed, not loaded (one dependent load fewer per
+  // small per-bucket launch).  one_nvec = 0: descriptors come from the table.
+  int64_t one_v0;        // the bucket's first 16-byte vector
+  int64_t one_tile0;     // the bucket's first tile
+  int32_t one_nvec;      // the bucket's length in vectors
+  int32_t one_svec;      // its shard length in vectors
+  int32_t one_bucket;
+  int32_t pad2_;
 };
 
 // ---- optional index checks (built with -DDPSYNC_CHECKED) ----
@@ -138,11 +147,13 @@ __device__ __forceinline__ Blk pack16_rne(const float (&f)[16]) {
 // owner is known from the block index), up to 8 blocks in flight per thread,
 // and folded with fp32 adds in the same order.  Then G = sum / N (sec. 1) as an
 // IEEE division, which a multiply by 1/P reproduces exactly for P = 2^k.
-template <int P>
+// KC: replica blocks in flight per thread (8, or 16 for the latency-bound small
+// launches, where one round of loads instead of two is worth the registers).
+template <int P, int KC = 8>
 __device__ __forceinline__ void ring_fold_chunk(const uint8_t* g, int64_t stride_bytes,
                                                 int64_t byte_off, int np, int r_first, int k0,
                                                 float (&acc)[16]) {
-  constexpr int K = (P > 0 && P < 8) ? P : 8;
+  constexpr int K = (P > 0 && P < KC) ? P : KC;
   Blk x[K];
 #pragma unroll
   for (int k = 0; k < K; ++k) {
@@ -166,19 +177,21 @@ __device__ __forceinline__ void ring_fold_chunk(const uint8_t* g, int64_t stride
   }
 }
 
-template <int P>
+template <int P, int KC = 8>
 __device__ __forceinline__ void ring_mean16(const uint8_t* g, int64_t stride_bytes,
                                             int64_t byte_off, int c, int p_rt,
                                             float (&acc)[16]) {
-  constexpr int K = (P > 0 && P < 8) ? P : 8;
+  constexpr int K = (P > 0 && P < KC) ? P : KC;
   const int np = P > 0 ? P : p_rt;
   const int r_first = (c + 1 == np) ? 0 : c + 1;
   if constexpr (P > 0) {
 #pragma unroll
-    for (int k0 = 0; k0 < P; k0 += K) ring_fold_chunk<P>(g, stride_bytes, byte_off, np, r_first, k0, acc);
+    for (int k0 = 0; k0 < P; k0 += K)
+      ring_fold_chunk<P, KC>(g, stride_bytes, byte_off, np, r_first, k0, acc);
   } else {
 #pragma unroll 1
-    for (int k0 = 0; k0 < np; k0 += K) ring_fold_chunk<P>(g, stride_bytes, byte_off, np, r_first, k0, acc);
+    for (int k0 = 0; k0 < np; k0 += K)
+      ring_fold_chunk<P, KC>(g, stride_bytes, byte_off, np, r_first, k0, acc);
   }
   if constexpr (P > 0 && (P & (P - 1)) == 0) {
     constexpr float inv = 1.0f / P;
@@ -309,11 +322,11 @@ __device__ __forceinline__ void mesh_mean16_ct(const uint8_t* g, int64_t stride_
 // The mean of block b for its owner: MS = 0 flat ring, MS > 0 hybrid mesh with
 // group size MS fixed at compile time, MS < 0 hybrid mesh with the shape read
 // at run time.  s = shard index in the bucket (the owner rank on a flat ring).
-template <int P, int MS>
+template <int P, int MS, int KC = 8>
 __device__ __forceinline__ void block_mean16(const KCommon& k, const uint8_t* g, int64_t b,
                                              const TileDesc& d, int s, float (&acc)[16]) {
   if constexpr (MS == 0) {
-    ring_mean16<P>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, k.P, acc);
+    ring_mean16<P, KC>(g, k.stride_bytes, 32 * (b - k.rep_block0), s, k.P, acc);
   } else {
     const uint32_t within = static_cast<uint32_t>(2 * b - d.bvoff) % static_cast<uint32_t>(d.svec);
     const int j = static_cast<int>(within / (static_cast<uint32_t>(d.svec) / k.R));
@@ -599,7 +612,40 @@ __device__ __forceinline__ bool plan_ok(const KCommon& k) {
   return false;
 }
 
+// Start of a kernel whose launch lies inside one bucket (k.one_nvec > 0): after
+// the dependency wait, the plan id is loaded, but not waited for, so the first
+// replica loads go out beside it; plan_matches() then gates the stores.  Such a
+// launch takes its tile descriptors from its parameters, so with another plan's
+// image in the workspace it still reads only the caller's buffers of this plan.
+// (Letting the next launch be scheduled early from here, griddepcontrol
+// .launch_dependents at entry, was measured: per-bucket launches of 64 KiB
+// buckets unchanged, of 1 MiB buckets 17% slower; not kept.)
+__device__ __forceinline__ uint64_t plan_id_deferred(const KCommon& k) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  uint64_t id;
+  asm volatile("ld.global.u64 %0, [%1];" : "=l"(id) : "l"(&k.hdr->plan_id) : "memory");
+  return id;
+}
+
+__device__ __forceinline__ bool plan_matches(const KCommon& k, uint64_t id) {
+  if (id == k.plan_id) return true;
+  if (threadIdx.x == 0) atomicOr(&k.hdr->status, DP_STATUS_PLAN_MISMATCH);
+  return false;
+}
+
 __device__ __forceinline__ TileDesc load_tile(const KCommon& k, int64_t tile) {
+  if (k.one_nvec > 0) {   // one bucket: tiles of kTileVec vectors from its start
+    const int64_t i = tile - k.one_tile0;
+    const int64_t rest = static_cast<int64_t>(k.one_nvec) - i * kTileVec;
+    TileDesc d;
+    d.v0 = k.one_v0 + i * kTileVec;
+    d.bvoff = k.one_v0;
+    d.nvec = static_cast<int32_t>(rest < kTileVec ? rest : kTileVec);
+    d.svec = k.one_svec;
+    d.bucket = k.one_bucket;
+    d.pad_ = 0;
+    return d;
+  }
   const int4* p = reinterpret_cast<const int4*>(k.tiles + tile);
   const int4 a = __ldg(p), b = __ldg(p + 1);
   TileDesc d;

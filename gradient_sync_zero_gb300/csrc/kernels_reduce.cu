@@ -31,11 +31,19 @@ constexpr int kAccumPerSm = 3;
 // size or on how the bucket range is split into launches.
 // ACC: the last micro-batch of gradient accumulation fused in — replica r's
 // value is bf16(g_r + micro_r), formed in registers (flat plans).
-template <int P, int MS, bool ACC>
+// SMALL (a launch inside one bucket, few tiles): the plan id is checked beside
+// the first loads (it gates the stores), and a block's replicas are all loaded
+// at once.
+template <int P, int MS, bool ACC, bool SMALL = false>
 __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint8_t* g,
                                                              float* mean, int sumsq,
                                                              const uint8_t* micro) {
-  if (!plan_ok(k)) return;
+  uint64_t id = k.plan_id;
+  if constexpr (SMALL) {
+    id = plan_id_deferred(k);
+  } else {
+    if (!plan_ok(k)) return;
+  }
   __shared__ FF warp_part[kWarps];
   // k.split = 2 (small launches) only without norm partials: a tile's partial has
   // one writer.  The common case keeps constant strides.
@@ -55,15 +63,16 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
         if constexpr (ACC) {
           ring_mean16_accum<P>(g, micro, k.stride_bytes, 32 * b, c, k.P, acc);
         } else {
-          block_mean16<P, MS>(k, g, b, d, c, acc);
+          block_mean16<P, MS, SMALL ? 16 : 8>(k, g, b, d, c, acc);
         }
+        if (SMALL && id != k.plan_id) continue;
         st_f16(mean, b, acc);
         if (sumsq) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
         }
       }
-      if (sumsq) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
+      if (sumsq && (!SMALL || id == k.plan_id)) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
     }
   };
   if (ACC || k.split == 1) {   // the accumulating form always launches unsplit
@@ -73,18 +82,26 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
     walk(k.tile_begin + cta_tile, gridDim.x / 2,
          static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
   }
+  if (SMALL) plan_matches(k, id);
 }
 
 // Fused mean all-reduce in place: sum in ring order, 1/P, bf16, written back to
 // every replica (the all-gather of the reduced shards).
-template <int P, int MS>
+// SMALL: as for k_reduce_scatter.
+template <int P, int MS, bool SMALL = false>
 __global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint8_t* g) {
-  if (!plan_ok(k)) return;
+  uint64_t id = k.plan_id;
+  if constexpr (SMALL) {
+    id = plan_id_deferred(k);
+  } else {
+    if (!plan_ok(k)) return;
+  }
   for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
     float acc[16];
-    block_mean16<P, MS>(k, g, b, d, c, acc);
-    store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(acc), k.P);
+    block_mean16<P, MS, SMALL ? 16 : 8>(k, g, b, d, c, acc);
+    if (!SMALL || id == k.plan_id) store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(acc), k.P);
   });
+  if (SMALL) plan_matches(k, id);
 }
 
 // acc[r] = bf16(acc[r] + micro[r]) for every replica.
@@ -182,6 +199,18 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
+      if constexpr (M == 0) {   // flat plans: small single-bucket launches take SMALL
+        if (sumsq && k.one_nvec > 0)
+          return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
+                                       k_reduce_scatter<P, M, false, true>, true, k,
+                                       static_cast<const uint8_t*>(grads), mean, 1,
+                                       static_cast<const uint8_t*>(nullptr));
+        if (!sumsq)
+          return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
+                                       k_reduce_scatter<P, M, false, true>, false, k,
+                                       static_cast<const uint8_t*>(grads), mean, 0,
+                                       static_cast<const uint8_t*>(nullptr));
+      }
       if (sumsq)
         return launch_tiles(L, k_reduce_scatter<P, M, false>, k, static_cast<const uint8_t*>(grads),
                             mean, 1, static_cast<const uint8_t*>(nullptr));
@@ -208,6 +237,9 @@ int launch_allreduce(const Launch& L, void* grads) {
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
+      if constexpr (M == 0)   // flat plans: small single-bucket launches take SMALL
+        return launch_small_or_split(L, kAllreducePerSm, k_allreduce<P, M>, k_allreduce<P, M, true>,
+                                     false, k, static_cast<uint8_t*>(grads));
       return launch_tiles_split(L, kAllreducePerSm, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
     });
   });

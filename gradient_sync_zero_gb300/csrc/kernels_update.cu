@@ -27,10 +27,12 @@ __device__ __forceinline__ bool header_scalars(const KCommon& k, AdamScalars& s)
   return true;
 }
 
+// coefp: the clip coefficient (device fp32: the workspace's, or the caller's own),
+// read once the previous kernel has finished; NULL = no clipping.
 __device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, float* master,
                                            float* m, float* v, uint8_t* params,
-                                           const AdamScalars& s, int use_coef) {
-  const float coef = use_coef ? k.hdr->coef : 1.0f;
+                                           const AdamScalars& s, const float* coefp) {
+  const float coef = coefp ? *coefp : 1.0f;
   for_each_block(k, [&](int64_t, int64_t b, int c) {
     float g[16], th[16], mm[16], vv[16];
     ld_f16(grad, b, g);
@@ -38,7 +40,7 @@ __device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, 
     ld_f16(m, b, mm);
     ld_f16(v, b, vv);
     const uint32_t dec = decay_bits2(k.decay, b);
-    if (use_coef) {
+    if (coefp) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) g[e] = __fmul_rn(g[e], coef);
     }
@@ -57,14 +59,14 @@ __device__ __forceinline__ void adamw_body(const KCommon& k, const float* grad, 
 template <bool DEV_S>
 __global__ void __launch_bounds__(kThreads)
     k_adamw(KCommon k, const float* grad, float* master, float* m, float* v, uint8_t* params,
-            AdamScalars s, int use_coef) {
+            AdamScalars s, const float* coefp) {
   if (!plan_ok(k)) return;
   if constexpr (DEV_S) {
     AdamScalars sd;
     if (!header_scalars(k, sd)) return;
-    adamw_body(k, grad, master, m, v, params, sd, use_coef);
+    adamw_body(k, grad, master, m, v, params, sd, coefp);
   } else {
-    adamw_body(k, grad, master, m, v, params, s, use_coef);
+    adamw_body(k, grad, master, m, v, params, s, coefp);
   }
 }
 
@@ -246,8 +248,8 @@ constexpr int kTmaStages = 2;
 template <int CH, int ST>
 __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mean, uint8_t* params,
                                               float* master, float* m, float* v,
-                                              const AdamScalars& s, int64_t L, int use_coef,
-                                              int rows, int64_t row_bytes) {
+                                              const AdamScalars& s, int64_t L,
+                                              const float* coefp, int rows, int64_t row_bytes) {
   using Stage = TmaStageT<CH>;
   constexpr int kPer = CH / kThreads;   // elements per thread per chunk (multiple of 4)
   static_assert(kPer % 4 == 0 && ST >= 2, "float4 lanes; at least double buffering");
@@ -257,7 +259,7 @@ __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mea
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Stage* buf = reinterpret_cast<Stage*>(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + ST * sizeof(Stage));
-  const float coef = use_coef ? k.hdr->coef : 1.0f;
+  const float coef = coefp ? *coefp : 1.0f;   // x 1 is exact: no clipping
   if (threadIdx.x == 0) {
     for (int q = 0; q < ST; ++q) mbar_init(&bar[q]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -338,15 +340,15 @@ __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mea
 template <bool DEV_S, int CH = kTmaChunk, int ST = kTmaStages>
 __global__ void __launch_bounds__(kThreads)
     k_adamw_all_gather(KCommon k, const float* mean, uint8_t* params, float* master, float* m,
-                       float* v, AdamScalars s, int64_t L, int use_coef, int rows,
+                       float* v, AdamScalars s, int64_t L, const float* coefp, int rows,
                        int64_t row_bytes) {
   if (!plan_ok(k)) return;
   if constexpr (DEV_S) {
     AdamScalars sd;
     if (!header_scalars(k, sd)) return;
-    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, sd, L, use_coef, rows, row_bytes);
+    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, sd, L, coefp, rows, row_bytes);
   } else {
-    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, s, L, use_coef, rows, row_bytes);
+    adamw_ag_body<CH, ST>(k, mean, params, master, m, v, s, L, coefp, rows, row_bytes);
   }
 }
 
@@ -422,8 +424,8 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
 // shard update).
 template <bool DEV_S, int CH, int ST>
 int launch_ag(const Launch& L, const KCommon& k, const float* stage, void* params,
-              float* master, float* m, float* v, const AdamScalars& s, bool use_coef, int rows,
-              int64_t row_bytes) {
+              float* master, float* m, float* v, const AdamScalars& s, const float* coefp,
+              int rows, int64_t row_bytes) {
   const int64_t Lp = L.plan->L;
   auto kern = k_adamw_all_gather<DEV_S, CH, ST>;
   constexpr size_t smem = tma_smem<CH, ST>();
@@ -438,12 +440,11 @@ int launch_ag(const Launch& L, const KCommon& k, const float* stage, void* param
   int64_t g = nchunks < cap ? nchunks : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
   return launch_k(kern, static_cast<int>(g), kThreads, smem, L.stream, k, stage,
-                  static_cast<uint8_t*>(params), master, m, v, s, Lp, use_coef ? 1 : 0, rows,
-                  row_bytes);
+                  static_cast<uint8_t*>(params), master, m, v, s, Lp, coefp, rows, row_bytes);
 }
 
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
-                 void* params, const AdamScalars& s, bool use_coef, bool flat_params,
+                 void* params, const AdamScalars& s, const float* coefp, bool flat_params,
                  bool dev_scalars) {
   // The ZeRO-3 shard update covers the whole plan and writes one flat bf16 array:
   // the bulk-copy pass with a single output row streams it (no owner rows needed).
@@ -453,25 +454,25 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
     if (L.plan->L == 0) return cudaSuccess;
     const KCommon k = make_common(L);
     return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, grad, params, master, m, v,
-                                                                s, use_coef, 1, 0)
+                                                                s, coefp, 1, 0)
                        : launch_ag<false, kTmaChunk, kTmaStages>(L, k, grad, params, master, m,
-                                                                 v, s, use_coef, 1, 0);
+                                                                 v, s, coefp, 1, 0);
   }
-  return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad, master, m, v,
-                      static_cast<uint8_t*>(params), s, use_coef ? 1 : 0);
+  return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad,
+                            master, m, v, static_cast<uint8_t*>(params), s, coefp);
 }
 
 int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, float* master,
-                            float* m, float* v, const AdamScalars& s, bool use_coef,
+                            float* m, float* v, const AdamScalars& s, const float* coefp,
                             bool dev_scalars) {
   const KCommon k = make_common(L);
   if (L.plan->L == 0) return cudaSuccess;
   const int rows = L.plan->P;
   const int64_t rb = k.stride_bytes;
   return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v, s,
-                                                              use_coef, rows, rb)
+                                                              coefp, rows, rb)
                      : launch_ag<false, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v,
-                                                               s, use_coef, rows, rb);
+                                                               s, coefp, rows, rb);
 }
 
 }  // namespace dps

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -32,6 +33,25 @@ inline KCommon make_common(const Launch& L) {
   k.rep_block0 = 0;
   k.split = 1;
   k.pad_ = 0;
+  k.one_v0 = 0;
+  k.one_tile0 = 0;
+  k.one_nvec = 0;
+  k.one_svec = 0;
+  k.one_bucket = 0;
+  k.pad2_ = 0;
+  // a launch inside one bucket carries the bucket (tile descriptors computed)
+  if (L.tile_end > L.tile_begin) {
+    const TileDesc& a = L.plan->tiles[L.tile_begin];
+    const int b = a.bucket;
+    if (L.plan->b_tile0[b] <= L.tile_begin && L.tile_end <= L.plan->b_tile0[b + 1] &&
+        L.plan->b_len[b] / kVecElems <= INT32_MAX) {
+      k.one_v0 = a.bvoff;
+      k.one_tile0 = L.plan->b_tile0[b];
+      k.one_nvec = static_cast<int32_t>(L.plan->b_len[b] / kVecElems);
+      k.one_svec = a.svec;
+      k.one_bucket = b;
+    }
+  }
   return k;
 }
 
@@ -182,6 +202,28 @@ int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... ar
   int64_t g = n * k.split < cap ? n * k.split : cap;
   g -= g % k.split;
   return launch_k(kernel, static_cast<int>(g), kThreads, 0, L.stream, k, args...);
+}
+
+// A launch inside one bucket (k.one_nvec > 0) that covers at most half as many
+// tiles as `small` fits on the GPU runs `small`: two CTAs per tile (split), or one
+// per tile with split1 (kernels whose tiles carry a norm partial).  Its kernel
+// issues all of a block's replica loads at once and checks the plan beside them
+// (latency, not bandwidth, bounds such a launch).  Otherwise `big` runs as
+// launch_tiles_split would launch it.
+template <class KB, class KS, class... A>
+int launch_small_or_split(const Launch& L, int per_sm, KB big, KS small, bool split1, KCommon k,
+                          A... args) {
+  const int64_t n = L.tile_end - L.tile_begin;
+  if (n <= 0) return cudaSuccess;
+  if (k.one_nvec > 0) {
+    int cap = resident_ctas(small, kThreads);
+    if (L.max_ctas > 0 && cap > L.max_ctas) cap = L.max_ctas;
+    if (cap > 0 && 2 * n <= cap) {
+      k.split = split1 ? 1 : 2;
+      return launch_k(small, static_cast<int>(n * k.split), kThreads, 0, L.stream, k, args...);
+    }
+  }
+  return launch_tiles_split(L, per_sm, big, k, args...);
 }
 
 // Rank counts with a fully unrolled instantiation; others use the runtime-P one.

@@ -349,6 +349,6 @@ void dp_plan_free(dp_plan* plan) { delete reinterpret_cast<Plan*>(plan); }
 
 const char* dp_last_error(void) { return dps::last_error_text(); }
 
-int dp_version(void) { return 1; }
+int dp_version(void) { return 2; }
 
 }  // extern "C"

@@ -53,6 +53,9 @@ struct Tracker {
   std::vector<int32_t> pending;     // per bucket: tensors not yet marked
   int32_t next = 0;                 // next bucket to fire, in plan order
   std::vector<int32_t> fired;
+  int32_t launches = 0;             // this step: kernel launches (a launch covers a bucket range)
+  int32_t waits = 0;                // this step: cudaStreamWaitEvent calls
+  std::vector<void*> wait_list;     // scratch: distinct events of the range being fired
   int error = DP_OK;                // sticky launch error of this step
   std::string error_text;
 };
@@ -67,35 +70,51 @@ void reset(Tracker& tr) {
     tr.pending[b] = static_cast<int32_t>(tr.bucket_tensors[b].size());
   tr.next = 0;
   tr.fired.clear();
+  tr.launches = 0;
+  tr.waits = 0;
   tr.error = DP_OK;
   tr.error_text.clear();
   (void)pl;
 }
 
-// Launch bucket b on the tracker's stream (lock held).
-int fire(Tracker& tr, int32_t b) {
-  tr.fired.push_back(b);
-  if (tr.flags & DP_TRACK_DRY_RUN) return DP_OK;
+// Launch buckets [b0, b1) on the tracker's stream as one launch over their
+// tiles (lock held), after the stream has waited once for each distinct event of
+// their tensors.  One launch over consecutive buckets computes what per-bucket
+// launches would, tile by tile (the norm partials are per tile).
+int fire(Tracker& tr, int32_t b0, int32_t b1) {
+  for (int32_t b = b0; b < b1; ++b) tr.fired.push_back(b);
+  tr.wait_list.clear();
+  for (int32_t b = b0; b < b1; ++b)
+    for (int32_t t : tr.bucket_tensors[b]) {
+      void* ev = tr.events[t];
+      if (ev && std::find(tr.wait_list.begin(), tr.wait_list.end(), ev) == tr.wait_list.end())
+        tr.wait_list.push_back(ev);
+    }
+  if (tr.flags & DP_TRACK_DRY_RUN) {   // count what would be issued
+    tr.waits += static_cast<int32_t>(tr.wait_list.size());
+    ++tr.launches;
+    return DP_OK;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(tr.stream);
-  for (int32_t t : tr.bucket_tensors[b]) {
-    if (!tr.events[t]) continue;
-    const cudaError_t e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(tr.events[t]), 0);
+  for (void* ev : tr.wait_list) {
+    const cudaError_t e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(ev), 0);
     if (e != cudaSuccess) {
       tr.error_text = std::string("dp_tracker: cudaStreamWaitEvent: ") + cudaGetErrorString(e);
       return DP_ECUDA;
     }
+    ++tr.waits;
   }
   Launch L;
   L.plan = tr.plan;
   L.ws = tr.ws;
-  L.tile_begin = tr.plan->b_tile0[b];
-  L.tile_end = tr.plan->b_tile0[b + 1];
+  L.tile_begin = tr.plan->b_tile0[b0];
+  L.tile_end = tr.plan->b_tile0[b1];
   L.stream = tr.stream;
   L.max_ctas = tr.max_ctas;
   int e;
   if (tr.mode == DP_TRACK_ZERO_STEP) {
     if (!tr.zero_set) {
-      tr.error_text = "dp_tracker: bucket " + std::to_string(b) +
+      tr.error_text = "dp_tracker: bucket " + std::to_string(b0) +
                       " became ready before dp_tracker_set_zero_step";
       return DP_EINVAL;
     }
@@ -110,7 +129,89 @@ int fire(Tracker& tr, int32_t b) {
                     cudaGetErrorString(static_cast<cudaError_t>(e));
     return DP_ECUDA;
   }
+  ++tr.launches;
   return DP_OK;
+}
+
+// The single event every tensor of bucket b was marked with (NULL included), or
+// uniform = false when its tensors carry different events.
+void* bucket_event(const Tracker& tr, int32_t b, bool* uniform) {
+  const std::vector<int32_t>& ts = tr.bucket_tensors[b];
+  void* ev = ts.empty() ? nullptr : tr.events[ts[0]];
+  *uniform = true;
+  for (int32_t t : ts)
+    if (tr.events[t] != ev) {
+      *uniform = false;
+      break;
+    }
+  return ev;
+}
+
+// Fire the buckets that have become complete, from tr.next on, in plan order.
+// Consecutive complete buckets whose tensors were all marked with the same event
+// (one layer marked with one event, or no events) become ready at the same moment
+// on the GPU and go out as one launch; a bucket whose tensors carry different
+// events goes out alone, right after the last of them, so it never waits for a
+// later bucket's readiness.
+int fire_ready(Tracker& tr) {
+  const int32_t nb = static_cast<int32_t>(tr.pending.size());
+  while (tr.next < nb && tr.pending[tr.next] == 0) {
+    bool uniform = false;
+    void* ev = bucket_event(tr, tr.next, &uniform);
+    int32_t end = tr.next + 1;
+    if (uniform) {
+      while (end < nb && tr.pending[end] == 0) {
+        bool u2 = false;
+        if (bucket_event(tr, end, &u2) != ev || !u2) break;
+        ++end;
+      }
+    }
+    const int rc = fire(tr, tr.next, end);
+    if (rc) return rc;
+    tr.next = end;
+  }
+  return DP_OK;
+}
+
+// Mark n tensors ready — tensor_at(i), written before event_at(i) — and fire what
+// became complete (lock held).  Nothing is marked if any tensor is out of range,
+// already marked in this step, or listed twice.
+template <class T, class E>
+int mark_tensors(Tracker& tr, int32_t n, T tensor_at, E event_at, const char* fn, std::string* text,
+                 bool* done) {
+  const int32_t nt = static_cast<int32_t>(tr.ready.size());
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t t = tensor_at(i);
+    std::string why;
+    if (t < 0 || t >= nt)
+      why = " outside [0, " + std::to_string(nt) + ")";
+    else if (tr.ready[t] == 2)
+      why = " listed twice";
+    else if (tr.ready[t])
+      why = " already marked in this step";
+    if (!why.empty()) {
+      *text = std::string(fn) + ": tensor " + std::to_string(t) + why;
+      for (int32_t j = 0; j < i; ++j) tr.ready[tensor_at(j)] = 0;   // undo this call's marks
+      return DP_EINVAL;
+    }
+    tr.ready[t] = 2;   // taken by this call (a repeat in the list is refused above)
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t t = tensor_at(i);
+    tr.ready[t] = 1;
+    tr.events[t] = event_at(i);
+    --tr.pending[tr.plan->t_bucket[t]];
+  }
+  int rc = DP_OK;
+  if (tr.error == DP_OK) {
+    rc = fire_ready(tr);
+    if (rc) {
+      tr.error = rc;
+      *text = tr.error_text;
+    }
+  }
+  *done = tr.next == static_cast<int32_t>(tr.pending.size()) || tr.error != DP_OK;
+  return rc;
 }
 
 }  // namespace
@@ -224,30 +325,62 @@ int dp_tracker_mark_ready(dp_tracker* tracker, int32_t tensor, void* ready_event
   clear_error();
   Tracker* tr = reinterpret_cast<Tracker*>(tracker);
   if (!tr) return fail(DP_EINVAL, "dp_tracker_mark_ready: NULL tracker");
+  std::string text;
+  bool done = false;
   std::unique_lock<std::mutex> g(tr->mu);
-  const int32_t nt = static_cast<int32_t>(tr->ready.size());
-  if (tensor < 0 || tensor >= nt) return fail(DP_EINVAL, "dp_tracker_mark_ready: tensor out of range");
-  if (tr->ready[tensor])
-    return fail(DP_EINVAL, "dp_tracker_mark_ready: tensor " + std::to_string(tensor) +
-                               " already marked in this step");
-  tr->ready[tensor] = 1;
-  tr->events[tensor] = ready_event;
-  --tr->pending[tr->plan->t_bucket[tensor]];
-  const int32_t nb = static_cast<int32_t>(tr->pending.size());
-  int rc = DP_OK;
-  while (tr->next < nb && tr->pending[tr->next] == 0 && tr->error == DP_OK) {
-    rc = fire(*tr, tr->next);
-    if (rc) {
-      tr->error = rc;
-      break;
-    }
-    ++tr->next;
-  }
-  const bool done = tr->next == nb || tr->error != DP_OK;
-  const std::string text = tr->error_text;
+  const int rc = mark_tensors(
+      *tr, 1, [&](int32_t) { return tensor; }, [&](int32_t) { return ready_event; },
+      "dp_tracker_mark_ready", &text, &done);
   g.unlock();
   if (done) tr->cv.notify_all();
   return rc ? fail(rc, text) : DP_OK;
+}
+
+int dp_tracker_mark_ready_range(dp_tracker* tracker, int32_t t0, int32_t t1, void* ready_event) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_mark_ready_range: NULL tracker");
+  if (t1 < t0)
+    return fail(DP_EINVAL, "dp_tracker_mark_ready_range: empty range [" + std::to_string(t0) +
+                               ", " + std::to_string(t1) + ")");
+  std::string text;
+  bool done = false;
+  std::unique_lock<std::mutex> g(tr->mu);
+  const int rc = mark_tensors(
+      *tr, t1 - t0, [&](int32_t i) { return t0 + i; }, [&](int32_t) { return ready_event; },
+      "dp_tracker_mark_ready_range", &text, &done);
+  g.unlock();
+  if (done) tr->cv.notify_all();
+  return rc ? fail(rc, text) : DP_OK;
+}
+
+int dp_tracker_mark_ready_batch(dp_tracker* tracker, const int32_t* tensors,
+                                void* const* ready_events, int32_t n) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_mark_ready_batch: NULL tracker");
+  if (n < 0 || (n > 0 && !tensors))
+    return fail(DP_EINVAL, "dp_tracker_mark_ready_batch: n < 0 or NULL tensors");
+  std::string text;
+  bool done = false;
+  std::unique_lock<std::mutex> g(tr->mu);
+  const int rc = mark_tensors(
+      *tr, n, [&](int32_t i) { return tensors[i]; },
+      [&](int32_t i) { return ready_events ? ready_events[i] : nullptr; },
+      "dp_tracker_mark_ready_batch", &text, &done);
+  g.unlock();
+  if (done) tr->cv.notify_all();
+  return rc ? fail(rc, text) : DP_OK;
+}
+
+int dp_tracker_stats(const dp_tracker* tracker, int32_t* launches, int32_t* waits) {
+  clear_error();
+  Tracker* tr = const_cast<Tracker*>(reinterpret_cast<const Tracker*>(tracker));
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_stats: NULL tracker");
+  std::lock_guard<std::mutex> g(tr->mu);
+  if (launches) *launches = tr->launches;
+  if (waits) *waits = tr->waits;
+  return DP_OK;
 }
 
 int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms) {

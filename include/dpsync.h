@@ -84,6 +84,22 @@ enum {
   DP_STATUS_NO_SCALARS = 8   /* an update ran without a cfg before dp_set_adamw_cfg */
 };
 
+/*
+ * Where a workspace keeps the results the kernels write, as byte offsets from
+ * the workspace's start (device memory): the squared global norm (double), the
+ * norm (double), the clip coefficient (float) and the status bits (int32,
+ * DP_STATUS_*).  dp_read_norm synchronises and reads them; a caller may instead
+ * copy them itself after ordering the copy after the kernels, or pass
+ * workspace + DP_WS_COEF_OFFSET as an update's coef_dev.
+ * dp_workspace_result_offsets reports the same four values from the library.
+ */
+enum {
+  DP_WS_NORM2_OFFSET = 112,
+  DP_WS_NORM_OFFSET = 120,
+  DP_WS_COEF_OFFSET = 128,
+  DP_WS_STATUS_OFFSET = 132
+};
+
 typedef struct dp_plan dp_plan;
 
 typedef struct {
@@ -224,12 +240,27 @@ int dp_clip_coef(const dp_plan* plan, void* workspace, double max_norm, int32_t 
                  void* stream);
 
 /*
+ * The clip coefficient of an update (use_clip_coef, coef_dev), shared by
+ * dp_sharded_adamw_step, dp_adamw_all_gather and dp_shard_adamw_step:
+ *   use_clip_coef = 0, coef_dev = NULL   coef = 1 (no clipping);
+ *   use_clip_coef != 0, coef_dev = NULL  coef = the workspace's, from the last
+ *                                        dp_clip_coef on it;
+ *   use_clip_coef != 0, coef_dev != NULL coef = *coef_dev, one device float the
+ *                                        caller formed itself (its own
+ *                                        clip_grad_norm_), 4-byte aligned, read
+ *                                        when the kernel runs (stream order);
+ *   use_clip_coef = 0, coef_dev != NULL  DP_EINVAL.
+ * The gradient is multiplied by coef in fp32 before AdamW
+ * ("Distributed Training: Data Parallel, Model Parallel and FSDP Strategies",
+ * "Inside DDP": clip after averaging, then optimizer.step()).
+ */
+
+/*
  * Sharded AdamW ("Data Parallelism: DDP, ZeRO and FSDP", "The three stages":
  * each rank updates the shard it owns; "Distributed Training: Data Parallel, Model Parallel and FSDP Strategies",
  * "Inside DDP": torch.optim.AdamW(lr, weight_decay)).  For every slot i of the
  * shards of buckets [b0,b1), owned by rank c:
- *   g = grad[i] * coef   (coef = the workspace's clip coefficient if
- *                         use_clip_coef, else 1)
+ *   g = grad[i] * coef   (coef from use_clip_coef / coef_dev, above)
  *   theta = master[i] * (1 - lr*wd)          if the slot's tensor decays
  *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*(g*g)
  *   theta -= (lr / (1-b1^t)) * (m / (sqrt(v) / sqrt(1-b2^t) + eps))
@@ -239,7 +270,8 @@ int dp_clip_coef(const dp_plan* plan, void* workspace, double max_norm, int32_t 
  */
 int dp_sharded_adamw_step(const dp_plan* plan, void* workspace, const float* grad, float* master,
                           float* m, float* v, void* params, const dp_adamw_cfg* cfg,
-                          int32_t use_clip_coef, int32_t b0, int32_t b1, void* stream);
+                          int32_t use_clip_coef, const float* coef_dev, int32_t b0, int32_t b1,
+                          void* stream);
 
 /*
  * All-gather, in place ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
@@ -294,11 +326,11 @@ int dp_fused_zero_step(const dp_plan* plan, void* workspace, const void* grads, 
  * reduce-scatters (e.g. from a tracker) and dp_clip_coef.
  *   mean     fp32 [L] (input: the reduce-scatter mean of every bucket)
  *   master, m, v fp32 [L] (in/out);  params bf16 [P][replica_stride] (out)
- *   use_clip_coef  non-zero: multiply by the workspace's clip coefficient.
+ *   use_clip_coef, coef_dev  the clip coefficient (see above dp_sharded_adamw_step).
  */
 int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean, float* master,
                         float* m, float* v, void* params, const dp_adamw_cfg* cfg,
-                        int32_t use_clip_coef, void* stream);
+                        int32_t use_clip_coef, const float* coef_dev, void* stream);
 
 /*
  * ZeRO-3 / FULL_SHARD unit flow ("Data Parallelism: DDP, ZeRO and FSDP", "How
@@ -318,7 +350,8 @@ int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean,
  *   reduced in ring order to the fp32 mean of each owner's shard:
  *   mean[offset_unit + i]; want_sumsq also stores the unit's norm partials.
  * dp_shard_adamw_step: AdamW over all buckets on mean (times the clip
- *   coefficient if use_clip_coef), writing bf16(theta) to param_shards.
+ *   coefficient chosen by use_clip_coef / coef_dev, as for dp_sharded_adamw_step),
+ *   writing bf16(theta) to param_shards.
  */
 int dp_unit_all_gather(const dp_plan* plan, void* workspace, const void* param_shards, int32_t unit,
                        void* unit_buf, int64_t unit_stride, void* stream);
@@ -327,7 +360,7 @@ int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* uni
                            void* stream);
 int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean, float* master,
                         float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
-                        int32_t use_clip_coef, void* stream);
+                        int32_t use_clip_coef, const float* coef_dev, void* stream);
 
 /*
  * Gradient accumulation ("Distributed Training: Data Parallel, Model Parallel and
@@ -429,6 +462,10 @@ int64_t dp_bounds_violations(int32_t reset);
  */
 int dp_set_adamw_cfg(const dp_plan* plan, void* workspace, const dp_adamw_cfg* cfg, void* stream);
 
+/* offsets[0..3] = DP_WS_NORM2_OFFSET, DP_WS_NORM_OFFSET, DP_WS_COEF_OFFSET,
+ * DP_WS_STATUS_OFFSET as the library was built (host only; DP_EINVAL on NULL). */
+int dp_workspace_result_offsets(int64_t* offsets);
+
 /* Number of kernel launches dp_fused_zero_step makes for cfg (1 or 3). */
 int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
 
@@ -444,9 +481,15 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  * A tracker belongs to one plan and one set of buffers.  Each step: begin, then
  * mark every tensor ready (from any host thread) as its gradient is written,
  * passing a CUDA event recorded after that write (or NULL when the write is
- * already ordered before comm_stream's work).  When bucket b and every bucket
- * before it in plan order are complete, the tracker makes comm_stream wait for
- * the bucket's events and launches the bucket's reduction there:
+ * already ordered before comm_stream's work); dp_tracker_mark_ready_batch marks
+ * many tensors, each with its own event, in one call, and
+ * dp_tracker_mark_ready_range a run of tensors (e.g. one layer's) with one event.
+ * When bucket b and every bucket before it in plan order are complete, the
+ * tracker makes comm_stream wait once for each distinct event of the bucket's
+ * tensors and launches the bucket's reduction there.  Consecutive complete
+ * buckets whose tensors all carry the same event (or none) become ready together
+ * and go out as one launch over their tiles (the same results as one launch per
+ * bucket); a bucket whose tensors carry different events goes out on its own:
  *   DP_TRACK_ALLREDUCE       the in-place mean all-reduce of `grads`;
  *   DP_TRACK_REDUCE_SCATTER  the reduce-scatter mean into `mean` with norm
  *                            partials (follow with dp_clip_coef and
@@ -500,6 +543,20 @@ int dp_tracker_set_zero_step(dp_tracker* tracker, void* params, float* master, f
                              const dp_adamw_cfg* cfg);
 int dp_tracker_begin(dp_tracker* tracker);
 int dp_tracker_mark_ready(dp_tracker* tracker, int32_t tensor, void* ready_event);
+/* Tensors [t0, t1) ready, all written before ready_event: one call, one event.
+ * DP_EINVAL for a range outside [0, n_tensors) or a tensor already marked in
+ * this step (then nothing is marked). */
+int dp_tracker_mark_ready_range(dp_tracker* tracker, int32_t t0, int32_t t1, void* ready_event);
+/* tensors[0..n) ready, tensor[i] written before ready_events[i] (ready_events NULL:
+ * no events): the per-tensor marks of dp_tracker_mark_ready in one call.
+ * DP_EINVAL for a tensor out of range, already marked, or listed twice (then
+ * nothing is marked). */
+int dp_tracker_mark_ready_batch(dp_tracker* tracker, const int32_t* tensors,
+                                void* const* ready_events, int32_t n);
+/* This step so far: kernel launches made and cudaStreamWaitEvent calls issued
+ * (with DP_TRACK_DRY_RUN: those that would have been; either pointer may be
+ * NULL). */
+int dp_tracker_stats(const dp_tracker* tracker, int32_t* launches, int32_t* waits);
 int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms);
 /* Buckets launched so far this step, in launch order (up to cap entries). */
 int dp_tracker_fired(const dp_tracker* tracker, int32_t* order, int32_t cap, int32_t* n_fired);
@@ -530,6 +587,10 @@ int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float
  *   max_norm  clip threshold (<= 0: coef = 1)
  *   coef_out  device float (output): min(1, max_norm / (norm + 1e-6))
  *   norm_out  device double (output): the global L2 norm of the mean
+ * The status bits the kernels set stay in the library's array, where the caller
+ * cannot read them: a non-finite gradient norm still returns DP_OK, with
+ * *norm_out inf or NaN and *coef_out NaN (1 when max_norm <= 0), so a caller
+ * checks *norm_out itself.
  * Every call shares the array and overwrites it; calls whose work overlaps on
  * the GPU (unordered streams, concurrent host threads) race and must be
  * serialised.  The first call on a device looks up the array's address; make
@@ -541,7 +602,7 @@ int dp_clip_coef_noalloc(const dp_plan* plan, const void* grads, float* mean, do
 /* Thread-local text of the last error on this thread ("" if none). */
 const char* dp_last_error(void);
 
-/* ABI version of this header (increments on incompatible change). */
+/* ABI version of this header (increments on incompatible change): 2. */
 int dp_version(void);
 
 #ifdef __cplusplus

@@ -35,6 +35,13 @@ int main(void) {
   dp_plan* bad = NULL;
   const int rc = dp_plan_buckets(sizes, decay, 3, 64 * 1024, 0, &bad);
   printf("%d %d\n", rc == DP_EINVAL, bad == NULL);
+  /* the workspace's result fields: the header's offsets, then the library's */
+  int64_t offs[4] = {-1, -1, -1, -1};
+  if (dp_workspace_result_offsets(offs) != DP_OK) return 5;
+  printf("%d %d %d %d\n", DP_WS_NORM2_OFFSET, DP_WS_NORM_OFFSET, DP_WS_COEF_OFFSET,
+         DP_WS_STATUS_OFFSET);
+  printf("%lld %lld %lld %lld\n", (long long)offs[0], (long long)offs[1], (long long)offs[2],
+         (long long)offs[3]);
   dp_plan_free(plan);
   return 0;
 }

@@ -71,7 +71,7 @@ def check_plan_invariants(sizes, cap_bytes, P, p):
     nb = p["n_buckets"]
     assert len(p["b_off"]) == nb
     off = 0
-    for b in range(nb):                       # contiguous, padded to 8P
+    for b in range(nb):                       # contiguous, padded to 16P
         assert p["b_off"][b] == off
         assert p["b_len"][b] % q == 0
         off += p["b_len"][b]

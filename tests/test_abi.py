@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
     lib = C.CDLL(dps.LIB_PATH)
     missing = [s for s in syms if not hasattr(lib, s)]
     assert not missing, missing
-    assert dps.dp_version() == 1
+    assert dps.dp_version() == 2
 
 
 def test_declared_entry_points_are_bound():
@@ -151,9 +151,19 @@ def test_compute_calls_validate_before_any_device_work():
     assert lib.dp_fused_zero_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), None,
                                   None) == dps.DP_EINVAL
     cfg = dps.adamw_cfg(beta1=1.0)
-    assert lib.dp_sharded_adamw_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), 0, 0, nb,
-                                     None) == dps.DP_EINVAL
+    assert lib.dp_sharded_adamw_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), 0, None, 0,
+                                     nb, None) == dps.DP_EINVAL
     assert "range" in lib.dp_last_error().decode() or lib.dp_last_error()
+    # a caller-given clip coefficient: only with use_clip_coef, 4-byte aligned
+    cfg = dps.adamw_cfg()
+    coef, coef_odd = C.c_void_p(1 << 22), C.c_void_p((1 << 22) + 2)
+    assert lib.dp_sharded_adamw_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), 0, coef, 0,
+                                     nb, None) == dps.DP_EINVAL
+    assert "use_clip_coef" in lib.dp_last_error().decode()
+    assert lib.dp_adamw_all_gather(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), 1, coef_odd,
+                                   None) == dps.DP_EALIGN
+    assert lib.dp_shard_adamw_step(p.handle, ws, ok, ok, ok, ok, ok, C.byref(cfg), 0, coef,
+                                   None) == dps.DP_EINVAL
 
 
 def test_launch_counts():
@@ -171,6 +181,15 @@ def test_empty_plan_accepts_null_pointers():
     assert lib.dp_all_gather(p.handle, ws, None, 0, 0, None) == dps.DP_OK
 
 
+NOALLOC_BYTES = 32 << 20
+
+
+def noalloc_need(plan):
+    """Bytes of the no-alloc call's static array a plan uses: the workspace
+    without its fp32 stage [L] (device tables and per-tile norm partials)."""
+    return plan.info.workspace_bytes - (-(-4 * plan.L // 256) * 256)
+
+
 def test_noalloc_refuses_oversized_plans_on_the_host():
     """dp_clip_coef_noalloc checks the static array's size before any device work."""
     lib = dps.lib()
@@ -180,8 +199,38 @@ def test_noalloc_refuses_oversized_plans_on_the_host():
     assert rc == dps.DP_EINVAL
     msg = lib.dp_last_error().decode()
     assert "static array holds 33554432 bytes" in msg
+    assert f"the plan needs {noalloc_need(plan)} bytes" in msg
     assert lib.dp_clip_coef_noalloc(plan.handle, ok, ok, C.c_double(1.0), None, ok,
                                     None) == dps.DP_EINVAL
+
+
+def test_noalloc_size_limit_at_the_boundary():
+    """The bench's 1.1B-parameter plan fits the static array, the 2.65B plan does
+    not, and a one-tensor plan one tile past the largest that fits is refused
+    (the calls that would pass the check are not made: they would launch)."""
+    lib = dps.lib()
+    ok = C.c_void_p(1 << 21)
+    llama = configs.llama_1b1_zero2()
+    assert noalloc_need(dps.Plan(llama.sizes, llama.bucket_bytes, llama.P)) <= NOALLOC_BYTES
+    big = configs.gpt_2b5_clip()
+    p_big = dps.Plan(big.sizes, big.bucket_bytes, big.P)
+    assert noalloc_need(p_big) > NOALLOC_BYTES
+    assert lib.dp_clip_coef_noalloc(p_big.handle, ok, ok, C.c_double(1.0), ok, ok,
+                                    None) == dps.DP_EINVAL
+    tile = 8192
+    lo, hi = 1, 1 << 20                   # in tiles of one tensor
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if noalloc_need(dps.Plan([mid * tile], 1 << 40, 2)) <= NOALLOC_BYTES:
+            lo = mid
+        else:
+            hi = mid
+    fits, over = dps.Plan([lo * tile], 1 << 40, 2), dps.Plan([hi * tile], 1 << 40, 2)
+    assert noalloc_need(fits) <= NOALLOC_BYTES < noalloc_need(over)
+    assert 1.5e9 < lo * tile < 1.7e9                       # "about 1.6e9 parameters"
+    assert lib.dp_clip_coef_noalloc(over.handle, ok, ok, C.c_double(1.0), ok, ok,
+                                    None) == dps.DP_EINVAL
+    assert f"the plan needs {noalloc_need(over)} bytes" in lib.dp_last_error().decode()
 
 
 @pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (8, 1), (1, 8), (3, 2)])

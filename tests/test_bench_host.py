@@ -135,3 +135,17 @@ def test_oracle_allreduce_rate_on_host_buffers():
     _, _, _, _, desc2 = bench.oracle_allreduce_rate(wl, plan.tensor_offsets(), grads,
                                                     budget_s=1e9, max_passes=2)
     assert desc2.startswith("2 pass(es)")
+
+
+def test_layer_groups_cover_every_tensor_once():
+    """--streamed --mark layer: one mark per layer, tensors in order, none lost."""
+    import bench
+    from workloads import configs
+    for wl, n_groups in ((configs.gpt2_small_allreduce(), 16), (configs.llama_1b1_zero2(), 25)):
+        g = bench.layer_groups(wl.names)
+        assert len(g) == n_groups
+        assert g[0][0] == 0 and g[-1][1] == len(wl.names)
+        assert all(a[1] == b[0] for a, b in zip(g, g[1:]))
+        for g0, g1 in g:
+            keys = {".".join(n.split(".")[:2]) for n in wl.names[g0:g1]}
+            assert len(keys) == 1

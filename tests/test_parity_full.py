@@ -4,10 +4,12 @@ all buckets).
 
 * GPT-2 small all-reduce (P=8, 124M): every element of every replica.
 * Llama 1.1B and GPT 2.5B fused ZeRO-2 with clipping (P=8), and the P=16 sweep
-  at 64 KiB and 256 MiB buckets: the oracle streams every bucket's input bytes
-  (copied back from the device before the step) to form the global clip norm,
-  then recomputes sampled buckets (first, middle, last, plus random ones)
-  element by element.
+  at 64 KiB and 256 MiB buckets, three steps each with fresh gradients: at every
+  step the oracle streams every bucket's input bytes (copied back from the
+  device) to form the global clip norm, then recomputes sampled buckets (first,
+  middle, last, random ones, and those holding the flat indices where a 32-bit
+  byte or element offset would wrap) element by element, carrying their
+  master, m and v on its own from step to step.
 """
 import math
 
@@ -60,7 +62,30 @@ def test_gpt2_small_allreduce_full(orc):
     assert_replicas_equal(grads, plan.L)
 
 
-def zero_clip_sampled(orc, wl, n_random=2, batch=16):
+def boundary_buckets(op, boundaries):
+    """Buckets holding the elements just below and at each flat index in
+    `boundaries` (those inside [0, L)): where 32-bit byte or element offsets
+    would wrap."""
+    b_off, b_len = op["b_off"], op["b_len"]
+    out = set()
+    for x in boundaries:
+        for e in (x - 1, x):
+            if 0 <= e < op["L"]:
+                out.add(int(np.searchsorted(b_off, e, side="right") - 1))
+    return out
+
+
+# flat indices where a 32-bit offset would wrap: fp32 byte offset 2^31 and 2^32,
+# bf16 byte offset 2^32 (element 2^31), and element 2^31 itself
+WRAP_POINTS = (1 << 29, 1 << 30, 1 << 31)
+
+
+def zero_clip_sampled(orc, wl, n_random=2, batch=16, steps=3):
+    """`steps` clipped ZeRO-2 steps over the whole plan, fresh gradients from
+    (seed, step, rank) every step.  The oracle carries master, m and v of the
+    sampled buckets from step to step on its own (each owner's optimizer state
+    persists across steps), and recomputes the global clip norm from every
+    bucket's input bytes at every step."""
     plan, off, ws, grads = setup(wl)
     master = plan.new_state()
     wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
@@ -69,59 +94,72 @@ def zero_clip_sampled(orc, wl, n_random=2, batch=16):
     nb = op["n_buckets"]
     assert nb == plan.n_buckets
     rng = np.random.default_rng(wl.seed)
-    sample = sorted(set([0, nb // 2, nb - 1] + rng.integers(0, nb, n_random).tolist()))
-    # inputs of the sampled buckets, copied before the step
-    keep = {}
+    sample = sorted(set([0, nb // 2, nb - 1] + rng.integers(0, nb, n_random).tolist())
+                    | boundary_buckets(op, WRAP_POINTS))
+    # the oracle's optimizer state of the sampled buckets: master from the
+    # generator (copied before the first step), m = v = 0
+    state = {}
     for b in sample:
         tb = bucket_tensors(op, b)
-        keep[b] = (tb, host_grads(grads, off, wl.sizes, tb), host_flat(master, off, wl.sizes, tb))
-    # oracle's global norm: every bucket's input bytes, streamed in batches
-    sums = []
-    for b0 in range(0, nb, batch):
-        tb = sorted(t for b in range(b0, min(nb, b0 + batch)) for t in bucket_tensors(op, b))
-        sub = [wl.sizes[t] for t in tb]
-        sums.extend(orc.bucket_sumsq(sub, wl.bucket_bytes, wl.P,
-                                     host_grads(grads, off, wl.sizes, tb)).tolist())
-    assert len(sums) == nb
-    coef_ref, norm_ref = orc.clip_coef(sums, wl.adamw.max_norm)
-    total = orc.sum(sums)
+        mb = host_flat(master, off, wl.sizes, tb)
+        state[b] = [mb, np.zeros_like(mb), np.zeros_like(mb)]
     a = wl.adamw
-    dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v,
-                           dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay,
-                                         a.max_norm, 1))
-    norm, coef, status = dps.dp_read_norm(plan, ws)
-    assert status == 0
-    assert math.isclose(norm, norm_ref, rel_tol=1e-10), (norm, norm_ref)
-    assert coef == coef_ref, (coef, coef_ref)
-    cfg = oracle_mod.adamw_cfg(a, 1)
-    for b in sample:
-        tb, g_b, m_b = keep[b]
-        sub = [wl.sizes[t] for t in tb]
-        dec = [wl.decay[t] for t in tb]
-        z = np.zeros_like(m_b)
-        p_ref, m_ref, mm_ref, v_ref, _, st = orc.zero_step(sub, dec, wl.bucket_bytes, wl.P, g_b,
-                                                           m_b, z, z, cfg, sumsq_total=total)
-        assert st.n_buckets == 1 and st.replicas_equal == 1
-        for name, dev, ref in (("master", master, m_ref), ("m", m, mm_ref), ("v", v, v_ref)):
-            got = host_flat(dev, off, wl.sizes, tb)
-            e = rel_err(got, ref)
-            assert np.all(e <= 1e-5), f"bucket {b} {name}: max rel err {e.max():.3g}"
-            assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"{b} {name} bits"
-        got_p = host_grads(params, off, wl.sizes, tb)
-        assert np.all(bf16_ulp_diff(got_p, p_ref) <= 1), f"bucket {b} params"
-        assert np.array_equal(got_p, p_ref), f"bucket {b} params bits"
-    assert_replicas_equal(params, plan.L)
-    return coef
+    coefs = []
+    for t in range(1, steps + 1):
+        if t > 1:
+            wdev.fill_grads(grads, off, wl, step=t)
+        keep = {b: host_grads(grads, off, wl.sizes, bucket_tensors(op, b)) for b in sample}
+        # oracle's global norm: every bucket's input bytes, streamed in batches
+        sums = []
+        for b0 in range(0, nb, batch):
+            tb = sorted(x for b in range(b0, min(nb, b0 + batch)) for x in bucket_tensors(op, b))
+            sub = [wl.sizes[x] for x in tb]
+            sums.extend(orc.bucket_sumsq(sub, wl.bucket_bytes, wl.P,
+                                         host_grads(grads, off, wl.sizes, tb)).tolist())
+        assert len(sums) == nb
+        coef_ref, norm_ref = orc.clip_coef(sums, a.max_norm)
+        total = orc.sum(sums)
+        dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v,
+                               dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay,
+                                             a.max_norm, t))
+        norm, coef, status = dps.dp_read_norm(plan, ws)
+        assert status == 0
+        assert math.isclose(norm, norm_ref, rel_tol=1e-10), (t, norm, norm_ref)
+        assert coef == coef_ref, (t, coef, coef_ref)
+        coefs.append(coef)
+        cfg = oracle_mod.adamw_cfg(a, t)
+        for b in sample:
+            tb = bucket_tensors(op, b)
+            sub = [wl.sizes[x] for x in tb]
+            dec = [wl.decay[x] for x in tb]
+            p_ref, m_ref, mm_ref, v_ref, _, st = orc.zero_step(sub, dec, wl.bucket_bytes, wl.P,
+                                                               keep[b], *state[b], cfg,
+                                                               sumsq_total=total)
+            assert st.n_buckets == 1 and st.replicas_equal == 1
+            for name, dev, ref in (("master", master, m_ref), ("m", m, mm_ref), ("v", v, v_ref)):
+                got = host_flat(dev, off, wl.sizes, tb)
+                e = rel_err(got, ref)
+                assert np.all(e <= 1e-5), f"step {t} bucket {b} {name}: max rel err {e.max():.3g}"
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
+                    f"step {t} bucket {b} {name} bits"
+            got_p = host_grads(params, off, wl.sizes, tb)
+            assert np.all(bf16_ulp_diff(got_p, p_ref) <= 1), f"step {t} bucket {b} params"
+            assert np.array_equal(got_p, p_ref), f"step {t} bucket {b} params bits"
+            state[b] = [m_ref, mm_ref, v_ref]     # the oracle's own state, carried on
+        assert_replicas_equal(params, plan.L)
+    return coefs
 
 
 def test_llama_1b1_zero2_clip_sampled(orc):
-    coef = zero_clip_sampled(orc, configs.llama_1b1_zero2())
-    assert coef < 1.0          # ||mean|| ~ 5.9: the clip is active
+    coefs = zero_clip_sampled(orc, configs.llama_1b1_zero2())
+    assert all(c < 1.0 for c in coefs)          # ||mean|| ~ 5.9: the clip is active
 
 
 def test_gpt_2b5_zero2_clip_sampled(orc):
-    coef = zero_clip_sampled(orc, configs.gpt_2b5_clip(), batch=8)
-    assert 0.2 < coef < 0.3    # ||mean|| ~ 4
+    wl = configs.gpt_2b5_clip()
+    assert wl.n_params > (1 << 31)              # buckets beyond element 2^31 are sampled
+    coefs = zero_clip_sampled(orc, wl, batch=8)
+    assert all(0.2 < c < 0.3 for c in coefs)    # ||mean|| ~ 4
 
 
 @pytest.mark.parametrize("cap", [64 * 1024, 256 << 20])

@@ -188,6 +188,44 @@ def test_staged_clip_equals_fused_clip():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("P", [4, 8])
+def test_caller_given_clip_coefficient_matches_oracle(orc, P):
+    """An update given the caller's own clip coefficient (coef_dev) uses it, not
+    the workspace's: the workspace holds the coefficient for max_norm 1.0, the
+    caller's device float is the oracle's for max_norm 0.3 on the same
+    gradients, and the result equals the oracle's step at max_norm 0.3, bit for
+    bit, over three steps, through dp_sharded_adamw_step + dp_all_gather and
+    through dp_adamw_all_gather."""
+    c = case_for("ragged", P, sigma=0.05, decay=[1, 0, 1, 1, 0, 1, 1])
+    adamw_ws = configs.AdamW(max_norm=1.0)
+    adamw_own = configs.AdamW(max_norm=0.3)
+    master0 = c.host_master()
+    grads = [c.host_grads(s) for s in (1, 2, 3)]
+    ref = run_oracle_steps(orc, c, grads, master0, [ocfg(adamw_own, s) for s in (1, 2, 3)])
+    pa, pb = c.plan.new_replicas(), c.plan.new_replicas()
+    sa = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    sb = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+    mean = c.plan.new_state()
+    coef_dev = torch.empty(1, dtype=torch.float32, device="cuda")
+    for s, g in zip((1, 2, 3), grads):
+        sums = orc.bucket_sumsq(c.sizes, c.wl.bucket_bytes, P, g)
+        own, _ = orc.clip_coef(sums, adamw_own.max_norm)
+        coef_dev.fill_(own)
+        dps.dp_reduce_scatter_mean(c.plan, c.ws, c.to_replicas(g), mean, want_sumsq=True)
+        dps.dp_clip_coef(c.plan, c.ws, adamw_ws.max_norm)
+        dps.dp_sharded_adamw_step(c.plan, c.ws, mean, *sa, pa, dcfg(adamw_own, s),
+                                  use_clip_coef=True, coef_dev=coef_dev)
+        dps.dp_all_gather(c.plan, c.ws, pa)
+        dps.dp_adamw_all_gather(c.plan, c.ws, mean, *sb, pb, dcfg(adamw_own, s),
+                                use_clip_coef=True, coef_dev=coef_dev)
+        _, ws_coef, status = dps.dp_read_norm(c.plan, c.ws)
+        assert status == 0
+        ost = ref[s - 1][4]
+        assert own == ost.coef < ws_coef < 1.0          # both clip, differently
+        check_state(c, pa, sa, ref[s - 1], exact=True)
+        check_state(c, pb, sb, ref[s - 1], exact=True)
+
+
 @pytest.mark.parametrize("P", [3, 8])
 def test_chained_per_bucket_launches_match_oracle(orc, P):
     """Hundreds of tiny launches back to back, each reading what the launch just
@@ -302,6 +340,57 @@ def test_plan_mismatch_is_refused():
         dps.dp_read_norm(b.plan, a.ws)
     assert e.value.code == dps.DP_EPLAN
     assert torch.equal(g, before)
+
+
+@pytest.mark.parametrize("P", [4, 16])
+def test_plan_mismatch_is_refused_by_small_per_bucket_launches(P):
+    """Per-bucket launches over a few tiles (the kernels that check the plan beside
+    their first loads) store nothing when the workspace holds another plan's
+    image: all-reduce, reduce-scatter with and without norm partials."""
+    a = case_for("ragged", P)
+    b = case_for("ragged", P)
+    assert b.plan.n_buckets >= 2
+    g = a.to_replicas(a.host_grads(1))
+    before = g.clone()
+    mean = torch.full((b.plan.L,), 3.0, dtype=torch.float32, device="cuda")
+    for k in range(b.plan.n_buckets):
+        dps.dp_allreduce_mean(b.plan, a.ws, g, k, k + 1)
+        dps.dp_reduce_scatter_mean(b.plan, a.ws, g, mean, k, k + 1)
+        dps.dp_reduce_scatter_mean(b.plan, a.ws, g, mean, k, k + 1, want_sumsq=True)
+    with pytest.raises(dps.DPError) as e:
+        dps.dp_read_norm(b.plan, a.ws)
+    assert e.value.code == dps.DP_EPLAN
+    assert torch.equal(g, before)
+    assert bool((mean == 3.0).all())
+
+
+@pytest.mark.parametrize("P", [3, 8, 16])
+def test_small_per_bucket_launches_equal_the_oracle(orc, P):
+    """Per-bucket launches of small buckets (tile descriptors from the launch's
+    parameters, the plan checked beside the loads, every replica block loaded at
+    once): the all-reduce and the reduce-scatter with norm partials equal the
+    oracle bit for bit, and the norm from per-bucket partials equals the one
+    from a single launch."""
+    c = case_for("ragged", P, cap=16 * 1024, sigma=0.05)
+    assert c.plan.n_buckets >= 5
+    g = c.host_grads(1)
+    dev = c.to_replicas(g)
+    mean = c.plan.new_state()
+    for k in reversed(range(c.plan.n_buckets)):
+        dps.dp_reduce_scatter_mean(c.plan, c.ws, dev, mean, k, k + 1, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 1.0)
+    norm_pb, coef_pb, st = dps.dp_read_norm(c.plan, c.ws)
+    want_ar, want_mean, _ = orc.allreduce_mean(c.sizes, c.wl.bucket_bytes, P, g)
+    got = c.from_flat(mean)
+    assert np.array_equal(got.view(np.uint32), want_mean.view(np.uint32))
+    dps.dp_reduce_scatter_mean(c.plan, c.ws, dev, mean, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 1.0)
+    assert dps.dp_read_norm(c.plan, c.ws)[:2] == (norm_pb, coef_pb)
+    for k in range(c.plan.n_buckets):
+        dps.dp_allreduce_mean(c.plan, c.ws, dev, k, k + 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.from_replicas(dev), want_ar)
+    assert_replicas_equal(dev, c.plan.L)
 
 
 def test_nonfinite_gradient_is_reported(orc):

@@ -53,6 +53,67 @@ def test_streamed_allreduce_equals_oracle(orc, P, max_ctas):
         del keep
 
 
+@pytest.mark.parametrize("mode", ["allreduce", "zero_step"])
+def test_range_marks_fire_bucket_ranges_that_equal_the_oracle(orc, mode):
+    """A producer that marks several tensors with one event (dp_tracker_mark_ready_range,
+    groups of three in backward order) completes several buckets per mark; each
+    such group is one launch over the buckets' tiles, after one stream wait.  The
+    result equals the oracle bit for bit, for the all-reduce and for the whole
+    unclipped ZeRO step per range."""
+    import oracle as oracle_mod
+    P = 4
+    sizes = [3, 1000, 65536, 13107, 26214, 4097, 27910, 9000, 700, 12000, 5, 31000]
+    wl = small_workload(sizes, P, 16 * 1024, seed=90)
+    c = Case(wl)
+    g = c.host_grads(1)
+    src = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).cuda()
+    base = wdev.tensor_bases(c.sizes)
+    grads = c.plan.new_replicas()
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    zero = mode == "zero_step"
+    tr = dps.Tracker(c.plan, dps.DP_TRACK_ZERO_STEP if zero else dps.DP_TRACK_ALLREDUCE, c.ws,
+                     grads, stream=comm)
+    adamw = configs.AdamW(max_norm=0.0)
+    if zero:
+        master0 = c.host_master()
+        params = c.plan.new_replicas()
+        st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+        cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
+                            adamw.max_norm, 1)
+        tr.set_zero_step(params, *st, cfg)
+    groups = [(t0, min(t0 + 3, len(sizes))) for t0 in range(0, len(sizes), 3)]
+    tr.begin()
+    events = []
+    with torch.cuda.stream(producer):
+        for t0, t1 in reversed(groups):
+            for t in reversed(range(t0, t1)):
+                o, n = c.off[t], c.sizes[t]
+                grads[:, o:o + n].copy_(src[:, base[t]:base[t] + n])
+            ev = torch.cuda.Event()
+            ev.record(producer)
+            events.append(ev)
+            tr.mark_ready_range(t0, t1, ev)
+    tr.wait(10000)
+    launches, waits = tr.stats()
+    assert tr.fired() == list(range(c.plan.n_buckets))
+    assert launches < c.plan.n_buckets            # some marks completed several buckets
+    assert waits <= len(groups)
+    torch.cuda.synchronize()
+    if zero:
+        z = np.zeros_like(master0)
+        p_ref, m_ref, mm_ref, v_ref, _, _ = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, P, g,
+                                                          master0, z, z,
+                                                          oracle_mod.adamw_cfg(adamw, 1))
+        assert np.array_equal(c.from_replicas(params), p_ref)
+        for dev, ref in zip(st, (m_ref, mm_ref, v_ref)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+    else:
+        want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+        assert np.array_equal(c.from_replicas(grads), want)
+        assert_replicas_equal(grads, c.plan.L)
+    del events
+
+
 def test_streamed_mesh_allreduce_equals_oracle(orc):
     """The tracker on a hybrid 2 x 4 plan fires the mesh all-reduce bucket by bucket."""
     P, R, S = 8, 2, 4

@@ -210,3 +210,110 @@ def test_set_zero_step_rules():
     tr.mark_ready(1)
     tr.mark_ready(0)
     assert lib.dp_tracker_set_zero_step(tr._h, ok, ok, ok, ok, C.byref(step2)) == dps.DP_OK
+
+
+class _Ev:
+    """Stands in for a torch.cuda.Event in dry runs (only its handle is passed)."""
+
+    def __init__(self, handle):
+        self.cuda_event = handle
+
+
+def test_range_mark_fires_completed_buckets_as_one_launch():
+    """One mark that completes several buckets fires them together, in plan order,
+    as one launch; its stream waits once per distinct event."""
+    sizes = [1000] * 8                                  # reverse packing: 4 buckets of 2
+    plan, tr = dry(sizes, 4000, 2)
+    assert plan.n_buckets == 4
+    tr.begin()
+    tr.mark_ready_range(4, 8, _Ev(0x1000))              # buckets 0 and 1 complete
+    assert tr.fired() == [0, 1]
+    assert tr.stats() == (1, 1)
+    tr.mark_ready_range(2, 4, _Ev(0x2000))              # bucket 2
+    assert tr.stats() == (2, 2)
+    tr.mark_ready(1, _Ev(0x3000))
+    tr.mark_ready(0, _Ev(0x4000))                       # bucket 3: two events, two waits
+    tr.wait(1000)
+    assert tr.fired() == [0, 1, 2, 3]
+    assert tr.stats() == (3, 4)
+    tr.begin()
+    assert tr.stats() == (0, 0)
+
+
+def test_range_mark_held_back_and_released_together():
+    """Buckets completed out of order are held, then fire in one launch when the
+    first of them completes."""
+    sizes = [1000] * 8
+    plan, tr = dry(sizes, 4000, 2)
+    tr.begin()
+    tr.mark_ready_range(0, 6)                           # buckets 1, 2, 3 complete; 0 is not
+    assert tr.fired() == [] and tr.stats() == (0, 0)
+    tr.mark_ready_range(6, 8)
+    assert tr.fired() == [0, 1, 2, 3] and tr.stats() == (1, 0)
+
+
+def test_range_mark_rejections_leave_nothing_marked():
+    sizes = [1000] * 8
+    plan, tr = dry(sizes, 4000, 2)
+    tr.begin()
+    tr.mark_ready(5)
+    with pytest.raises(dps.DPError) as e:
+        tr.mark_ready_range(4, 8)                       # tensor 5 already marked
+    assert e.value.code == dps.DP_EINVAL and "tensor 5" in str(e.value)
+    with pytest.raises(dps.DPError):
+        tr.mark_ready_range(6, 9)                       # outside [0, 8)
+    with pytest.raises(dps.DPError):
+        tr.mark_ready_range(3, 2)
+    tr.mark_ready_range(6, 8)                           # 4 and 7 were not marked by the refusals
+    tr.mark_ready(4)
+    assert tr.fired() == [0, 1]
+
+
+def test_batch_mark_keeps_per_tensor_events_apart():
+    """dp_tracker_mark_ready_batch: one call, each tensor its own event.  A bucket
+    whose tensors carry different events goes out alone (it must not wait for a
+    later bucket's readiness); buckets whose tensors share one event go out
+    together."""
+    sizes = [1000] * 8                                  # 4 buckets: {7,6} {5,4} {3,2} {1,0}
+    plan, tr = dry(sizes, 4000, 2)
+    tr.begin()
+    evs = [_Ev(0x100 * (t + 1)) for t in range(8)]
+    tr.mark_ready_batch([7, 6, 5, 4], [evs[t] for t in (7, 6, 5, 4)])
+    assert tr.fired() == [0, 1]
+    assert tr.stats() == (2, 4)                          # two launches, one wait per event
+    shared = _Ev(0x9000)
+    tr.mark_ready_batch([3, 2, 1, 0], [shared] * 4)     # both buckets: one event
+    assert tr.fired() == [0, 1, 2, 3]
+    assert tr.stats() == (3, 5)
+    tr.wait(1000)
+
+
+def test_batch_mark_rejections_leave_nothing_marked():
+    sizes = [1000] * 8
+    plan, tr = dry(sizes, 4000, 2)
+    tr.begin()
+    tr.mark_ready(2)
+    for bad in ([7, 6, 7], [7, 2], [7, 8], [-1]):
+        with pytest.raises(dps.DPError) as e:
+            tr.mark_ready_batch(bad)
+        assert e.value.code == dps.DP_EINVAL
+    tr.mark_ready_batch([7, 6])                         # none of them was left marked
+    assert tr.fired() == [0]
+    with pytest.raises(ValueError):
+        tr.mark_ready_batch([5, 4], [_Ev(1)])
+    tr.mark_ready_batch([5, 4, 3, 1, 0])
+    tr.wait(1000)
+    assert tr.fired() == [0, 1, 2, 3]
+
+
+def test_batch_refusal_messages():
+    sizes = [1000] * 4
+    plan, tr = dry(sizes, 4000, 2)
+    tr.begin()
+    with pytest.raises(dps.DPError, match="listed twice"):
+        tr.mark_ready_batch([1, 1])
+    tr.mark_ready(3)
+    with pytest.raises(dps.DPError, match="already marked"):
+        tr.mark_ready_batch([2, 3])
+    with pytest.raises(dps.DPError, match="outside"):
+        tr.mark_ready_batch([4])

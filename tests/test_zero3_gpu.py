@@ -13,7 +13,9 @@ from workloads import configs, device as wdev
 pytestmark = pytest.mark.gpu
 
 
-def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf):
+def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf, coef_dev=None, ws_max_norm=None):
+    """coef_dev: the update multiplies by the caller's own coefficient instead of
+    the workspace's (which dp_clip_coef still forms, at ws_max_norm)."""
     plan = c.plan
     nb = plan.n_buckets
     gathered = []
@@ -25,8 +27,9 @@ def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf):
         dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
         o, ln, _ = plan.bucket(b)
         dps.dp_unit_reduce_scatter(plan, c.ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
-    dps.dp_clip_coef(plan, c.ws, cfg.max_norm)
-    dps.dp_shard_adamw_step(plan, c.ws, mean, *st, shards, cfg, use_clip_coef=True)
+    dps.dp_clip_coef(plan, c.ws, cfg.max_norm if ws_max_norm is None else ws_max_norm)
+    dps.dp_shard_adamw_step(plan, c.ws, mean, *st, shards, cfg, use_clip_coef=True,
+                            coef_dev=coef_dev)
     return gathered
 
 
@@ -66,6 +69,46 @@ def test_zero3_flow_matches_oracle(orc, P):
         assert np.array_equal(u16(wdev.gather_flat(shards, c.off, c.sizes)), shards_h)
         for dev, ref in zip(st, (master, m, v)):
             assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+
+
+def test_zero3_shard_update_with_caller_coefficient(orc):
+    """dp_shard_adamw_step given the caller's coefficient (the oracle's at
+    max_norm 0.3) while the workspace holds the one for max_norm 1.0: the shards
+    and state equal the oracle's ZeRO-3 step at max_norm 0.3, bit for bit."""
+    P = 4
+    wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910], P, 64 * 1024, sigma=0.05,
+                        seed=34)
+    c = Case(wl)
+    own = configs.AdamW(max_norm=0.3)
+    master = c.host_master()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    shards_h = u16(torch.from_numpy(master).to(torch.bfloat16))
+    shards = c.plan.new_state().to(torch.bfloat16)
+    wdev.fill_flat(shards, c.off, c.sizes, torch.from_numpy(master).to(torch.bfloat16).cuda())
+    st = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    mean = c.plan.new_state()
+    max_len = max(c.plan.bucket(b)[1] for b in range(c.plan.n_buckets))
+    unit_buf = torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda")
+    coef_dev = torch.empty(1, dtype=torch.float32, device="cuda")
+    for step in (1, 2):
+        g = c.host_grads(step)
+        coef, _ = orc.clip_coef(orc.bucket_sumsq(c.sizes, wl.bucket_bytes, P, g), own.max_norm)
+        coef_dev.fill_(coef)
+        cfg = dps.adamw_cfg(own.lr, own.beta1, own.beta2, own.eps, own.weight_decay,
+                            own.max_norm, step)
+        zero3_flow(c, c.to_replicas(g), shards, mean, st, cfg, unit_buf, coef_dev=coef_dev,
+                   ws_max_norm=1.0)
+        shards_h, master, m, v, so = orc.zero3_step(c.sizes, c.decay, wl.bucket_bytes, P, g,
+                                                    shards_h, master, m, v,
+                                                    oracle_mod.adamw_cfg(own, step))
+        _, ws_coef, status = dps.dp_read_norm(c.plan, c.ws)
+        assert status == 0 and so.coef == coef < ws_coef < 1.0
+        got = u16(wdev.gather_flat(shards, c.off, c.sizes))
+        assert np.array_equal(got, shards_h)
+        for name, dev, ref in (("master", st[0], master), ("m", st[1], m), ("v", st[2], v)):
+            a = c.from_flat(dev)
+            assert np.array_equal(a.view(np.uint32), ref.view(np.uint32)), name
 
 
 def test_unit_all_gather_fills_every_rank_row():
