@@ -830,7 +830,8 @@ def run_zero3(args):
     nb, P = plan.n_buckets, plan.P
     buckets = [plan.bucket(b) for b in range(nb)]
     unit_buf = torch.empty(P, max(ln for _, ln, _ in buckets), dtype=torch.bfloat16, device="cuda")
-    unit_bufs = [unit_buf, torch.empty_like(unit_buf)] if args.prefetch else [unit_buf]
+    unit_bufs = [unit_buf, torch.empty_like(unit_buf)] if (args.prefetch or args.fused_backward) \
+        else [unit_buf]
     s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
     a = wl.adamw
     stream = torch.cuda.current_stream()
@@ -853,6 +854,15 @@ def run_zero3(args):
         cur.wait_stream(s_b)
 
     def backward():
+        if args.fused_backward:
+            # one launch per unit: the next unit's gather beside this unit's reduce-scatter
+            dps.dp_unit_all_gather(plan, ws, shards, 0, unit_bufs[0])
+            for b in range(nb):
+                o, ln, _ = buckets[b]
+                dps.dp_unit_backward(plan, ws, shards, b + 1 if b + 1 < nb else -1,
+                                     unit_bufs[(b + 1) % 2], grads[:, o:o + ln], b, mean,
+                                     want_sumsq=True)
+            return
         if not args.prefetch:
             for b in range(nb):
                 o, ln, _ = buckets[b]
@@ -942,7 +952,9 @@ def run_zero3(args):
         "config": {"workload": wl.name, "P": P, "n_units": nb,
                    "mesh": f"{plan.info.R}x{plan.info.S} (replicate x shard)",
                    "launch": ("CUDA graph of the whole step" if graph is not None else "host launches")
-                   + (", prefetch on two streams" if args.prefetch else "")},
+                   + (", prefetch on two streams" if args.prefetch and not args.fused_backward else "")
+                   + (", backward as one launch per unit (next unit's gather beside this unit's "
+                      "reduce-scatter)" if args.fused_backward else "")},
     }
 
 
@@ -1058,9 +1070,11 @@ def run_sweep(args):
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / reps
 
-    for cap in configs.SWEEP_BUCKETS:
-        for mode in ("allreduce", "zero"):
-            wl = configs.sweep_small_tensors(cap, mode)
+    caps = [int(c) for c in args.sweep_caps.split(",")] if args.sweep_caps else configs.SWEEP_BUCKETS
+    modes = args.sweep_modes.split(",")
+    for cap in caps:
+        for mode in modes:
+            wl = configs.sweep_small_tensors(cap, mode, args.sweep_groups)
             plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
             off = plan.tensor_offsets()
             ws = plan.new_workspace()
@@ -1142,10 +1156,9 @@ def run_sweep(args):
             torch.cuda.empty_cache()
     return {"metric": "bucket-size sweep: ms per step, single launch vs per-bucket launches",
             "unit": "ms", "rows": rows,
-            "config": {"workload": "sweep-P16 (6024 tensors)", "P": 16,
-                       "n_params": configs.sweep_small_tensors().n_params,
-                       "clip_max_norm": configs.sweep_small_tensors().adamw.max_norm,
-                       "l2": "inputs > L2 (7.5 GB per replica set)"}}
+            "config": {"workload": f"sweep-P16 ({len(wl.sizes)} tensors)", "P": 16,
+                       "n_params": wl.n_params, "clip_max_norm": wl.adamw.max_norm,
+                       "l2": f"inputs > L2 ({wl.n_params * 32 / 1e9:.1f} GB per replica set)"}}
 
 
 def run_kernels(args):
@@ -1310,12 +1323,21 @@ def main(argv=None):
                     help="override the workload's clip threshold (0 = no clipping: one fused pass)")
     ap.add_argument("--prefetch", action="store_true",
                     help="with --zero3: gather the next unit while the current one reduce-scatters")
+    ap.add_argument("--fused-backward", action="store_true",
+                    help="--zero3: the backward as dp_unit_backward launches (gather of the next "
+                         "unit and reduce-scatter of this one in one launch)")
     ap.add_argument("--graph", action="store_true",
                     help="with --zero3: replay the unit passes from a CUDA graph")
     ap.add_argument("--kernels", action="store_true",
                     help="time every entry point's kernel on the workload")
     ap.add_argument("--sweep", action="store_true",
                     help="bucket-size sweep: single launch vs per-bucket launches")
+    ap.add_argument("--sweep-caps", default="",
+                    help="--sweep: comma-separated bucket caps in bytes (default: the four caps)")
+    ap.add_argument("--sweep-modes", default="allreduce,zero",
+                    help="--sweep: allreduce, zero or both")
+    ap.add_argument("--sweep-groups", type=int, default=24,
+                    help="--sweep: groups of (matrix + 250 vectors) in the workload (24 = full)")
     ap.add_argument("--accum", type=int, default=0,
                     help="time k-micro-batch gradient accumulation and the bf16-wire ring")
     ap.add_argument("--streamed", action="store_true",

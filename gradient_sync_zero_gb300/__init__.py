@@ -89,6 +89,7 @@ def lib():
             "dp_unit_reduce_scatter": [vp, vp, vp, i64, i32, vp, i32, vp],
             "dp_shard_adamw_step": [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp],
             "dp_workspace_result_offsets": [vp],
+            "dp_unit_backward": [vp, vp, vp, i32, vp, i64, vp, i64, i32, vp, i32, vp],
             "dp_tracker_begin": [vp],
             "dp_tracker_set_micro": [vp, vp],
             "dp_tracker_mark_ready": [vp, i32, vp],
@@ -362,6 +363,32 @@ def dp_unit_reduce_scatter(plan, ws, unit_grads, unit, mean, want_sumsq=False, s
     _check(lib().dp_unit_reduce_scatter(plan.handle, _ws(plan, ws), _ptr(unit_grads),
                                         int(unit_grads.stride(0)), int(unit), _ptr(mean),
                                         1 if want_sumsq else 0, _stream(stream)))
+
+
+def dp_unit_backward(plan, ws, param_shards, gather_unit, gather_buf, unit_grads, rs_unit, mean,
+                     want_sumsq=False, stream=None):
+    """ZeRO-3 backward in one launch: gather unit `gather_unit` into gather_buf
+    [P][>= len] and reduce-scatter unit `rs_unit`'s gradients (unit_grads, a
+    [P][stride] view) into mean.  Either unit may be -1 (that part left out)."""
+    _need(param_shards, torch.bfloat16, plan.L, "param_shards")
+    gb, gstride = None, 0
+    if gather_unit >= 0:
+        if gather_buf.dim() != 2 or gather_buf.shape[0] < plan.P or not gather_buf.is_contiguous():
+            raise ValueError("gather_buf must be a contiguous [P][unit_stride] tensor")
+        _need(gather_buf, torch.bfloat16, plan.P * gather_buf.shape[1], "gather_buf")
+        gb, gstride = _ptr(gather_buf), int(gather_buf.shape[1])
+    ug, ustride = None, 0
+    if rs_unit >= 0:
+        if unit_grads.dim() != 2 or unit_grads.shape[0] < plan.P or unit_grads.stride(1) != 1:
+            raise ValueError("unit_grads must be a [P][stride] view with unit element stride")
+        if unit_grads.dtype != torch.bfloat16 or not unit_grads.is_cuda:
+            raise TypeError("unit_grads must be a CUDA bf16 tensor")
+        _need(mean, torch.float32, plan.L, "mean")
+        ug, ustride = _ptr(unit_grads), int(unit_grads.stride(0))
+    _check(lib().dp_unit_backward(plan.handle, _ws(plan, ws), _ptr(param_shards), int(gather_unit),
+                                  gb, gstride, ug, ustride, int(rs_unit),
+                                  _ptr(mean) if mean is not None else None,
+                                  1 if want_sumsq else 0, _stream(stream)))
 
 
 def dp_shard_adamw_step(plan, ws, mean, master, m, v, param_shards, cfg, use_clip_coef=False,

@@ -235,6 +235,51 @@ int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* uni
   return e ? cuda_fail(e, "dp_unit_reduce_scatter") : DP_OK;
 }
 
+int dp_unit_backward(const dp_plan* plan, void* workspace, const void* param_shards,
+                     int32_t gather_unit, void* gather_buf, int64_t gather_stride,
+                     const void* unit_grads, int64_t grads_stride, int32_t rs_unit, float* mean,
+                     int32_t want_sumsq, void* stream) {
+  const char* fn = "dp_unit_backward";
+  const Plan* pl = as_plan(plan);
+  const int32_t nb = pl ? static_cast<int32_t>(pl->b_off.size()) : 0;
+  if (pl && (gather_unit < -1 || gather_unit >= nb || rs_unit < -1 || rs_unit >= nb)) {
+    clear_error();
+    return fail(DP_EINVAL, std::string(fn) + ": unit outside [-1, " + std::to_string(nb) + ")");
+  }
+  if (gather_unit < 0 && rs_unit < 0) {
+    Launch L;
+    return prepare(fn, plan, workspace, 0, 0, stream, &L);
+  }
+  if (gather_unit < 0)
+    return dp_unit_reduce_scatter(plan, workspace, unit_grads, grads_stride, rs_unit, mean,
+                                  want_sumsq, stream);
+  if (rs_unit < 0)
+    return dp_unit_all_gather(plan, workspace, param_shards, gather_unit, gather_buf, gather_stride,
+                              stream);
+  Launch La, Lr;
+  int rc = prepare(fn, plan, workspace, gather_unit, gather_unit + 1, stream, &La);
+  if (rc) return rc;
+  if ((rc = prepare(fn, plan, workspace, rs_unit, rs_unit + 1, stream, &Lr))) return rc;
+  if ((rc = check_ptrs(fn, pl, {param_shards, gather_buf, unit_grads, mean}))) return rc;
+  if (gather_stride < pl->b_len[gather_unit] || gather_stride % 16 || grads_stride < pl->b_len[rs_unit] ||
+      grads_stride % 16)
+    return fail(DP_EINVAL, std::string(fn) +
+                               ": a stride is shorter than its unit or not a multiple of 16");
+  // the gather's destination must not overlap what the reduce-scatter reads or writes
+  const uintptr_t gb0 = reinterpret_cast<uintptr_t>(gather_buf);
+  const uintptr_t gb1 = gb0 + 2 * static_cast<uintptr_t>(pl->P) * static_cast<uintptr_t>(gather_stride);
+  const uintptr_t ug0 = reinterpret_cast<uintptr_t>(unit_grads);
+  const uintptr_t ug1 = ug0 + 2 * static_cast<uintptr_t>(pl->P) * static_cast<uintptr_t>(grads_stride);
+  const uintptr_t mn0 = reinterpret_cast<uintptr_t>(mean);
+  const uintptr_t mn1 = mn0 + 4 * static_cast<uintptr_t>(pl->L);
+  if ((gb0 < ug1 && ug0 < gb1) || (gb0 < mn1 && mn0 < gb1))
+    return fail(DP_EINVAL, std::string(fn) + ": gather_buf overlaps unit_grads or mean");
+  const int e = launch_unit_backward(Lr, unit_grads, mean, want_sumsq != 0, grads_stride,
+                                     pl->b_off[rs_unit] / kPairElems, La, param_shards, gather_buf,
+                                     gather_stride, pl->b_off[gather_unit] / kPairElems);
+  return e ? cuda_fail(e, fn) : DP_OK;
+}
+
 int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean, float* master,
                         float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
                         int32_t use_clip_coef, const float* coef_dev, void* stream) {

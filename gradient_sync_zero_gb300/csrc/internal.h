@@ -12,6 +12,11 @@
 namespace dps {
 
 constexpr int kThreads = 256;                 // threads per CTA
+// Launches inside one bucket over few tiles: CTAs of kSmallThreads threads,
+// kSmallSplit per tile, so one thread moves one 32-byte block and the launch's
+// loads and stores are spread over kSmallSplit times more SMs.
+constexpr int kSmallThreads = 64;
+constexpr int kSmallSplit = 8;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecElems = 8;                  // bf16 elements per 16-byte vector
 constexpr int kPairElems = 16;                // bf16 elements per 32-byte (256-bit) access
@@ -116,6 +121,11 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
                           int64_t rep_stride = 0, int64_t rep_block0 = 0);
 int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64_t out_stride,
                            int64_t block0);
+// One launch: the reduce-scatter of Lrs's unit (replicas at rep_stride, first
+// block rep_block0) and the gather of Lag's unit into out (both non-empty).
+int launch_unit_backward(const Launch& Lrs, const void* grads, float* mean, bool sumsq,
+                         int64_t rep_stride, int64_t rep_block0, const Launch& Lag,
+                         const void* shards, void* out, int64_t out_stride, int64_t block0);
 int launch_allreduce(const Launch& L, void* grads);
 int launch_accumulate(const Launch& L, void* acc, const void* micro);
 int launch_selftest_wait(int32_t* status, uint64_t limit_ns, void* stream);

@@ -38,7 +38,7 @@ struct KCommon {
   int32_t R;             // mesh: replicate groups (1 = flat ring)
   int32_t S;             // mesh: shard ranks per group (P = R * S)
   int64_t rep_block0;    // replica buffers start at this 32-byte block (unit buffers)
-  int32_t split;         // CTAs per tile (1, or 2 for launches with few tiles)
+  int32_t split;         // CTAs per tile (1; 2 or kSmallSplit for launches with few tiles)
   int32_t pad_;
   // A launch inside one bucket carries that bucket in its parameters, so its
   // tile descriptors are computed, not loaded (one dependent load fewer per
@@ -674,11 +674,12 @@ __device__ __forceinline__ int owner_of(const TileDesc& d, int64_t v) {
 
 // Loop over the 32-byte blocks of the CTA's tiles: f(tile, block index b,
 // owner c).  Tiles start at even 16-byte vectors and hold an even count.  With
-// k.split = 2 (launches over few tiles) two CTAs share each tile, alternating
-// runs of kThreads blocks, so every thread of a small launch moves one block.
-template <bool SPLIT = true, class F>
+// k.split = s > 1 (launches over few tiles) s CTAs share each tile, taking
+// turns at runs of NT blocks (NT = threads per CTA), so every thread of a small
+// launch moves one block.
+template <bool SPLIT = true, int NT = kThreads, class F>
 __device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
-  // the common case (split 1) keeps constant strides; split 2 is for small launches
+  // the common case (split 1) keeps constant strides; splits are for small launches
   // (SPLIT = false: a kernel always launched unsplit compiles the first walk only)
   auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
     for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
@@ -696,18 +697,18 @@ __device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
     }
   };
   if (!SPLIT || k.split == 1) {
-    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, kThreads);
+    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, NT);
   } else {
-    const int64_t cta_tile = blockIdx.x / 2;
-    walk(k.tile_begin + cta_tile, gridDim.x / 2,
-         static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
+    const int64_t cta_tile = blockIdx.x / k.split;
+    walk(k.tile_begin + cta_tile, gridDim.x / k.split,
+         static_cast<int>(blockIdx.x - k.split * cta_tile) * NT + threadIdx.x, k.split * NT);
   }
 }
 
 // Same loop, giving the body the tile descriptor: f(desc, block b, owner c).
-template <bool SPLIT = true, class F>
+template <bool SPLIT = true, int NT = kThreads, class F>
 __device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
-  // the common case (split 1) keeps constant strides; split 2 is for small launches
+  // the common case (split 1) keeps constant strides; splits are for small launches
   auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
     for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
       const TileDesc d = load_tile(k, tile);
@@ -724,11 +725,68 @@ __device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
     }
   };
   if (!SPLIT || k.split == 1) {
-    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, kThreads);
+    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, NT);
   } else {
-    const int64_t cta_tile = blockIdx.x / 2;
-    walk(k.tile_begin + cta_tile, gridDim.x / 2,
-         static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
+    const int64_t cta_tile = blockIdx.x / k.split;
+    walk(k.tile_begin + cta_tile, gridDim.x / k.split,
+         static_cast<int>(blockIdx.x - k.split * cta_tile) * NT + threadIdx.x, k.split * NT);
+  }
+}
+
+// The reduce-scatter's tile walk for CTA `cta` of `ncta` (a kernel may give the
+// role to part of its grid): shard c of each block's bucket gets the fp32 mean
+// rank c owns; with sumsq, one float-float partial of sum(mean^2) per tile.
+// The partials are accumulated in float-float arithmetic (value = hi + lo):
+// each square is split exactly into p + q with the FMA-based TwoProduct and
+// added with Knuth's TwoSum (Ogita, Rump & Oishi, "Accurate sum and dot
+// product", SIAM J. Sci. Comput. 26(6), 2005).  The norm is then good to
+// ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
+// the exact sum.  Partials are per tile, so the norm does not depend on the grid
+// size or on how the bucket range is split into launches.
+// k.split > 1 (small launches) only without norm partials: a tile's partial has
+// one writer (and needs NT = kThreads).  The common case keeps constant strides.  ACC: the last
+// micro-batch of gradient accumulation fused in (flat plans, always unsplit);
+// SMALL: stores gated on the plan id `id` loaded beside the first loads.
+template <int P, int MS, bool ACC, bool SMALL, int NT = kThreads>
+__device__ __forceinline__ void rs_tiles(const KCommon& k, const uint8_t* g, float* mean, int sumsq,
+                                         const uint8_t* micro, uint64_t id, int64_t cta,
+                                         int64_t ncta, FF* warp_part) {
+  auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
+    for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
+      const TileDesc d = load_tile(k, tile);
+      if (!tile_ok(k, tile, d)) continue;
+      const int nblk = d.nvec >> 1;
+      const int64_t b0 = d.v0 >> 1;
+      FF ss{0.0f, 0.0f};
+#pragma unroll 1
+      for (int j = j0; j < nblk; j += jstep) {
+        const int64_t b = b0 + j;
+        const int c = owner_of(d, 2 * b);
+        if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+        float acc[16];
+        if constexpr (ACC) {
+          ring_mean16_accum<P>(g, micro, k.stride_bytes, 32 * b, c, k.P, acc);
+        } else {
+          block_mean16<P, MS, SMALL ? 16 : 8>(k, g, b, d, c, acc);
+        }
+        if (SMALL && id != k.plan_id) continue;
+        st_f16(mean, b, acc);
+        if (sumsq) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
+        }
+      }
+      if constexpr (NT == kThreads) {   // a tile's partial needs the whole tile in one CTA
+        if (sumsq && (!SMALL || id == k.plan_id)) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
+      }
+    }
+  };
+  if (ACC || k.split == 1) {
+    walk(k.tile_begin + cta, ncta, threadIdx.x, NT);
+  } else {
+    const int64_t cta_tile = cta / k.split;
+    walk(k.tile_begin + cta_tile, ncta / k.split,
+         static_cast<int>(cta - k.split * cta_tile) * NT + threadIdx.x, k.split * NT);
   }
 }
 

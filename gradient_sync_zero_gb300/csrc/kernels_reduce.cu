@@ -20,24 +20,17 @@ constexpr int kAllreducePerSm = 2;
 constexpr int kAccumPerSm = 3;
 
 // Reduce-scatter + 1/P: shard c of each bucket receives the fp32 mean rank c
-// owns; optionally one partial of sum(mean^2) per tile for the clip norm.
-//
-// The partials are accumulated in float-float arithmetic (value = hi + lo):
-// each square is split exactly into p + q with the FMA-based TwoProduct and
-// added with Knuth's TwoSum (Ogita, Rump & Oishi, "Accurate sum and dot
-// product", SIAM J. Sci. Comput. 26(6), 2005).  The norm is then good to
-// ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
-// the exact sum.  Partials are per tile, so the norm does not depend on the grid
-// size or on how the bucket range is split into launches.
+// owns; optionally one partial of sum(mean^2) per tile for the clip norm (the
+// walk, the float-float partials and the split rule are rs_tiles in kernels.cuh).
 // ACC: the last micro-batch of gradient accumulation fused in — replica r's
 // value is bf16(g_r + micro_r), formed in registers (flat plans).
 // SMALL (a launch inside one bucket, few tiles): the plan id is checked beside
 // the first loads (it gates the stores), and a block's replicas are all loaded
 // at once.
-template <int P, int MS, bool ACC, bool SMALL = false>
-__global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const uint8_t* g,
-                                                             float* mean, int sumsq,
-                                                             const uint8_t* micro) {
+// NT: threads per CTA (kSmallThreads for small launches without norm partials).
+template <int P, int MS, bool ACC, bool SMALL = false, int NT = kThreads>
+__global__ void __launch_bounds__(NT) k_reduce_scatter(KCommon k, const uint8_t* g, float* mean,
+                                                       int sumsq, const uint8_t* micro) {
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
@@ -45,43 +38,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
     if (!plan_ok(k)) return;
   }
   __shared__ FF warp_part[kWarps];
-  // k.split = 2 (small launches) only without norm partials: a tile's partial has
-  // one writer.  The common case keeps constant strides.
-  auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
-    for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
-      const TileDesc d = load_tile(k, tile);
-      if (!tile_ok(k, tile, d)) continue;
-      const int nblk = d.nvec >> 1;
-      const int64_t b0 = d.v0 >> 1;
-      FF ss{0.0f, 0.0f};
-#pragma unroll 1
-      for (int j = j0; j < nblk; j += jstep) {
-        const int64_t b = b0 + j;
-        const int c = owner_of(d, 2 * b);
-        if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
-        float acc[16];
-        if constexpr (ACC) {
-          ring_mean16_accum<P>(g, micro, k.stride_bytes, 32 * b, c, k.P, acc);
-        } else {
-          block_mean16<P, MS, SMALL ? 16 : 8>(k, g, b, d, c, acc);
-        }
-        if (SMALL && id != k.plan_id) continue;
-        st_f16(mean, b, acc);
-        if (sumsq) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
-        }
-      }
-      if (sumsq && (!SMALL || id == k.plan_id)) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
-    }
-  };
-  if (ACC || k.split == 1) {   // the accumulating form always launches unsplit
-    walk(k.tile_begin + blockIdx.x, gridDim.x, threadIdx.x, kThreads);
-  } else {
-    const int64_t cta_tile = blockIdx.x / 2;
-    walk(k.tile_begin + cta_tile, gridDim.x / 2,
-         static_cast<int>(blockIdx.x - 2 * cta_tile) * kThreads + threadIdx.x, 2 * kThreads);
-  }
+  rs_tiles<P, MS, ACC, SMALL, NT>(k, g, mean, sumsq, micro, id, blockIdx.x, gridDim.x, warp_part);
   if (SMALL) plan_matches(k, id);
 }
 
@@ -89,14 +46,14 @@ __global__ void __launch_bounds__(kThreads) k_reduce_scatter(KCommon k, const ui
 // every replica (the all-gather of the reduced shards).
 // SMALL: as for k_reduce_scatter.
 template <int P, int MS, bool SMALL = false>
-__global__ void __launch_bounds__(kThreads) k_allreduce(KCommon k, uint8_t* g) {
+__global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads) k_allreduce(KCommon k, uint8_t* g) {
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
   } else {
     if (!plan_ok(k)) return;
   }
-  for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
+  for_each_block2<true, SMALL ? kSmallThreads : kThreads>(k, [&](const TileDesc& d, int64_t b, int c) {
     float acc[16];
     block_mean16<P, MS, SMALL ? 16 : 8>(k, g, b, d, c, acc);
     if (!SMALL || id == k.plan_id) store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(acc), k.P);
@@ -200,14 +157,15 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
       if constexpr (M == 0) {   // flat plans: small single-bucket launches take SMALL
-        if (sumsq && k.one_nvec > 0)
+        if (sumsq && k.one_nvec > 0)   // one CTA per tile: each tile's partial has one writer
           return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
-                                       k_reduce_scatter<P, M, false, true>, true, k,
+                                       k_reduce_scatter<P, M, false, true>, kThreads, 1, k,
                                        static_cast<const uint8_t*>(grads), mean, 1,
                                        static_cast<const uint8_t*>(nullptr));
         if (!sumsq)
           return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
-                                       k_reduce_scatter<P, M, false, true>, false, k,
+                                       k_reduce_scatter<P, M, false, true, kSmallThreads>,
+                                       kSmallThreads, kSmallSplit, k,
                                        static_cast<const uint8_t*>(grads), mean, 0,
                                        static_cast<const uint8_t*>(nullptr));
       }
@@ -239,7 +197,7 @@ int launch_allreduce(const Launch& L, void* grads) {
       constexpr int M = decltype(mc)::value;
       if constexpr (M == 0)   // flat plans: small single-bucket launches take SMALL
         return launch_small_or_split(L, kAllreducePerSm, k_allreduce<P, M>, k_allreduce<P, M, true>,
-                                     false, k, static_cast<uint8_t*>(grads));
+                                     kSmallThreads, kSmallSplit, k, static_cast<uint8_t*>(grads));
       return launch_tiles_split(L, kAllreducePerSm, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));
     });
   });

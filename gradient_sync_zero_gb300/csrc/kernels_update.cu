@@ -99,14 +99,15 @@ struct RepArgs {
   int src_rank;           // broadcast
 };
 
-__global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
-  if (!plan_ok(k)) return;
-  if (threadIdx.x != 0) return;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + kRepStages * kRepStageBytes);
-  for (int q = 0; q < kRepStages; ++q) mbar_init(&bar[q]);
+// The replicate walk for CTA `cta` of `ncta`, run by one thread with an ST-deep
+// ring of 16 KB stages at `smem` (ST * kRepStageBytes + ST barriers).
+template <int ST>
+__device__ __forceinline__ void replicate_tiles(const KCommon& k, const RepArgs& a, int64_t cta,
+                                                int64_t ncta, uint8_t* smem) {
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + ST * kRepStageBytes);
+  for (int q = 0; q < ST; ++q) mbar_init(&bar[q]);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  const int64_t first = k.tile_begin + blockIdx.x, step = gridDim.x;
+  const int64_t first = k.tile_begin + cta, step = ncta;
   const int64_t mine = first < k.tile_end ? (k.tile_end - first + step - 1) / step : 0;
 
   // f(x, e, c) for each run [x, e) of 16-byte vectors of the tile with one source row
@@ -128,12 +129,12 @@ __global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
     if (i >= mine) return;
     const int64_t tile = first + i * step;
     const TileDesc d = load_tile(k, tile);
-    uint64_t* q = &bar[i % kRepStages];
+    uint64_t* q = &bar[i % ST];
     if (!tile_ok(k, tile, d)) {
       mbar_arrive_expect_tx(q, 0u);   // checked build: the stage completes empty
       return;
     }
-    uint8_t* stage = smem_raw + (i % kRepStages) * kRepStageBytes;
+    uint8_t* stage = smem + (i % ST) * kRepStageBytes;
     mbar_arrive_expect_tx(q, 16u * static_cast<uint32_t>(d.nvec));
     segments(d, [&](int64_t x, int64_t e, int c) {
       const uint8_t* src = a.mode == kRepUnit ? a.src + 16 * x : a.src + c * k.stride_bytes + 16 * x;
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
     const int64_t tile = first + i * step;
     const TileDesc d = load_tile(k, tile);
     if (!tile_ok(k, tile, d)) return;
-    const uint8_t* stage = smem_raw + (i % kRepStages) * kRepStageBytes;
+    const uint8_t* stage = smem + (i % ST) * kRepStageBytes;
     segments(d, [&](int64_t x, int64_t e, int c) {
       const uint32_t bytes = 16u * static_cast<uint32_t>(e - x);
       const uint8_t* sm = stage + 16 * (x - d.v0);
@@ -158,27 +159,62 @@ __global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
     });
   };
 
-  for (int q = 0; q < kRepStages - 1; ++q) issue_load(q);
+  for (int q = 0; q < ST - 1; ++q) issue_load(q);
   bool timed_out = false;
   int64_t i = 0;
   for (; i < mine; ++i) {
-    if (!mbar_wait_bounded(&bar[i % kRepStages], static_cast<uint32_t>((i / kRepStages) & 1))) {
+    if (!mbar_wait_bounded(&bar[i % ST], static_cast<uint32_t>((i / ST) & 1))) {
       timed_out = true;
       break;
     }
     issue_stores(i);
     bulk_commit();
     bulk_wait_read<1>();                // tile i-1's stores have left its stage ...
-    issue_load(i + kRepStages - 1);     // ... which now receives the tile ST-1 ahead
+    issue_load(i + ST - 1);             // ... which now receives the tile ST-1 ahead
   }
   if (timed_out) {
     atomicOr(&k.hdr->status, DP_STATUS_TIMEOUT);
-    for (int64_t q = i; q < i + kRepStages - 1 && q < mine; ++q)   // loads in flight (bounded)
-      mbar_wait_bounded(&bar[q % kRepStages], static_cast<uint32_t>((q / kRepStages) & 1));
+    for (int64_t q = i; q < i + ST - 1 && q < mine; ++q)   // loads in flight (bounded)
+      mbar_wait_bounded(&bar[q % ST], static_cast<uint32_t>((q / ST) & 1));
   }
   bulk_wait_all();
 }
 
+__global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
+  if (!plan_ok(k)) return;
+  if (threadIdx.x != 0) return;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  replicate_tiles<kRepStages>(k, a, blockIdx.x, gridDim.x, smem_raw);
+}
+
+// ZeRO-3 backward, two units in one launch: the gather of one unit's parameters
+// (the next unit's, FSDP's prefetch) and the reduce-scatter of another unit's
+// gradients ("Data Parallelism: DDP, ZeRO and FSDP", "How FSDP actually runs":
+// the next unit is gathered while the current one's gradients are reduced).  The
+// two touch disjoint memory, so the grid splits: CTAs [0, n_rs) run the
+// reduce-scatter's tile walk (256 threads each), the rest the replicate walk
+// (one thread, a 3-deep ring of 16 KB stages, which leaves room for three CTAs
+// per SM).  One launch instead of two removes a launch ramp and tail per unit,
+// and mixes the reduce-scatter's read-heavy traffic with the gather's
+// write-heavy traffic.
+constexpr int kUnitBwdStages = 3;
+constexpr size_t kUnitBwdSmem = kUnitBwdStages * static_cast<size_t>(kRepStageBytes) +
+                                kUnitBwdStages * sizeof(uint64_t);
+
+template <int P, int MS>
+__global__ void __launch_bounds__(kThreads)
+    k_unit_backward(KCommon krs, const uint8_t* g, float* mean, int sumsq, KCommon kag, RepArgs a,
+                    int n_rs) {
+  if (!plan_ok(krs)) return;
+  if (static_cast<int>(blockIdx.x) < n_rs) {
+    __shared__ FF warp_part[kWarps];
+    rs_tiles<P, MS, false, false>(krs, g, mean, sumsq, nullptr, krs.plan_id, blockIdx.x, n_rs,
+                                  warp_part);
+  } else if (threadIdx.x == 0) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    replicate_tiles<kUnitBwdStages>(kag, a, blockIdx.x - n_rs, gridDim.x - n_rs, smem_raw);
+  }
+}
 
 int launch_replicate(const Launch& L, const RepArgs& a) {
   if (L.tile_end <= L.tile_begin) return cudaSuccess;
@@ -392,6 +428,50 @@ int launch_unit_all_gather(const Launch& L, const void* shards, void* out, int64
   RepArgs a{static_cast<const uint8_t*>(shards), static_cast<uint8_t*>(out), 2 * out_stride,
             2 * block0, out_stride / kVecElems, kRepUnit, 0};
   return launch_replicate(L, a);
+}
+
+int launch_unit_backward(const Launch& Lrs, const void* grads, float* mean, bool sumsq,
+                         int64_t rep_stride, int64_t rep_block0, const Launch& Lag,
+                         const void* shards, void* out, int64_t out_stride, int64_t block0) {
+  KCommon krs = make_common(Lrs);
+  krs.stride_bytes = 2 * rep_stride;
+  krs.rep_block0 = rep_block0;
+  krs.split = 1;
+  const KCommon kag = make_common(Lag);
+  const RepArgs a{static_cast<const uint8_t*>(shards), static_cast<uint8_t*>(out), 2 * out_stride,
+                  2 * block0, out_stride / kVecElems, kRepUnit, 0};
+  const int64_t n_rs_tiles = Lrs.tile_end - Lrs.tile_begin;
+  const int64_t n_ag_tiles = Lag.tile_end - Lag.tile_begin;
+  return with_P(Lrs.plan->P, [&](auto pc) {
+    constexpr int P = decltype(pc)::value;
+    return with_mesh<P>(Lrs.plan, [&](auto mc) {
+      constexpr int M = decltype(mc)::value;
+      auto kern = k_unit_backward<P, M>;
+      cudaError_t e = ensure_dyn_smem(kern, kUnitBwdSmem);
+      if (e != cudaSuccess) return static_cast<int>(e);
+      const int64_t cap = resident_ctas(kern, kThreads, kUnitBwdSmem);
+      const int sms = sm_count();
+      if (cap < 2 || sms <= 0) {
+        e = cudaGetLastError();
+        return static_cast<int>(e != cudaSuccess ? e : cudaErrorUnknown);
+      }
+      // one gathering CTA per SM (its one thread keeps a tile's copies in flight),
+      // the rest of the resident grid reduce-scatters; DPSYNC_UNIT_AG_CTAS
+      // overrides the gathering CTAs' count for tuning sweeps
+      static const int64_t ag_env = [] {
+        const char* e = std::getenv("DPSYNC_UNIT_AG_CTAS");
+        return e ? static_cast<int64_t>(std::atoll(e)) : int64_t(0);
+      }();
+      int64_t n_ag = ag_env > 0 ? ag_env : sms;
+      if (n_ag > n_ag_tiles) n_ag = n_ag_tiles;
+      if (n_ag > cap / 2) n_ag = cap / 2;
+      int64_t n_rs = cap - n_ag;
+      if (n_rs > n_rs_tiles) n_rs = n_rs_tiles;
+      return launch_k(kern, static_cast<int>(n_rs + n_ag), kThreads, kUnitBwdSmem, Lrs.stream, krs,
+                      static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0, kag, a,
+                      static_cast<int>(n_rs));
+    });
+  });
 }
 
 int launch_all_gather(const Launch& L, void* params) {

@@ -204,23 +204,22 @@ int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... ar
   return launch_k(kernel, static_cast<int>(g), kThreads, 0, L.stream, k, args...);
 }
 
-// A launch inside one bucket (k.one_nvec > 0) that covers at most half as many
-// tiles as `small` fits on the GPU runs `small`: two CTAs per tile (split), or one
-// per tile with split1 (kernels whose tiles carry a norm partial).  Its kernel
-// issues all of a block's replica loads at once and checks the plan beside them
-// (latency, not bandwidth, bounds such a launch).  Otherwise `big` runs as
+// A launch inside one bucket (k.one_nvec > 0) whose tiles, `split` CTAs of
+// `threads` threads each, all fit on the GPU at once runs `small` (its kernel
+// issues all of a block's replica loads at once and checks the plan beside
+// them: latency, not bandwidth, bounds such a launch).  Otherwise `big` runs as
 // launch_tiles_split would launch it.
 template <class KB, class KS, class... A>
-int launch_small_or_split(const Launch& L, int per_sm, KB big, KS small, bool split1, KCommon k,
-                          A... args) {
+int launch_small_or_split(const Launch& L, int per_sm, KB big, KS small, int threads, int split,
+                          KCommon k, A... args) {
   const int64_t n = L.tile_end - L.tile_begin;
   if (n <= 0) return cudaSuccess;
   if (k.one_nvec > 0) {
-    int cap = resident_ctas(small, kThreads);
+    int cap = resident_ctas(small, threads);
     if (L.max_ctas > 0 && cap > L.max_ctas) cap = L.max_ctas;
-    if (cap > 0 && 2 * n <= cap) {
-      k.split = split1 ? 1 : 2;
-      return launch_k(small, static_cast<int>(n * k.split), kThreads, 0, L.stream, k, args...);
+    if (cap > 0 && n * split <= cap && (split > 1 || 2 * n <= cap)) {
+      k.split = split;
+      return launch_k(small, static_cast<int>(n * split), threads, 0, L.stream, k, args...);
     }
   }
   return launch_tiles_split(L, per_sm, big, k, args...);

@@ -361,6 +361,21 @@ int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* uni
 int dp_shard_adamw_step(const dp_plan* plan, void* workspace, const float* mean, float* master,
                         float* m, float* v, void* param_shards, const dp_adamw_cfg* cfg,
                         int32_t use_clip_coef, const float* coef_dev, void* stream);
+/*
+ * dp_unit_backward: one backward step of the unit flow in one launch — the
+ * gather of unit gather_unit into gather_buf (the next unit's parameters, FSDP's
+ * prefetch) and the reduce-scatter of unit rs_unit's gradients into mean: the
+ * same results as dp_unit_all_gather(gather_unit) and
+ * dp_unit_reduce_scatter(rs_unit), in either order.  gather_unit = -1 or
+ * rs_unit = -1 leaves that part out (one of the two calls above; both -1: no
+ * work).  Arguments as for those calls; gather_buf must not overlap unit_grads
+ * or mean (DP_EINVAL), and the caller must not let unit_grads alias
+ * param_shards.  Units outside [-1, n_buckets) are DP_EINVAL.
+ */
+int dp_unit_backward(const dp_plan* plan, void* workspace, const void* param_shards,
+                     int32_t gather_unit, void* gather_buf, int64_t gather_stride,
+                     const void* unit_grads, int64_t grads_stride, int32_t rs_unit, float* mean,
+                     int32_t want_sumsq, void* stream);
 
 /*
  * Gradient accumulation ("Distributed Training: Data Parallel, Model Parallel and

@@ -166,6 +166,26 @@ def test_compute_calls_validate_before_any_device_work():
                                    None) == dps.DP_EINVAL
 
 
+def test_unit_backward_validates_before_any_device_work():
+    """dp_unit_backward refuses units out of range, short strides and a gather
+    buffer that overlaps the gradients or the mean, on the host."""
+    lib = dps.lib()
+    p = dps.Plan([1000, 4096, 333], 8192, 4)
+    nb = p.n_buckets
+    ws, sh = C.c_void_p(1 << 20), C.c_void_p(1 << 22)
+    gb, ug, mean = C.c_void_p(1 << 30), C.c_void_p(1 << 31), C.c_void_p(1 << 32)
+    st = 4096
+    assert lib.dp_unit_backward(p.handle, ws, sh, nb, gb, st, ug, st, 0, mean, 1, None) == dps.DP_EINVAL
+    assert lib.dp_unit_backward(p.handle, ws, sh, 0, gb, st, ug, st, -2, mean, 1, None) == dps.DP_EINVAL
+    assert lib.dp_unit_backward(p.handle, ws, sh, 1, gb, 16, ug, st, 0, mean, 1, None) == dps.DP_EINVAL
+    assert lib.dp_unit_backward(p.handle, ws, sh, 1, ug, st, ug, st, 0, mean, 1, None) == dps.DP_EINVAL
+    assert "overlaps" in lib.dp_last_error().decode()
+    assert lib.dp_unit_backward(p.handle, ws, sh, 1, gb, st, ug, st, 0, C.c_void_p((1 << 30) + 64), 1,
+                                None) == dps.DP_EINVAL
+    assert lib.dp_unit_backward(p.handle, ws, sh, -1, gb, st, ug, st, -1, mean, 1, None) == dps.DP_OK
+    assert lib.dp_unit_backward(None, ws, sh, 0, gb, st, ug, st, 1, mean, 1, None) == dps.DP_EINVAL
+
+
 def test_launch_counts():
     assert dps.dp_fused_zero_step_launches(dps.adamw_cfg(max_norm=0.0)) == 1
     assert dps.dp_fused_zero_step_launches(dps.adamw_cfg(max_norm=1.0)) == 3

@@ -13,9 +13,12 @@ from workloads import configs, device as wdev
 pytestmark = pytest.mark.gpu
 
 
-def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf, coef_dev=None, ws_max_norm=None):
+def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf, coef_dev=None, ws_max_norm=None,
+               unit_buf2=None):
     """coef_dev: the update multiplies by the caller's own coefficient instead of
-    the workspace's (which dp_clip_coef still forms, at ws_max_norm)."""
+    the workspace's (which dp_clip_coef still forms, at ws_max_norm).  unit_buf2:
+    the backward runs as dp_unit_backward launches, each gathering the next unit
+    into the other buffer while the current unit's gradients reduce-scatter."""
     plan = c.plan
     nb = plan.n_buckets
     gathered = []
@@ -23,7 +26,16 @@ def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf, coef_dev=None, ws_max_
         dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
         o, ln, _ = plan.bucket(b)
         gathered.append((b, unit_buf[:, :ln].clone()))
-    for b in range(nb):                                     # backward
+    if unit_buf2 is not None:                               # backward, fused launches
+        bufs = [unit_buf, unit_buf2]
+        dps.dp_unit_all_gather(plan, c.ws, shards, 0, bufs[0])
+        for b in range(nb):
+            o, ln, _ = plan.bucket(b)
+            gathered.append((b, bufs[b % 2][:, :ln].clone()))   # unit b's backward reads it
+            nxt = b + 1 if b + 1 < nb else -1
+            dps.dp_unit_backward(plan, c.ws, shards, nxt, bufs[(b + 1) % 2], grads[:, o:o + ln], b,
+                                 mean, want_sumsq=True)
+    for b in range(nb if unit_buf2 is None else 0):         # backward
         dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
         o, ln, _ = plan.bucket(b)
         dps.dp_unit_reduce_scatter(plan, c.ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
@@ -33,8 +45,9 @@ def zero3_flow(c, grads, shards, mean, st, cfg, unit_buf, coef_dev=None, ws_max_
     return gathered
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["two-launches", "fused-backward"])
 @pytest.mark.parametrize("P", [2, 4, 5, 8, 12, 16])
-def test_zero3_flow_matches_oracle(orc, P):
+def test_zero3_flow_matches_oracle(orc, P, fused):
     wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910], P, 64 * 1024, sigma=0.05,
                         seed=30 + P)
     c = Case(wl)
@@ -49,12 +62,14 @@ def test_zero3_flow_matches_oracle(orc, P):
     mean = c.plan.new_state()
     max_len = max(c.plan.bucket(b)[1] for b in range(c.plan.n_buckets))
     unit_buf = torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda")
+    unit_buf2 = torch.zeros_like(unit_buf) if fused else None
     for step in (1, 2):
         g = c.host_grads(step)
         cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
                             adamw.max_norm, step)
         before = shards.clone()
-        gathered = zero3_flow(c, c.to_replicas(g), shards, mean, st, cfg, unit_buf)
+        gathered = zero3_flow(c, c.to_replicas(g), shards, mean, st, cfg, unit_buf,
+                              unit_buf2=unit_buf2)
         shards_h, master, m, v, so = orc.zero3_step(c.sizes, c.decay, wl.bucket_bytes, P, g,
                                                     shards_h, master, m, v,
                                                     oracle_mod.adamw_cfg(adamw, step))
@@ -159,6 +174,7 @@ def test_prefetch_schedule_on_two_streams_equals_sequential():
     max_len = max(plan.bucket(b)[1] for b in range(nb))
 
     def run(prefetch):
+        """prefetch: False (sequential), True (two streams) or "fused" (dp_unit_backward)."""
         shards = master0.to(torch.bfloat16)
         st = [master0.clone(), plan.new_state(), plan.new_state()]
         mean = plan.new_state()
@@ -171,6 +187,13 @@ def test_prefetch_schedule_on_two_streams_equals_sequential():
                 dps.dp_unit_all_gather(plan, ws, shards, b, bufs[0])
                 seen.append(bufs[0][:, :ln].clone())
                 dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+        elif prefetch == "fused":
+            dps.dp_unit_all_gather(plan, ws, shards, 0, bufs[0])
+            for b in range(nb):
+                o, ln, _ = plan.bucket(b)
+                seen.append(bufs[b % 2][:, :ln].clone())
+                dps.dp_unit_backward(plan, ws, shards, b + 1 if b + 1 < nb else -1, bufs[(b + 1) % 2],
+                                     grads[:, o:o + ln], b, mean, want_sumsq=True)
         else:
             main = torch.cuda.current_stream()
             s_a, s_b = torch.cuda.Stream(), torch.cuda.Stream()
@@ -200,14 +223,16 @@ def test_prefetch_schedule_on_two_streams_equals_sequential():
         return mean, dps.dp_read_norm(plan, ws), st, shards, seen
 
     m1, n1, st1, sh1, seen1 = run(False)
-    m2, n2, st2, sh2, seen2 = run(True)
-    assert n1 == n2 and n1[2] == 0
-    assert torch.equal(m1.view(torch.int32), m2.view(torch.int32))
-    assert torch.equal(sh1, sh2)
-    for a, b in zip(st1, st2):
-        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
-    for a, b in zip(seen1, seen2):
-        assert torch.equal(a, b)
+    for mode in (True, "fused"):
+        m2, n2, st2, sh2, seen2 = run(mode)
+        assert n1 == n2 and n1[2] == 0
+        assert torch.equal(m1.view(torch.int32), m2.view(torch.int32))
+        assert torch.equal(sh1, sh2)
+        for a, b in zip(st1, st2):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert len(seen1) == len(seen2)
+        for a, b in zip(seen1, seen2):
+            assert torch.equal(a, b)
 
 
 def test_captured_prefetch_step_equals_eager():
@@ -274,6 +299,70 @@ def test_captured_prefetch_step_equals_eager():
     dps.dp_unit_all_gather(plan, ws_g, sh_g, 0, bufs[0])
     o0, ln0, _ = plan.bucket(0)
     dps.dp_unit_reduce_scatter(plan, ws_g, grads[:, o0:o0 + ln0], 0, scratch[0])
+    dps.dp_shard_adamw_step(plan, ws_g, scratch[0], *scratch[1:], plan.new_state().to(torch.bfloat16),
+                            cfg(1))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    for t in (1, 2):
+        dps.dp_set_adamw_cfg(plan, ws_g, cfg(t))
+        graph.replay()
+    torch.cuda.synchronize()
+    assert dps.dp_read_norm(plan, ws_g) == dps.dp_read_norm(plan, ws_e)
+    assert torch.equal(sh_g, sh_e)
+    assert torch.equal(mean_g.view(torch.int32), mean_e.view(torch.int32))
+    for x, y in zip(st_g, st_e):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_captured_fused_backward_step_equals_eager():
+    """The ZeRO-3 backward as dp_unit_backward launches (the next unit's gather
+    beside this unit's reduce-scatter) plus the update, captured once as a CUDA
+    graph and replayed for steps 1 and 2, equals the eager sequential flow bit for
+    bit (mean, norm, shards, master/m/v)."""
+    wl = configs.llama_1b1_zero2(layers=2, embeddings=False)
+    wl.bucket_bytes = 4 << 20
+    c = Case(wl)
+    plan, nb, P = c.plan, c.plan.n_buckets, wl.P
+    grads = plan.new_replicas()
+    wdev.fill_grads(grads, c.off, wl, 1)
+    master0 = torch.randn(plan.L, device="cuda") * 0.02
+    max_len = max(plan.bucket(b)[1] for b in range(nb))
+
+    def cfg(t):
+        return dps.adamw_cfg(2e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, t)
+
+    sh_e = master0.to(torch.bfloat16)
+    st_e = [master0.clone(), plan.new_state(), plan.new_state()]
+    mean_e, ws_e = plan.new_state(), plan.new_workspace()
+    buf = torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda")
+    for t in (1, 2):
+        for b in range(nb):
+            o, ln, _ = plan.bucket(b)
+            dps.dp_unit_all_gather(plan, ws_e, sh_e, b, buf)
+            dps.dp_unit_reduce_scatter(plan, ws_e, grads[:, o:o + ln], b, mean_e, want_sumsq=True)
+        dps.dp_clip_coef(plan, ws_e, 1.0)
+        dps.dp_shard_adamw_step(plan, ws_e, mean_e, *st_e, sh_e, cfg(t), use_clip_coef=True)
+
+    sh_g = master0.to(torch.bfloat16)
+    st_g = [master0.clone(), plan.new_state(), plan.new_state()]
+    mean_g, ws_g = plan.new_state(), plan.new_workspace()
+    bufs = [torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+
+    def body():
+        dps.dp_unit_all_gather(plan, ws_g, sh_g, 0, bufs[0])
+        for b in range(nb):
+            o, ln, _ = plan.bucket(b)
+            dps.dp_unit_backward(plan, ws_g, sh_g, b + 1 if b + 1 < nb else -1, bufs[(b + 1) % 2],
+                                 grads[:, o:o + ln], b, mean_g, want_sumsq=True)
+        dps.dp_clip_coef(plan, ws_g, 1.0)
+        dps.dp_shard_adamw_step(plan, ws_g, mean_g, *st_g, sh_g, None, use_clip_coef=True)
+
+    # launcher setup outside the capture, on scratch state
+    scratch = [plan.new_state() for _ in range(4)]
+    o0, ln0, _ = plan.bucket(0)
+    dps.dp_unit_backward(plan, ws_g, sh_g, 1, bufs[1], grads[:, o0:o0 + ln0], 0, scratch[0])
     dps.dp_shard_adamw_step(plan, ws_g, scratch[0], *scratch[1:], plan.new_state().to(torch.bfloat16),
                             cfg(1))
     torch.cuda.synchronize()

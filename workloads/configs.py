@@ -142,20 +142,24 @@ def gpt_2b5_clip() -> Workload:
                     decay_rule="ndim>=2", seed=3)
 
 
-def sweep_small_tensors(bucket_bytes: int = 25 * MiB, mode: str = "zero") -> Workload:
+def sweep_small_tensors(bucket_bytes: int = 25 * MiB, mode: str = "zero",
+                        groups: int = 24) -> Workload:
+    """24 groups of (one 1024 x 4096 matrix + 250 log-uniform 4K-64K vectors);
+    `groups` < 24 keeps the first groups only (a smaller case of the same shapes)."""
     import numpy as np
     rng = np.random.default_rng(4)
     small = np.exp(rng.uniform(math.log(4096), math.log(65536), size=6000))
     small = np.floor(small).astype(np.int64)
     names, shapes = [], []
-    for g in range(24):
+    for g in range(groups):
         names.append(f"mat.{g}")
         shapes.append((1024, 4096))
         for j in range(250):
             k = g * 250 + j
             names.append(f"small.{k}")
             shapes.append((int(small[k]),))
-    return Workload(name=f"sweep-P16-{bucket_bytes // 1024}KiB-{mode}", P=16, names=names,
+    tag = "" if groups == 24 else f"-{groups}g"
+    return Workload(name=f"sweep-P16-{bucket_bytes // 1024}KiB-{mode}{tag}", P=16, names=names,
                     shapes=shapes, bucket_bytes=bucket_bytes, sigma=1e-3, mode=mode, seed=4)
 
 
