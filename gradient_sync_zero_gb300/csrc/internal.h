@@ -17,11 +17,22 @@ constexpr int kThreads = 256;                 // threads per CTA
 // loads and stores are spread over kSmallSplit times more SMs.
 constexpr int kSmallThreads = 64;
 constexpr int kSmallSplit = 8;
+// Norm partials: one float-float pair per sub-tile of kSubTileBlocks 32-byte
+// blocks (1024 elements), kSubTiles per tile, so that CTAs of kSmallThreads
+// threads can form them exactly as a whole-tile CTA does.
+constexpr int kSubTileBlocks = 64;
+constexpr int kSubTiles = 8;
+// The norm pass: each CTA merges up to kFinPerCta consecutive partials, at most
+// kFinMaxCtas CTAs (the count depends only on the number of partials).
+constexpr int kFinPerCta = 8192;
+constexpr int kFinMaxCtas = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecElems = 8;                  // bf16 elements per 16-byte vector
 constexpr int kPairElems = 16;                // bf16 elements per 32-byte (256-bit) access
 constexpr int kTileVec = 1024;                // vectors per tile (8192 elements)
 constexpr int kTileElems = kTileVec * kVecElems;
+static_assert(kSubTiles * kSubTileBlocks * 2 == kTileVec, "sub-tiles cover a tile");
+static_assert(kSmallSplit * kSmallThreads * 2 == kTileVec, "a small CTA's threads cover a sub-tile pair");
 constexpr int kMaxP = 64;
 constexpr uint64_t kMagic = 0x31304e5953435044ull;  // "DPCSYN01"
 
@@ -55,9 +66,10 @@ struct DevHeader {
   int64_t off_tiles;      // byte offsets of the arrays inside the workspace
   int64_t off_btile;      // int64 [n_buckets+1]: first tile of each bucket
   int64_t off_decay;      // uint32 [ceil(n_vec/32)]
-  int64_t off_sumsq;      // float2 [n_tiles]: per-tile sum of mean^2, hi + lo (scratch)
+  int64_t off_sumsq;      // float2 [n_tiles * kSubTiles]: per-sub-tile sum of mean^2, hi + lo (scratch)
   int64_t off_stage;      // float [L] (scratch)
-  int64_t reserved_[3];
+  int64_t off_fin;        // float2 [kFinMaxCtas]: the norm pass's per-CTA sums (scratch)
+  int64_t reserved_[2];
   // ---- written by kernels ----
   double norm2;
   double norm;
@@ -66,7 +78,9 @@ struct DevHeader {
   AdamScalars adam;       // set by dp_set_adamw_cfg, read by the update kernels when
   uint32_t adam_tag;      // called without a cfg (graph-captured steps); kAdamTag
   int32_t pad3_;
-  int64_t reserved2_[2];
+  uint32_t fin_count;     // norm pass: CTAs done (the last one resets it to 0)
+  uint32_t pad4_;
+  int64_t reserved2_;
 };
 static_assert(sizeof(DevHeader) % 64 == 0, "header keeps the arrays aligned");
 // the results part's layout is public (include/dpsync.h, DP_WS_*_OFFSET)

@@ -29,7 +29,8 @@ struct KCommon {
   DevHeader* hdr;
   const TileDesc* __restrict__ tiles;
   const uint32_t* __restrict__ decay;
-  float* sumsq;          // per tile: sum of squares of the mean as float-float (hi, lo)
+  float* sumsq;          // per sub-tile: sum of squares of the mean as float-float (hi, lo)
+  float* fin;            // the norm pass's per-CTA float-float sums
   uint64_t plan_id;
   int64_t stride_bytes;  // replica stride in bytes
   int64_t tile_begin;
@@ -500,16 +501,36 @@ __device__ __forceinline__ FF warp_ff_sum(FF a) {
   return a;
 }
 
-// Merge the CTA's per-thread partials in a fixed order and store hi, lo at out.
-__device__ __forceinline__ void block_ff_store(FF a, FF* warp_part, float* out) {
+// Norm partials of one tile: one float-float value per sub-tile of
+// kSubTileBlocks consecutive 32-byte blocks, formed the same way whatever the
+// launch's shape: each lane's squares of its block, a butterfly over the warp's
+// 32 lanes (32 consecutive blocks), then the two warps of the sub-tile merged,
+// lower blocks first.  ss[p] is the thread's sum for its p-th block of the tile
+// (blocks j0 + p * jstep, j0 = this CTA's first block in the tile plus
+// threadIdx.x); out receives the tile's kSubTiles (hi, lo) pairs, every slot
+// this CTA covers written (zero for blocks past the tile's end).
+template <int NT>
+__device__ __forceinline__ void subtile_ff_store(const FF (&ss)[2], int cta_j0, int jstep,
+                                                 FF* warp_part, float* out) {
+  constexpr int W = NT / 32;
+  constexpr int kTileBlocks = kTileVec / 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  a = warp_ff_sum(a);
-  if (lane == 0) warp_part[warp] = a;
+  const int npass = (kTileBlocks + jstep - 1) / jstep;   // 2 (256 threads, one CTA) or 1
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (p < npass) {
+      const FF a = warp_ff_sum(ss[p]);
+      if (lane == 0) warp_part[p * W + warp] = a;
+    }
+  }
   __syncthreads();
-  if (warp == 0) {
-    FF b = lane < kWarps ? warp_part[lane] : FF{0.0f, 0.0f};
-    b = warp_ff_sum(b);
-    if (lane == 0) *reinterpret_cast<float2*>(out) = make_float2(b.hi, b.lo);
+  constexpr int pairs = W / 2;                           // sub-tiles per pass
+  if (static_cast<int>(threadIdx.x) < npass * pairs) {
+    const int p = threadIdx.x / pairs, q = threadIdx.x % pairs;
+    const FF m = ff_merge(warp_part[p * W + 2 * q], warp_part[p * W + 2 * q + 1]);
+    const int sub = (cta_j0 + p * jstep) / kSubTileBlocks + q;
+    if (DP_IN_BOUNDS(sub >= 0 && sub < kSubTiles))
+      *reinterpret_cast<float2*>(out + 2 * sub) = make_float2(m.hi, m.lo);
   }
   __syncthreads();
 }
@@ -735,18 +756,19 @@ __device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
 
 // The reduce-scatter's tile walk for CTA `cta` of `ncta` (a kernel may give the
 // role to part of its grid): shard c of each block's bucket gets the fp32 mean
-// rank c owns; with sumsq, one float-float partial of sum(mean^2) per tile.
-// The partials are accumulated in float-float arithmetic (value = hi + lo):
-// each square is split exactly into p + q with the FMA-based TwoProduct and
-// added with Knuth's TwoSum (Ogita, Rump & Oishi, "Accurate sum and dot
-// product", SIAM J. Sci. Comput. 26(6), 2005).  The norm is then good to
-// ~1e-15 relative, so its fp32 clip coefficient rounds like one computed from
-// the exact sum.  Partials are per tile, so the norm does not depend on the grid
-// size or on how the bucket range is split into launches.
-// k.split > 1 (small launches) only without norm partials: a tile's partial has
-// one writer (and needs NT = kThreads).  The common case keeps constant strides.  ACC: the last
-// micro-batch of gradient accumulation fused in (flat plans, always unsplit);
-// SMALL: stores gated on the plan id `id` loaded beside the first loads.
+// rank c owns; with sumsq, kSubTiles float-float partials of sum(mean^2) per
+// tile (subtile_ff_store).  The partials are accumulated in float-float
+// arithmetic (value = hi + lo): each square is split exactly into p + q with the
+// FMA-based TwoProduct and added with Knuth's TwoSum (Ogita, Rump & Oishi,
+// "Accurate sum and dot product", SIAM J. Sci. Comput. 26(6), 2005).  The norm
+// is then good to ~1e-15 relative, so its fp32 clip coefficient rounds like one
+// computed from the exact sum.  The partials are formed per sub-tile in a fixed
+// order, so the norm does not depend on the grid, the CTA shape (NT threads,
+// k.split CTAs per tile: 256 x 1 or 64 x kSmallSplit with sumsq) or on how the
+// bucket range is split into launches.  ACC: the last micro-batch of gradient
+// accumulation fused in (flat plans, always unsplit); SMALL: stores gated on
+// the plan id `id` loaded beside the first loads.  warp_part: 2 * NT / 32 FF of
+// shared memory.
 template <int P, int MS, bool ACC, bool SMALL, int NT = kThreads>
 __device__ __forceinline__ void rs_tiles(const KCommon& k, const uint8_t* g, float* mean, int sumsq,
                                          const uint8_t* micro, uint64_t id, int64_t cta,
@@ -757,9 +779,10 @@ __device__ __forceinline__ void rs_tiles(const KCommon& k, const uint8_t* g, flo
       if (!tile_ok(k, tile, d)) continue;
       const int nblk = d.nvec >> 1;
       const int64_t b0 = d.v0 >> 1;
-      FF ss{0.0f, 0.0f};
+      FF ss[2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+      int pass = 0;
 #pragma unroll 1
-      for (int j = j0; j < nblk; j += jstep) {
+      for (int j = j0; j < nblk; j += jstep, ++pass) {
         const int64_t b = b0 + j;
         const int c = owner_of(d, 2 * b);
         if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
@@ -772,13 +795,14 @@ __device__ __forceinline__ void rs_tiles(const KCommon& k, const uint8_t* g, flo
         if (SMALL && id != k.plan_id) continue;
         st_f16(mean, b, acc);
         if (sumsq) {
+          FF& sp = ss[pass & 1];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ff_add_square(ss, acc[e]);
+          for (int e = 0; e < 16; ++e) ff_add_square(sp, acc[e]);
         }
       }
-      if constexpr (NT == kThreads) {   // a tile's partial needs the whole tile in one CTA
-        if (sumsq && (!SMALL || id == k.plan_id)) block_ff_store(ss, warp_part, k.sumsq + 2 * tile);
-      }
+      if (sumsq && (!SMALL || id == k.plan_id))
+        subtile_ff_store<NT>(ss, j0 - static_cast<int>(threadIdx.x), jstep, warp_part,
+                             k.sumsq + 2 * kSubTiles * tile);
     }
   };
   if (ACC || k.split == 1) {

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(NT) k_reduce_scatter(KCommon k, const uint8_t*
   } else {
     if (!plan_ok(k)) return;
   }
-  __shared__ FF warp_part[kWarps];
+  __shared__ FF warp_part[2 * kWarps];
   rs_tiles<P, MS, ACC, SMALL, NT>(k, g, mean, sumsq, micro, id, blockIdx.x, gridDim.x, warp_part);
   if (SMALL) plan_matches(k, id);
 }
@@ -102,48 +102,73 @@ __global__ void __launch_bounds__(kThreads) k_allreduce_bf16wire(KCommon k, uint
   });
 }
 
-// One CTA: merge the tile partials of [tile_begin, tile_end) in float-float in a
-// fixed order, then norm and the clip coefficient min(1, max_norm / (norm +
-// 1e-6)) in double ("Distributed Training: Data Parallel, Model Parallel and
-// FSDP Strategies", "Inside DDP": clip_grad_norm_ after the averaged gradients).
-constexpr int kFinalThreads = 1024;
-__global__ void __launch_bounds__(kFinalThreads) k_norm_finalize(KCommon k, double max_norm) {
+// The global norm over tiles [tile_begin, tile_end): their sub-tile partials
+// merged in float-float in a fixed order, then the norm and the clip coefficient
+// min(1, max_norm / (norm + 1e-6)) in double ("Distributed Training: Data
+// Parallel, Model Parallel and FSDP Strategies", "Inside DDP": clip_grad_norm_
+// after the averaged gradients).  The grid's size depends only on the number of
+// partials n (ceil(n / kFinPerCta), at most kFinMaxCtas): CTA i merges its
+// contiguous share, thread t every 256th partial of it in order, then the warps'
+// butterflies and the warps in order; the CTA that finishes last (a counter in
+// the workspace header, no waiting) merges the CTAs' sums in CTA order and
+// writes the results.  So the norm depends only on the partials, whatever
+// launches produced them.
+constexpr int kFinThreads = 256;
+
+__device__ __forceinline__ FF ld_ff(const float* p) {
+  const float2 q = __ldcg(reinterpret_cast<const float2*>(p));
+  return FF{q.x, q.y};
+}
+
+__global__ void __launch_bounds__(kFinThreads) k_norm_finalize(KCommon k, double max_norm) {
   if (!plan_ok(k)) return;
-  __shared__ FF warp_part[kFinalThreads / 32];
-  FF acc{0.0f, 0.0f};
-  const float2* part = reinterpret_cast<const float2*>(k.sumsq);
-  int64_t i = k.tile_begin + threadIdx.x;
-  for (; i + 3 * kFinalThreads < k.tile_end; i += 4 * kFinalThreads) {
-    float2 q[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) q[u] = __ldcg(part + i + u * kFinalThreads);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) acc = ff_merge(acc, FF{q[u].x, q[u].y});
-  }
-  for (; i < k.tile_end; i += kFinalThreads) {
-    const float2 q = __ldcg(part + i);
-    acc = ff_merge(acc, FF{q.x, q.y});
-  }
-  acc = warp_ff_sum(acc);
+  __shared__ FF warp_part[kFinThreads / 32];
+  __shared__ int is_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t p0 = kSubTiles * k.tile_begin, n = kSubTiles * (k.tile_end - k.tile_begin);
+  const int64_t share = (n + gridDim.x - 1) / gridDim.x;
+  const int64_t c0 = p0 + blockIdx.x * share;
+  const int64_t c1 = c0 + share < p0 + n ? c0 + share : p0 + n;
+  FF acc{0.0f, 0.0f};
+  int64_t i = c0 + threadIdx.x;
+  for (; i + 3 * kFinThreads < c1; i += 4 * kFinThreads) {
+    FF q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) q[u] = ld_ff(k.sumsq + 2 * (i + u * kFinThreads));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc = ff_merge(acc, q[u]);
+  }
+  for (; i < c1; i += kFinThreads) acc = ff_merge(acc, ld_ff(k.sumsq + 2 * i));
+  acc = warp_ff_sum(acc);
   if (lane == 0) warp_part[warp] = acc;
   __syncthreads();
-  if (warp == 0) {
-    acc = warp_ff_sum(warp_part[lane]);
-    if (lane == 0) {
-      const double n2 = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
-      const double norm = sqrt(n2);
-      float coef = 1.0f;
-      if (!isfinite(norm)) {
-        atomicOr(&k.hdr->status, DP_STATUS_NONFINITE);
-        if (max_norm > 0.0) coef = __int_as_float(0x7fc00000);
-      } else if (max_norm > 0.0) {
-        coef = __double2float_rn(fmin(1.0, max_norm / (norm + 1e-6)));
-      }
-      k.hdr->norm2 = n2;
-      k.hdr->norm = norm;
-      k.hdr->coef = coef;
+  if (threadIdx.x == 0) {
+    FF c = warp_part[0];
+    for (int w = 1; w < kFinThreads / 32; ++w) c = ff_merge(c, warp_part[w]);
+    *reinterpret_cast<float2*>(k.fin + 2 * blockIdx.x) = make_float2(c.hi, c.lo);
+    __threadfence();
+    is_last = atomicAdd(&k.hdr->fin_count, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last || warp != 0) return;
+  __threadfence();
+  FF a{0.0f, 0.0f};
+  for (int64_t c = lane; c < gridDim.x; c += 32) a = ff_merge(a, ld_ff(k.fin + 2 * c));
+  a = warp_ff_sum(a);
+  if (lane == 0) {
+    const double n2 = static_cast<double>(a.hi) + static_cast<double>(a.lo);
+    const double norm = sqrt(n2);
+    float coef = 1.0f;
+    if (!isfinite(norm)) {
+      atomicOr(&k.hdr->status, DP_STATUS_NONFINITE);
+      if (max_norm > 0.0) coef = __int_as_float(0x7fc00000);
+    } else if (max_norm > 0.0) {
+      coef = __double2float_rn(fmin(1.0, max_norm / (norm + 1e-6)));
     }
+    k.hdr->norm2 = n2;
+    k.hdr->norm = norm;
+    k.hdr->coef = coef;
+    k.hdr->fin_count = 0;   // ready for the next norm pass on this workspace
   }
 }
 
@@ -157,9 +182,11 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
       if constexpr (M == 0) {   // flat plans: small single-bucket launches take SMALL
-        if (sumsq && k.one_nvec > 0)   // one CTA per tile: each tile's partial has one writer
+        // each small CTA forms its sub-tile's norm partial as a whole-tile CTA would
+        if (sumsq && k.one_nvec > 0)
           return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
-                                       k_reduce_scatter<P, M, false, true>, kThreads, 1, k,
+                                       k_reduce_scatter<P, M, false, true, kSmallThreads>,
+                                       kSmallThreads, kSmallSplit, k,
                                        static_cast<const uint8_t*>(grads), mean, 1,
                                        static_cast<const uint8_t*>(nullptr));
         if (!sumsq)
@@ -243,7 +270,11 @@ int launch_allreduce_bf16wire(const Launch& L, void* grads) {
 
 int launch_norm_finalize(const Launch& L, double max_norm) {
   const KCommon k = make_common(L);
-  return launch_k(k_norm_finalize, 1, kFinalThreads, 0, L.stream, k, max_norm);
+  const int64_t n = kSubTiles * (L.tile_end - L.tile_begin);
+  int64_t g = (n + kFinPerCta - 1) / kFinPerCta;
+  if (g < 1) g = 1;
+  if (g > kFinMaxCtas) g = kFinMaxCtas;
+  return launch_k(k_norm_finalize, static_cast<int>(g), kFinThreads, 0, L.stream, k, max_norm);
 }
 
 }  // namespace dps

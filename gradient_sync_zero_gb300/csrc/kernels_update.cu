@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads)
                     int n_rs) {
   if (!plan_ok(krs)) return;
   if (static_cast<int>(blockIdx.x) < n_rs) {
-    __shared__ FF warp_part[kWarps];
+    __shared__ FF warp_part[2 * kWarps];
     rs_tiles<P, MS, false, false>(krs, g, mean, sumsq, nullptr, krs.plan_id, blockIdx.x, n_rs,
                                   warp_part);
   } else if (threadIdx.x == 0) {

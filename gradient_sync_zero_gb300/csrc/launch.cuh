@@ -23,6 +23,7 @@ inline KCommon make_common(const Launch& L) {
   k.tiles = reinterpret_cast<const TileDesc*>(L.ws + h.off_tiles);
   k.decay = reinterpret_cast<const uint32_t*>(L.ws + h.off_decay);
   k.sumsq = reinterpret_cast<float*>(L.ws + h.off_sumsq);
+  k.fin = reinterpret_cast<float*>(L.ws + h.off_fin);
   k.plan_id = L.plan->id;
   k.stride_bytes = L.plan->stride * 2;
   k.tile_begin = L.tile_begin;

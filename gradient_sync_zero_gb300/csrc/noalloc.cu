@@ -14,8 +14,8 @@
 // The array.  kNoallocScratchBytes (32 MiB) in a file-scope __device__ array;
 // every GPU that loads this library's code for it holds those 32 MiB until the
 // process exits.  It must hold the plan's device tables (about 160 bytes per
-// 8192 parameters: the tile table and the weight-decay bits) and one 8-byte norm
-// partial per 8192-parameter tile, so plans up to about 1.6e9 parameters fit;
+// 8192 parameters: the tile table and the weight-decay bits) and eight 8-byte
+// norm partials per 8192-parameter tile, so plans up to about 1.2e9 parameters fit;
 // the call refuses larger plans with DP_EINVAL and says why.
 //
 // Sharing.  Every call, on every stream, uses the same array, and the array

@@ -137,7 +137,9 @@ void build_image(Plan& pl) {
   off = round_up(off + static_cast<int64_t>(pl.decay_bits.size()) * 4, 256);
   pl.table_bytes = off;
   h.off_sumsq = off;
-  off = round_up(off + h.n_tiles * 8, 256);
+  off = round_up(off + h.n_tiles * 8 * kSubTiles, 256);
+  h.off_fin = off;
+  off = round_up(off + int64_t(8) * kFinMaxCtas, 256);
   h.off_stage = off;
   off = round_up(off + pl.L * 4, 256);
   pl.workspace_bytes = off;

@@ -595,7 +595,7 @@ int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float
  * allocator must account for every byte, a loop where a cudaMalloc/cudaFree
  * that may synchronise the device is not acceptable).  Instead of a workspace
  * it uses a 32 MiB library-owned device array, held by every GPU that loads it
- * until the process exits; plans up to about 1.6e9 parameters fit (larger ones:
+ * until the process exits; plans up to about 1.2e9 parameters fit (larger ones:
  * DP_EINVAL with the sizes in dp_last_error()).  It allocates nothing.
  *   grads     bf16 [P][replica_stride] (input, 32-byte aligned)
  *   mean      fp32 [L] (output, 32-byte aligned): the reduce-scatter mean

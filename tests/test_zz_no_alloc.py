@@ -105,7 +105,7 @@ def _largest_fitting_plan(limit=32 << 20, tile=8192, P=2):
 
 def test_noalloc_near_the_size_limit():
     """A plan that uses all but the last tile's worth of the static array
-    (1.6e9 parameters, P = 2): the call equals the workspace path bit for bit on
+    (1.2e9 parameters, P = 2): the call equals the workspace path bit for bit on
     every element, twice in a row."""
     plan = _largest_fitting_plan()
     wl = small_workload(plan.sizes, plan.P, 1 << 40, sigma=1e-3, seed=13)
