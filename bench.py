@@ -196,6 +196,57 @@ def stored_traffic(workload, kernel):
     return rec["bytes_per_launch"], rec.get("how", "")
 
 
+_BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+
+
+def traffic_record(csv_path, target, captured, commands, out_dir=None):
+    """Write profiles/dram_traffic_<target>.txt from an ncu CSV of
+    dram__bytes_read.sum / dram__bytes_write.sum per launch taken on workload
+    `captured`: per kernel, the mean read + write bytes of its launches, scaled by
+    parameters from `captured` to `target` (every kernel streams each parameter's
+    bytes once, so its traffic grows in proportion).  `commands`: the ncu command
+    lines, recorded in the file's header."""
+    import csv
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    h = rows[hi]
+    col = {k: h.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit", "Metric Value")}
+    launches = {}
+    for r in rows[hi + 1:]:
+        if len(r) < len(h):
+            continue
+        name = r[col["Kernel Name"]]
+        key = next((k for k in KERNEL_BYTES_PER_PARAM if f"k_{k}<" in name or f"k_{k}(" in name), None)
+        if key is None or r[col["Metric Name"]] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        v = float(r[col["Metric Value"]].replace(",", "")) * _BYTE_UNITS[r[col["Metric Unit"]]]
+        launches.setdefault(key, {}).setdefault(r[col["ID"]], []).append(v)
+    wt, wc = workload_by_name(target), workload_by_name(captured)
+    scale = wt.n_params / wc.n_params
+    sha = kernel_source_hash()
+    lines = [f"# DRAM traffic per launch on {target} ({wt.n_params:,} params), the `traffic` field",
+             "# of bench.py's roofline (read only while kernel_src_sha matches the kernel sources'",
+             "# code, comments and whitespace removed).  Made on a GB300 by, after the same bench",
+             "# command exited 0 without ncu:"]
+    lines += [f"#   {c}" for c in commands]
+    rec = {}
+    for key, per in sorted(launches.items()):
+        vals = [sum(v) for v in per.values()]
+        mean = sum(vals) / len(vals)
+        alg = KERNEL_BYTES_PER_PARAM[key](wc.P) * wc.n_params
+        lines.append(f"# {key}: {len(vals)} launch(es) on {captured}, read + write "
+                     f"{mean / 1e9:.4f} GB (algorithmic {alg / 1e9:.4f} GB)"
+                     + (f", x {scale:.4f} (parameters) = {mean * scale / 1e9:.4f} GB" if scale != 1 else ""))
+        how = "ncu dram__bytes_read.sum + dram__bytes_write.sum" + (
+            f" on {captured} ({wc.n_params:,} params), scaled by parameters to {wt.n_params:,}"
+            if scale != 1 else f" on the full workload, mean of {len(vals)} launch(es)")
+        rec[f"{target}:{key}"] = {"bytes_per_launch": mean * scale, "kernel_src_sha": sha, "how": how}
+    out = os.path.join(out_dir or os.path.join(ROOT, "profiles"), f"dram_traffic_{target}.txt")
+    with open(out, "w") as f:
+        f.write("\n".join(lines) + "\n" + json.dumps(rec, indent=1) + "\n")
+    return out
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_sample_rate(wl, plan_sizes_offsets, grads_dev, master_dev, budget_s=15.0,
                        max_passes=3, step=1):
@@ -1303,6 +1354,12 @@ def run_reference(args, rank, world):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--traffic-record", default="",
+                    help="write profiles/dram_traffic_<--workload>.txt from this ncu CSV (no GPU)")
+    ap.add_argument("--traffic-captured-on", default="",
+                    help="--traffic-record: the workload the CSV was captured on (default: --workload)")
+    ap.add_argument("--traffic-command", action="append", default=[],
+                    help="--traffic-record: an ncu command line to record in the file (repeatable)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
@@ -1352,6 +1409,10 @@ def main(argv=None):
     if args.warmup < 3 and args.impl == "ours":
         print("note: warm-up raised to the minimum of 3", file=sys.stderr)
         args.warmup = 3
+    if args.traffic_record:
+        print(traffic_record(args.traffic_record, args.workload,
+                             args.traffic_captured_on or args.workload, args.traffic_command))
+        return
     if args.impl == "reference":
         # the CPU oracle runs on rank 0 only; other ranks exit without work
         rank = int(os.environ.get("RANK", "0"))

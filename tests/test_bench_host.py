@@ -149,3 +149,36 @@ def test_layer_groups_cover_every_tensor_once():
         for g0, g1 in g:
             keys = {".".join(n.split(".")[:2]) for n in wl.names[g0:g1]}
             assert len(keys) == 1
+
+
+def test_traffic_record_from_an_ncu_csv(tmp_path):
+    """--traffic-record: per kernel the mean read + write bytes of its launches,
+    scaled by parameters from the captured workload, with the current kernel hash;
+    bench.py's roofline reads it back."""
+    import json as js
+    import bench
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"')
+    rows = []
+    for i, (name, rd, wr) in enumerate([("void k_reduce_scatter<8, 0, 0, 0, 256>(KCommon)", 1000, 200),
+                                        ("k_norm_finalize(KCommon, double)", 5, 0),
+                                        ("void k_adamw_all_gather<0, 2048, 2>(KCommon)", 3000, 5000),
+                                        ("void k_reduce_scatter<8, 0, 0, 0, 256>(KCommon)", 1002, 198)]):
+        for metric, unit, v in (("dram__bytes_read.sum", "Mbyte", rd), ("dram__bytes_write.sum", "Mbyte", wr),
+                                ("gpu__time_duration.sum", "ns", 100)):
+            rows.append(f'"{i}","1","python","h","{name}","1","7","(256, 1, 1)","(456, 1, 1)","0",'
+                        f'"10.3","Command line profiler metrics","{metric}","{unit}","{v}"')
+    csv_path = tmp_path / "dram.csv"
+    csv_path.write_text("==PROF== noise\n" + hdr + "\n" + "\n".join(rows) + "\n")
+    out = bench.traffic_record(str(csv_path), "llama-1.1B-P8-zero2", "llama-2L-P8-zero2",
+                               ["ncu ..."], out_dir=str(tmp_path))
+    text = open(out).read()
+    rec = js.loads(text[text.index("{"):])
+    scale = 1_100_048_384 / 88_090_624
+    rs = rec["llama-1.1B-P8-zero2:reduce_scatter"]
+    ag = rec["llama-1.1B-P8-zero2:adamw_all_gather"]
+    assert abs(rs["bytes_per_launch"] - 1200e6 * scale) < 1.0
+    assert abs(ag["bytes_per_launch"] - 8000e6 * scale) < 1.0
+    assert rs["kernel_src_sha"] == bench.kernel_source_hash()
+    assert "# ncu ..." in text.replace("#   ", "# ")
