@@ -713,6 +713,14 @@ def run_streamed(args):
             dps.DP_TRACK_REDUCE_SCATTER if zero else dps.DP_TRACK_ALLREDUCE)
     tr = dps.Tracker(plan, mode, ws, grads, mean if zero else None, stream=comm,
                      max_ctas=args.comm_ctas)
+    side = None
+    producer = compute
+    if args.side_sms:
+        # the GPU split in two SM partitions: the streamed step's backward on the
+        # larger, every bucket but the last on the smaller; the last bucket on comm
+        side = dps.SmStreams(args.side_sms, priority=args.comm_priority, with_rest=True)
+        tr.set_side_stream(side.part, args.side_ctas or 3 * side.n_part)
+        producer = side.rest
 
     events = [torch.cuda.Event() for _ in wl.sizes]
     # marking: "tensor" = an event and a mark call per tensor; "batch" = an event
@@ -784,10 +792,15 @@ def run_streamed(args):
         if whole:
             tr.set_zero_step(params, master, m, v, cfg)
         tr.begin()
-        backward(compute, True)
+        producer.wait_stream(torch.cuda.current_stream())
+        backward(producer, True)
         tr.wait(60000)
         finish(comm)
         comm.synchronize()
+
+    def backward_on_producer():
+        producer.wait_stream(torch.cuda.current_stream())
+        backward(producer, False)
 
     def only_sync():
         sync_all(compute)
@@ -824,6 +837,7 @@ def run_streamed(args):
         return (t1 - t0) / reps * 1e3, host_mark_s[0] / reps * 1e3
 
     reps = max(3, args.steps // 5)
+    t_bp = timed(backward_on_producer, reps) if side is not None else None
     t_b = timed(only_backward, reps)
     t_s = timed(only_sync, reps)
     t_seq = timed(sequential, reps)
@@ -838,12 +852,16 @@ def run_streamed(args):
         "metric": "streamed per-bucket sync: share of sync time hidden under a synthetic backward",
         "value": hidden, "unit": "fraction", "higher_is_better": True,
         "ms": {"backward": t_b, "sync": t_s, "backward_then_sync": t_seq, "streamed": t_str,
-               "backward_beside_sync_no_waits": t_con, "backward_with_marks_dry": t_mrk},
+               "backward_beside_sync_no_waits": t_con, "backward_with_marks_dry": t_mrk,
+               **({"backward_on_the_larger_partition": t_bp} if t_bp is not None else {})},
         "host_ms": {"backward_issue": hb, "backward_issue_with_marks": hm,
                     "in_record_and_mark_calls": hmark},
         "per_step": {"marks": len(groups), "launches": n_launch, "stream_waits": n_wait},
         "config": {"workload": wl.name, "tokens": T, "comm_ctas": args.comm_ctas,
                    "mark": args.mark,
+                   "partitions": (f"backward on {side.n_rest} SMs, buckets but the last on "
+                                  f"{side.n_part} SMs ({args.side_ctas or 3 * side.n_part} CTAs)"
+                                  if side is not None else None),
                    "n_buckets": plan.n_buckets, "mode": wl.mode, "clip_max_norm": a.max_norm,
                    "comm_priority": args.comm_priority,
                    "tracker_mode": ("whole zero step per bucket" if whole else
@@ -1247,6 +1265,15 @@ def run_kernels(args):
         for b in range(nb):
             dps.dp_unit_reduce_scatter(plan, ws, unit_buf[:, :buckets[b][1]], b, mean, want_sumsq=True)
 
+    unit_bufs = [unit_buf, torch.empty_like(unit_buf)]
+
+    def unit_bwd_pass():
+        dps.dp_unit_all_gather(plan, ws, shards, 0, unit_bufs[0])
+        for b in range(nb):
+            o, ln, _ = buckets[b]
+            dps.dp_unit_backward(plan, ws, shards, b + 1 if b + 1 < nb else -1, unit_bufs[(b + 1) % 2],
+                                 grads[:, o:o + ln], b, mean, want_sumsq=True)
+
     table = [  # name, kernel, bytes per parameter, call
         ("dp_reduce_scatter_mean", "k_reduce_scatter", 2 * P + 4,
          lambda: dps.dp_reduce_scatter_mean(plan, ws, grads, mean, want_sumsq=True)),
@@ -1269,6 +1296,7 @@ def run_kernels(args):
          lambda: dps.dp_reduce_scatter_mean_accum(plan, ws, grads, micro, mean, want_sumsq=True)),
         ("dp_unit_all_gather (all units)", "k_unit_all_gather", 2 + 2 * P, unit_ag_pass),
         ("dp_unit_reduce_scatter (all units)", "k_reduce_scatter", 2 * P + 4, unit_rs_pass),
+        ("dp_unit_backward (all units)", "k_unit_backward", (2 + 2 * P) + (2 * P + 4), unit_bwd_pass),
         ("dp_shard_adamw_step", "k_adamw_all_gather (1 row)", 30,
          lambda: dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)),
     ]
@@ -1405,6 +1433,10 @@ def main(argv=None):
                          "an event and a call per layer (layer), or per tensor (tensor)")
     ap.add_argument("--comm-ctas", type=int, default=152,
                     help="grid cap of the streamed sync kernels")
+    ap.add_argument("--side-sms", type=int, default=0,
+                    help="--streamed: every bucket but the last on a stream confined to this many SMs")
+    ap.add_argument("--side-ctas", type=int, default=0,
+                    help="--streamed: grid cap on the SM-partition stream (default 3 per SM)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("note: warm-up raised to the minimum of 3", file=sys.stderr)

@@ -96,6 +96,9 @@ def lib():
             "dp_tracker_mark_ready_range": [vp, i32, i32, vp],
             "dp_tracker_mark_ready_batch": [vp, vp, vp, i32],
             "dp_tracker_stats": [vp, vp, vp],
+            "dp_tracker_set_side_stream": [vp, vp, i32],
+            "dp_sm_streams_create": [i32, i32, vp, vp, vp, vp, vp],
+            "dp_sm_streams_destroy": [vp],
             "dp_tracker_wait": [vp, i64],
             "dp_tracker_fired": [vp, vp, i32, vp],
             "dp_plan_fingerprint": [vp, vp],
@@ -478,6 +481,13 @@ class Tracker:
             evs = (C.c_void_p * max(len(ts), 1))(*[e.cuda_event for e in events])
         _check(lib().dp_tracker_mark_ready_batch(self._h, arr, evs, len(ts)))
 
+    def set_side_stream(self, stream, max_ctas=0):
+        """Every bucket but the last fires on `stream` (a torch stream, an SmStream,
+        or None to undo), grids capped at max_ctas."""
+        self._side = stream
+        _check(lib().dp_tracker_set_side_stream(self._h, None if stream is None else _stream(stream),
+                                                int(max_ctas)))
+
     def stats(self):
         """(launches, cudaStreamWaitEvent calls) of this step so far."""
         n, w = C.c_int32(), C.c_int32()
@@ -493,6 +503,31 @@ class Tracker:
         arr = (C.c_int32 * max(cap, 1))()
         _check(lib().dp_tracker_fired(self._h, arr, cap, C.byref(n)))
         return list(arr[:n.value])
+
+
+class SmStreams:
+    """CUDA streams confined to SM partitions (dp_sm_streams_create): .part runs on
+    n_sms SMs, .rest (with_rest=True) on all the others.  Each is a
+    torch.cuda.ExternalStream; close() (or garbage collection) destroys them."""
+
+    def __init__(self, n_sms, priority=0, with_rest=False):
+        s, r, h = C.c_void_p(), C.c_void_p(), C.c_void_p()
+        n_part, n_rest = C.c_int32(), C.c_int32()
+        _check(lib().dp_sm_streams_create(int(n_sms), int(priority), C.byref(s),
+                                          C.byref(r) if with_rest else None, C.byref(h),
+                                          C.byref(n_part), C.byref(n_rest)))
+        self._h = h
+        self.n_part, self.n_rest = n_part.value, n_rest.value
+        self.part = torch.cuda.ExternalStream(s.value)
+        self.rest = torch.cuda.ExternalStream(r.value) if with_rest else None
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and _lib is not None:
+            _lib.dp_sm_streams_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
 
 
 def dp_accumulate(plan, ws, acc, micro, b0=0, b1=None, stream=None):

@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdpsync.so")
 LIB_CHECKED = os.path.join(HERE, "libdpsync_checked.so")   # -DDPSYNC_CHECKED: index checks
 SOURCES = ["plan.cpp", "api.cu", "kernels_reduce.cu", "kernels_update.cu", "noalloc.cu",
-           "tracker.cu", "checkpoint.cpp"]
+           "tracker.cu", "smstream.cu", "checkpoint.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -53,6 +53,9 @@ struct Tracker {
   std::vector<int32_t> pending;     // per bucket: tensors not yet marked
   int32_t next = 0;                 // next bucket to fire, in plan order
   std::vector<int32_t> fired;
+  void* side = nullptr;             // set: every bucket but the last fires here (dp_tracker_set_side_stream)
+  int side_ctas = 0;
+  cudaEvent_t side_done = nullptr;  // recorded on `side` before the last bucket fires on `stream`
   int32_t launches = 0;             // this step: kernel launches (a launch covers a bucket range)
   int32_t waits = 0;                // this step: cudaStreamWaitEvent calls
   std::vector<void*> wait_list;     // scratch: distinct events of the range being fired
@@ -81,7 +84,31 @@ void reset(Tracker& tr) {
 // tiles (lock held), after the stream has waited once for each distinct event of
 // their tensors.  One launch over consecutive buckets computes what per-bucket
 // launches would, tile by tile (the norm partials are per tile).
+int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas);
+
+// With a side stream, buckets before the plan's last fire there; the last bucket
+// (ready only when backward ends) fires on the tracker's stream after that stream
+// has waited for the side stream's work, so every reduction is ordered before
+// the tracker's stream.
 int fire(Tracker& tr, int32_t b0, int32_t b1) {
+  const int32_t nb = static_cast<int32_t>(tr.pending.size());
+  if (!tr.side || (tr.flags & DP_TRACK_DRY_RUN)) return fire_on(tr, b0, b1, tr.stream, tr.max_ctas);
+  const int32_t mid = b1 == nb ? nb - 1 : b1;   // [b0, mid) on the side stream
+  if (mid > b0) {
+    const int rc = fire_on(tr, b0, mid, tr.side, tr.side_ctas);
+    if (rc) return rc;
+  }
+  if (b1 < nb) return DP_OK;
+  cudaError_t e = cudaEventRecord(tr.side_done, static_cast<cudaStream_t>(tr.side));
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(tr.stream), tr.side_done, 0);
+  if (e != cudaSuccess) {
+    tr.error_text = std::string("dp_tracker: ordering after the side stream: ") + cudaGetErrorString(e);
+    return DP_ECUDA;
+  }
+  return fire_on(tr, nb - 1, nb, tr.stream, tr.max_ctas);
+}
+
+int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas) {
   for (int32_t b = b0; b < b1; ++b) tr.fired.push_back(b);
   tr.wait_list.clear();
   for (int32_t b = b0; b < b1; ++b)
@@ -95,7 +122,7 @@ int fire(Tracker& tr, int32_t b0, int32_t b1) {
     ++tr.launches;
     return DP_OK;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(tr.stream);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (void* ev : tr.wait_list) {
     const cudaError_t e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(ev), 0);
     if (e != cudaSuccess) {
@@ -109,8 +136,8 @@ int fire(Tracker& tr, int32_t b0, int32_t b1) {
   L.ws = tr.ws;
   L.tile_begin = tr.plan->b_tile0[b0];
   L.tile_end = tr.plan->b_tile0[b1];
-  L.stream = tr.stream;
-  L.max_ctas = tr.max_ctas;
+  L.stream = stream;
+  L.max_ctas = max_ctas;
   int e;
   if (tr.mode == DP_TRACK_ZERO_STEP) {
     if (!tr.zero_set) {
@@ -312,6 +339,24 @@ int dp_tracker_set_zero_step(dp_tracker* tracker, void* params, float* master, f
   return DP_OK;
 }
 
+int dp_tracker_set_side_stream(dp_tracker* tracker, void* side_stream, int32_t side_ctas) {
+  clear_error();
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (!tr) return fail(DP_EINVAL, "dp_tracker_set_side_stream: NULL tracker");
+  if (side_ctas < 0) return fail(DP_EINVAL, "dp_tracker_set_side_stream: side_ctas must be >= 0");
+  std::lock_guard<std::mutex> g(tr->mu);
+  if (tr->next != 0 && tr->next != static_cast<int32_t>(tr->pending.size()))
+    return fail(DP_EINVAL, "dp_tracker_set_side_stream: a step is in progress (some buckets fired)");
+  if (side_stream && !tr->side_done && !(tr->flags & DP_TRACK_DRY_RUN)) {
+    const cudaError_t e = cudaEventCreateWithFlags(&tr->side_done, cudaEventDisableTiming);
+    if (e != cudaSuccess)
+      return fail(DP_ECUDA, std::string("dp_tracker_set_side_stream: ") + cudaGetErrorString(e));
+  }
+  tr->side = side_stream;
+  tr->side_ctas = side_ctas;
+  return DP_OK;
+}
+
 int dp_tracker_begin(dp_tracker* tracker) {
   clear_error();
   Tracker* tr = reinterpret_cast<Tracker*>(tracker);
@@ -418,6 +463,10 @@ int dp_tracker_fired(const dp_tracker* tracker, int32_t* order, int32_t cap, int
   return DP_OK;
 }
 
-void dp_tracker_free(dp_tracker* tracker) { delete reinterpret_cast<Tracker*>(tracker); }
+void dp_tracker_free(dp_tracker* tracker) {
+  Tracker* tr = reinterpret_cast<Tracker*>(tracker);
+  if (tr && tr->side_done) cudaEventDestroy(tr->side_done);
+  delete tr;
+}
 
 }  // extern "C"

@@ -568,6 +568,14 @@ int dp_tracker_mark_ready_range(dp_tracker* tracker, int32_t t0, int32_t t1, voi
  * nothing is marked). */
 int dp_tracker_mark_ready_batch(dp_tracker* tracker, const int32_t* tensors,
                                 void* const* ready_events, int32_t n);
+/* Fire every bucket but the plan's last on side_stream (NULL: all on the tracker's
+ * stream), with each launch's grid capped at side_ctas CTAs (0: no cap).  The last
+ * bucket, ready only when backward ends, fires on the tracker's stream after it
+ * has waited for side_stream's work, so all reductions are still ordered before
+ * the tracker's stream.  Meant for the partition stream of dp_sm_streams_create,
+ * with the backward on its rest stream.  Not while a step has
+ * fired some but not all buckets (DP_EINVAL). */
+int dp_tracker_set_side_stream(dp_tracker* tracker, void* side_stream, int32_t side_ctas);
 /* This step so far: kernel launches made and cudaStreamWaitEvent calls issued
  * (with DP_TRACK_DRY_RUN: those that would have been; either pointer may be
  * NULL). */
@@ -576,6 +584,28 @@ int dp_tracker_wait(dp_tracker* tracker, int64_t timeout_ms);
 /* Buckets launched so far this step, in launch order (up to cap entries). */
 int dp_tracker_fired(const dp_tracker* tracker, int32_t* order, int32_t cap, int32_t* n_fired);
 void dp_tracker_free(dp_tracker* tracker);
+
+/*
+ * Streams whose kernels run only on a partition of the GPU's SMs (green
+ * contexts).  The GPU's SMs are split into groups of n_sms (rounded up to the
+ * driver's partition granularity, 8 on this GPU family); *part_stream runs on the
+ * first group, *rest_stream (if rest_stream is not NULL) on all the others.
+ * n_sms must leave SMs outside the partition.  *n_part and *n_rest (nullable)
+ * receive the two SM counts.  On one GPU the streamed mode's "communication" is
+ * SM work: reductions on part_stream beside a backward whose GEMMs run on
+ * rest_stream never take SMs from each other ("4.1 Data parallelism in depth",
+ * sec. 4.2: the bucket's collective runs while backward continues); a backward
+ * left on the whole GPU can still take the partition's SMs.  Measured on a
+ * GEMM-heavy synthetic backward (cuBLAS, 2-CTA clusters): its GEMMs ran 21% slower
+ * on 144 of 152 SMs, more than the reductions beside them gained, so the split
+ * pays only where the producer does not need every SM.  Streams belong to
+ * the current device; dp_sm_streams_destroy(handle) destroys both.  DP_ECUDA when
+ * the driver lacks green contexts.  The library's kernels launch on them like on
+ * any stream.
+ */
+int dp_sm_streams_create(int32_t n_sms, int32_t priority, void** part_stream, void** rest_stream,
+                         void** handle, int32_t* n_part, int32_t* n_rest);
+int dp_sm_streams_destroy(void* handle);
 
 /*
  * Synchronise `stream` and read the workspace's last clip results: norm

@@ -114,6 +114,80 @@ def test_range_marks_fire_bucket_ranges_that_equal_the_oracle(orc, mode):
     del events
 
 
+@pytest.mark.parametrize("side", ["stream", "sm-partition"])
+@pytest.mark.parametrize("mode", ["allreduce", "reduce_scatter", "zero_step"])
+def test_side_stream_results_equal_the_oracle(orc, side, mode):
+    """Every bucket but the last on a side stream (a plain stream, or one confined to
+    an SM partition), the last on the tracker's stream after it: the results equal
+    the oracle bit for bit, and everything is ordered before the tracker's stream."""
+    import oracle as oracle_mod
+    P = 8
+    sizes = [3, 1000, 65536, 13107, 26214, 4097, 27910, 9000, 700, 12000, 5, 31000]
+    wl = small_workload(sizes, P, 16 * 1024, seed=91, sigma=0.05)
+    c = Case(wl)
+    g = c.host_grads(1)
+    src = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).cuda()
+    base = wdev.tensor_bases(c.sizes)
+    grads = c.plan.new_replicas()
+    comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
+    if side == "sm-partition":
+        try:
+            sm = dps.SmStreams(8, with_rest=True)
+        except dps.DPError as e:                       # a driver without green contexts
+            pytest.skip(f"no SM-partition stream: {e}")
+        assert sm.n_part >= 8 and sm.n_part + sm.n_rest <= torch.cuda.get_device_properties(0).multi_processor_count
+        side_stream, cap, producer = sm.part, 2 * sm.n_part, sm.rest   # the producer on the rest
+    else:
+        side_stream, cap = torch.cuda.Stream(), 0
+    kinds = {"allreduce": dps.DP_TRACK_ALLREDUCE, "reduce_scatter": dps.DP_TRACK_REDUCE_SCATTER,
+             "zero_step": dps.DP_TRACK_ZERO_STEP}
+    mean = c.plan.new_state()
+    tr = dps.Tracker(c.plan, kinds[mode], c.ws, grads, mean, stream=comm)
+    tr.set_side_stream(side_stream, cap)
+    adamw = configs.AdamW(max_norm=0.0)
+    master0 = c.host_master()
+    if mode == "zero_step":
+        params = c.plan.new_replicas()
+        st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+        tr.set_zero_step(params, *st, dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps,
+                                                    adamw.weight_decay, 0.0, 1))
+    tr.begin()
+    events = []
+    with torch.cuda.stream(producer):
+        for t in reversed(range(len(sizes))):
+            o, n = c.off[t], c.sizes[t]
+            grads[:, o:o + n].copy_(src[:, base[t]:base[t] + n])
+            ev = torch.cuda.Event()
+            ev.record(producer)
+            events.append(ev)
+            tr.mark_ready(t, ev)
+    tr.wait(10000)
+    assert tr.fired() == list(range(c.plan.n_buckets))
+    comm.synchronize()                                 # the tracker's stream alone orders it all
+    if mode == "allreduce":
+        want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+        assert np.array_equal(c.from_replicas(grads), want)
+    elif mode == "reduce_scatter":
+        _, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+        assert np.array_equal(c.from_flat(mean).view(np.uint32), want_mean.view(np.uint32))
+        dps.dp_clip_coef(c.plan, c.ws, 1.0, stream=comm)
+        norm, _, _ = dps.dp_read_norm(c.plan, c.ws, stream=comm)
+        _, onorm = orc.clip_coef(orc.bucket_sumsq(c.sizes, wl.bucket_bytes, P, g), 1.0)
+        assert abs(norm - onorm) <= 1e-10 * onorm
+    else:
+        z = np.zeros_like(master0)
+        p_ref, m_ref, mm_ref, v_ref, _, _ = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, P, g,
+                                                          master0, z, z,
+                                                          oracle_mod.adamw_cfg(adamw, 1))
+        assert np.array_equal(c.from_replicas(params), p_ref)
+        for dev, ref in zip(st, (m_ref, mm_ref, v_ref)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+    del events
+    tr.set_side_stream(None)
+    if side == "sm-partition":
+        sm.close()
+
+
 def test_streamed_mesh_allreduce_equals_oracle(orc):
     """The tracker on a hybrid 2 x 4 plan fires the mesh all-reduce bucket by bucket."""
     P, R, S = 8, 2, 4

@@ -317,3 +317,21 @@ def test_batch_refusal_messages():
         tr.mark_ready_batch([2, 3])
     with pytest.raises(dps.DPError, match="outside"):
         tr.mark_ready_batch([4])
+
+
+def test_side_stream_rules_in_a_dry_run():
+    """A side stream changes where buckets run, not the firing order; it cannot be
+    changed while a step has fired some but not all buckets."""
+    sizes = [1000] * 8
+    plan, tr = dry(sizes, 4000, 2)
+    tr.set_side_stream(0x1234, 16)           # dry run: nothing is launched on it
+    tr.begin()
+    tr.mark_ready_range(4, 8)
+    with pytest.raises(dps.DPError, match="in progress"):
+        tr.set_side_stream(None)
+    with pytest.raises(dps.DPError):
+        tr.set_side_stream(0x1234, -1)
+    tr.mark_ready_range(0, 4)
+    tr.wait(1000)
+    assert tr.fired() == [0, 1, 2, 3]
+    tr.set_side_stream(None)
