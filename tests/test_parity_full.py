@@ -185,3 +185,78 @@ def test_sweep_p16_allreduce_sampled(orc, cap):
         want, _, _ = orc.allreduce_mean([wl.sizes[t] for t in tb], wl.bucket_bytes, wl.P, g_b)
         assert np.array_equal(host_grads(grads, off, wl.sizes, tb), want), f"bucket {b}"
     assert_replicas_equal(grads, plan.L)
+
+
+def test_llama_1b1_zero3_fused_backward_sampled(orc):
+    """The ZeRO-3 unit flow at the 1.1B workload's full size, its backward as
+    dp_unit_backward launches (the next unit's gather beside this unit's
+    reduce-scatter), two clipped steps: the global norm and coefficient equal the
+    oracle's; for sampled units (first, middle, last, random, and those holding
+    flat indices 2^29 and 2^30) the gathered rows equal the parameter shards, and
+    the mean, master/m/v and updated shards equal the oracle's step bit for bit
+    (the oracle pins that the ZeRO-3 update equals the ZeRO-2 step's on the same
+    mean, so its ZeRO-2 step on the sampled buckets is the reference)."""
+    wl = configs.llama_1b1_zero2()
+    plan, off, ws, grads = setup(wl)
+    master = plan.new_state()
+    wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
+    m, v, mean = plan.new_state(), plan.new_state(), plan.new_state()
+    shards = master.to(torch.bfloat16)
+    op = orc.plan(wl.sizes, wl.bucket_bytes, wl.P)
+    nb, P = op["n_buckets"], wl.P
+    rng = np.random.default_rng(wl.seed + 3)
+    sample = sorted(set([0, nb // 2, nb - 1] + rng.integers(0, nb, 2).tolist())
+                    | boundary_buckets(op, WRAP_POINTS))
+    buckets = [plan.bucket(b) for b in range(nb)]
+    max_len = max(ln for _, ln, _ in buckets)
+    bufs = [torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    state = {}
+    for b in sample:
+        mb = host_flat(master, off, wl.sizes, bucket_tensors(op, b))
+        state[b] = [mb, np.zeros_like(mb), np.zeros_like(mb)]
+    a = wl.adamw
+    for t in (1, 2):
+        if t > 1:
+            wdev.fill_grads(grads, off, wl, step=t)
+        keep = {b: host_grads(grads, off, wl.sizes, bucket_tensors(op, b)) for b in sample}
+        before = {b: shards[buckets[b][0]:buckets[b][0] + buckets[b][1]].clone() for b in sample}
+        sums = []
+        for b0 in range(0, nb, 16):
+            tb = sorted(x for b in range(b0, min(nb, b0 + 16)) for x in bucket_tensors(op, b))
+            sums.extend(orc.bucket_sumsq([wl.sizes[x] for x in tb], wl.bucket_bytes, P,
+                                         host_grads(grads, off, wl.sizes, tb)).tolist())
+        coef_ref, norm_ref = orc.clip_coef(sums, a.max_norm)
+        total = orc.sum(sums)
+        gathered = {}
+        dps.dp_unit_all_gather(plan, ws, shards, 0, bufs[0])
+        for b in range(nb):
+            o, ln, _ = buckets[b]
+            if b in sample:
+                gathered[b] = bufs[b % 2][:, :ln].clone()       # unit b's backward reads it
+            dps.dp_unit_backward(plan, ws, shards, b + 1 if b + 1 < nb else -1, bufs[(b + 1) % 2],
+                                 grads[:, o:o + ln], b, mean, want_sumsq=True)
+        dps.dp_clip_coef(plan, ws, a.max_norm)
+        dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards,
+                                dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay,
+                                              a.max_norm, t), use_clip_coef=True)
+        norm, coef, status = dps.dp_read_norm(plan, ws)
+        assert status == 0
+        assert math.isclose(norm, norm_ref, rel_tol=1e-10), (t, norm, norm_ref)
+        assert coef == coef_ref < 1.0
+        cfg = oracle_mod.adamw_cfg(a, t)
+        for b in sample:
+            tb = bucket_tensors(op, b)
+            for r in range(P):
+                assert torch.equal(gathered[b][r], before[b]), f"step {t} unit {b} row {r}"
+            p_ref, m_ref, mm_ref, v_ref, mean_ref, _ = orc.zero_step(
+                [wl.sizes[x] for x in tb], [wl.decay[x] for x in tb], wl.bucket_bytes, P, keep[b],
+                *state[b], cfg, sumsq_total=total)
+            got_mean = host_flat(mean, off, wl.sizes, tb)
+            assert np.array_equal(got_mean.view(np.uint32), mean_ref.view(np.uint32)), f"{t} {b} mean"
+            for name, dev, ref in (("master", master, m_ref), ("m", m, mm_ref), ("v", v, v_ref)):
+                got = host_flat(dev, off, wl.sizes, tb)
+                assert np.all(rel_err(got, ref) <= 1e-5), f"step {t} unit {b} {name}"
+                assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"{t} {b} {name}"
+            got_sh = u16(torch.cat([shards[off[x]:off[x] + wl.sizes[x]] for x in tb if wl.sizes[x]]))
+            assert np.array_equal(got_sh, p_ref[0]), f"step {t} unit {b} shards"
+            state[b] = [m_ref, mm_ref, v_ref]
