@@ -211,6 +211,7 @@ int dp_unit_all_gather(const dp_plan* plan, void* workspace, const void* param_s
   if (rc) return rc;
   if (unit < 0 || unit >= static_cast<int32_t>(L.plan->b_off.size()))
     return fail(DP_EINVAL, "dp_unit_all_gather: unit out of range");
+  if (L.plan->b_len[unit] == 0) return DP_OK;   // an empty unit: nothing to gather
   if ((rc = check_ptrs("dp_unit_all_gather", L.plan, {param_shards, unit_buf}))) return rc;
   if (unit_stride < L.plan->b_len[unit] || unit_stride % 16)
     return fail(DP_EINVAL, "dp_unit_all_gather: unit_stride must be >= the unit length and a multiple of 16");
@@ -227,6 +228,7 @@ int dp_unit_reduce_scatter(const dp_plan* plan, void* workspace, const void* uni
   if (rc) return rc;
   if (unit < 0 || unit >= static_cast<int32_t>(L.plan->b_off.size()))
     return fail(DP_EINVAL, "dp_unit_reduce_scatter: unit out of range");
+  if (L.plan->b_len[unit] == 0) return DP_OK;   // an empty unit: no elements, no partials
   if ((rc = check_ptrs("dp_unit_reduce_scatter", L.plan, {unit_grads, mean}))) return rc;
   if (unit_stride < L.plan->b_len[unit] || unit_stride % 16)
     return fail(DP_EINVAL, "dp_unit_reduce_scatter: unit_stride must be >= the unit length and a multiple of 16");
@@ -246,6 +248,8 @@ int dp_unit_backward(const dp_plan* plan, void* workspace, const void* param_sha
     clear_error();
     return fail(DP_EINVAL, std::string(fn) + ": unit outside [-1, " + std::to_string(nb) + ")");
   }
+  if (pl && gather_unit >= 0 && pl->b_len[gather_unit] == 0) gather_unit = -1;   // empty units:
+  if (pl && rs_unit >= 0 && pl->b_len[rs_unit] == 0) rs_unit = -1;               // nothing to do
   if (gather_unit < 0 && rs_unit < 0) {
     Launch L;
     return prepare(fn, plan, workspace, 0, 0, stream, &L);

@@ -467,6 +467,7 @@ int launch_unit_backward(const Launch& Lrs, const void* grads, float* mean, bool
       if (n_ag > cap / 2) n_ag = cap / 2;
       int64_t n_rs = cap - n_ag;
       if (n_rs > n_rs_tiles) n_rs = n_rs_tiles;
+      if (n_rs + n_ag == 0) return static_cast<int>(cudaSuccess);   // two empty units
       return launch_k(kern, static_cast<int>(n_rs + n_ag), kThreads, kUnitBwdSmem, Lrs.stream, krs,
                       static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0, kag, a,
                       static_cast<int>(n_rs));

@@ -349,6 +349,8 @@ int dp_adamw_all_gather(const dp_plan* plan, void* workspace, const float* mean,
  * dp_unit_reduce_scatter: the unit's gradients, rank r's in unit_grads[r][0..len),
  *   reduced in ring order to the fp32 mean of each owner's shard:
  *   mean[offset_unit + i]; want_sumsq also stores the unit's norm partials.
+ * An empty unit (a bucket of zero-size tensors only) is a no-op for both calls;
+ * its buffer pointers are not checked.
  * dp_shard_adamw_step: AdamW over all buckets on mean (times the clip
  *   coefficient chosen by use_clip_coef / coef_dev, as for dp_sharded_adamw_step),
  *   writing bf16(theta) to param_shards.

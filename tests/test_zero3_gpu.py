@@ -126,6 +126,41 @@ def test_zero3_shard_update_with_caller_coefficient(orc):
             assert np.array_equal(a.view(np.uint32), ref.view(np.uint32)), name
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["two-launches", "fused-backward"])
+def test_zero3_flow_with_an_empty_unit(orc, fused):
+    """A plan whose last unit is empty (zero-size tensors after an oversized one):
+    the unit calls, the fused backward included, launch nothing for it and the flow
+    still equals the oracle bit for bit."""
+    P = 4
+    sizes = [0, 0, 100, 3000]
+    wl = small_workload(sizes, P, 64, sigma=0.05, seed=5)
+    c = Case(wl)
+    assert [c.plan.bucket(b)[1] for b in range(c.plan.n_buckets)][-1] == 0
+    adamw = configs.AdamW(max_norm=1.0)
+    master = c.host_master()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    shards_h = u16(torch.from_numpy(master).to(torch.bfloat16))
+    shards = c.plan.new_state().to(torch.bfloat16)
+    wdev.fill_flat(shards, c.off, c.sizes, torch.from_numpy(master).to(torch.bfloat16).cuda())
+    st = [c.to_flat(master), c.plan.new_state(), c.plan.new_state()]
+    mean = c.plan.new_state()
+    max_len = max(c.plan.bucket(b)[1] for b in range(c.plan.n_buckets))
+    unit_buf = torch.zeros(P, max_len, dtype=torch.bfloat16, device="cuda")
+    g = c.host_grads(1)
+    cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
+                        adamw.max_norm, 1)
+    zero3_flow(c, c.to_replicas(g), shards, mean, st, cfg, unit_buf,
+               unit_buf2=torch.zeros_like(unit_buf) if fused else None)
+    shards_h, master, m, v, so = orc.zero3_step(c.sizes, c.decay, wl.bucket_bytes, P, g, shards_h,
+                                                master, m, v, oracle_mod.adamw_cfg(adamw, 1))
+    norm, coef, status = dps.dp_read_norm(c.plan, c.ws)
+    assert status == 0 and coef == so.coef
+    assert np.array_equal(u16(wdev.gather_flat(shards, c.off, c.sizes)), shards_h)
+    for dev, ref in zip(st, (master, m, v)):
+        assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+
+
 def test_unit_all_gather_fills_every_rank_row():
     wl = small_workload([3, 1000, 65536, 4097], 4, 64 * 1024, seed=3)
     c = Case(wl)
