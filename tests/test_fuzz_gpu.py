@@ -78,3 +78,33 @@ def test_random_mesh_allreduce(orc, seed):
     torch.cuda.synchronize()
     want, _, _ = orc.mesh_allreduce_mean(c.sizes, wl.bucket_bytes, R, S, g)
     assert np.array_equal(c.from_replicas(buf), want)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_plan_per_bucket_launches(orc, seed):
+    """Random plans launched bucket by bucket in backward order (the small-launch
+    kernels wherever a bucket's tiles fit): the all-reduce and the reduce-scatter
+    mean equal the oracle, and the clip norm from per-bucket norm partials equals
+    the one from a single launch, bit for bit."""
+    wl, _ = random_case(seed)
+    c = Case(wl)
+    g = c.host_grads(1)
+    nb = c.plan.n_buckets
+    buf = c.to_replicas(g)
+    mean_a, mean_b = c.plan.new_state(), c.plan.new_state()
+    dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean_a, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 0.05)
+    single = dps.dp_read_norm(c.plan, c.ws)
+    for b in reversed(range(nb)):
+        dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean_b, b, b + 1, want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 0.05)
+    per_bucket = dps.dp_read_norm(c.plan, c.ws)
+    assert per_bucket == single
+    assert torch.equal(mean_a.view(torch.int32), mean_b.view(torch.int32))
+    _, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
+    assert np.array_equal(c.from_flat(mean_b).view(np.uint32), want_mean.view(np.uint32))
+    for b in reversed(range(nb)):
+        dps.dp_allreduce_mean(c.plan, c.ws, buf, b, b + 1)
+    torch.cuda.synchronize()
+    want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
+    assert np.array_equal(c.from_replicas(buf), want)
