@@ -80,10 +80,11 @@ void reset(Tracker& tr) {
   (void)pl;
 }
 
-// Launch buckets [b0, b1) on the tracker's stream as one launch over their
-// tiles (lock held), after the stream has waited once for each distinct event of
-// their tensors.  One launch over consecutive buckets computes what per-bucket
-// launches would, tile by tile (the norm partials are per tile).
+// Launch buckets [b0, b1) on `stream` as one launch over their tiles, grid
+// capped at max_ctas (lock held), after the stream has waited once for each
+// distinct event of their tensors.  One launch over consecutive buckets computes
+// what per-bucket launches would, tile by tile (the norm partials are per
+// sub-tile).
 int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas);
 
 // With a side stream, buckets before the plan's last fire there; the last bucket
