@@ -88,8 +88,9 @@ def test_mesh_staged_equals_fused(R, S):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["two-launches", "fused-backward"])
 @pytest.mark.parametrize("R,S", [(2, 4), (4, 2), (3, 2)])
-def test_hybrid_full_shard_unit_flow_matches_oracle(orc, R, S):
+def test_hybrid_full_shard_unit_flow_matches_oracle(orc, R, S, fused):
     """HYBRID_SHARD proper: full sharding inside each group and data parallelism
     between groups ("4.1 Data parallelism in depth", sec. 6.3) — the ZeRO-3 unit
     flow on a mesh plan.  Each unit is gathered from the flat shard array, its
@@ -108,19 +109,28 @@ def test_hybrid_full_shard_unit_flow_matches_oracle(orc, R, S):
     mean = c.plan.new_state()
     unit_buf = torch.zeros(P, max(plan.bucket(b)[1] for b in range(nb)), dtype=torch.bfloat16,
                            device="cuda")
+    bufs = [unit_buf, torch.zeros_like(unit_buf)]
     for step in (1, 2):
         g = c.host_grads(step)
         grads = c.to_replicas(g)
         cfg = dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps, adamw.weight_decay,
                             adamw.max_norm, step)
         before = shards.clone()
+        if fused:      # the next unit's gather beside this unit's reduce-scatter, one launch
+            dps.dp_unit_all_gather(plan, c.ws, shards, 0, bufs[0])
         for b in range(nb):
             o, ln, _ = plan.bucket(b)
-            dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
+            if not fused:
+                dps.dp_unit_all_gather(plan, c.ws, shards, b, unit_buf)
             torch.cuda.synchronize()
             for r in range(P):
-                assert torch.equal(unit_buf[r, :ln], before[o:o + ln])
-            dps.dp_unit_reduce_scatter(plan, c.ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
+                assert torch.equal(bufs[b % 2 if fused else 0][r, :ln], before[o:o + ln])
+            if fused:
+                dps.dp_unit_backward(plan, c.ws, shards, b + 1 if b + 1 < nb else -1,
+                                     bufs[(b + 1) % 2], grads[:, o:o + ln], b, mean,
+                                     want_sumsq=True)
+            else:
+                dps.dp_unit_reduce_scatter(plan, c.ws, grads[:, o:o + ln], b, mean, want_sumsq=True)
         dps.dp_clip_coef(plan, c.ws, adamw.max_norm)
         dps.dp_shard_adamw_step(plan, c.ws, mean, *st, shards, cfg, use_clip_coef=True)
         p_o, master, m, v, so = orc.mesh_zero_step(c.sizes, c.decay, c.wl.bucket_bytes, R, S, g,
