@@ -672,8 +672,11 @@ def run_streamed(args):
     """DDP's overlap, measured: a synthetic backward (one bf16 GEMM per weight
     tensor, dW = dY^T X with `--tokens` rows, last tensor first) on a compute
     stream marks each tensor ready; the tracker fires every complete bucket's
-    reduction on a high-priority communication stream with a capped grid.
-    Compared with the backward alone and with backward-then-sync on one stream.
+    reduction on a communication stream: by default as short-lived CTAs on a
+    stream of the lowest priority, the backward's stream at the highest, so the
+    GEMM waves take the SMs first (`--launch persistent`: a persistent grid capped
+    at --comm-ctas).  Compared with the backward alone and with backward-then-sync
+    on one stream.
     ZeRO without clipping (--max-norm 0) fires each bucket's whole step
     (DP_TRACK_ZERO_STEP); with clipping the tracker reduce-scatters per bucket and
     the clip and the AdamW + all-gather pass follow the backward.  The GEMMs only
@@ -707,12 +710,12 @@ def run_streamed(args):
                          torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")))
         else:
             mats.append(None)
-    compute = torch.cuda.Stream()
+    compute = torch.cuda.Stream(priority=args.compute_priority)
     comm = torch.cuda.Stream(priority=args.comm_priority)
     mode = (dps.DP_TRACK_ZERO_STEP if whole else
             dps.DP_TRACK_REDUCE_SCATTER if zero else dps.DP_TRACK_ALLREDUCE)
     tr = dps.Tracker(plan, mode, ws, grads, mean if zero else None, stream=comm,
-                     max_ctas=args.comm_ctas)
+                     max_ctas=args.comm_ctas, short_ctas=args.launch == "short")
     side = None
     producer = compute
     if args.side_sms:
@@ -857,13 +860,16 @@ def run_streamed(args):
         "host_ms": {"backward_issue": hb, "backward_issue_with_marks": hm,
                     "in_record_and_mark_calls": hmark},
         "per_step": {"marks": len(groups), "launches": n_launch, "stream_waits": n_wait},
-        "config": {"workload": wl.name, "tokens": T, "comm_ctas": args.comm_ctas,
+        "config": {"workload": wl.name, "tokens": T,
+                   "launch": ("short-lived CTAs, one launch per bucket" if args.launch == "short"
+                              else f"persistent grid of at most {args.comm_ctas} CTAs"),
                    "mark": args.mark,
                    "partitions": (f"backward on {side.n_rest} SMs, buckets but the last on "
                                   f"{side.n_part} SMs ({args.side_ctas or 3 * side.n_part} CTAs)"
                                   if side is not None else None),
                    "n_buckets": plan.n_buckets, "mode": wl.mode, "clip_max_norm": a.max_norm,
                    "comm_priority": args.comm_priority,
+                   "compute_priority": args.compute_priority,
                    "tracker_mode": ("whole zero step per bucket" if whole else
                                     "reduce-scatter per bucket" if zero else
                                     "all-reduce per bucket")},
@@ -1402,8 +1408,15 @@ def main(argv=None):
     ap.add_argument("--mesh", default="",
                     help="R,S: hybrid mesh of R replicate groups x S shard ranks (R*S = P)")
     ap.add_argument("--zero3", action="store_true", help="time the ZeRO-3 unit flow")
-    ap.add_argument("--comm-priority", type=int, default=-1,
-                    help="with --streamed: CUDA priority of the communication stream (-1 high, 0 normal)")
+    ap.add_argument("--comm-priority", type=int, default=0,
+                    help="with --streamed: CUDA priority of the communication stream (0 lowest; "
+                         "lower numbers are higher priorities)")
+    ap.add_argument("--compute-priority", type=int, default=-16,
+                    help="with --streamed: CUDA priority of the backward's stream (clamped to "
+                         "the device's range; -16 = the highest)")
+    ap.add_argument("--launch", choices=["short", "persistent"], default="short",
+                    help="with --streamed: each bucket as short-lived CTAs (DP_TRACK_SHORT_CTAS) "
+                         "or as a persistent grid capped at --comm-ctas")
     ap.add_argument("--max-norm", type=float, default=None,
                     help="override the workload's clip threshold (0 = no clipping: one fused pass)")
     ap.add_argument("--prefetch", action="store_true",

@@ -23,6 +23,7 @@ DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ET
     0, -1, -2, -3, -4, -5, -6, -7
 DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT, DP_STATUS_NO_SCALARS = 1, 2, 4, 8
 DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_ZERO_STEP, DP_TRACK_DRY_RUN = 0, 1, 2, 1
+DP_TRACK_SHORT_CTAS = 2
 DP_CKPT_HOST = 1
 
 
@@ -410,10 +411,12 @@ class Tracker:
     mode: DP_TRACK_ALLREDUCE (in place on `grads`), DP_TRACK_REDUCE_SCATTER
     (into `mean`, with norm partials) or DP_TRACK_ZERO_STEP (each bucket's whole
     unclipped ZeRO step; targets from set_zero_step).  dry_run=True records the
-    firing order and launches nothing (no GPU needed)."""
+    firing order and launches nothing (no GPU needed).  short_ctas=True launches
+    each bucket as short-lived CTAs (DP_TRACK_SHORT_CTAS): pair it with a
+    low-priority `stream` and a higher-priority stream for the backward."""
 
     def __init__(self, plan, mode, ws=None, grads=None, mean=None, stream=None, max_ctas=0,
-                 dry_run=False):
+                 dry_run=False, short_ctas=False):
         self.plan = plan
         self._keep = (ws, grads, mean, stream)
         if not dry_run:
@@ -426,7 +429,9 @@ class Tracker:
             s = None
         h = C.c_void_p()
         _check(lib().dp_tracker_create(plan.handle, int(mode), _ptr(ws), _ptr(grads), _ptr(mean), s,
-                                       int(max_ctas), DP_TRACK_DRY_RUN if dry_run else 0,
+                                       int(max_ctas),
+                                       (DP_TRACK_DRY_RUN if dry_run else 0) |
+                                       (DP_TRACK_SHORT_CTAS if short_ctas else 0),
                                        C.byref(h)))
         self._h = h
         self._dry = dry_run

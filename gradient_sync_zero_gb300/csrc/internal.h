@@ -128,6 +128,8 @@ struct Launch {
   int64_t tile_end;
   void* stream;
   int max_ctas = 0;     // > 0: cap on the grid (leave SMs to concurrent work)
+  bool short_ctas = false;   // one short-lived CTA per tile (piece) instead of a
+                             // persistent grid; max_ctas is then ignored
 };
 
 // Each returns a cudaError_t value (0 = success).

@@ -173,6 +173,7 @@ int launch_tiles_per_sm(const Launch& L, int per_sm, K kernel, A... args) {
   }
   int64_t g = n < cap ? n : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
+  if (L.short_ctas && n <= INT_MAX) g = n;   // one CTA per tile
   return launch_k(kernel, static_cast<int>(g), kThreads, 0, L.stream, args...);
 }
 
@@ -198,6 +199,10 @@ int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... ar
     const int sms = sm_count();
     if (sms > 0 && cap > sms * per_sm) cap = sms * per_sm;
   }
+  if (L.short_ctas && n <= INT_MAX) {   // one CTA per tile
+    k.split = 1;
+    return launch_k(kernel, static_cast<int>(n), kThreads, 0, L.stream, k, args...);
+  }
   if (L.max_ctas > 0 && cap > L.max_ctas) cap = L.max_ctas;
   k.split = 2 * n <= cap ? 2 : 1;
   int64_t g = n * k.split < cap ? n * k.split : cap;
@@ -209,12 +214,19 @@ int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... ar
 // `threads` threads each, all fit on the GPU at once runs `small` (its kernel
 // issues all of a block's replica loads at once and checks the plan beside
 // them: latency, not bandwidth, bounds such a launch).  Otherwise `big` runs as
-// launch_tiles_split would launch it.
+// launch_tiles_split would launch it.  With L.short_ctas a launch inside one
+// bucket runs `small` whatever its size, one CTA per piece of a tile: each CTA
+// holds its SM for a few microseconds, so work of higher priority waiting for
+// SMs (a GEMM wave of the backward) gets them almost at once.
 template <class KB, class KS, class... A>
 int launch_small_or_split(const Launch& L, int per_sm, KB big, KS small, int threads, int split,
                           KCommon k, A... args) {
   const int64_t n = L.tile_end - L.tile_begin;
   if (n <= 0) return cudaSuccess;
+  if (L.short_ctas && k.one_nvec > 0 && n * split <= INT_MAX) {
+    k.split = split;
+    return launch_k(small, static_cast<int>(n * split), threads, 0, L.stream, k, args...);
+  }
   if (k.one_nvec > 0) {
     int cap = resident_ctas(small, threads);
     if (L.max_ctas > 0 && cap > L.max_ctas) cap = L.max_ctas;

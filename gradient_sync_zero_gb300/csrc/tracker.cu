@@ -84,7 +84,8 @@ void reset(Tracker& tr) {
 // capped at max_ctas (lock held), after the stream has waited once for each
 // distinct event of their tensors.  One launch over consecutive buckets computes
 // what per-bucket launches would, tile by tile (the norm partials are per
-// sub-tile).
+// sub-tile).  With DP_TRACK_SHORT_CTAS each bucket is its own launch of
+// short-lived CTAs (the single-bucket kernels), max_ctas ignored.
 int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas);
 
 // With a side stream, buckets before the plan's last fire there; the last bucket
@@ -118,9 +119,10 @@ int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas) {
       if (ev && std::find(tr.wait_list.begin(), tr.wait_list.end(), ev) == tr.wait_list.end())
         tr.wait_list.push_back(ev);
     }
+  const bool short_ctas = (tr.flags & DP_TRACK_SHORT_CTAS) != 0;
   if (tr.flags & DP_TRACK_DRY_RUN) {   // count what would be issued
     tr.waits += static_cast<int32_t>(tr.wait_list.size());
-    ++tr.launches;
+    tr.launches += short_ctas ? b1 - b0 : 1;
     return DP_OK;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -132,32 +134,37 @@ int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas) {
     }
     ++tr.waits;
   }
-  Launch L;
-  L.plan = tr.plan;
-  L.ws = tr.ws;
-  L.tile_begin = tr.plan->b_tile0[b0];
-  L.tile_end = tr.plan->b_tile0[b1];
-  L.stream = stream;
-  L.max_ctas = max_ctas;
-  int e;
-  if (tr.mode == DP_TRACK_ZERO_STEP) {
-    if (!tr.zero_set) {
-      tr.error_text = "dp_tracker: bucket " + std::to_string(b0) +
-                      " became ready before dp_tracker_set_zero_step";
-      return DP_EINVAL;
-    }
-    e = launch_zero_fused(L, tr.grads, tr.params, tr.master, tr.m, tr.v, tr.adam);
-  } else if (tr.mode == DP_TRACK_ALLREDUCE)
-    e = tr.micro ? launch_allreduce_accum(L, tr.grads, tr.micro) : launch_allreduce(L, tr.grads);
-  else
-    e = tr.micro ? launch_reduce_scatter_accum(L, tr.grads, tr.micro, tr.mean, true)
-                 : launch_reduce_scatter(L, tr.grads, tr.mean, true);
-  if (e) {
-    tr.error_text = std::string("dp_tracker: bucket launch: ") +
-                    cudaGetErrorString(static_cast<cudaError_t>(e));
-    return DP_ECUDA;
+  if (tr.mode == DP_TRACK_ZERO_STEP && !tr.zero_set) {
+    tr.error_text = "dp_tracker: bucket " + std::to_string(b0) +
+                    " became ready before dp_tracker_set_zero_step";
+    return DP_EINVAL;
   }
-  ++tr.launches;
+  for (int32_t lb = b0; lb < b1;) {
+    const int32_t le = short_ctas ? lb + 1 : b1;
+    Launch L;
+    L.plan = tr.plan;
+    L.ws = tr.ws;
+    L.tile_begin = tr.plan->b_tile0[lb];
+    L.tile_end = tr.plan->b_tile0[le];
+    L.stream = stream;
+    L.max_ctas = max_ctas;
+    L.short_ctas = short_ctas;
+    int e;
+    if (tr.mode == DP_TRACK_ZERO_STEP)
+      e = launch_zero_fused(L, tr.grads, tr.params, tr.master, tr.m, tr.v, tr.adam);
+    else if (tr.mode == DP_TRACK_ALLREDUCE)
+      e = tr.micro ? launch_allreduce_accum(L, tr.grads, tr.micro) : launch_allreduce(L, tr.grads);
+    else
+      e = tr.micro ? launch_reduce_scatter_accum(L, tr.grads, tr.micro, tr.mean, true)
+                   : launch_reduce_scatter(L, tr.grads, tr.mean, true);
+    if (e) {
+      tr.error_text = std::string("dp_tracker: bucket launch: ") +
+                      cudaGetErrorString(static_cast<cudaError_t>(e));
+      return DP_ECUDA;
+    }
+    ++tr.launches;
+    lb = le;
+  }
   return DP_OK;
 }
 
@@ -259,6 +266,8 @@ int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* 
   if (mode != DP_TRACK_ALLREDUCE && mode != DP_TRACK_REDUCE_SCATTER && mode != DP_TRACK_ZERO_STEP)
     return fail(DP_EINVAL, "dp_tracker_create: unknown mode");
   if (max_ctas < 0) return fail(DP_EINVAL, "dp_tracker_create: max_ctas must be >= 0");
+  if (flags & ~(DP_TRACK_DRY_RUN | DP_TRACK_SHORT_CTAS))
+    return fail(DP_EINVAL, "dp_tracker_create: unknown flags " + std::to_string(flags));
   const bool dry = (flags & DP_TRACK_DRY_RUN) != 0;
   if (!dry) {
     if (!workspace || (pl->L > 0 && (!grads || (mode == DP_TRACK_REDUCE_SCATTER && !mean))))

@@ -506,7 +506,8 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  * tensors and launches the bucket's reduction there.  Consecutive complete
  * buckets whose tensors all carry the same event (or none) become ready together
  * and go out as one launch over their tiles (the same results as one launch per
- * bucket); a bucket whose tensors carry different events goes out on its own:
+ * bucket; with DP_TRACK_SHORT_CTAS one launch per bucket all the same); a bucket
+ * whose tensors carry different events goes out on its own:
  *   DP_TRACK_ALLREDUCE       the in-place mean all-reduce of `grads`;
  *   DP_TRACK_REDUCE_SCATTER  the reduce-scatter mean into `mean` with norm
  *                            partials (follow with dp_clip_coef and
@@ -526,6 +527,18 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  *   max_ctas   cap on each launch's grid (0 = the full persistent grid), to leave
  *              SMs to the backward running beside it.
  *   flags      DP_TRACK_DRY_RUN: record the firing order, launch nothing.
+ *              DP_TRACK_SHORT_CTAS: every bucket goes out as its own launch of
+ *              short-lived CTAs, one per piece of a tile (an eighth of a tile
+ *              for the flat all-reduce and reduce-scatter, a tile otherwise),
+ *              instead of a persistent grid; max_ctas (and side_ctas) are then
+ *              ignored.  Such a CTA holds its SM for microseconds, so a kernel of
+ *              higher priority waiting for SMs gets them almost at once.  Meant
+ *              for comm_stream at the lowest priority and the backward's stream
+ *              at a higher one (cudaStreamCreateWithPriority): its GEMM waves
+ *              then take the SMs first and the reductions fill the SMs the GEMMs
+ *              leave idle and the gaps between them.  Results are those of the
+ *              persistent launches, bit for bit.
+ *              Other bits: DP_EINVAL.
  * Events are the caller's: keep them alive and unrecorded until their bucket
  * fires.  Marking a tensor twice in one step is DP_EINVAL.
  * Parameters that a step does not use (a skipped branch) never get a gradient,
@@ -536,7 +549,7 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  */
 typedef struct dp_tracker dp_tracker;
 enum { DP_TRACK_ALLREDUCE = 0, DP_TRACK_REDUCE_SCATTER = 1, DP_TRACK_ZERO_STEP = 2 };
-enum { DP_TRACK_DRY_RUN = 1 };
+enum { DP_TRACK_DRY_RUN = 1, DP_TRACK_SHORT_CTAS = 2 };
 
 int dp_tracker_create(const dp_plan* plan, int32_t mode, void* workspace, void* grads, float* mean,
                       void* comm_stream, int32_t max_ctas, int32_t flags, dp_tracker** out);

@@ -255,11 +255,13 @@ def test_streamed_zero_step_equals_fused(orc):
     assert np.array_equal(c.from_flat(st[0]).view(np.uint32), m_o.view(np.uint32))
 
 
+@pytest.mark.parametrize("short_ctas", [False, True], ids=["persistent", "short-ctas"])
 @pytest.mark.parametrize("mode", [dps.DP_TRACK_ALLREDUCE, dps.DP_TRACK_REDUCE_SCATTER])
-def test_streamed_last_micro_batch_equals_fused_single_launch(mode):
+def test_streamed_last_micro_batch_equals_fused_single_launch(mode, short_ctas):
     """Accumulation: grads holds the earlier micro-batches' sum; the last micro-batch's
     gradients arrive tensor by tensor in backward order into `micro`, and each bucket
-    fires the fused add + sync.  Equal, bit for bit, to one fused launch."""
+    fires the fused add + sync (persistent grids, or short-lived CTAs).  Equal, bit for
+    bit, to one fused launch."""
     P = 8
     wl = small_workload([3, 1000, 65536, 13107, 26214, 4097, 27910, 9000], P, 32 * 1024, seed=91)
     c = Case(wl)
@@ -283,7 +285,7 @@ def test_streamed_last_micro_batch_equals_fused_single_launch(mode):
     comm, producer = torch.cuda.Stream(), torch.cuda.Stream()
     torch.cuda.synchronize()
     tr = dps.Tracker(c.plan, mode, ws2, acc, mean if mode == dps.DP_TRACK_REDUCE_SCATTER else None,
-                     stream=comm)
+                     stream=comm, short_ctas=short_ctas)
     tr.set_micro(micro)
     tr.begin()
     keep = produce(c, g_last, micro, tr, producer, P)
@@ -346,3 +348,125 @@ def test_streamed_whole_zero_step_per_bucket_matches_oracle(orc, P, mesh, max_ct
         for dev, ref in zip(st, (master, m, v)):
             assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
         del keep
+
+
+def priority_streams():
+    """The communication stream at the lowest priority, the producer at the highest
+    (out-of-range priorities are clamped to the device's range)."""
+    return torch.cuda.Stream(priority=0), torch.cuda.Stream(priority=-16)
+
+
+@pytest.mark.parametrize("mode,mesh,marks", [
+    ("allreduce", None, "tensor"), ("allreduce", None, "range"), ("allreduce", (2, 4), "tensor"),
+    ("reduce_scatter", None, "tensor"), ("reduce_scatter", None, "range"),
+    ("zero_step", None, "range"), ("zero_step", (2, 4), "tensor")])
+def test_short_ctas_results_equal_the_oracle(orc, mode, mesh, marks):
+    """DP_TRACK_SHORT_CTAS: every bucket is its own launch of short-lived CTAs (one
+    per piece of a tile), the communication stream at the lowest priority and the
+    producer above it.  The results equal the oracle bit for bit (the norm to
+    1e-10), and range marks that complete several buckets at once still launch
+    once per bucket."""
+    import oracle as oracle_mod
+    P = 8
+    sizes = [3, 1000, 65536, 13107, 26214, 4097, 27910, 9000, 700, 12000, 5, 31000]
+    wl = small_workload(sizes, P, 16 * 1024, seed=92, sigma=0.05)
+    c = Case(wl)
+    if mesh:
+        c.plan = dps.Plan(wl.sizes, wl.bucket_bytes, P, c.decay, mesh=mesh)
+        c.off, c.ws = c.plan.tensor_offsets(), c.plan.new_workspace()
+    nb = c.plan.n_buckets
+    g = c.host_grads(1)
+    src = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).cuda()
+    base = wdev.tensor_bases(c.sizes)
+    grads, mean = c.plan.new_replicas(), c.plan.new_state()
+    comm, producer = priority_streams()
+    kinds = {"allreduce": dps.DP_TRACK_ALLREDUCE, "reduce_scatter": dps.DP_TRACK_REDUCE_SCATTER,
+             "zero_step": dps.DP_TRACK_ZERO_STEP}
+    tr = dps.Tracker(c.plan, kinds[mode], c.ws, grads, mean, stream=comm, max_ctas=4,
+                     short_ctas=True)
+    adamw = configs.AdamW(max_norm=0.0)
+    master0 = c.host_master()
+    if mode == "zero_step":
+        params = c.plan.new_replicas()
+        st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+        tr.set_zero_step(params, *st, dps.adamw_cfg(adamw.lr, adamw.beta1, adamw.beta2, adamw.eps,
+                                                    adamw.weight_decay, 0.0, 1))
+    groups = ([(t, t + 1) for t in range(len(sizes))] if marks == "tensor" else
+              [(t0, min(t0 + 3, len(sizes))) for t0 in range(0, len(sizes), 3)])
+    tr.begin()
+    events = []
+    with torch.cuda.stream(producer):
+        for t0, t1 in reversed(groups):
+            for t in reversed(range(t0, t1)):
+                o, n = c.off[t], c.sizes[t]
+                grads[:, o:o + n].copy_(src[:, base[t]:base[t] + n])
+            ev = torch.cuda.Event()
+            ev.record(producer)
+            events.append(ev)
+            tr.mark_ready_range(t0, t1, ev)
+    tr.wait(10000)
+    assert tr.fired() == list(range(nb))
+    assert tr.stats()[0] == nb                       # one launch per bucket
+    comm.synchronize()
+    if mode == "allreduce":
+        if mesh:
+            want = orc.mesh_allreduce_mean(c.sizes, wl.bucket_bytes, *mesh, g)
+            want = want[0] if isinstance(want, tuple) else want
+        else:
+            want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+        assert np.array_equal(c.from_replicas(grads), want)
+        assert_replicas_equal(grads, c.plan.L)
+    elif mode == "reduce_scatter":
+        _, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+        assert np.array_equal(c.from_flat(mean).view(np.uint32), want_mean.view(np.uint32))
+        dps.dp_clip_coef(c.plan, c.ws, 1.0, stream=comm)
+        norm, _, status = dps.dp_read_norm(c.plan, c.ws, stream=comm)
+        _, onorm = orc.clip_coef(orc.bucket_sumsq(c.sizes, wl.bucket_bytes, P, g), 1.0)
+        assert status == 0 and abs(norm - onorm) <= 1e-10 * onorm
+    else:
+        z = np.zeros_like(master0)
+        ocfg = oracle_mod.adamw_cfg(adamw, 1)
+        if mesh:
+            p_ref, m_ref, mm_ref, v_ref, _ = orc.mesh_zero_step(c.sizes, c.decay, wl.bucket_bytes,
+                                                                *mesh, g, master0, z, z, ocfg)
+        else:
+            p_ref, m_ref, mm_ref, v_ref, _, _ = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, P,
+                                                              g, master0, z, z, ocfg)
+        assert np.array_equal(c.from_replicas(params), p_ref)
+        for dev, ref in zip(st, (m_ref, mm_ref, v_ref)):
+            assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+    del events
+
+
+def test_short_ctas_bucket_larger_than_the_gpu_holds_at_once(orc):
+    """A bucket whose short CTAs (64 threads, eight per 16384-element tile) are more
+    than twice what the GPU can hold at once (32 CTAs per SM at most): the
+    all-reduce and the reduce-scatter with its norm partials still equal the oracle
+    bit for bit."""
+    P = 8
+    sizes = [3, 24_000_003, 70000]
+    wl = small_workload(sizes, P, 32 << 20, seed=93, sigma=0.05)
+    c = Case(wl)
+    big = max(range(c.plan.n_buckets), key=lambda b: c.plan.bucket(b)[1])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert c.plan.bucket(big)[1] // 16384 * 8 > 2 * 32 * sms
+    g = c.host_grads(1)
+    want, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, P, g)
+    for kind in (dps.DP_TRACK_REDUCE_SCATTER, dps.DP_TRACK_ALLREDUCE):
+        grads, mean = c.to_replicas(g), c.plan.new_state()
+        comm, _ = priority_streams()
+        torch.cuda.synchronize()
+        tr = dps.Tracker(c.plan, kind, c.ws, grads, mean, stream=comm, short_ctas=True)
+        tr.begin()
+        tr.mark_ready_range(0, len(sizes))
+        tr.wait(10000)
+        comm.synchronize()
+        if kind == dps.DP_TRACK_ALLREDUCE:
+            assert np.array_equal(c.from_replicas(grads), want)
+        else:
+            assert np.array_equal(c.from_flat(mean).view(np.uint32), want_mean.view(np.uint32))
+            dps.dp_clip_coef(c.plan, c.ws, 1.0, stream=comm)
+            norm, _, status = dps.dp_read_norm(c.plan, c.ws, stream=comm)
+            _, onorm = orc.clip_coef(orc.bucket_sumsq(c.sizes, wl.bucket_bytes, P, g), 1.0)
+            assert status == 0 and abs(norm - onorm) <= 1e-10 * onorm
+        del tr

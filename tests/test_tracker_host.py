@@ -136,6 +136,13 @@ def test_create_validates_buffers():
                                  C.byref(h)) == dps.DP_EINVAL    # reduce-scatter needs `mean`
     assert lib.dp_tracker_create(plan.handle, 7, ok, ok, ok, None, 0, 0,
                                  C.byref(h)) == dps.DP_EINVAL
+    for bad_flags in (4, 8, -1):                      # bits other than DRY_RUN | SHORT_CTAS
+        assert lib.dp_tracker_create(plan.handle, 0, None, None, None, None, 0,
+                                     dps.DP_TRACK_DRY_RUN | bad_flags, C.byref(h)) == dps.DP_EINVAL
+        assert b"unknown flags" in lib.dp_last_error()
+    assert lib.dp_tracker_create(plan.handle, 0, None, None, None, None, 0,
+                                 dps.DP_TRACK_DRY_RUN | dps.DP_TRACK_SHORT_CTAS, C.byref(h)) == 0
+    lib.dp_tracker_free(h)
 
 
 def test_set_micro_rules():
@@ -238,6 +245,20 @@ def test_range_mark_fires_completed_buckets_as_one_launch():
     assert tr.stats() == (3, 4)
     tr.begin()
     assert tr.stats() == (0, 0)
+
+
+def test_short_ctas_launch_every_bucket_on_its_own():
+    """DP_TRACK_SHORT_CTAS: a mark that completes several buckets still waits once
+    per distinct event, but launches each bucket separately, in plan order."""
+    sizes = [1000] * 8
+    plan = dps.Plan(sizes, 4000, 2)
+    tr = dps.Tracker(plan, dps.DP_TRACK_ALLREDUCE, dry_run=True, short_ctas=True)
+    tr.begin()
+    tr.mark_ready_range(4, 8, _Ev(0x1000))              # buckets 0 and 1: one wait, two launches
+    assert tr.fired() == [0, 1] and tr.stats() == (2, 1)
+    tr.mark_ready_range(0, 4)                           # buckets 2 and 3, no event
+    tr.wait(1000)
+    assert tr.fired() == [0, 1, 2, 3] and tr.stats() == (4, 1)
 
 
 def test_range_mark_held_back_and_released_together():
