@@ -876,6 +876,199 @@ def run_streamed(args):
     }
 
 
+def run_zero3_overlap(args):
+    """FSDP's overlap, measured (--zero3 --overlap): the ZeRO-3 unit flow beside a
+    synthetic forward and backward ("Data Parallelism: DDP, ZeRO and FSDP", "How
+    FSDP actually runs").  Forward, first layers first: unit u's GEMMs (Y = X W^T
+    per weight tensor, W read from the unit's gathered buffer) wait for u's
+    all-gather, which a gather stream issues one unit ahead.  Backward, last layers
+    first: the gather stream gathers the unit ahead while the current unit's GEMMs
+    (dX = dY W and dW = dY^T X per weight tensor) run; each unit's reduce-scatter
+    follows its GEMMs on a reduce-scatter stream.  A buffer is gathered into again
+    only after the GEMMs that read it are done.  Then the clip coefficient and the
+    shard update.  The gradients reduce-scattered are the workload's synthetic
+    replicas (the GEMM outputs only model the compute's time).  Compared with the
+    GEMMs alone, the flow alone, and both on one stream in the same order.  The
+    collectives run as short-lived CTAs on low-priority streams beside the compute
+    stream at the highest priority (--launch persistent: persistent grids on
+    high-priority streams)."""
+    import gradient_sync_zero_gb300 as dps
+
+    torch.cuda.set_device(0)
+    wl = workload_by_name(args.workload)
+    plan = dps.Plan(wl.sizes, wl.bucket_bytes, wl.P, wl.decay)
+    off = plan.tensor_offsets()
+    ws = plan.new_workspace()
+    grads = plan.new_replicas()
+    wdev.fill_grads(grads, off, wl, step=1)
+    master = plan.new_state()
+    wdev.fill_flat(master, off, wl.sizes, gen.master_values(wl, 0, wl.n_params, "cuda"))
+    shards = master.to(torch.bfloat16)
+    m, v, mean = plan.new_state(), plan.new_state(), plan.new_state()
+    nb, P, T = plan.n_buckets, plan.P, args.tokens
+    buckets = [plan.bucket(b) for b in range(nb)]
+    bufs = [torch.zeros(P, max(ln for _, ln, _ in buckets), dtype=torch.bfloat16, device="cuda")
+            for _ in range(2)]
+    short = args.launch == "short"
+    compute = torch.cuda.Stream(priority=args.compute_priority if short else 0)
+    s_gather = torch.cuda.Stream(priority=args.comm_priority if short else -1)
+    s_rs = torch.cuda.Stream(priority=args.comm_priority if short else -1)
+    a = wl.adamw
+    # weight tensors of each unit (views into a unit buffer's row 0) and GEMM operands
+    # shared by shape
+    unit_w = [[] for _ in range(nb)]
+    ops = {}
+    for t, shape in enumerate(wl.shapes):
+        if len(shape) < 2:
+            continue
+        rows, cols = shape[0], int(math.prod(shape[1:]))
+        b = plan.tensor(t)[0]
+        unit_w[b].append((off[t] - buckets[b][0], rows, cols))
+        if (rows, cols) not in ops:
+            ops[(rows, cols)] = dict(
+                x=torch.randn(T, cols, dtype=torch.bfloat16, device="cuda") * 0.01,
+                dy=torch.randn(T, rows, dtype=torch.bfloat16, device="cuda") * 0.01,
+                y=torch.empty(T, rows, dtype=torch.bfloat16, device="cuda"),
+                dx=torch.empty(T, cols, dtype=torch.bfloat16, device="cuda"),
+                dw=torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda"))
+
+    def gemms(b, buf, backward):
+        for o, rows, cols in unit_w[b]:
+            w = buf[0, o:o + rows * cols].view(rows, cols)
+            op = ops[(rows, cols)]
+            if backward:
+                torch.matmul(op["dy"], w, out=op["dx"])
+                torch.matmul(op["dy"].t(), op["x"], out=op["dw"])
+            else:
+                torch.matmul(op["x"], w.t(), out=op["y"])
+
+    def update(stream):
+        dps.dp_clip_coef(plan, ws, a.max_norm, stream=stream)
+        dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True,
+                                stream=stream)
+
+    cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, a.max_norm, 1)
+    fwd, bwd = list(reversed(range(nb))), list(range(nb))
+
+    def rs(b, stream):
+        o, ln, _ = buckets[b]
+        dps.dp_unit_reduce_scatter(plan, ws, grads[:, o:o + ln], b, mean, want_sumsq=True,
+                                   stream=stream)
+
+    def one_stream(with_gemms, with_flow):
+        with torch.cuda.stream(compute):
+            for i, b in enumerate(fwd):
+                if with_flow:
+                    dps.dp_unit_all_gather(plan, ws, shards, b, bufs[i % 2])
+                if with_gemms:
+                    gemms(b, bufs[i % 2], False)
+            for i, b in enumerate(bwd):
+                if with_flow:
+                    dps.dp_unit_all_gather(plan, ws, shards, b, bufs[i % 2])
+                if with_gemms:
+                    gemms(b, bufs[i % 2], True)
+                if with_flow:
+                    rs(b, compute)
+            if with_flow:
+                update(compute)
+
+    def overlapped():
+        cur = torch.cuda.current_stream()
+        for s_ in (compute, s_gather, s_rs):
+            s_.wait_stream(cur)
+        released = [None, None]
+
+        def gather(i, order):
+            with torch.cuda.stream(s_gather):
+                if released[i % 2] is not None:
+                    s_gather.wait_event(released[i % 2])
+                dps.dp_unit_all_gather(plan, ws, shards, order[i], bufs[i % 2], stream=s_gather)
+                ev = torch.cuda.Event()
+                ev.record(s_gather)
+            return ev
+
+        for order, backward in ((fwd, False), (bwd, True)):
+            ready = gather(0, order)
+            for i, b in enumerate(order):
+                nxt = gather(i + 1, order) if i + 1 < len(order) else None
+                compute.wait_event(ready)
+                with torch.cuda.stream(compute):
+                    gemms(b, bufs[i % 2], backward)
+                    done = torch.cuda.Event()
+                    done.record(compute)
+                released[i % 2] = done
+                if backward:
+                    s_rs.wait_event(done)
+                    rs(b, s_rs)
+                ready = nxt
+        compute.wait_stream(s_rs)
+        compute.wait_stream(s_gather)
+        update(compute)
+        cur.wait_stream(compute)
+
+    def timed(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps * 1e3
+
+    def flow_on(stream):
+        cur = torch.cuda.current_stream()
+        stream.wait_stream(cur)
+        with torch.cuda.stream(stream):
+            for i, b in enumerate(fwd):
+                dps.dp_unit_all_gather(plan, ws, shards, b, bufs[i % 2])
+            for i, b in enumerate(bwd):
+                dps.dp_unit_all_gather(plan, ws, shards, b, bufs[i % 2])
+                rs(b, stream)
+            update(stream)
+        cur.wait_stream(stream)
+
+    if short:
+        for s_ in (s_gather, s_rs):
+            dps.set_stream_launch(s_, True)
+    try:
+        reps = max(3, args.steps // 5)
+        t_c = timed(lambda: one_stream(True, False), reps)
+        t_f = timed(lambda: one_stream(False, True), reps)
+        t_seq = timed(lambda: one_stream(True, True), reps)
+        t_ov = timed(overlapped, reps)
+        t_part = None
+        if args.side_sms:
+            # the flow alone on a partition of the SMs the GEMMs leave idle: what the
+            # collectives can do beside the GEMMs without taking SMs from them
+            part = dps.SmStreams(args.side_sms)
+            try:
+                t_part = timed(lambda: flow_on(part.part), reps)
+            finally:
+                part.close()
+    finally:
+        for s_ in (s_gather, s_rs):
+            dps.set_stream_launch(s_, False)
+    n_gemm = sum(len(u) for u in unit_w)
+    return {
+        "metric": "ZeRO-3 unit flow beside a synthetic forward + backward: share of the flow's "
+                  "time hidden",
+        "value": (t_seq - t_ov) / max(t_seq - t_c, 1e-9), "unit": "fraction",
+        "higher_is_better": True,
+        "ms": {"gemms": t_c, "flow": t_f, "gemms_then_flow_one_stream": t_seq,
+               "overlapped": t_ov,
+               **({f"flow_alone_on_{part.n_part}_sms": t_part} if t_part is not None else {})},
+        "config": {"workload": wl.name, "P": P, "n_units": nb, "tokens": T,
+                   "gemms_per_step": 3 * n_gemm,
+                   "gemm_tflops_per_step": 6 * T * sum(r * c for u in unit_w for _, r, c in u) / 1e12,
+                   "launch": ("short-lived CTAs on low-priority gather and reduce-scatter streams, "
+                              "compute at the highest priority" if short else
+                              "persistent grids on high-priority gather and reduce-scatter streams"),
+                   "data": "synthetic gradients resident; GEMM operands random, W from the "
+                           "gathered unit buffer"},
+    }
+
+
 def run_zero3(args):
     """ZeRO-3 unit flow on the bench workload: per step, every unit's forward
     all-gather (last bucket first), its backward all-gather and gradient
@@ -1426,6 +1619,9 @@ def main(argv=None):
                          "unit and reduce-scatter of this one in one launch)")
     ap.add_argument("--graph", action="store_true",
                     help="with --zero3: replay the unit passes from a CUDA graph")
+    ap.add_argument("--overlap", action="store_true",
+                    help="with --zero3: the unit flow beside a synthetic forward and backward "
+                         "(FSDP's overlap; --tokens GEMM rows, --launch)")
     ap.add_argument("--kernels", action="store_true",
                     help="time every entry point's kernel on the workload")
     ap.add_argument("--sweep", action="store_true",
@@ -1470,7 +1666,7 @@ def main(argv=None):
         print(json.dumps(run_streamed(args)), flush=True)
         return
     if args.zero3:
-        print(json.dumps(run_zero3(args)), flush=True)
+        print(json.dumps(run_zero3_overlap(args) if args.overlap else run_zero3(args)), flush=True)
         return
     if args.accum:
         print(json.dumps(run_accum(args)), flush=True)

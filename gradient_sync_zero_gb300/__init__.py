@@ -24,6 +24,7 @@ DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ET
 DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT, DP_STATUS_NO_SCALARS = 1, 2, 4, 8
 DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_ZERO_STEP, DP_TRACK_DRY_RUN = 0, 1, 2, 1
 DP_TRACK_SHORT_CTAS = 2
+DP_LAUNCH_PERSISTENT, DP_LAUNCH_SHORT_CTAS = 0, 1
 DP_CKPT_HOST = 1
 
 
@@ -105,6 +106,8 @@ def lib():
             "dp_plan_fingerprint": [vp, vp],
             "dp_plan_check_match": [vp, vp, i32],
             "dp_tracker_set_zero_step": [vp, vp, vp, vp, vp, vp],
+            "dp_stream_set_launch": [vp, i32],
+            "dp_stream_get_launch": [vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -282,6 +285,22 @@ def _ws(plan, ws):
 
 def _range(plan, b0, b1):
     return int(b0), int(plan.n_buckets if b1 is None else b1)
+
+
+def set_stream_launch(stream, short_ctas):
+    """Launch shape of every later compute call on `stream` (dp_stream_set_launch):
+    short_ctas=True for short-lived CTAs (a low-priority stream beside a
+    high-priority compute stream), False for the default persistent grids.  Set
+    False again before the stream is destroyed."""
+    _check(lib().dp_stream_set_launch(_stream(stream),
+                                      DP_LAUNCH_SHORT_CTAS if short_ctas else DP_LAUNCH_PERSISTENT))
+
+
+def stream_launch(stream):
+    """True when `stream` is set to short-lived CTAs."""
+    out = C.c_int32()
+    _check(lib().dp_stream_get_launch(_stream(stream), C.byref(out)))
+    return out.value == DP_LAUNCH_SHORT_CTAS
 
 
 def dp_plan_upload(plan, ws, stream=None):

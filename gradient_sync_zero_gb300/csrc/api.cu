@@ -5,10 +5,13 @@
 
 #include <cstddef>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "internal.h"
 
@@ -32,6 +35,23 @@ int adam_scalars(const char* fn, const dp_adamw_cfg* cfg, AdamScalars* s) {
   s->sqrt_bc2 = static_cast<float>(std::sqrt(1.0 - std::pow(cfg->beta2, t)));
   s->eps = static_cast<float>(cfg->eps);
   return DP_OK;
+}
+
+namespace {
+
+// Streams set to DP_LAUNCH_SHORT_CTAS, by handle.  The count lets the common
+// case (no stream set) skip the lock.
+std::mutex g_shape_mu;
+std::unordered_map<void*, int32_t> g_shape;
+std::atomic<int> g_shape_count{0};
+
+}  // namespace
+
+bool stream_short_ctas(void* stream) {
+  if (g_shape_count.load(std::memory_order_acquire) == 0) return false;
+  std::lock_guard<std::mutex> lock(g_shape_mu);
+  const auto it = g_shape.find(stream);
+  return it != g_shape.end() && it->second == DP_LAUNCH_SHORT_CTAS;
 }
 
 }  // namespace dps
@@ -64,6 +84,7 @@ int prepare(const char* fn, const dp_plan* plan, void* ws, int32_t b0, int32_t b
   L->tile_begin = pl->b_tile0[b0];
   L->tile_end = pl->b_tile0[b1];
   L->stream = stream;
+  L->short_ctas = stream_short_ctas(stream);
   return DP_OK;
 }
 
@@ -110,6 +131,30 @@ int record(void* const* ev, int i, void* stream) {
 }  // namespace
 
 extern "C" {
+
+int dp_stream_set_launch(void* stream, int32_t shape) {
+  clear_error();
+  if (shape != DP_LAUNCH_PERSISTENT && shape != DP_LAUNCH_SHORT_CTAS)
+    return fail(DP_EINVAL, "dp_stream_set_launch: unknown launch shape " + std::to_string(shape));
+  std::lock_guard<std::mutex> lock(g_shape_mu);
+  try {
+    if (shape == DP_LAUNCH_PERSISTENT)
+      g_shape.erase(stream);
+    else
+      g_shape[stream] = shape;
+  } catch (const std::bad_alloc&) {
+    return fail(DP_ENOMEM, "dp_stream_set_launch: out of host memory");
+  }
+  g_shape_count.store(static_cast<int>(g_shape.size()), std::memory_order_release);
+  return DP_OK;
+}
+
+int dp_stream_get_launch(void* stream, int32_t* shape) {
+  clear_error();
+  if (!shape) return fail(DP_EINVAL, "dp_stream_get_launch: NULL shape");
+  *shape = stream_short_ctas(stream) ? DP_LAUNCH_SHORT_CTAS : DP_LAUNCH_PERSISTENT;
+  return DP_OK;
+}
 
 int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream) {
   clear_error();

@@ -132,6 +132,9 @@ struct Launch {
                              // persistent grid; max_ctas is then ignored
 };
 
+// The launch shape set for `stream` by dp_stream_set_launch (host registry).
+bool stream_short_ctas(void* stream);
+
 // Each returns a cudaError_t value (0 = success).
 int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool sumsq,
                           int64_t rep_stride = 0, int64_t rep_block0 = 0);

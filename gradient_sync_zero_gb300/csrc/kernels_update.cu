@@ -228,6 +228,7 @@ int launch_replicate(const Launch& L, const RepArgs& a) {
   const int64_t n = L.tile_end - L.tile_begin;
   int64_t g = n < cap ? n : cap;
   if (L.max_ctas > 0 && g > L.max_ctas) g = L.max_ctas;
+  if (L.short_ctas && n <= INT_MAX) g = n;   // one CTA per tile
   return launch_k(k_replicate, static_cast<int>(g), 32, kRepSmem, L.stream, make_common(L), a);
 }
 
@@ -467,6 +468,10 @@ int launch_unit_backward(const Launch& Lrs, const void* grads, float* mean, bool
       if (n_ag > cap / 2) n_ag = cap / 2;
       int64_t n_rs = cap - n_ag;
       if (n_rs > n_rs_tiles) n_rs = n_rs_tiles;
+      if (Lrs.short_ctas && n_rs_tiles + n_ag_tiles <= INT_MAX) {   // one CTA per tile
+        n_rs = n_rs_tiles;
+        n_ag = n_ag_tiles;
+      }
       if (n_rs + n_ag == 0) return static_cast<int>(cudaSuccess);   // two empty units
       return launch_k(kern, static_cast<int>(n_rs + n_ag), kThreads, kUnitBwdSmem, Lrs.stream, krs,
                       static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0, kag, a,

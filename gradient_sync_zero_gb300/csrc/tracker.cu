@@ -119,7 +119,7 @@ int fire_on(Tracker& tr, int32_t b0, int32_t b1, void* stream, int max_ctas) {
       if (ev && std::find(tr.wait_list.begin(), tr.wait_list.end(), ev) == tr.wait_list.end())
         tr.wait_list.push_back(ev);
     }
-  const bool short_ctas = (tr.flags & DP_TRACK_SHORT_CTAS) != 0;
+  const bool short_ctas = (tr.flags & DP_TRACK_SHORT_CTAS) != 0 || stream_short_ctas(stream);
   if (tr.flags & DP_TRACK_DRY_RUN) {   // count what would be issued
     tr.waits += static_cast<int32_t>(tr.wait_list.size());
     tr.launches += short_ctas ? b1 - b0 : 1;

@@ -214,6 +214,35 @@ int dp_plan_check_match(const dp_plan* plan, const uint64_t* fingerprints, int32
 int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream);
 
 /*
+ * Launch shape of the compute calls enqueued on one stream.  DDP and FSDP run
+ * their collectives beside the backward ("4.1 Data parallelism in depth",
+ * sec. 4.2; "Data Parallelism: DDP, ZeRO and FSDP", "How FSDP actually runs");
+ * here those collectives are kernels that share the SMs with the backward's.
+ *   DP_LAUNCH_PERSISTENT  (every stream's default) a grid of at most the CTAs the
+ *                         GPU holds at once, each walking many tiles: fastest
+ *                         when the kernel has the GPU to itself.
+ *   DP_LAUNCH_SHORT_CTAS  one short-lived CTA per tile (per eighth of a tile for
+ *                         the flat all-reduce and reduce-scatter inside one
+ *                         bucket): each holds its SM for microseconds, so a kernel
+ *                         of a higher-priority stream waiting for SMs (a GEMM wave)
+ *                         gets them almost at once.  For a stream of the lowest
+ *                         priority beside a compute stream of a higher one
+ *                         (cudaStreamCreateWithPriority).
+ * Every call enqueued on `stream` afterwards, from any host thread, takes the
+ * shape, except dp_adamw_all_gather, dp_shard_adamw_step and the clipped
+ * dp_fused_zero_step's update pass (bulk-copy kernels that keep their persistent
+ * grid) and dp_clip_coef_noalloc; a tracker whose stream is set fires as with
+ * DP_TRACK_SHORT_CTAS.  Results do not depend on the shape, bit for bit.
+ * The setting is host state kept per stream handle (NULL: the legacy default
+ * stream); it costs an uncontended lock per call while any stream is set.  Set
+ * DP_LAUNCH_PERSISTENT again before destroying a stream: CUDA may give its
+ * handle to a later stream.  DP_EINVAL for another shape.
+ */
+enum { DP_LAUNCH_PERSISTENT = 0, DP_LAUNCH_SHORT_CTAS = 1 };
+int dp_stream_set_launch(void* stream, int32_t shape);
+int dp_stream_get_launch(void* stream, int32_t* shape);
+
+/*
  * Reduce-scatter + mean ("Data Parallelism: From Parameter Server to Ring All-Reduce", sec. 5:
  * the first N-1 ring steps leave each rank holding the complete sum of one
  * chunk; sec. 1: the synchronised gradient is the ranks' average).

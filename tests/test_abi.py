@@ -290,3 +290,35 @@ def test_binding_rejects_wrong_buffers_before_any_call():
     with pytest.raises(dps.DPError) as e:
         dps.Plan([1000], 1 << 20, 65)
     assert e.value.code == dps.DP_EINVAL
+
+
+def test_stream_launch_shape_registry():
+    """dp_stream_set_launch / dp_stream_get_launch keep a shape per stream handle on
+    the host (no device work): set, read back, reset, other handles untouched, NULL
+    (the legacy default stream) allowed, unknown shapes refused."""
+    lib = dps.lib()
+    a, b = C.c_void_p(0x5000), C.c_void_p(0x6000)
+    out = C.c_int32(-1)
+
+    def get(h):
+        assert lib.dp_stream_get_launch(h, C.byref(out)) == 0
+        return out.value
+
+    assert get(a) == dps.DP_LAUNCH_PERSISTENT and get(None) == dps.DP_LAUNCH_PERSISTENT
+    assert lib.dp_stream_set_launch(a, dps.DP_LAUNCH_SHORT_CTAS) == 0
+    assert get(a) == dps.DP_LAUNCH_SHORT_CTAS and get(b) == dps.DP_LAUNCH_PERSISTENT
+    assert lib.dp_stream_set_launch(None, dps.DP_LAUNCH_SHORT_CTAS) == 0
+    assert get(None) == dps.DP_LAUNCH_SHORT_CTAS
+    for bad in (2, -1, 7):
+        assert lib.dp_stream_set_launch(a, bad) == dps.DP_EINVAL
+        assert b"unknown launch shape" in lib.dp_last_error()
+    assert get(a) == dps.DP_LAUNCH_SHORT_CTAS          # a refused call changes nothing
+    assert lib.dp_stream_get_launch(a, None) == dps.DP_EINVAL
+    assert lib.dp_stream_set_launch(a, dps.DP_LAUNCH_PERSISTENT) == 0
+    assert lib.dp_stream_set_launch(None, dps.DP_LAUNCH_PERSISTENT) == 0
+    assert get(a) == dps.DP_LAUNCH_PERSISTENT and get(None) == dps.DP_LAUNCH_PERSISTENT
+    assert dps.stream_launch(0x5000) is False
+    dps.set_stream_launch(0x5000, True)
+    assert dps.stream_launch(0x5000) is True
+    dps.set_stream_launch(0x5000, False)
+    assert dps.stream_launch(0x5000) is False
