@@ -1,7 +1,7 @@
 """Seeded random plans against the oracle: tensor counts and sizes (zero-size,
 one-element, larger than the cap), bucket caps, rank counts 1..64 and mesh shapes
 drawn at random; the mean all-reduce, the clipped ZeRO-2 step and, on mesh plans,
-the hybrid all-reduce must match the oracle bit for bit."""
+the hybrid all-reduce must match the oracle bit for bit, on both launch shapes."""
 import numpy as np
 import pytest
 import torch
@@ -80,31 +80,70 @@ def test_random_mesh_allreduce(orc, seed):
     assert np.array_equal(c.from_replicas(buf), want)
 
 
+@pytest.mark.parametrize("shape", ["persistent", "short-ctas"])
 @pytest.mark.parametrize("seed", range(12))
-def test_random_plan_per_bucket_launches(orc, seed):
+def test_random_plan_per_bucket_launches(orc, seed, shape):
     """Random plans launched bucket by bucket in backward order (the small-launch
-    kernels wherever a bucket's tiles fit): the all-reduce and the reduce-scatter
-    mean equal the oracle, and the clip norm from per-bucket norm partials equals
-    the one from a single launch, bit for bit."""
+    kernels wherever a bucket's tiles fit, or, on a stream set to short-lived CTAs,
+    always): the all-reduce and the reduce-scatter mean equal the oracle, and the
+    clip norm from per-bucket norm partials equals the one from a single launch,
+    bit for bit."""
     wl, _ = random_case(seed)
     c = Case(wl)
     g = c.host_grads(1)
     nb = c.plan.n_buckets
-    buf = c.to_replicas(g)
-    mean_a, mean_b = c.plan.new_state(), c.plan.new_state()
-    dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean_a, want_sumsq=True)
-    dps.dp_clip_coef(c.plan, c.ws, 0.05)
-    single = dps.dp_read_norm(c.plan, c.ws)
-    for b in reversed(range(nb)):
-        dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean_b, b, b + 1, want_sumsq=True)
-    dps.dp_clip_coef(c.plan, c.ws, 0.05)
-    per_bucket = dps.dp_read_norm(c.plan, c.ws)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    if shape == "short-ctas":
+        dps.set_stream_launch(stream, True)
+    try:
+        with torch.cuda.stream(stream):
+            buf = c.to_replicas(g)
+            mean_a, mean_b = c.plan.new_state(), c.plan.new_state()
+            dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean_a, want_sumsq=True)
+            dps.dp_clip_coef(c.plan, c.ws, 0.05)
+            single = dps.dp_read_norm(c.plan, c.ws)
+            for b in reversed(range(nb)):
+                dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean_b, b, b + 1, want_sumsq=True)
+            dps.dp_clip_coef(c.plan, c.ws, 0.05)
+            per_bucket = dps.dp_read_norm(c.plan, c.ws)
+            for b in reversed(range(nb)):
+                dps.dp_allreduce_mean(c.plan, c.ws, buf, b, b + 1)
+        stream.synchronize()
+    finally:
+        dps.set_stream_launch(stream, False)
     assert per_bucket == single
     assert torch.equal(mean_a.view(torch.int32), mean_b.view(torch.int32))
-    _, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
+    want, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
     assert np.array_equal(c.from_flat(mean_b).view(np.uint32), want_mean.view(np.uint32))
-    for b in reversed(range(nb)):
-        dps.dp_allreduce_mean(c.plan, c.ws, buf, b, b + 1)
-    torch.cuda.synchronize()
-    want, _, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
     assert np.array_equal(c.from_replicas(buf), want)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_plan_unclipped_zero_step_short_ctas(orc, seed):
+    """The one-pass ZeRO step (no clip) on a stream set to short-lived CTAs (one CTA
+    per tile) over random plans: every replica and master/m/v equal the oracle."""
+    wl, _ = random_case(seed)
+    wl.adamw = configs.AdamW(max_norm=0.0)
+    c = Case(wl)
+    g = c.host_grads(1)
+    master0 = c.host_master()
+    a = wl.adamw
+    cfg = dps.adamw_cfg(a.lr, a.beta1, a.beta2, a.eps, a.weight_decay, 0.0, 1)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    dps.set_stream_launch(stream, True)
+    try:
+        with torch.cuda.stream(stream):
+            params = c.plan.new_replicas()
+            st = [c.to_flat(master0), c.plan.new_state(), c.plan.new_state()]
+            dps.dp_fused_zero_step(c.plan, c.ws, c.to_replicas(g), params, *st, cfg)
+        stream.synchronize()
+    finally:
+        dps.set_stream_launch(stream, False)
+    z = np.zeros_like(master0)
+    p_o, m_o, mo, vo, _, _ = orc.zero_step(c.sizes, c.decay, wl.bucket_bytes, wl.P, g, master0, z,
+                                           z, oracle_mod.adamw_cfg(a, 1))
+    assert np.array_equal(c.from_replicas(params), p_o)
+    for dev, ref in zip(st, (m_o, mo, vo)):
+        assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
