@@ -907,8 +907,9 @@ def run_zero3_overlap(args):
     m, v, mean = plan.new_state(), plan.new_state(), plan.new_state()
     nb, P, T = plan.n_buckets, plan.P, args.tokens
     buckets = [plan.bucket(b) for b in range(nb)]
+    depth = max(1, args.prefetch_depth)
     bufs = [torch.zeros(P, max(ln for _, ln, _ in buckets), dtype=torch.bfloat16, device="cuda")
-            for _ in range(2)]
+            for _ in range(depth + 1)]
     short = args.launch == "short"
     compute = torch.cuda.Stream(priority=args.compute_priority if short else 0)
     s_gather = torch.cuda.Stream(priority=args.comm_priority if short else -1)
@@ -976,31 +977,34 @@ def run_zero3_overlap(args):
         cur = torch.cuda.current_stream()
         for s_ in (compute, s_gather, s_rs):
             s_.wait_stream(cur)
-        released = [None, None]
+        nbuf = len(bufs)
+        released = [None] * nbuf
 
         def gather(i, order):
             with torch.cuda.stream(s_gather):
-                if released[i % 2] is not None:
-                    s_gather.wait_event(released[i % 2])
-                dps.dp_unit_all_gather(plan, ws, shards, order[i], bufs[i % 2], stream=s_gather)
+                if released[i % nbuf] is not None:
+                    s_gather.wait_event(released[i % nbuf])
+                dps.dp_unit_all_gather(plan, ws, shards, order[i], bufs[i % nbuf], stream=s_gather)
                 ev = torch.cuda.Event()
                 ev.record(s_gather)
             return ev
 
         for order, backward in ((fwd, False), (bwd, True)):
-            ready = gather(0, order)
+            ready = {}
+            for i in range(min(depth, len(order))):          # `depth` units ahead
+                ready[i] = gather(i, order)
             for i, b in enumerate(order):
-                nxt = gather(i + 1, order) if i + 1 < len(order) else None
-                compute.wait_event(ready)
+                if i + depth < len(order):
+                    ready[i + depth] = gather(i + depth, order)
+                compute.wait_event(ready.pop(i))
                 with torch.cuda.stream(compute):
-                    gemms(b, bufs[i % 2], backward)
+                    gemms(b, bufs[i % nbuf], backward)
                     done = torch.cuda.Event()
                     done.record(compute)
-                released[i % 2] = done
+                released[i % nbuf] = done
                 if backward:
                     s_rs.wait_event(done)
                     rs(b, s_rs)
-                ready = nxt
         compute.wait_stream(s_rs)
         compute.wait_stream(s_gather)
         update(compute)
@@ -1059,7 +1063,7 @@ def run_zero3_overlap(args):
                "overlapped": t_ov,
                **({f"flow_alone_on_{part.n_part}_sms": t_part} if t_part is not None else {})},
         "config": {"workload": wl.name, "P": P, "n_units": nb, "tokens": T,
-                   "gemms_per_step": 3 * n_gemm,
+                   "prefetch_depth": depth, "gemms_per_step": 3 * n_gemm,
                    "gemm_tflops_per_step": 6 * T * sum(r * c for u in unit_w for _, r, c in u) / 1e12,
                    "launch": ("short-lived CTAs on low-priority gather and reduce-scatter streams, "
                               "compute at the highest priority" if short else
@@ -1619,6 +1623,8 @@ def main(argv=None):
                          "unit and reduce-scatter of this one in one launch)")
     ap.add_argument("--graph", action="store_true",
                     help="with --zero3: replay the unit passes from a CUDA graph")
+    ap.add_argument("--prefetch-depth", type=int, default=1,
+                    help="--zero3 --overlap: units gathered ahead of the compute (buffers = depth + 1)")
     ap.add_argument("--overlap", action="store_true",
                     help="with --zero3: the unit flow beside a synthetic forward and backward "
                          "(FSDP's overlap; --tokens GEMM rows, --launch)")
