@@ -24,6 +24,7 @@ parameters / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import dataclasses
 import json
 import math
@@ -483,7 +484,8 @@ def run_gpu(args, rank, local, world):
     # ---- end to end through the public call, host buffers ----
     if not args.no_e2e:
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
-        host = torch.empty_like(grads, device="cpu", pin_memory=True)
+        host_buf = PinnedHost(tuple(grads.shape), grads.dtype)
+        host = host_buf.t
         host.copy_(grads)
         torch.cuda.synchronize()
         for _ in range(1):                  # untimed: first transfer from fresh pinned pages
@@ -526,7 +528,8 @@ def run_gpu(args, rank, local, world):
         if readback:
             d2h_stream = torch.cuda.Stream()
             out_rep = params if zero else grads
-            host_out = torch.empty(L, dtype=torch.bfloat16, pin_memory=True)
+            host_out_buf = PinnedHost((L,), torch.bfloat16)
+            host_out = host_out_buf.t
         read_done = [None]                   # event: the last step's read-back finished
 
         def grouped_copies_ms():
@@ -635,9 +638,15 @@ def run_gpu(args, rank, local, world):
                                   + ("; one updated replica read back to pinned host memory every "
                                      "step, beside the next step's copy" if readback else "")
                                   if pipelined else "copy, then the step")}
+        result["e2e"]["host_memory"] = ("cudaHostAlloc, exact size" if host_buf.exact
+                                        else "torch pinned memory")
         if pipelined and zero:
             del mean_buf
         del host
+        host_buf.release()
+        if readback:
+            del host_out
+            host_out_buf.release()
 
     # ---- CPU oracle baseline (rank 0, N=1 only) ----
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -651,6 +660,43 @@ def run_gpu(args, rank, local, world):
         result["cpu_baseline"] = {"value": rate, "unit": "params/s", "cores": thr, "kind": "oracle",
                                   "sample": desc, "seconds": secs}
     return result
+
+
+class PinnedHost:
+    """A page-locked host tensor of exactly its size.  torch's pinned allocator rounds
+    each request up to a power of two (32 GB for the 17.6 GB of gradient replicas), so
+    large buffers come from cudaHostAlloc directly, through the CUDA runtime torch
+    loaded; torch's own pinned memory is the fallback."""
+
+    def __init__(self, shape, dtype):
+        self.ptr, self.rt = None, None
+        nbytes = int(math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        try:
+            path = next(ln.split()[-1] for ln in open("/proc/self/maps") if "libcudart.so" in ln)
+            self.rt = ctypes.CDLL(path)
+        except (OSError, StopIteration):
+            self.rt = None
+        p = ctypes.c_void_p()
+        if self.rt is not None and nbytes and \
+                self.rt.cudaHostAlloc(ctypes.byref(p), ctypes.c_size_t(nbytes), 0) == 0:
+            self.ptr = p.value
+            raw = (ctypes.c_uint8 * nbytes).from_address(self.ptr)
+            self.t = torch.frombuffer(raw, dtype=torch.uint8).view(dtype).view(shape)
+        else:
+            if self.rt is not None:
+                self.rt.cudaGetLastError()        # a refused allocation's error, read off
+            self.t = torch.empty(shape, dtype=dtype, pin_memory=True)
+
+    @property
+    def exact(self):
+        return self.ptr is not None
+
+    def release(self):
+        self.t = None
+        if self.ptr is not None:
+            torch.cuda.synchronize()
+            self.rt.cudaFreeHost(ctypes.c_void_p(self.ptr))
+            self.ptr = None
 
 
 def layer_groups(names):
