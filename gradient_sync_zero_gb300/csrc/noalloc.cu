@@ -26,8 +26,7 @@
 // wrong results: serialise them.
 //
 // Set-up.  The first call on each device looks up the array's device address
-// (cudaGetSymbolAddress) with that device current and caches it; that first call
-// should come before any stream capture.
+// (cudaGetSymbolAddress) with that device current and caches it.
 #include <cuda_runtime.h>
 
 #include <cstddef>

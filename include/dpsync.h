@@ -682,8 +682,8 @@ int dp_read_norm(const dp_plan* plan, const void* workspace, double* norm, float
  * checks *norm_out itself.
  * Every call shares the array and overwrites it; calls whose work overlaps on
  * the GPU (unordered streams, concurrent host threads) race and must be
- * serialised.  The first call on a device looks up the array's address; make
- * that first call before any stream capture.
+ * serialised.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it.
  */
 int dp_clip_coef_noalloc(const dp_plan* plan, const void* grads, float* mean, double max_norm,
                          float* coef_out, double* norm_out, void* stream);
