@@ -52,7 +52,7 @@ def _cuda_home():
     return os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
 
-GPU_PROGRAMS = ["allreduce_gpu", "zero_step_gpu"]
+GPU_PROGRAMS = ["allreduce_gpu", "zero_step_gpu", "tracker_gpu"]
 
 
 def _build_gpu_program(tmp_path, name="allreduce_gpu"):
@@ -85,6 +85,20 @@ def test_c_program_allreduces_on_the_gpu(tmp_path):
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, run.stdout + run.stderr
     assert "mismatches 0" in run.stdout
+
+
+@pytest.mark.gpu
+def test_c_program_streams_buckets_through_the_tracker(tmp_path):
+    """A C99 process with no Python in it: a high-priority producer stream uploads
+    tensors last first and marks them ready; the tracker fires every bucket's
+    all-reduce as short-lived CTAs on a lowest-priority stream, in plan order, one
+    launch per bucket; every replica holds the exact mean, and a single
+    dp_allreduce_mean on a stream set to short-lived CTAs gives the same bits."""
+    exe, r = _build_gpu_program(tmp_path, "tracker_gpu")
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "order ok mismatches 0" in run.stdout
 
 
 # the workload tests/c/zero_step_gpu.c runs (its sizes, decay flags, rank count,
