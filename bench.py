@@ -845,7 +845,11 @@ def run_streamed(args):
         backward(producer, True)
         tr.wait(60000)
         finish(comm)
-        comm.synchronize()
+        # the next step follows this one on the GPU, not after a host sync (the
+        # other variants do not sync either; the next step's events are recorded
+        # after this step's waits were enqueued)
+        torch.cuda.current_stream().wait_stream(comm)
+        torch.cuda.current_stream().wait_stream(producer)
 
     def backward_on_producer():
         producer.wait_stream(torch.cuda.current_stream())
