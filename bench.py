@@ -1373,7 +1373,8 @@ def run_sweep(args):
     6000 log-uniform 4K-64K vectors): per bucket cap and mode, the bucket and launch
     counts, the padding fraction, and the step time with one launch over the whole
     tile table, with one launch per bucket (DDP's granularity) issued from the host,
-    and with those per-bucket launches replayed from a CUDA graph."""
+    and with those per-bucket launches replayed from a CUDA graph, as one chain and as
+    --sweep-chains independent chains (the buckets touch disjoint memory)."""
     import gradient_sync_zero_gb300 as dps
 
     torch.cuda.set_device(0)
@@ -1414,9 +1415,12 @@ def run_sweep(args):
                 def single():
                     dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg)
 
+                def one_bucket(b):
+                    dps.dp_reduce_scatter_mean(plan, ws, grads, mean, b, b + 1, want_sumsq=True)
+
                 def buckets():
                     for b in range(nb):
-                        dps.dp_reduce_scatter_mean(plan, ws, grads, mean, b, b + 1, want_sumsq=True)
+                        one_bucket(b)
 
                 def tail():
                     dps.dp_clip_coef(plan, ws, a.max_norm)
@@ -1429,9 +1433,12 @@ def run_sweep(args):
                 def single():
                     dps.dp_allreduce_mean(plan, ws, grads)
 
+                def one_bucket(b):
+                    dps.dp_allreduce_mean(plan, ws, grads, b, b + 1)
+
                 def buckets():
                     for b in range(nb):
-                        dps.dp_allreduce_mean(plan, ws, grads, b, b + 1)
+                        one_bucket(b)
 
                 def tail():
                     pass
@@ -1445,7 +1452,7 @@ def run_sweep(args):
                 tail()
 
             t_bucket = timed(per_bucket, reps)
-            graph_ms, graph_note = None, ""
+            graph_ms, chains_ms, graph_note = None, None, ""
             try:
                 g = torch.cuda.CUDAGraph()
                 side = torch.cuda.Stream()
@@ -1462,13 +1469,42 @@ def run_sweep(args):
 
                 graph_ms = timed(graphed, reps)
                 del g
+                # the same launches as independent chains: the buckets touch disjoint
+                # memory, so bucket b goes to chain b mod K, forked from and joined
+                # to the capture stream (K graph branches instead of one chain)
+                chains = [torch.cuda.Stream() for _ in range(args.sweep_chains)]
+
+                def branched():
+                    cur = torch.cuda.current_stream()
+                    for s_ in chains:
+                        s_.wait_stream(cur)
+                    for b in range(nb):
+                        with torch.cuda.stream(chains[b % len(chains)]):
+                            one_bucket(b)
+                    for s_ in chains:
+                        cur.wait_stream(s_)
+
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(side):
+                    branched()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g2):
+                    branched()
+
+                def graphed2():
+                    g2.replay()
+                    tail()
+
+                chains_ms = timed(graphed2, reps)
+                del g2
             except Exception as e:  # noqa: BLE001  (reported in the line, not hidden)
                 graph_note = f"graph capture failed: {e}"
             rows.append({
                 "bucket_bytes": cap, "mode": mode, "n_buckets": nb, "n_tiles": plan.info.n_tiles,
                 "padding_frac": (plan.L - n) / n,
                 "launches": {"single": launches_single, "per_bucket": launches_bucket},
-                "ms": {"single": t_single, "per_bucket_host": t_bucket, "per_bucket_graph": graph_ms},
+                "ms": {"single": t_single, "per_bucket_host": t_bucket, "per_bucket_graph": graph_ms,
+                       f"per_bucket_graph_{args.sweep_chains}_chains": chains_ms},
                 "gbs_single": bpp * n / (t_single * 1e-3) / 1e9, "bytes_per_param": bpp,
                 **({"note": graph_note} if graph_note else {}),
             })
@@ -1686,6 +1722,8 @@ def main(argv=None):
                     help="--sweep: comma-separated bucket caps in bytes (default: the four caps)")
     ap.add_argument("--sweep-modes", default="allreduce,zero",
                     help="--sweep: allreduce, zero or both")
+    ap.add_argument("--sweep-chains", type=int, default=8,
+                    help="--sweep: independent graph chains the per-bucket launches are spread over")
     ap.add_argument("--sweep-groups", type=int, default=24,
                     help="--sweep: groups of (matrix + 250 vectors) in the workload (24 = full)")
     ap.add_argument("--accum", type=int, default=0,

@@ -633,11 +633,13 @@ __device__ __forceinline__ bool plan_ok(const KCommon& k) {
   return false;
 }
 
-// Start of a kernel whose launch lies inside one bucket (k.one_nvec > 0): after
-// the dependency wait, the plan id is loaded, but not waited for, so the first
-// replica loads go out beside it; plan_matches() then gates the stores.  Such a
-// launch takes its tile descriptors from its parameters, so with another plan's
-// image in the workspace it still reads only the caller's buffers of this plan.
+// Start of a SMALL kernel: after the dependency wait, the plan id is loaded, but
+// not waited for.  A launch inside one bucket (k.one_nvec > 0) takes its tile
+// descriptors from its parameters, so its first replica loads go out beside the
+// id and plan_matches() gates the stores: with another plan's image in the
+// workspace it still reads only the caller's buffers of this plan.  A launch over
+// several buckets reads descriptors from the workspace's table and so checks the
+// id first.
 // (Letting the next launch be scheduled early from here, griddepcontrol
 // .launch_dependents at entry, was measured: per-bucket launches of 64 KiB
 // buckets unchanged, of 1 MiB buckets 17% slower; not kept.)

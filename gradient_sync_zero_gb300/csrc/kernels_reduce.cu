@@ -24,9 +24,11 @@ constexpr int kAccumPerSm = 3;
 // walk, the float-float partials and the split rule are rs_tiles in kernels.cuh).
 // ACC: the last micro-batch of gradient accumulation fused in — replica r's
 // value is bf16(g_r + micro_r), formed in registers (flat plans).
-// SMALL (a launch inside one bucket, few tiles): the plan id is checked beside
-// the first loads (it gates the stores), and a block's replicas are all loaded
-// at once.
+// SMALL (eight 64-thread CTAs per tile, one block per thread): a block's
+// replicas are all loaded at once; inside one bucket (descriptors from the
+// launch's parameters) the plan id is checked beside the first loads and gates
+// the stores, over several buckets (descriptors from the workspace's table) it
+// is checked before the table is read.
 // NT: threads per CTA (kSmallThreads for small launches without norm partials).
 template <int P, int MS, bool ACC, bool SMALL = false, int NT = kThreads>
 __global__ void __launch_bounds__(NT) k_reduce_scatter(KCommon k, const uint8_t* g, float* mean,
@@ -34,6 +36,7 @@ __global__ void __launch_bounds__(NT) k_reduce_scatter(KCommon k, const uint8_t*
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
+    if (k.one_nvec == 0 && !plan_matches(k, id)) return;   // descriptors from the workspace
   } else {
     if (!plan_ok(k)) return;
   }
@@ -50,6 +53,7 @@ __global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads) k_allreduce(
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
+    if (k.one_nvec == 0 && !plan_matches(k, id)) return;   // descriptors from the workspace
   } else {
     if (!plan_ok(k)) return;
   }
@@ -181,21 +185,13 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      if constexpr (M == 0) {   // flat plans: small single-bucket launches take SMALL
-        // each small CTA forms its sub-tile's norm partial as a whole-tile CTA would
-        if (sumsq && k.one_nvec > 0)
-          return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
-                                       k_reduce_scatter<P, M, false, true, kSmallThreads>,
-                                       kSmallThreads, kSmallSplit, k,
-                                       static_cast<const uint8_t*>(grads), mean, 1,
-                                       static_cast<const uint8_t*>(nullptr));
-        if (!sumsq)
-          return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
-                                       k_reduce_scatter<P, M, false, true, kSmallThreads>,
-                                       kSmallThreads, kSmallSplit, k,
-                                       static_cast<const uint8_t*>(grads), mean, 0,
-                                       static_cast<const uint8_t*>(nullptr));
-      }
+      if constexpr (M == 0)   // flat plans: the SMALL kernel (launch_small_or_split); each
+        // small CTA forms its sub-tile's norm partial as a whole-tile CTA would
+        return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
+                                     k_reduce_scatter<P, M, false, true, kSmallThreads>,
+                                     kSmallThreads, kSmallSplit, k,
+                                     static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0,
+                                     static_cast<const uint8_t*>(nullptr));
       if (sumsq)
         return launch_tiles(L, k_reduce_scatter<P, M, false>, k, static_cast<const uint8_t*>(grads),
                             mean, 1, static_cast<const uint8_t*>(nullptr));
@@ -222,7 +218,7 @@ int launch_allreduce(const Launch& L, void* grads) {
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      if constexpr (M == 0)   // flat plans: small single-bucket launches take SMALL
+      if constexpr (M == 0)   // flat plans: the SMALL kernel (launch_small_or_split)
         return launch_small_or_split(L, kAllreducePerSm, k_allreduce<P, M>, k_allreduce<P, M, true>,
                                      kSmallThreads, kSmallSplit, k, static_cast<uint8_t*>(grads));
       return launch_tiles_split(L, kAllreducePerSm, k_allreduce<P, M>, k, static_cast<uint8_t*>(grads));

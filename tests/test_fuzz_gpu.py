@@ -147,3 +147,40 @@ def test_random_plan_unclipped_zero_step_short_ctas(orc, seed):
     assert np.array_equal(c.from_replicas(params), p_o)
     for dev, ref in zip(st, (m_o, mo, vo)):
         assert np.array_equal(c.from_flat(dev).view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_plan_buckets_on_concurrent_streams(orc, seed):
+    """Buckets touch disjoint memory, so per-bucket launches may run at once: bucket b
+    on stream b mod 4 (reduce-scatter with norm partials, then all-reduce), joined
+    before the clip norm.  The results equal the oracle and the single launch."""
+    wl, _ = random_case(seed)
+    c = Case(wl)
+    g = c.host_grads(1)
+    nb = c.plan.n_buckets
+    buf, mean = c.to_replicas(g), c.plan.new_state()
+    dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, c.plan.new_state(), want_sumsq=True)
+    dps.dp_clip_coef(c.plan, c.ws, 0.05)
+    single = dps.dp_read_norm(c.plan, c.ws)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    cur = torch.cuda.current_stream()
+    for s_ in streams:
+        s_.wait_stream(cur)
+    for b in range(nb):
+        with torch.cuda.stream(streams[b % 4]):
+            dps.dp_reduce_scatter_mean(c.plan, c.ws, buf, mean, b, b + 1, want_sumsq=True)
+    for s_ in streams:
+        cur.wait_stream(s_)
+    dps.dp_clip_coef(c.plan, c.ws, 0.05)
+    assert dps.dp_read_norm(c.plan, c.ws) == single
+    for s_ in streams:
+        s_.wait_stream(cur)
+    for b in reversed(range(nb)):
+        with torch.cuda.stream(streams[b % 4]):
+            dps.dp_allreduce_mean(c.plan, c.ws, buf, b, b + 1)
+    for s_ in streams:
+        cur.wait_stream(s_)
+    torch.cuda.synchronize()
+    want, want_mean, _ = orc.allreduce_mean(c.sizes, wl.bucket_bytes, wl.P, g)
+    assert np.array_equal(c.from_flat(mean).view(np.uint32), want_mean.view(np.uint32))
+    assert np.array_equal(c.from_replicas(buf), want)

@@ -331,15 +331,22 @@ def test_empty_plan_calls_succeed():
 
 
 def test_plan_mismatch_is_refused():
+    """Whole-plan launches (the small kernels over several buckets check the plan
+    before they read the workspace's tile table) store nothing when the workspace
+    holds another plan's image."""
     a = case_for("ragged", 4)
     b = case_for("ragged", 4)
     g = a.to_replicas(a.host_grads(1))
     before = g.clone()
+    mean = torch.full((b.plan.L,), 3.0, dtype=torch.float32, device="cuda")
     dps.dp_allreduce_mean(b.plan, a.ws, g)           # a's image, b's plan
+    dps.dp_reduce_scatter_mean(b.plan, a.ws, g, mean)
+    dps.dp_reduce_scatter_mean(b.plan, a.ws, g, mean, want_sumsq=True)
     with pytest.raises(dps.DPError) as e:
         dps.dp_read_norm(b.plan, a.ws)
     assert e.value.code == dps.DP_EPLAN
     assert torch.equal(g, before)
+    assert bool((mean == 3.0).all())
 
 
 @pytest.mark.parametrize("P", [4, 16])
