@@ -234,15 +234,25 @@ int launch_replicate(const Launch& L, const RepArgs& a) {
 
 // The whole ZeRO-1/2 step without clipping, one pass.  The replica blocks are
 // loaded and folded first, then the fp32 state is loaded, which bounds the live
-// registers to one of the two groups.
-template <int P, int MS>
-__global__ void __launch_bounds__(kThreads)
+// registers to one of the two groups.  SMALL: eight 64-thread CTAs per tile, one
+// block per thread with all of its replica loads at once, the plan checked as in
+// the small all-reduce (beside the first loads inside one bucket, before the tile
+// table is read over several), every store gated on it.
+template <int P, int MS, bool SMALL = false>
+__global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads)
     k_zero_fused(KCommon k, const uint8_t* grads, uint8_t* params, float* master, float* m,
                  float* v, AdamScalars s) {
-  if (!plan_ok(k)) return;
-  for_each_block2(k, [&](const TileDesc& d, int64_t b, int c) {
+  uint64_t id = k.plan_id;
+  if constexpr (SMALL) {
+    id = plan_id_deferred(k);
+    if (k.one_nvec == 0 && !plan_matches(k, id)) return;   // descriptors from the workspace
+  } else {
+    if (!plan_ok(k)) return;
+  }
+  for_each_block2<true, SMALL ? kSmallThreads : kThreads>(k, [&](const TileDesc& d, int64_t b, int c) {
     float g[16];
-    block_mean16<P, MS>(k, grads, b, d, c, g);
+    block_mean16<P, MS, SMALL ? 16 : 8>(k, grads, b, d, c, g);
+    if (SMALL && id != k.plan_id) return;
     float th[16], mm[16], vv[16];
     ld_f16(master, b, th);
     ld_f16(m, b, mm);
@@ -254,6 +264,7 @@ __global__ void __launch_bounds__(kThreads)
     st_f16(v, b, vv);
     store_replicas<P>(params, k.stride_bytes, 32 * b, pack16_rne(th), k.P);
   });
+  if (SMALL) plan_matches(k, id);
 }
 
 // ---- second pass of the clipped step, staged through shared memory by bulk copies ----
@@ -371,6 +382,40 @@ __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mea
     }
     bulk_wait_all();
   }
+}
+
+// The same pass as eight 64-thread CTAs per tile, one 16-element block per thread
+// with all of its loads issued at once (plain 256-bit loads and stores, no
+// staging): g = mean x coef, AdamW on master/m/v, bf16(theta) into each of
+// `rows` rows.  The pass covers every bucket, so the plan is checked before the
+// tile table is read.
+template <bool DEV_S>
+__global__ void __launch_bounds__(kSmallThreads)
+    k_adamw_all_gather_small(KCommon k, const float* mean, uint8_t* params, float* master,
+                             float* m, float* v, AdamScalars s, const float* coefp, int rows,
+                             int64_t row_bytes) {
+  if (!plan_matches(k, plan_id_deferred(k))) return;
+  if constexpr (DEV_S) {
+    if (!header_scalars(k, s)) return;
+  }
+  const float coef = coefp ? *coefp : 1.0f;   // x 1 is exact: no clipping
+  for_each_block2<true, kSmallThreads>(k, [&](const TileDesc&, int64_t b, int) {
+    float g[16], th[16], mm[16], vv[16];
+    ld_f16(mean, b, g);
+    ld_f16(master, b, th);
+    ld_f16(m, b, mm);
+    ld_f16(v, b, vv);
+    const uint32_t dec = decay_bits2(k.decay, b);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) g[e] = __fmul_rn(g[e], coef);
+    adamw16(g, th, mm, vv, dec, s);
+    st_f16(master, b, th);
+    st_f16(m, b, mm);
+    st_f16(v, b, vv);
+    const Blk val = pack16_rne(th);
+#pragma unroll 1
+    for (int r = 0; r < rows; ++r) st_blk(params + r * row_bytes + 32 * b, val);
+  });
 }
 
 // DEV_S: the scalars come from the workspace header (see k_adamw).
@@ -499,6 +544,11 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
+      if constexpr (M == 0)   // flat plans: the SMALL kernel (launch_small_or_split)
+        return launch_small_or_split(L, 0, k_zero_fused<P, M>, k_zero_fused<P, M, true>,
+                                     kSmallThreads, kSmallSplit, k,
+                                     static_cast<const uint8_t*>(grads),
+                                     static_cast<uint8_t*>(params), master, m, v, s);
       return launch_tiles_split(L, 0, k_zero_fused<P, M>, k, static_cast<const uint8_t*>(grads),
                                 static_cast<uint8_t*>(params), master, m, v, s);
     });
@@ -529,6 +579,25 @@ int launch_ag(const Launch& L, const KCommon& k, const float* stage, void* param
                   static_cast<uint8_t*>(params), master, m, v, s, Lp, coefp, rows, row_bytes);
 }
 
+// The small-CTA pass over the whole plan (k_adamw_all_gather_small).
+template <bool DEV_S>
+int launch_ag_small(const Launch& L, KCommon k, const float* stage, void* params, float* master,
+                    float* m, float* v, const AdamScalars& s, const float* coefp, int rows,
+                    int64_t row_bytes) {
+  const int64_t n = L.tile_end - L.tile_begin;
+  if (n <= 0) return cudaSuccess;
+  if (n * kSmallSplit > INT_MAX) return cudaErrorInvalidValue;
+  k.split = kSmallSplit;
+  return launch_k(k_adamw_all_gather_small<DEV_S>, static_cast<int>(n * kSmallSplit), kSmallThreads,
+                  0, L.stream, k, stage, static_cast<uint8_t*>(params), master, m, v, s, coefp,
+                  rows, row_bytes);
+}
+
+bool ag_bulk() {
+  static const bool bulk = std::getenv("DPSYNC_AG_BULK") != nullptr;
+  return bulk;
+}
+
 int launch_adamw(const Launch& L, const float* grad, float* master, float* m, float* v,
                  void* params, const AdamScalars& s, const float* coefp, bool flat_params,
                  bool dev_scalars) {
@@ -539,6 +608,9 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
       return cudaErrorInvalidValue;   // only whole-plan flat updates exist
     if (L.plan->L == 0) return cudaSuccess;
     const KCommon k = make_common(L);
+    if (!ag_bulk())
+      return dev_scalars ? launch_ag_small<true>(L, k, grad, params, master, m, v, s, coefp, 1, 0)
+                         : launch_ag_small<false>(L, k, grad, params, master, m, v, s, coefp, 1, 0);
     return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, grad, params, master, m, v,
                                                                 s, coefp, 1, 0)
                        : launch_ag<false, kTmaChunk, kTmaStages>(L, k, grad, params, master, m,
@@ -555,6 +627,9 @@ int launch_adamw_all_gather(const Launch& L, const float* stage, void* params, f
   if (L.plan->L == 0) return cudaSuccess;
   const int rows = L.plan->P;
   const int64_t rb = k.stride_bytes;
+  if (!ag_bulk())
+    return dev_scalars ? launch_ag_small<true>(L, k, stage, params, master, m, v, s, coefp, rows, rb)
+                       : launch_ag_small<false>(L, k, stage, params, master, m, v, s, coefp, rows, rb);
   return dev_scalars ? launch_ag<true, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v, s,
                                                               coefp, rows, rb)
                      : launch_ag<false, kTmaChunk, kTmaStages>(L, k, stage, params, master, m, v,
