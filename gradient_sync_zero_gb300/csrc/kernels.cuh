@@ -728,7 +728,35 @@ __device__ __forceinline__ void for_each_block(const KCommon& k, F&& f) {
   }
 }
 
-// Same loop, giving the body the tile descriptor: f(desc, block b, owner c).
+// Same loop, giving the body the tile descriptor: f(desc, block b, owner c);
+// CTA `cta` of `ncta` (a kernel may give the walk to part of its grid).
+template <bool SPLIT = true, int NT = kThreads, class F>
+__device__ __forceinline__ void for_each_block2_of(const KCommon& k, int64_t cta, int64_t ncta,
+                                                   F&& f) {
+  auto walk = [&](int64_t t0, int64_t tstride, int j0, int jstep) {
+    for (int64_t tile = t0; tile < k.tile_end; tile += tstride) {
+      const TileDesc d = load_tile(k, tile);
+      if (!tile_ok(k, tile, d)) continue;
+      const int nblk = d.nvec >> 1;
+      const int64_t b0 = d.v0 >> 1;
+#pragma unroll 1
+      for (int j = j0; j < nblk; j += jstep) {
+        const int64_t b = b0 + j;
+        const int c = owner_of(d, 2 * b);
+        if (!DP_IN_BOUNDS(c >= 0 && c < k.S)) continue;
+        f(d, b, c);
+      }
+    }
+  };
+  if (!SPLIT || k.split == 1) {
+    walk(k.tile_begin + cta, ncta, threadIdx.x, NT);
+  } else {
+    const int64_t cta_tile = cta / k.split;
+    walk(k.tile_begin + cta_tile, ncta / k.split,
+         static_cast<int>(cta - k.split * cta_tile) * NT + threadIdx.x, k.split * NT);
+  }
+}
+
 template <bool SPLIT = true, int NT = kThreads, class F>
 __device__ __forceinline__ void for_each_block2(const KCommon& k, F&& f) {
   // the common case (split 1) keeps constant strides; splits are for small launches

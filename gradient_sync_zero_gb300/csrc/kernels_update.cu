@@ -187,6 +187,44 @@ __global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
   replicate_tiles<kRepStages>(k, a, blockIdx.x, gridDim.x, smem_raw);
 }
 
+// The same write-back as eight 64-thread CTAs per tile, one 32-byte block per
+// thread: one load, then a store to every destination row.  Short CTAs that
+// each own one block keep the stores spread over the whole GPU, where a
+// persistent grid of such threads queued on the LSU (above).  The plan is checked
+// before the tile table is read.
+__device__ __forceinline__ void replicate_small(const KCommon& k, const RepArgs& a, int64_t cta,
+                                                int64_t ncta) {
+  for_each_block2_of<true, kSmallThreads>(k, cta, ncta, [&](const TileDesc&, int64_t b, int c) {
+    const int64_t x = 2 * b;   // the block's first 16-byte vector
+    if (a.mode == kRepUnit) {
+      const int64_t col = x - a.dst_vec0;
+      if (!DP_IN_BOUNDS(col >= 0 && col + 2 <= a.dst_vec_limit)) return;
+      const Blk val = ld_blk(a.src + 16 * x);
+#pragma unroll 1
+      for (int r = 0; r < k.P; ++r) st_blk(a.dst + r * a.dst_stride + 16 * col, val);
+      return;
+    }
+    const int src_row = a.mode == kRepAllGather ? c : a.src_rank;
+    const Blk val = ld_blk(a.src + src_row * k.stride_bytes + 16 * x);
+#pragma unroll 1
+    for (int r = 0; r < k.P; ++r) {
+      if (a.mode == kRepAllGather && r % k.S == c) continue;
+      if (a.mode == kRepBroadcast && r == a.src_rank) continue;
+      st_blk(a.dst + r * a.dst_stride + 16 * x, val);
+    }
+  });
+}
+
+__global__ void __launch_bounds__(kSmallThreads) k_replicate_small(KCommon k, RepArgs a) {
+  if (!plan_matches(k, plan_id_deferred(k))) return;
+  replicate_small(k, a, blockIdx.x, gridDim.x);
+}
+
+bool rep_bulk() {
+  static const bool bulk = std::getenv("DPSYNC_REP_BULK") != nullptr;
+  return bulk;
+}
+
 // ZeRO-3 backward, two units in one launch: the gather of one unit's parameters
 // (the next unit's, FSDP's prefetch) and the reduce-scatter of another unit's
 // gradients ("Data Parallelism: DDP, ZeRO and FSDP", "How FSDP actually runs":
@@ -216,8 +254,34 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// The same two jobs as eight 64-thread CTAs per tile each: CTAs [0, n_rs) take
+// the reduce-scatter's pieces, the rest the gather's.  Both units are single
+// buckets, so the reduce-scatter checks the plan beside its first loads; the
+// gather checks it first.
+template <int P, int MS>
+__global__ void __launch_bounds__(kSmallThreads)
+    k_unit_backward_small(KCommon krs, const uint8_t* g, float* mean, int sumsq, KCommon kag,
+                          RepArgs a, int n_rs) {
+  const uint64_t id = plan_id_deferred(krs);
+  if (static_cast<int>(blockIdx.x) < n_rs) {
+    __shared__ FF warp_part[2 * (kSmallThreads / 32)];
+    rs_tiles<P, MS, false, true, kSmallThreads>(krs, g, mean, sumsq, nullptr, id, blockIdx.x, n_rs,
+                                               warp_part);
+    plan_matches(krs, id);
+  } else if (plan_matches(kag, id)) {
+    replicate_small(kag, a, blockIdx.x - n_rs, gridDim.x - n_rs);
+  }
+}
+
 int launch_replicate(const Launch& L, const RepArgs& a) {
   if (L.tile_end <= L.tile_begin) return cudaSuccess;
+  if (!rep_bulk() && (L.max_ctas <= 0 || L.short_ctas) &&
+      (L.tile_end - L.tile_begin) * kSmallSplit <= INT_MAX) {
+    KCommon k = make_common(L);
+    k.split = kSmallSplit;
+    return launch_k(k_replicate_small, static_cast<int>((L.tile_end - L.tile_begin) * kSmallSplit),
+                    kSmallThreads, 0, L.stream, k, a);
+  }
   cudaError_t e = ensure_dyn_smem(k_replicate, kRepSmem);
   if (e != cudaSuccess) return static_cast<int>(e);
   const int64_t cap = resident_ctas(k_replicate, 32, kRepSmem);
@@ -389,7 +453,9 @@ __device__ __forceinline__ void adamw_ag_body(const KCommon& k, const float* mea
 // staging): g = mean x coef, AdamW on master/m/v, bf16(theta) into each of
 // `rows` rows.  The pass covers every bucket, so the plan is checked before the
 // tile table is read.
-template <bool DEV_S>
+// OWNER: the staged step's AdamW instead, bf16(theta) into the owner's row of
+// each group only (the all-gather follows as its own pass).
+template <bool DEV_S, bool OWNER = false>
 __global__ void __launch_bounds__(kSmallThreads)
     k_adamw_all_gather_small(KCommon k, const float* mean, uint8_t* params, float* master,
                              float* m, float* v, AdamScalars s, const float* coefp, int rows,
@@ -399,7 +465,7 @@ __global__ void __launch_bounds__(kSmallThreads)
     if (!header_scalars(k, s)) return;
   }
   const float coef = coefp ? *coefp : 1.0f;   // x 1 is exact: no clipping
-  for_each_block2<true, kSmallThreads>(k, [&](const TileDesc&, int64_t b, int) {
+  for_each_block2<true, kSmallThreads>(k, [&](const TileDesc&, int64_t b, int c) {
     float g[16], th[16], mm[16], vv[16];
     ld_f16(mean, b, g);
     ld_f16(master, b, th);
@@ -413,8 +479,13 @@ __global__ void __launch_bounds__(kSmallThreads)
     st_f16(m, b, mm);
     st_f16(v, b, vv);
     const Blk val = pack16_rne(th);
+    if constexpr (OWNER) {
 #pragma unroll 1
-    for (int r = 0; r < rows; ++r) st_blk(params + r * row_bytes + 32 * b, val);
+      for (int g2 = 0; g2 < k.R; ++g2) st_blk(params + (g2 * k.S + c) * k.stride_bytes + 32 * b, val);
+    } else {
+#pragma unroll 1
+      for (int r = 0; r < rows; ++r) st_blk(params + r * row_bytes + 32 * b, val);
+    }
   });
 }
 
@@ -517,6 +588,15 @@ int launch_unit_backward(const Launch& Lrs, const void* grads, float* mean, bool
         n_rs = n_rs_tiles;
         n_ag = n_ag_tiles;
       }
+      if (!rep_bulk() && (n_rs_tiles + n_ag_tiles) * kSmallSplit <= INT_MAX) {
+        KCommon krs8 = krs, kag8 = kag;
+        krs8.split = kag8.split = kSmallSplit;
+        const int64_t rs8 = n_rs_tiles * kSmallSplit, ag8 = n_ag_tiles * kSmallSplit;
+        if (rs8 + ag8 == 0) return static_cast<int>(cudaSuccess);
+        return launch_k(k_unit_backward_small<P, M>, static_cast<int>(rs8 + ag8), kSmallThreads, 0,
+                        Lrs.stream, krs8, static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0,
+                        kag8, a, static_cast<int>(rs8));
+      }
       if (n_rs + n_ag == 0) return static_cast<int>(cudaSuccess);   // two empty units
       return launch_k(kern, static_cast<int>(n_rs + n_ag), kThreads, kUnitBwdSmem, Lrs.stream, krs,
                       static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0, kag, a,
@@ -615,6 +695,16 @@ int launch_adamw(const Launch& L, const float* grad, float* master, float* m, fl
                                                                 s, coefp, 1, 0)
                        : launch_ag<false, kTmaChunk, kTmaStages>(L, k, grad, params, master, m,
                                                                  v, s, coefp, 1, 0);
+  }
+  const int64_t n = L.tile_end - L.tile_begin;
+  if (!ag_bulk() && (L.max_ctas <= 0 || L.short_ctas) && n * kSmallSplit <= INT_MAX) {
+    if (n <= 0) return cudaSuccess;
+    KCommon k = make_common(L);
+    k.split = kSmallSplit;
+    return launch_k(dev_scalars ? k_adamw_all_gather_small<true, true>
+                                : k_adamw_all_gather_small<false, true>,
+                    static_cast<int>(n * kSmallSplit), kSmallThreads, 0, L.stream, k, grad,
+                    static_cast<uint8_t*>(params), master, m, v, s, coefp, 0, int64_t(0));
   }
   return launch_tiles_split(L, 0, dev_scalars ? k_adamw<true> : k_adamw<false>, make_common(L), grad,
                             master, m, v, static_cast<uint8_t*>(params), s, coefp);
