@@ -29,6 +29,7 @@ import dataclasses
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -49,6 +50,16 @@ KERNEL_BYTES_PER_PARAM = {
     "zero_fused": lambda P: 2 * P + 12 + 12 + 2 * P,
     "allreduce": lambda P: 4 * P,
 }
+
+
+def kernel_key(name):
+    """KERNEL_BYTES_PER_PARAM's key of an ncu kernel name (k_<key>, with the _small
+    suffix of a small-CTA variant or without, then its template or argument
+    list), or None."""
+    for k in KERNEL_BYTES_PER_PARAM:
+        if re.search(rf"\bk_{k}(_small)?[<(]", name):
+            return k
+    return None
 
 
 def workload_by_name(name):
@@ -217,7 +228,7 @@ def traffic_record(csv_path, target, captured, commands, out_dir=None):
         if len(r) < len(h):
             continue
         name = r[col["Kernel Name"]]
-        key = next((k for k in KERNEL_BYTES_PER_PARAM if f"k_{k}<" in name or f"k_{k}(" in name), None)
+        key = kernel_key(name)
         if key is None or r[col["Metric Name"]] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             continue
         v = float(r[col["Metric Value"]].replace(",", "")) * _BYTE_UNITS[r[col["Metric Unit"]]]

@@ -624,13 +624,11 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
     constexpr int P = decltype(pc)::value;
     return with_mesh<P>(L.plan, [&](auto mc) {
       constexpr int M = decltype(mc)::value;
-      if constexpr (M == 0)   // flat plans: the SMALL kernel (launch_small_or_split)
-        return launch_small_or_split(L, 0, k_zero_fused<P, M>, k_zero_fused<P, M, true>,
-                                     kSmallThreads, kSmallSplit, k,
-                                     static_cast<const uint8_t*>(grads),
-                                     static_cast<uint8_t*>(params), master, m, v, s);
-      return launch_tiles_split(L, 0, k_zero_fused<P, M>, k, static_cast<const uint8_t*>(grads),
-                                static_cast<uint8_t*>(params), master, m, v, s);
+      // the SMALL kernel (launch_small_or_split)
+      return launch_small_or_split(L, 0, k_zero_fused<P, M>, k_zero_fused<P, M, true>,
+                                   kSmallThreads, kSmallSplit, k,
+                                   static_cast<const uint8_t*>(grads),
+                                   static_cast<uint8_t*>(params), master, m, v, s);
     });
   });
 }
