@@ -1575,18 +1575,18 @@ def run_kernels(args):
                                  grads[:, o:o + ln], b, mean, want_sumsq=True)
 
     table = [  # name, kernel, bytes per parameter, call
-        ("dp_reduce_scatter_mean", "k_reduce_scatter", 2 * P + 4,
+        ("dp_reduce_scatter_mean", "k_reduce_scatter (small)", 2 * P + 4,
          lambda: dps.dp_reduce_scatter_mean(plan, ws, grads, mean, want_sumsq=True)),
         ("dp_clip_coef", "k_norm_finalize", 0, lambda: dps.dp_clip_coef(plan, ws, 1.0)),
-        ("dp_sharded_adamw_step", "k_adamw", 30,
+        ("dp_sharded_adamw_step", "k_adamw_all_gather_small (owner rows)", 30,
          lambda: dps.dp_sharded_adamw_step(plan, ws, mean, master, m, v, params, cfg, use_clip_coef=True)),
-        ("dp_all_gather", "k_all_gather", 2 * P, lambda: dps.dp_all_gather(plan, ws, params)),
-        ("dp_broadcast", "k_broadcast", 2 * P, lambda: dps.dp_broadcast(plan, ws, params, 0)),
-        ("dp_adamw_all_gather", "k_adamw_all_gather", 28 + 2 * P,
+        ("dp_all_gather", "k_replicate_small (all-gather)", 2 * P, lambda: dps.dp_all_gather(plan, ws, params)),
+        ("dp_broadcast", "k_replicate_small (broadcast)", 2 * P, lambda: dps.dp_broadcast(plan, ws, params, 0)),
+        ("dp_adamw_all_gather", "k_adamw_all_gather_small", 28 + 2 * P,
          lambda: dps.dp_adamw_all_gather(plan, ws, mean, master, m, v, params, cfg)),
-        ("dp_fused_zero_step (no clip)", "k_zero_fused", 4 * P + 24,
+        ("dp_fused_zero_step (no clip)", "k_zero_fused (small)", 4 * P + 24,
          lambda: dps.dp_fused_zero_step(plan, ws, grads, params, master, m, v, cfg0)),
-        ("dp_allreduce_mean", "k_allreduce", 4 * P, lambda: dps.dp_allreduce_mean(plan, ws, grads)),
+        ("dp_allreduce_mean", "k_allreduce (small)", 4 * P, lambda: dps.dp_allreduce_mean(plan, ws, grads)),
         ("dp_allreduce_mean_bf16wire", "k_allreduce_bf16wire", 4 * P,
          lambda: dps.dp_allreduce_mean_bf16wire(plan, ws, grads)),
         ("dp_accumulate", "k_accumulate", 6 * P, lambda: dps.dp_accumulate(plan, ws, grads, micro)),
@@ -1594,10 +1594,10 @@ def run_kernels(args):
          lambda: dps.dp_allreduce_mean_accum(plan, ws, grads, micro)),
         ("dp_reduce_scatter_mean_accum", "k_reduce_scatter (accumulating)", 4 * P + 4,
          lambda: dps.dp_reduce_scatter_mean_accum(plan, ws, grads, micro, mean, want_sumsq=True)),
-        ("dp_unit_all_gather (all units)", "k_unit_all_gather", 2 + 2 * P, unit_ag_pass),
-        ("dp_unit_reduce_scatter (all units)", "k_reduce_scatter", 2 * P + 4, unit_rs_pass),
-        ("dp_unit_backward (all units)", "k_unit_backward", (2 + 2 * P) + (2 * P + 4), unit_bwd_pass),
-        ("dp_shard_adamw_step", "k_adamw_all_gather (1 row)", 30,
+        ("dp_unit_all_gather (all units)", "k_replicate_small (unit)", 2 + 2 * P, unit_ag_pass),
+        ("dp_unit_reduce_scatter (all units)", "k_reduce_scatter (small)", 2 * P + 4, unit_rs_pass),
+        ("dp_unit_backward (all units)", "k_unit_backward_small", (2 + 2 * P) + (2 * P + 4), unit_bwd_pass),
+        ("dp_shard_adamw_step", "k_adamw_all_gather_small (1 row)", 30,
          lambda: dps.dp_shard_adamw_step(plan, ws, mean, master, m, v, shards, cfg, use_clip_coef=True)),
     ]
     peak, peak_src = measured_peaks()
