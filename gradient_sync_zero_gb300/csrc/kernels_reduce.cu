@@ -30,13 +30,17 @@ constexpr int kAccumPerSm = 3;
 // the stores, over several buckets (descriptors from the workspace's table) it
 // is checked before the table is read.
 // NT: threads per CTA (kSmallThreads for small launches without norm partials).
-template <int P, int MS, bool ACC, bool SMALL = false, int NT = kThreads>
+// TBL: a SMALL launch over several buckets (descriptors from the workspace's table:
+// the plan is checked before the table is read).
+template <int P, int MS, bool ACC, bool SMALL = false, int NT = kThreads, bool TBL = false>
 __global__ void __launch_bounds__(NT) k_reduce_scatter(KCommon k, const uint8_t* g, float* mean,
                                                        int sumsq, const uint8_t* micro) {
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
-    if (k.one_nvec == 0 && !plan_matches(k, id)) return;   // descriptors from the workspace
+    if constexpr (TBL) {
+      if (!plan_matches(k, id)) return;
+    }
   } else {
     if (!plan_ok(k)) return;
   }
@@ -48,12 +52,15 @@ __global__ void __launch_bounds__(NT) k_reduce_scatter(KCommon k, const uint8_t*
 // Fused mean all-reduce in place: sum in ring order, 1/P, bf16, written back to
 // every replica (the all-gather of the reduced shards).
 // SMALL: as for k_reduce_scatter.
-template <int P, int MS, bool SMALL = false>
+// TBL: as for k_reduce_scatter.
+template <int P, int MS, bool SMALL = false, bool TBL = false>
 __global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads) k_allreduce(KCommon k, uint8_t* g) {
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
-    if (k.one_nvec == 0 && !plan_matches(k, id)) return;   // descriptors from the workspace
+    if constexpr (TBL) {
+      if (!plan_matches(k, id)) return;
+    }
   } else {
     if (!plan_ok(k)) return;
   }
@@ -200,6 +207,7 @@ int launch_reduce_scatter(const Launch& L, const void* grads, float* mean, bool 
       // its sub-tile's norm partial as a whole-tile CTA would
       return launch_small_or_split(L, 0, k_reduce_scatter<P, M, false>,
                                    k_reduce_scatter<P, M, false, true, kSmallThreads>,
+                                   k_reduce_scatter<P, M, false, true, kSmallThreads, true>,
                                    kSmallThreads, kSmallSplit, k,
                                    static_cast<const uint8_t*>(grads), mean, sumsq ? 1 : 0,
                                    static_cast<const uint8_t*>(nullptr));
@@ -225,6 +233,7 @@ int launch_allreduce(const Launch& L, void* grads) {
       constexpr int M = decltype(mc)::value;
       // the SMALL kernel (launch_small_or_split)
       return launch_small_or_split(L, kAllreducePerSm, k_allreduce<P, M>, k_allreduce<P, M, true>,
+                                   k_allreduce<P, M, true, true>,
                                    kSmallThreads, kSmallSplit, k, static_cast<uint8_t*>(grads));
     });
   });

@@ -192,20 +192,25 @@ __global__ void __launch_bounds__(32) k_replicate(KCommon k, RepArgs a) {
 // each own one block keep the stores spread over the whole GPU, where a
 // persistent grid of such threads queued on the LSU (above).  The plan is checked
 // before the tile table is read.
+// id: the plan id this launch read, compared before the stores (inside one bucket the
+// walk reads descriptors from the launch's parameters, so the check can wait until
+// the loads are out; over several buckets the caller checks it before the walk).
 __device__ __forceinline__ void replicate_small(const KCommon& k, const RepArgs& a, int64_t cta,
-                                                int64_t ncta) {
+                                                int64_t ncta, uint64_t id) {
   for_each_block2_of<true, kSmallThreads>(k, cta, ncta, [&](const TileDesc&, int64_t b, int c) {
     const int64_t x = 2 * b;   // the block's first 16-byte vector
     if (a.mode == kRepUnit) {
       const int64_t col = x - a.dst_vec0;
       if (!DP_IN_BOUNDS(col >= 0 && col + 2 <= a.dst_vec_limit)) return;
       const Blk val = ld_blk(a.src + 16 * x);
+      if (id != k.plan_id) return;
 #pragma unroll 1
       for (int r = 0; r < k.P; ++r) st_blk(a.dst + r * a.dst_stride + 16 * col, val);
       return;
     }
     const int src_row = a.mode == kRepAllGather ? c : a.src_rank;
     const Blk val = ld_blk(a.src + src_row * k.stride_bytes + 16 * x);
+    if (id != k.plan_id) return;
 #pragma unroll 1
     for (int r = 0; r < k.P; ++r) {
       if (a.mode == kRepAllGather && r % k.S == c) continue;
@@ -215,9 +220,15 @@ __device__ __forceinline__ void replicate_small(const KCommon& k, const RepArgs&
   });
 }
 
+// TBL: descriptors from the workspace's table (a launch over several buckets).
+template <bool TBL>
 __global__ void __launch_bounds__(kSmallThreads) k_replicate_small(KCommon k, RepArgs a) {
-  if (!plan_matches(k, plan_id_deferred(k))) return;
-  replicate_small(k, a, blockIdx.x, gridDim.x);
+  const uint64_t id = plan_id_deferred(k);
+  if constexpr (TBL) {
+    if (!plan_matches(k, id)) return;
+  }
+  replicate_small(k, a, blockIdx.x, gridDim.x, id);
+  if constexpr (!TBL) plan_matches(k, id);
 }
 
 bool rep_bulk() {
@@ -256,8 +267,8 @@ __global__ void __launch_bounds__(kThreads)
 
 // The same two jobs as eight 64-thread CTAs per tile each: CTAs [0, n_rs) take
 // the reduce-scatter's pieces, the rest the gather's.  Both units are single
-// buckets, so the reduce-scatter checks the plan beside its first loads; the
-// gather checks it first.
+// buckets (descriptors from the launch's parameters), so both check the plan
+// beside their first loads and gate their stores on it.
 template <int P, int MS>
 __global__ void __launch_bounds__(kSmallThreads)
     k_unit_backward_small(KCommon krs, const uint8_t* g, float* mean, int sumsq, KCommon kag,
@@ -268,8 +279,9 @@ __global__ void __launch_bounds__(kSmallThreads)
     rs_tiles<P, MS, false, true, kSmallThreads>(krs, g, mean, sumsq, nullptr, id, blockIdx.x, n_rs,
                                                warp_part);
     plan_matches(krs, id);
-  } else if (plan_matches(kag, id)) {
-    replicate_small(kag, a, blockIdx.x - n_rs, gridDim.x - n_rs);
+  } else {
+    replicate_small(kag, a, blockIdx.x - n_rs, gridDim.x - n_rs, id);
+    plan_matches(kag, id);
   }
 }
 
@@ -279,8 +291,9 @@ int launch_replicate(const Launch& L, const RepArgs& a) {
       (L.tile_end - L.tile_begin) * kSmallSplit <= INT_MAX) {
     KCommon k = make_common(L);
     k.split = kSmallSplit;
-    return launch_k(k_replicate_small, static_cast<int>((L.tile_end - L.tile_begin) * kSmallSplit),
-                    kSmallThreads, 0, L.stream, k, a);
+    const int grid = static_cast<int>((L.tile_end - L.tile_begin) * kSmallSplit);
+    if (k.one_nvec > 0) return launch_k(k_replicate_small<false>, grid, kSmallThreads, 0, L.stream, k, a);
+    return launch_k(k_replicate_small<true>, grid, kSmallThreads, 0, L.stream, k, a);
   }
   cudaError_t e = ensure_dyn_smem(k_replicate, kRepSmem);
   if (e != cudaSuccess) return static_cast<int>(e);
@@ -302,14 +315,16 @@ int launch_replicate(const Launch& L, const RepArgs& a) {
 // block per thread with all of its replica loads at once, the plan checked as in
 // the small all-reduce (beside the first loads inside one bucket, before the tile
 // table is read over several), every store gated on it.
-template <int P, int MS, bool SMALL = false>
+template <int P, int MS, bool SMALL = false, bool TBL = false>
 __global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads)
     k_zero_fused(KCommon k, const uint8_t* grads, uint8_t* params, float* master, float* m,
                  float* v, AdamScalars s) {
   uint64_t id = k.plan_id;
   if constexpr (SMALL) {
     id = plan_id_deferred(k);
-    if (k.one_nvec == 0 && !plan_matches(k, id)) return;   // descriptors from the workspace
+    if constexpr (TBL) {   // descriptors from the workspace: check before reading them
+      if (!plan_matches(k, id)) return;
+    }
   } else {
     if (!plan_ok(k)) return;
   }
@@ -626,6 +641,7 @@ int launch_zero_fused(const Launch& L, const void* grads, void* params, float* m
       constexpr int M = decltype(mc)::value;
       // the SMALL kernel (launch_small_or_split)
       return launch_small_or_split(L, 0, k_zero_fused<P, M>, k_zero_fused<P, M, true>,
+                                   k_zero_fused<P, M, true, true>,
                                    kSmallThreads, kSmallSplit, k,
                                    static_cast<const uint8_t*>(grads),
                                    static_cast<uint8_t*>(params), master, m, v, s);

