@@ -72,11 +72,30 @@ __global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads) k_allreduce(
   if (SMALL) plan_matches(k, id);
 }
 
+// The start of the accumulation kernels: SMALL (eight 64-thread CTAs per tile, one
+// block per thread) checks the plan as the small all-reduce does (TBL: before the
+// workspace's tile table is read), the persistent form before anything.  Returns
+// false when the kernel stops; *id is the plan id that gates a SMALL kernel's stores.
+template <bool SMALL, bool TBL>
+__device__ __forceinline__ bool accum_start(const KCommon& k, uint64_t* id) {
+  *id = k.plan_id;
+  if constexpr (SMALL) {
+    *id = plan_id_deferred(k);
+    if constexpr (TBL) return plan_matches(k, *id);
+    return true;
+  } else {
+    return plan_ok(k);
+  }
+}
+
 // acc[r] = bf16(acc[r] + micro[r]) for every replica.
-__global__ void __launch_bounds__(kThreads) k_accumulate(KCommon k, uint8_t* acc,
-                                                         const uint8_t* micro) {
-  if (!plan_ok(k)) return;
-  for_each_block(k, [&](int64_t, int64_t b, int) {
+template <bool SMALL = false, bool TBL = false>
+__global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads)
+    k_accumulate(KCommon k, uint8_t* acc, const uint8_t* micro) {
+  uint64_t id;
+  if (!accum_start<SMALL, TBL>(k, &id)) return;
+  for_each_block2<true, SMALL ? kSmallThreads : kThreads>(k, [&](const TileDesc&, int64_t b, int) {
+#pragma unroll 4
     for (int r = 0; r < k.P; ++r) {
       const Blk x = ld_blk(acc + r * k.stride_bytes + 32 * b);
       const Blk y = ld_blk(micro + r * k.stride_bytes + 32 * b);
@@ -85,32 +104,39 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(KCommon k, uint8_t* acc
       unpack16(y, c);
 #pragma unroll
       for (int e = 0; e < 16; ++e) a[e] = __fadd_rn(a[e], c[e]);
+      if (SMALL && id != k.plan_id) continue;
       st_blk(acc + r * k.stride_bytes + 32 * b, pack16_rne(a));
     }
   });
+  if (SMALL) plan_matches(k, id);
 }
 
 // Last micro-batch: accumulate and mean all-reduce in one pass, result in acc.
-template <int P>
-__global__ void __launch_bounds__(kThreads) k_allreduce_accum(KCommon k, uint8_t* acc,
-                                                              const uint8_t* micro) {
-  if (!plan_ok(k)) return;
-  for_each_block<false>(k, [&](int64_t, int64_t b, int c) {
+template <int P, bool SMALL = false, bool TBL = false>
+__global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads)
+    k_allreduce_accum(KCommon k, uint8_t* acc, const uint8_t* micro) {
+  uint64_t id;
+  if (!accum_start<SMALL, TBL>(k, &id)) return;
+  for_each_block2<SMALL, SMALL ? kSmallThreads : kThreads>(k, [&](const TileDesc&, int64_t b, int c) {
     float mean[16];
     ring_mean16_accum<P>(acc, micro, k.stride_bytes, 32 * b, c, k.P, mean);
-    store_replicas<P>(acc, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
+    if (!SMALL || id == k.plan_id) store_replicas<P>(acc, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
   });
+  if (SMALL) plan_matches(k, id);
 }
 
 // Mean all-reduce with bf16 partial sums on the ring.
-template <int P>
-__global__ void __launch_bounds__(kThreads) k_allreduce_bf16wire(KCommon k, uint8_t* g) {
-  if (!plan_ok(k)) return;
-  for_each_block<false>(k, [&](int64_t, int64_t b, int c) {
+template <int P, bool SMALL = false, bool TBL = false>
+__global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads)
+    k_allreduce_bf16wire(KCommon k, uint8_t* g) {
+  uint64_t id;
+  if (!accum_start<SMALL, TBL>(k, &id)) return;
+  for_each_block2<SMALL, SMALL ? kSmallThreads : kThreads>(k, [&](const TileDesc&, int64_t b, int c) {
     float mean[16];
     ring_mean16_bf16wire<P>(g, k.stride_bytes, 32 * b, c, k.P, mean);
-    store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
+    if (!SMALL || id == k.plan_id) store_replicas<P>(g, k.stride_bytes, 32 * b, pack16_rne(mean), k.P);
   });
+  if (SMALL) plan_matches(k, id);
 }
 
 // The global norm over tiles [tile_begin, tile_end): their sub-tile partials
@@ -255,16 +281,18 @@ int64_t bounds_violations_reduce(bool reset) {
 }
 
 int launch_accumulate(const Launch& L, void* acc, const void* micro) {
-  return launch_tiles_split(L, kAccumPerSm, k_accumulate, make_common(L), static_cast<uint8_t*>(acc),
-                            static_cast<const uint8_t*>(micro));
+  return launch_small_or_split(L, kAccumPerSm, k_accumulate<>, k_accumulate<true>,
+                               k_accumulate<true, true>, kSmallThreads, kSmallSplit, make_common(L),
+                               static_cast<uint8_t*>(acc), static_cast<const uint8_t*>(micro));
 }
 
 int launch_allreduce_accum(const Launch& L, void* acc, const void* micro) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
     constexpr int P = decltype(pc)::value;
-    return launch_tiles_per_sm(L, kAccumPerSm, k_allreduce_accum<P>, k, static_cast<uint8_t*>(acc),
-                               static_cast<const uint8_t*>(micro));
+    return launch_small_or_split(L, kAccumPerSm, k_allreduce_accum<P>, k_allreduce_accum<P, true>,
+                                 k_allreduce_accum<P, true, true>, kSmallThreads, kSmallSplit, k,
+                                 static_cast<uint8_t*>(acc), static_cast<const uint8_t*>(micro));
   });
 }
 
@@ -272,8 +300,9 @@ int launch_allreduce_bf16wire(const Launch& L, void* grads) {
   const KCommon k = make_common(L);
   return with_P(L.plan->P, [&](auto pc) {
     constexpr int P = decltype(pc)::value;
-    return launch_tiles_per_sm(L, kAllreducePerSm, k_allreduce_bf16wire<P>, k,
-                               static_cast<uint8_t*>(grads));
+    return launch_small_or_split(L, kAllreducePerSm, k_allreduce_bf16wire<P>,
+                                 k_allreduce_bf16wire<P, true>, k_allreduce_bf16wire<P, true, true>,
+                                 kSmallThreads, kSmallSplit, k, static_cast<uint8_t*>(grads));
   });
 }
 
