@@ -24,7 +24,8 @@ DP_OK, DP_EINVAL, DP_EALIGN, DP_EPLAN, DP_ECUDA, DP_ENONFINITE, DP_ENOMEM, DP_ET
 DP_STATUS_PLAN_MISMATCH, DP_STATUS_NONFINITE, DP_STATUS_TIMEOUT, DP_STATUS_NO_SCALARS = 1, 2, 4, 8
 DP_TRACK_ALLREDUCE, DP_TRACK_REDUCE_SCATTER, DP_TRACK_ZERO_STEP, DP_TRACK_DRY_RUN = 0, 1, 2, 1
 DP_TRACK_SHORT_CTAS = 2
-DP_LAUNCH_PERSISTENT, DP_LAUNCH_SHORT_CTAS = 0, 1
+DP_LAUNCH_DEFAULT, DP_LAUNCH_SHORT_CTAS = 0, 1
+DP_LAUNCH_PERSISTENT = DP_LAUNCH_DEFAULT     # the older name
 DP_CKPT_HOST = 1
 
 
@@ -289,11 +290,11 @@ def _range(plan, b0, b1):
 
 def set_stream_launch(stream, short_ctas):
     """Launch shape of every later compute call on `stream` (dp_stream_set_launch):
-    short_ctas=True for short-lived CTAs (a low-priority stream beside a
-    high-priority compute stream), False for the default persistent grids.  Set
-    False again before the stream is destroyed."""
+    short_ctas=True for short-lived CTAs in every kernel (a low-priority stream
+    beside a high-priority compute stream), False for each kernel's default shape.
+    Set False again before the stream is destroyed."""
     _check(lib().dp_stream_set_launch(_stream(stream),
-                                      DP_LAUNCH_SHORT_CTAS if short_ctas else DP_LAUNCH_PERSISTENT))
+                                      DP_LAUNCH_SHORT_CTAS if short_ctas else DP_LAUNCH_DEFAULT))
 
 
 def stream_launch(stream):

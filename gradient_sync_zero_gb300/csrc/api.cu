@@ -134,11 +134,11 @@ extern "C" {
 
 int dp_stream_set_launch(void* stream, int32_t shape) {
   clear_error();
-  if (shape != DP_LAUNCH_PERSISTENT && shape != DP_LAUNCH_SHORT_CTAS)
+  if (shape != DP_LAUNCH_DEFAULT && shape != DP_LAUNCH_SHORT_CTAS)
     return fail(DP_EINVAL, "dp_stream_set_launch: unknown launch shape " + std::to_string(shape));
   std::lock_guard<std::mutex> lock(g_shape_mu);
   try {
-    if (shape == DP_LAUNCH_PERSISTENT)
+    if (shape == DP_LAUNCH_DEFAULT)
       g_shape.erase(stream);
     else
       g_shape[stream] = shape;
@@ -152,7 +152,7 @@ int dp_stream_set_launch(void* stream, int32_t shape) {
 int dp_stream_get_launch(void* stream, int32_t* shape) {
   clear_error();
   if (!shape) return fail(DP_EINVAL, "dp_stream_get_launch: NULL shape");
-  *shape = stream_short_ctas(stream) ? DP_LAUNCH_SHORT_CTAS : DP_LAUNCH_PERSISTENT;
+  *shape = stream_short_ctas(stream) ? DP_LAUNCH_SHORT_CTAS : DP_LAUNCH_DEFAULT;
   return DP_OK;
 }
 

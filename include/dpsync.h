@@ -218,27 +218,30 @@ int dp_plan_upload(const dp_plan* plan, void* workspace, void* stream);
  * their collectives beside the backward ("4.1 Data parallelism in depth",
  * sec. 4.2; "Data Parallelism: DDP, ZeRO and FSDP", "How FSDP actually runs");
  * here those collectives are kernels that share the SMs with the backward's.
- *   DP_LAUNCH_PERSISTENT  (every stream's default) a grid of at most the CTAs the
- *                         GPU holds at once, each walking many tiles: fastest
- *                         when the kernel has the GPU to itself.
- *   DP_LAUNCH_SHORT_CTAS  one short-lived CTA per tile (per eighth of a tile for
- *                         the flat all-reduce and reduce-scatter inside one
- *                         bucket): each holds its SM for microseconds, so a kernel
- *                         of a higher-priority stream waiting for SMs (a GEMM wave)
- *                         gets them almost at once.  For a stream of the lowest
- *                         priority beside a compute stream of a higher one
- *                         (cudaStreamCreateWithPriority).
+ *   DP_LAUNCH_DEFAULT     (every stream's default; DP_LAUNCH_PERSISTENT is its
+ *                         older name) each kernel's own shape: short-lived CTAs,
+ *                         eight 64-thread CTAs per tile, one block per thread, for
+ *                         the all-reduce, the reduce-scatter, the update passes and
+ *                         the write-back; a persistent grid (at most the CTAs the
+ *                         GPU holds at once, each walking many tiles) for the mesh
+ *                         reduce-scatter, the accumulating reduce-scatter and any
+ *                         launch a tracker's max_ctas caps below its pieces.
+ *   DP_LAUNCH_SHORT_CTAS  short-lived CTAs for every kernel, the persistent ones
+ *                         as one CTA per tile, caps ignored.  Each CTA holds its SM
+ *                         for microseconds, so a kernel of a higher-priority stream
+ *                         waiting for SMs (a GEMM wave) gets them almost at once.
+ *                         For a stream of the lowest priority beside a compute
+ *                         stream of a higher one (cudaStreamCreateWithPriority).
  * Every call enqueued on `stream` afterwards, from any host thread, takes the
- * shape, except dp_adamw_all_gather, dp_shard_adamw_step and the clipped
- * dp_fused_zero_step's update pass (bulk-copy kernels that keep their persistent
- * grid) and dp_clip_coef_noalloc; a tracker whose stream is set fires as with
- * DP_TRACK_SHORT_CTAS.  Results do not depend on the shape, bit for bit.
- * The setting is host state kept per stream handle (NULL: the legacy default
- * stream); it costs an uncontended lock per call while any stream is set.  Set
- * DP_LAUNCH_PERSISTENT again before destroying a stream: CUDA may give its
- * handle to a later stream.  DP_EINVAL for another shape.
+ * shape, except the bulk-copy kernels selected by DPSYNC_AG_BULK / DPSYNC_REP_BULK
+ * (kept for comparison) and dp_clip_coef_noalloc; a tracker whose stream is set
+ * fires as with DP_TRACK_SHORT_CTAS.  Results do not depend on the shape, bit for
+ * bit.  The setting is host state kept per stream handle (NULL: the legacy
+ * default stream); it costs an uncontended lock per call while any stream is
+ * set.  Set DP_LAUNCH_DEFAULT again before destroying a stream: CUDA may give
+ * its handle to a later stream.  DP_EINVAL for another shape.
  */
-enum { DP_LAUNCH_PERSISTENT = 0, DP_LAUNCH_SHORT_CTAS = 1 };
+enum { DP_LAUNCH_DEFAULT = 0, DP_LAUNCH_PERSISTENT = 0, DP_LAUNCH_SHORT_CTAS = 1 };
 int dp_stream_set_launch(void* stream, int32_t shape);
 int dp_stream_get_launch(void* stream, int32_t* shape);
 
@@ -553,20 +556,22 @@ int dp_fused_zero_step_launches(const dp_adamw_cfg* cfg);
  * dp_tracker_wait returns once every bucket has been launched, or DP_ETIMEOUT
  * after timeout_ms naming tensors never marked (DDP would hang there).  It does
  * not synchronise the GPU: order later work after comm_stream.
- *   max_ctas   cap on each launch's grid (0 = the full persistent grid), to leave
- *              SMs to the backward running beside it.
+ *   max_ctas   cap on each launch's grid (0 = no cap), to leave SMs to the
+ *              backward running beside it: a launch whose short CTAs exceed the
+ *              cap runs on a persistent grid of at most max_ctas CTAs.
  *   flags      DP_TRACK_DRY_RUN: record the firing order, launch nothing.
- *              DP_TRACK_SHORT_CTAS: every bucket goes out as its own launch of
- *              short-lived CTAs, one per piece of a tile (an eighth of a tile
- *              for the flat all-reduce and reduce-scatter, a tile otherwise),
- *              instead of a persistent grid; max_ctas (and side_ctas) are then
+ *              DP_TRACK_SHORT_CTAS: every bucket goes out as its own launch
+ *              (no merging of buckets that became ready together) of
+ *              short-lived CTAs, as DP_LAUNCH_SHORT_CTAS gives them (eight
+ *              64-thread CTAs per tile, one CTA per tile for the kernels that
+ *              are otherwise persistent); max_ctas (and side_ctas) are then
  *              ignored.  Such a CTA holds its SM for microseconds, so a kernel of
  *              higher priority waiting for SMs gets them almost at once.  Meant
  *              for comm_stream at the lowest priority and the backward's stream
  *              at a higher one (cudaStreamCreateWithPriority): its GEMM waves
  *              then take the SMs first and the reductions fill the SMs the GEMMs
  *              leave idle and the gaps between them.  Results are those of the
- *              persistent launches, bit for bit.
+ *              other launches, bit for bit.
  *              Other bits: DP_EINVAL.
  * Events are the caller's: keep them alive and unrecorded until their bucket
  * fires.  Marking a tensor twice in one step is DP_EINVAL.

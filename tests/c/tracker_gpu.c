@@ -106,7 +106,7 @@ int main(void) {
     return 8;
   if (dp_stream_set_launch(comm, DP_LAUNCH_SHORT_CTAS) != DP_OK ||
       dp_allreduce_mean(plan, d_ws, d_rep2, 0, info.n_buckets, comm) != DP_OK ||
-      dp_stream_set_launch(comm, DP_LAUNCH_PERSISTENT) != DP_OK || cudaStreamSynchronize(comm) != cudaSuccess)
+      dp_stream_set_launch(comm, DP_LAUNCH_DEFAULT) != DP_OK || cudaStreamSynchronize(comm) != cudaSuccess)
     return 8;
   cudaMemcpy(back2, d_rep2, n_rep * 2, cudaMemcpyDeviceToHost);
 

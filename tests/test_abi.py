@@ -304,9 +304,9 @@ def test_stream_launch_shape_registry():
         assert lib.dp_stream_get_launch(h, C.byref(out)) == 0
         return out.value
 
-    assert get(a) == dps.DP_LAUNCH_PERSISTENT and get(None) == dps.DP_LAUNCH_PERSISTENT
+    assert get(a) == dps.DP_LAUNCH_DEFAULT and get(None) == dps.DP_LAUNCH_DEFAULT
     assert lib.dp_stream_set_launch(a, dps.DP_LAUNCH_SHORT_CTAS) == 0
-    assert get(a) == dps.DP_LAUNCH_SHORT_CTAS and get(b) == dps.DP_LAUNCH_PERSISTENT
+    assert get(a) == dps.DP_LAUNCH_SHORT_CTAS and get(b) == dps.DP_LAUNCH_DEFAULT
     assert lib.dp_stream_set_launch(None, dps.DP_LAUNCH_SHORT_CTAS) == 0
     assert get(None) == dps.DP_LAUNCH_SHORT_CTAS
     for bad in (2, -1, 7):
@@ -314,9 +314,10 @@ def test_stream_launch_shape_registry():
         assert b"unknown launch shape" in lib.dp_last_error()
     assert get(a) == dps.DP_LAUNCH_SHORT_CTAS          # a refused call changes nothing
     assert lib.dp_stream_get_launch(a, None) == dps.DP_EINVAL
-    assert lib.dp_stream_set_launch(a, dps.DP_LAUNCH_PERSISTENT) == 0
-    assert lib.dp_stream_set_launch(None, dps.DP_LAUNCH_PERSISTENT) == 0
-    assert get(a) == dps.DP_LAUNCH_PERSISTENT and get(None) == dps.DP_LAUNCH_PERSISTENT
+    assert lib.dp_stream_set_launch(a, dps.DP_LAUNCH_DEFAULT) == 0
+    assert lib.dp_stream_set_launch(None, dps.DP_LAUNCH_DEFAULT) == 0
+    assert get(a) == dps.DP_LAUNCH_DEFAULT and get(None) == dps.DP_LAUNCH_DEFAULT
+    assert dps.DP_LAUNCH_PERSISTENT == dps.DP_LAUNCH_DEFAULT == 0   # the older name
     assert dps.stream_launch(0x5000) is False
     dps.set_stream_launch(0x5000, True)
     assert dps.stream_launch(0x5000) is True
