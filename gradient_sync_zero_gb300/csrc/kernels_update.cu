@@ -71,12 +71,14 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---- replica write-back with bulk copies: all-gather, broadcast, unit all-gather ----
+// (Kept for comparison, selected with DPSYNC_REP_BULK: the default is the small-CTA
+// write-back, k_replicate_small, 10% faster on GB300.)
 // Each tile (<= 8192 elements, inside one bucket) is one job: one thread streams
 // the tile's source segments into a shared-memory stage (bulk loads counted on an
 // mbarrier) and writes the stage to every destination row with bulk stores.
-// Written with per-thread 32-byte accesses, one load feeds P-1 stores and the
-// LSU queue limits the kernel (lg_throttle 23 stalls per issue at P = 8); a bulk
-// store moves a whole segment per instruction.  A 6-deep ring of 16 KB stages
+// Written with per-thread 32-byte accesses on a persistent grid, one load feeds
+// P-1 stores and the LSU queue limited the kernel (lg_throttle 23 stalls per issue
+// at P = 8); a bulk store moves a whole segment per instruction.  A 6-deep ring of 16 KB stages
 // (96 KB, 2 CTAs per SM): against 2-4 stages it changes the all-gather by <0.5%
 // and makes each short ZeRO-3 unit gather 5% faster.  Every wait is bounded
 // (DP_STATUS_TIMEOUT, the CTA still drains its copies).
@@ -347,21 +349,24 @@ __global__ void __launch_bounds__(SMALL ? kSmallThreads : kThreads)
 }
 
 // ---- second pass of the clipped step, staged through shared memory by bulk copies ----
-// The pass needs no shard owner (every replica gets the same parameters), so it
-// walks [0, L) in chunks of kTmaChunk elements.  One elected thread streams the
+// (Kept for comparison, selected with DPSYNC_AG_BULK: the default is the small-CTA
+// pass below, 10% faster on GB300.)  The pass needs no shard owner (every replica
+// gets the same parameters), so it walks [0, L) in chunks of kTmaChunk elements.  One elected thread streams the
 // four fp32 inputs of a chunk (mean, master, m, v) into a shared-memory ring
 // with cp.async.bulk (completion counted on an mbarrier), the CTA updates
 // the chunk in place, and the elected thread streams master, m, v and the bf16
 // parameters back out with bulk stores, the parameters once per replica.  Large
 // contiguous bulk transfers run the 36%-read / 64%-write mix of this pass closer
-// to the HBM limit than per-thread 32-byte accesses.  Every wait is bounded: a
+// to the HBM limit than per-thread 32-byte accesses from a persistent grid did
+// (short-lived CTAs with one block per thread do better still).  Every wait is bounded: a
 // timeout sets DP_STATUS_TIMEOUT, and the CTA still drains its own copies.
 //
 // Chunk and ring depth: 2048 elements and 2 stages (36 KB per stage, 3 CTAs per
 // SM), one chunk loading while the previous one is updated and stored.  Measured
 // on the 1.1B case against 1024 x {2, 3, 4} stages, 2048 x 3 and 3072 / 4096 x 2:
 // 3.3% faster than 1024 x 3 (the deeper rings keep more reads in flight and run
-// the read/write mix worse); per-thread 32-byte accesses are slower still.
+// the read/write mix worse); per-thread 32-byte accesses on a persistent grid were
+// slower still.
 template <int CH>
 struct TmaStageT {
   float in[4][CH];           // mean, master, m, v
