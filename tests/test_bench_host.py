@@ -182,3 +182,24 @@ def test_traffic_record_from_an_ncu_csv(tmp_path):
     assert abs(ag["bytes_per_launch"] - 8000e6 * scale) < 1.0
     assert rs["kernel_src_sha"] == bench.kernel_source_hash()
     assert "# ncu ..." in text.replace("#   ", "# ")
+
+
+def test_kernel_key_maps_ncu_names_of_every_variant():
+    """The traffic record and the roofline key ncu's kernel names by what the bench
+    times: persistent, small-CTA (the _small suffix or a template flag) and
+    bulk-copy variants of one kernel share a key; other kernels have none."""
+    import bench
+    cases = {
+        "void k_adamw_all_gather_small<0, 0>(KCommon, const float *, unsigned char *)": "adamw_all_gather",
+        "void k_adamw_all_gather<0, 2048, 2>(KCommon, const float *)": "adamw_all_gather",
+        "void k_reduce_scatter<8, 0, 0, 1, 64, 1>(KCommon, const unsigned char *)": "reduce_scatter",
+        "void k_reduce_scatter<8, 0, 0, 0, 256>(KCommon)": "reduce_scatter",
+        "void k_allreduce<8, 0, 1, 0>(KCommon, unsigned char *)": "allreduce",
+        "void k_zero_fused<8, 0, 1, 1>(KCommon)": "zero_fused",
+        "k_norm_finalize(KCommon, double)": None,
+        "void k_allreduce_accum<8, 1, 0>(KCommon)": None,
+        "void k_allreduce_bf16wire<8, 1, 1>(KCommon)": None,
+        "void k_replicate_small<1>(KCommon, RepArgs)": None,
+    }
+    for name, key in cases.items():
+        assert bench.kernel_key(name) == key, name
