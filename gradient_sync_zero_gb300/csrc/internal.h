@@ -12,9 +12,10 @@
 namespace dps {
 
 constexpr int kThreads = 256;                 // threads per CTA
-// Launches inside one bucket over few tiles: CTAs of kSmallThreads threads,
-// kSmallSplit per tile, so one thread moves one 32-byte block and the launch's
-// loads and stores are spread over kSmallSplit times more SMs.
+// The small-CTA launch shape (the default for the step's kernels): CTAs of
+// kSmallThreads threads, kSmallSplit per tile, one CTA per piece of a tile for the
+// whole launch, so one thread moves one 32-byte block with all of its loads in
+// flight and the launch's loads and stores spread over the whole GPU.
 constexpr int kSmallThreads = 64;
 constexpr int kSmallSplit = 8;
 // Norm partials: one float-float pair per sub-tile of kSubTileBlocks 32-byte
